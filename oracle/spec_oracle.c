@@ -1,0 +1,507 @@
+/*
+ * spec_oracle.c -- CPU oracle for the tree-verification step of lossless greedy
+ * speculative decoding on a hybrid Gated-DeltaNet / attention target.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
+ * definition that the CUDA library is checked against.  Only the test suite,
+ * the smoke check and the CPU-baseline leg of the benchmark may load it.  It
+ * shares no code, header, table or constant with the CUDA path, and the CUDA
+ * path never calls it.
+ *
+ * Source of every definition below: the paper digest "SpecPilot: Autonomous
+ * Algorithm Discovery and Systems Optimization for Speculative Decoding"
+ * (rainbus.top), cited by its section names:
+ *   [SD]    prerequisites / speculative decoding   -- greedy acceptance rule,
+ *           tau in [1, m+1], one bonus token;
+ *   [LAT]   prerequisites / parallel drafter        -- per-position top-16
+ *           candidates with scores form the lattice;
+ *   [TREE]  prerequisites / draft-tree verification -- every node sees only its
+ *           ancestors; accept the longest root path matching the target argmax
+ *           plus a bonus; nodes added greedily by path log-prob up to N;
+ *   [GDN]   prerequisites / hybrid recurrent target -- the gated delta rule
+ *           h_t = a_t (I - b_t k_t k_t^T) h_{t-1} + b_t k_t v_t^T,
+ *           o_t = h_t^T q_t;
+ *   [NOV]   technical novelty + Figure 6 ("Best-first tree on a hybrid
+ *           target") -- best-first tree with edges scored log p(child|parent);
+ *           node states recomputed along root paths, no per-node snapshots.
+ *
+ * Precision: every floating-point result is accumulated in double from the
+ * exact values of the (bf16 or fp32) inputs.  The one exception is the tree
+ * key, a root-path sum of fp32 edge scores, which the readings below fix as an
+ * fp32 sum; it is computed in float on purpose.
+ *
+ * Readings of points the page leaves open (listed again in the design notes):
+ *   R1  N counts draft nodes; the root (the pending bonus token) is one more
+ *       verified row, so a tree has T = 1 + min(N, sum_d K^d) rows.
+ *   R2  The best-first key is the fp32 sum of edge scores along the root path.
+ *   R3  Ties: score desc, depth asc, parent index asc, rank asc.  Argmax takes
+ *       the lowest index; a repeated child token takes the lowest node index.
+ *   R7  q has no 1/sqrt(d_k) scale; alpha arrives directly; qk-head of v-head
+ *       j is j / (Hv / Hk).
+ *   R8  Attention scale 1/sqrt(D); q-head h reads kv-head h / (Hq / Hkv).
+ *   R9  Commit: the state after the last accepted node becomes the committed
+ *       state; the tree K/V rows of the accepted path are appended.
+ *
+ * Layouts (all row-major, outermost first):
+ *   lattice     tok int32 [B][m][K], score f32 [B][m][K]
+ *   tree        node_* [B][T], anc uint64 [B][T][2] (bit a of node n set iff
+ *               node a is n or an ancestor of n), n_nodes [B]
+ *   gdn         h0 double [B][Hv][dk][dv]; q,k [B][T][Hk][dk]; v [B][T][Hv][dv];
+ *               alpha, beta f32 [B][T][Hv]; o double [B][T][Hv][dv]
+ *   attention   q [B][T][Hq][D]; k_tree, v_tree [B][T][Hkv][D];
+ *               k_cache, v_cache [B][Lmax][Hkv][D]; kv_len int32 [B];
+ *               o double [B][T][Hq][D]
+ *   logits      [rows][V]
+ * Element type of q/k/v/logits/caches: io_bf16 = 1 -> raw bf16 bits (uint16),
+ * io_bf16 = 0 -> float.
+ *
+ * Return value of every entry point: 0 on success, a negative number when the
+ * input breaks a precondition (documented per function).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_ANC_WORDS 2   /* trees hold at most 128 rows */
+#define ORC_MAX_ROWS 128
+
+/* ---- element access ---------------------------------------------------- */
+
+/* Exact widening of one stored element to double. */
+static double orc_elem(const void *base, size_t idx, int io_bf16)
+{
+    if (io_bf16) {
+        uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
+        float f;
+        memcpy(&f, &bits, sizeof f);
+        return (double)f;
+    }
+    return (double)((const float *)base)[idx];
+}
+
+/* ---- C1/C2: lattice canonicalisation and best-first tree [LAT][TREE][NOV] */
+
+/* One frontier entry: the child with lattice rank `rank` of inserted node
+ * `parent`. */
+typedef struct {
+    int parent;
+    int rank;
+    int depth;
+    float score;
+} orc_cand;
+
+/* Strict total order of R3: a precedes b. */
+static int orc_cand_before(const orc_cand *a, const orc_cand *b)
+{
+    if (a->score != b->score) return a->score > b->score;
+    if (a->depth != b->depth) return a->depth < b->depth;
+    if (a->parent != b->parent) return a->parent < b->parent;
+    return a->rank < b->rank;
+}
+
+/*
+ * orc_tree_build: best-first draft tree over a lattice [TREE][NOV].
+ *
+ * Per request: candidates of each position are stable-sorted by score
+ * (descending, input index ascending); a candidate's rank is its sorted
+ * position.  Node 0 is the root (token root_tok, depth 0, score 0, parent -1).
+ * The frontier holds every child of every inserted node of depth < m; the
+ * child of rank r of node p has depth d_p + 1, token and score taken from the
+ * rank-r candidate of lattice position d_p (0-based, i.e. depth d_p + 1), and
+ * key fl32(score_p + edge score).  Until N drafts are inserted or the frontier
+ * is empty, the frontier entry first in the R3 order becomes the next node.
+ *
+ * Rows n >= n_nodes[b] are padding: tok/parent/depth/rank = -1, score 0,
+ * anc 0.  Requires 1 <= m, 1 <= K, 0 <= N, N + 1 <= 128 (returns -1
+ * otherwise) and distinct tokens within a position (returns -2 otherwise).
+ */
+int orc_tree_build(int B, int m, int K, int N,
+                   const int32_t *lat_tok, const float *lat_score,
+                   const int32_t *root_tok,
+                   int32_t *node_tok, int32_t *node_parent, int32_t *node_depth,
+                   int32_t *node_rank, float *node_score, uint64_t *node_anc,
+                   int32_t *n_nodes)
+{
+    if (B < 0 || m < 1 || K < 1 || N < 0 || N + 1 > ORC_MAX_ROWS) return -1;
+    const int T = N + 1;
+    int *order = (int *)malloc(sizeof(int) * (size_t)m * (size_t)K);
+    orc_cand *front = (orc_cand *)malloc(sizeof(orc_cand) * (size_t)(T * K + K));
+    if (!order || !front) { free(order); free(front); return -3; }
+    int rc = 0;
+
+    for (int b = 0; b < B && rc == 0; ++b) {
+        const int32_t *tok = lat_tok + (size_t)b * m * K;
+        const float *sc = lat_score + (size_t)b * m * K;
+
+        /* canonical order per position: insertion sort is stable */
+        for (int s = 0; s < m; ++s) {
+            int *o = order + (size_t)s * K;
+            for (int i = 0; i < K; ++i) {
+                int j = i;
+                while (j > 0 && sc[s * K + i] > sc[s * K + o[j - 1]]) {
+                    o[j] = o[j - 1];
+                    --j;
+                }
+                o[j] = i;
+            }
+            for (int i = 0; i < K; ++i)
+                for (int j = i + 1; j < K; ++j)
+                    if (tok[s * K + i] == tok[s * K + j]) rc = -2;
+        }
+        if (rc) break;
+
+        int32_t *ntok = node_tok + (size_t)b * T, *npar = node_parent + (size_t)b * T;
+        int32_t *ndep = node_depth + (size_t)b * T, *nrank = node_rank + (size_t)b * T;
+        float *nsc = node_score + (size_t)b * T;
+        uint64_t *nanc = node_anc + (size_t)b * T * ORC_ANC_WORDS;
+        for (int n = 0; n < T; ++n) {
+            ntok[n] = -1; npar[n] = -1; ndep[n] = -1; nrank[n] = -1; nsc[n] = 0.0f;
+            for (int w = 0; w < ORC_ANC_WORDS; ++w) nanc[n * ORC_ANC_WORDS + w] = 0;
+        }
+
+        ntok[0] = root_tok[b]; npar[0] = -1; ndep[0] = 0; nrank[0] = -1; nsc[0] = 0.0f;
+        nanc[0] = 1ull;
+        int count = 1, nfront = 0;
+        for (int r = 0; r < K; ++r) {            /* children of the root */
+            orc_cand c = { 0, r, 1, nsc[0] + sc[0 * K + order[r]] };
+            front[nfront++] = c;
+        }
+        while (count < T && nfront > 0) {
+            int best = 0;
+            for (int i = 1; i < nfront; ++i)
+                if (orc_cand_before(&front[i], &front[best])) best = i;
+            orc_cand c = front[best];
+            front[best] = front[--nfront];
+
+            const int n = count++;
+            const int s = c.depth - 1;           /* lattice position of depth d */
+            ntok[n] = tok[s * K + order[s * K + c.rank]];
+            npar[n] = c.parent;
+            ndep[n] = c.depth;
+            nrank[n] = c.rank;
+            nsc[n] = c.score;
+            for (int w = 0; w < ORC_ANC_WORDS; ++w)
+                nanc[n * ORC_ANC_WORDS + w] = nanc[c.parent * ORC_ANC_WORDS + w];
+            nanc[n * ORC_ANC_WORDS + n / 64] |= 1ull << (n % 64);
+
+            if (c.depth < m) {
+                for (int r = 0; r < K; ++r) {
+                    float e = sc[c.depth * K + order[c.depth * K + r]];
+                    orc_cand ch = { n, r, c.depth + 1, nsc[n] + e };
+                    front[nfront++] = ch;
+                }
+            }
+        }
+        n_nodes[b] = count;
+    }
+    free(order);
+    free(front);
+    return rc;
+}
+
+/* Root path of node n (root first); returns its length (depth + 1). */
+static int orc_root_path(const int32_t *parent, int n, int *path)
+{
+    int len = 0, x = n;
+    while (x >= 0) { path[len++] = x; x = parent[x]; }
+    for (int i = 0; i < len / 2; ++i) {
+        int t = path[i]; path[i] = path[len - 1 - i]; path[len - 1 - i] = t;
+    }
+    return len;
+}
+
+/* ---- C3: Gated DeltaNet along root paths [GDN][NOV] --------------------- */
+
+/*
+ * One gated-delta step on a dk x dv state held in double:
+ *   u = h^T k;  h <- alpha (h - beta k u^T) + beta k v^T,
+ * which is h <- alpha (I - beta k k^T) h + beta k v^T written out.
+ */
+static void orc_gdn_step(double *h, int dk, int dv, const double *k,
+                         const double *v, double alpha, double beta, double *u)
+{
+    for (int c = 0; c < dv; ++c) {
+        double acc = 0.0;
+        for (int r = 0; r < dk; ++r) acc += h[(size_t)r * dv + c] * k[r];
+        u[c] = acc;
+    }
+    for (int r = 0; r < dk; ++r)
+        for (int c = 0; c < dv; ++c) {
+            double x = h[(size_t)r * dv + c];
+            h[(size_t)r * dv + c] = alpha * (x - beta * k[r] * u[c]) + beta * k[r] * v[c];
+        }
+}
+
+/*
+ * orc_gdn_tree: output of every tree node of one GDN layer.
+ *
+ * For node n, v-head j (qk-head i = j / (Hv/Hk)) and root path
+ * 0 = p_0, ..., p_l = n: start from h = h0[b][j], apply the gated-delta step
+ * of every node on the path in root-to-leaf order (the root's own row
+ * included), then o[b][n][j] = h^T q_n.  This is the sequential linear-chain
+ * decode of the node's root path; nothing is shared between nodes.
+ * Padding rows (n >= n_nodes[b]) get o = 0.  Requires Hv % Hk == 0.
+ */
+int orc_gdn_tree(int B, int T, int Hk, int Hv, int dk, int dv,
+                 const int32_t *node_parent, const int32_t *n_nodes,
+                 const double *h0, const void *q, const void *k, const void *v,
+                 int io_bf16, const float *alpha, const float *beta, double *o)
+{
+    if (Hk <= 0 || Hv % Hk != 0 || T > ORC_MAX_ROWS) return -1;
+    const int grp = Hv / Hk;
+    double *h = (double *)malloc(sizeof(double) * (size_t)dk * dv);
+    double *kk = (double *)malloc(sizeof(double) * (size_t)dk);
+    double *qq = (double *)malloc(sizeof(double) * (size_t)dk);
+    double *vv = (double *)malloc(sizeof(double) * (size_t)dv);
+    double *u = (double *)malloc(sizeof(double) * (size_t)dv);
+    int path[ORC_MAX_ROWS];
+    if (!h || !kk || !qq || !vv || !u) { free(h); free(kk); free(qq); free(vv); free(u); return -3; }
+
+    for (int b = 0; b < B; ++b) {
+        const int32_t *par = node_parent + (size_t)b * T;
+        for (int n = 0; n < T; ++n) {
+            for (int j = 0; j < Hv; ++j) {
+                double *out = o + (((size_t)b * T + n) * Hv + j) * dv;
+                if (n >= n_nodes[b]) { for (int c = 0; c < dv; ++c) out[c] = 0.0; continue; }
+                const int i = j / grp;
+                memcpy(h, h0 + ((size_t)b * Hv + j) * dk * dv, sizeof(double) * (size_t)dk * dv);
+                const int len = orc_root_path(par, n, path);
+                for (int s = 0; s < len; ++s) {
+                    const int t = path[s];
+                    for (int r = 0; r < dk; ++r)
+                        kk[r] = orc_elem(k, (((size_t)b * T + t) * Hk + i) * dk + r, io_bf16);
+                    for (int c = 0; c < dv; ++c)
+                        vv[c] = orc_elem(v, (((size_t)b * T + t) * Hv + j) * dv + c, io_bf16);
+                    const double a = alpha[((size_t)b * T + t) * Hv + j];
+                    const double be = beta[((size_t)b * T + t) * Hv + j];
+                    orc_gdn_step(h, dk, dv, kk, vv, a, be, u);
+                }
+                for (int r = 0; r < dk; ++r)
+                    qq[r] = orc_elem(q, (((size_t)b * T + n) * Hk + i) * dk + r, io_bf16);
+                for (int c = 0; c < dv; ++c) {
+                    double acc = 0.0;
+                    for (int r = 0; r < dk; ++r) acc += h[(size_t)r * dv + c] * qq[r];
+                    out[c] = acc;
+                }
+            }
+        }
+    }
+    free(h); free(kk); free(qq); free(vv); free(u);
+    return 0;
+}
+
+/* ---- C4: tree-ancestor-masked attention [TREE] --------------------------- */
+
+/*
+ * orc_attn_tree: for node n and q-head h (kv-head g = h / (Hq/Hkv)) the
+ * visible keys are the cache rows [0, kv_len[b]) and the tree rows a with bit
+ * a set in anc[b][n] (the node and its ancestors).  Scores are
+ * <q, k_x> / sqrt(D); o = sum_x softmax(s)_x v_x.  Padding rows get o = 0.
+ * Requires Hq % Hkv == 0 and 0 <= kv_len[b] <= Lmax.
+ */
+int orc_attn_tree(int B, int T, int Hq, int Hkv, int D, int Lmax,
+                  const int32_t *n_nodes, const uint64_t *node_anc,
+                  const void *q, const void *k_tree, const void *v_tree,
+                  const void *k_cache, const void *v_cache, const int32_t *kv_len,
+                  int io_bf16, double *o)
+{
+    if (Hkv <= 0 || Hq % Hkv != 0 || T > ORC_MAX_ROWS) return -1;
+    for (int b = 0; b < B; ++b)
+        if (kv_len[b] < 0 || kv_len[b] > Lmax) return -1;
+    const int grp = Hq / Hkv;
+    const double scale = 1.0 / sqrt((double)D);
+    double *qq = (double *)malloc(sizeof(double) * (size_t)D);
+    double *s = (double *)malloc(sizeof(double) * (size_t)(Lmax + T));
+    if (!qq || !s) { free(qq); free(s); return -3; }
+
+    for (int b = 0; b < B; ++b) {
+        const int L = kv_len[b];
+        for (int n = 0; n < T; ++n) {
+            const uint64_t *anc = node_anc + ((size_t)b * T + n) * ORC_ANC_WORDS;
+            for (int hq = 0; hq < Hq; ++hq) {
+                double *out = o + (((size_t)b * T + n) * Hq + hq) * D;
+                for (int d = 0; d < D; ++d) out[d] = 0.0;
+                if (n >= n_nodes[b]) continue;
+                const int g = hq / grp;
+                for (int d = 0; d < D; ++d)
+                    qq[d] = orc_elem(q, (((size_t)b * T + n) * Hq + hq) * D + d, io_bf16);
+
+                /* scores over the visible set: cache rows, then tree rows */
+                int nv = 0;
+                double mx = -INFINITY;
+                for (int x = 0; x < L; ++x) {
+                    double acc = 0.0;
+                    for (int d = 0; d < D; ++d)
+                        acc += qq[d] * orc_elem(k_cache, (((size_t)b * Lmax + x) * Hkv + g) * D + d, io_bf16);
+                    s[nv] = acc * scale;
+                    if (s[nv] > mx) mx = s[nv];
+                    ++nv;
+                }
+                for (int a = 0; a < n_nodes[b]; ++a) {
+                    if (!((anc[a / 64] >> (a % 64)) & 1ull)) continue;
+                    double acc = 0.0;
+                    for (int d = 0; d < D; ++d)
+                        acc += qq[d] * orc_elem(k_tree, (((size_t)b * T + a) * Hkv + g) * D + d, io_bf16);
+                    s[nv] = acc * scale;
+                    if (s[nv] > mx) mx = s[nv];
+                    ++nv;
+                }
+
+                double den = 0.0;
+                for (int x = 0; x < nv; ++x) { s[x] = exp(s[x] - mx); den += s[x]; }
+                nv = 0;
+                for (int x = 0; x < L; ++x, ++nv)
+                    for (int d = 0; d < D; ++d)
+                        out[d] += s[nv] * orc_elem(v_cache, (((size_t)b * Lmax + x) * Hkv + g) * D + d, io_bf16);
+                for (int a = 0; a < n_nodes[b]; ++a) {
+                    if (!((anc[a / 64] >> (a % 64)) & 1ull)) continue;
+                    for (int d = 0; d < D; ++d)
+                        out[d] += s[nv] * orc_elem(v_tree, (((size_t)b * T + a) * Hkv + g) * D + d, io_bf16);
+                    ++nv;
+                }
+                for (int d = 0; d < D; ++d) out[d] /= den;
+            }
+        }
+    }
+    free(qq);
+    free(s);
+    return 0;
+}
+
+/* ---- C5: vocabulary argmax [SD] ----------------------------------------- */
+
+/*
+ * orc_argmax: first index of the maximum of each row, values compared as
+ * floats after widening.  margin[row] = max - (largest value at any other
+ * index); it is +inf for V == 1.
+ */
+int orc_argmax(int rows, int V, const void *logits, int io_bf16,
+               int32_t *idx, float *margin)
+{
+    if (V < 1) return -1;
+    for (int r = 0; r < rows; ++r) {
+        int best = 0;
+        float bv = (float)orc_elem(logits, (size_t)r * V, io_bf16);
+        for (int x = 1; x < V; ++x) {
+            float f = (float)orc_elem(logits, (size_t)r * V + x, io_bf16);
+            if (f > bv) { bv = f; best = x; }
+        }
+        double second = -INFINITY;
+        for (int x = 0; x < V; ++x) {
+            if (x == best) continue;
+            double f = orc_elem(logits, (size_t)r * V + x, io_bf16);
+            if (f > second) second = f;
+        }
+        idx[r] = best;
+        if (margin) margin[r] = (float)((double)bv - second);
+    }
+    return 0;
+}
+
+/* ---- C6: greedy acceptance of the longest matching root path [SD][TREE] -- */
+
+/*
+ * orc_accept: starting at the root, repeatedly look up the target argmax t of
+ * the current row and move to the child of the current node whose token is t
+ * (lowest node index when tokens repeat); stop when there is none.
+ * tau = number of nodes on the accepted path (root included) in [1, m+1];
+ * accept_nodes[b][0..tau) = the path; out_tok[b][0..tau) = tokens of the
+ * accepted drafts followed by the bonus token (the argmax of the last accepted
+ * row); slots >= tau hold -1.  new_root[b] = the bonus token.
+ * argmax is [B][T].
+ */
+int orc_accept(int B, int T, int m,
+               const int32_t *node_tok, const int32_t *node_parent,
+               const int32_t *n_nodes, const int32_t *argmax,
+               int32_t *accept_len, int32_t *accept_nodes, int32_t *out_tok,
+               int32_t *new_root)
+{
+    for (int b = 0; b < B; ++b) {
+        const int32_t *tok = node_tok + (size_t)b * T, *par = node_parent + (size_t)b * T;
+        const int32_t *am = argmax + (size_t)b * T;
+        int32_t *path = accept_nodes + (size_t)b * (m + 1), *ot = out_tok + (size_t)b * (m + 1);
+        for (int i = 0; i <= m; ++i) { path[i] = -1; ot[i] = -1; }
+        int cur = 0, len = 0;
+        path[len++] = 0;
+        for (;;) {
+            const int t = am[cur];
+            int next = -1;
+            for (int c = 0; c < n_nodes[b]; ++c)
+                if (par[c] == cur && tok[c] == t) { next = c; break; }
+            if (next < 0 || len > m) break;
+            ot[len - 1] = tok[next];
+            path[len++] = next;
+            cur = next;
+        }
+        ot[len - 1] = am[cur];
+        accept_len[b] = len;
+        new_root[b] = am[cur];
+    }
+    return 0;
+}
+
+/* ---- C7: commit of the accepted path [GDN][NOV] -------------------------- */
+
+/*
+ * orc_commit_gdn: h[b][j] <- the state after applying the gated-delta steps
+ * of accept_nodes[b][0..tau) in order (root first) to h[b][j], for one GDN
+ * layer.  Inputs as in orc_gdn_tree; h is updated in place (double).
+ */
+int orc_commit_gdn(int B, int T, int m, int Hk, int Hv, int dk, int dv,
+                   const int32_t *accept_len, const int32_t *accept_nodes,
+                   double *h, const void *k, const void *v, int io_bf16,
+                   const float *alpha, const float *beta)
+{
+    if (Hk <= 0 || Hv % Hk != 0) return -1;
+    const int grp = Hv / Hk;
+    double *kk = (double *)malloc(sizeof(double) * (size_t)dk);
+    double *vv = (double *)malloc(sizeof(double) * (size_t)dv);
+    double *u = (double *)malloc(sizeof(double) * (size_t)dv);
+    if (!kk || !vv || !u) { free(kk); free(vv); free(u); return -3; }
+    for (int b = 0; b < B; ++b) {
+        for (int j = 0; j < Hv; ++j) {
+            const int i = j / grp;
+            double *hj = h + ((size_t)b * Hv + j) * dk * dv;
+            for (int s = 0; s < accept_len[b]; ++s) {
+                const int t = accept_nodes[(size_t)b * (m + 1) + s];
+                for (int r = 0; r < dk; ++r)
+                    kk[r] = orc_elem(k, (((size_t)b * T + t) * Hk + i) * dk + r, io_bf16);
+                for (int c = 0; c < dv; ++c)
+                    vv[c] = orc_elem(v, (((size_t)b * T + t) * Hv + j) * dv + c, io_bf16);
+                orc_gdn_step(hj, dk, dv, kk, vv, alpha[((size_t)b * T + t) * Hv + j],
+                             beta[((size_t)b * T + t) * Hv + j], u);
+            }
+        }
+    }
+    free(kk); free(vv); free(u);
+    return 0;
+}
+
+/*
+ * orc_commit_kv: for one attention layer, copy the tree K/V rows of the
+ * accepted path to cache rows [kv_len[b], kv_len[b] + tau) (raw element
+ * copies, bit-exact).  kv_len is NOT advanced here: the caller advances it
+ * once after every layer is committed.  Returns -4 (and copies nothing for
+ * any request) if some kv_len[b] + tau > Lmax.
+ */
+int orc_commit_kv(int B, int T, int m, int Hkv, int D, int Lmax,
+                  const int32_t *accept_len, const int32_t *accept_nodes,
+                  const void *k_tree, const void *v_tree, void *k_cache, void *v_cache,
+                  const int32_t *kv_len, int io_bf16)
+{
+    const size_t esz = io_bf16 ? 2 : 4;
+    const size_t row = (size_t)Hkv * D * esz;
+    for (int b = 0; b < B; ++b)
+        if (kv_len[b] + accept_len[b] > Lmax) return -4;
+    for (int b = 0; b < B; ++b) {
+        for (int s = 0; s < accept_len[b]; ++s) {
+            const int t = accept_nodes[(size_t)b * (m + 1) + s];
+            const size_t dst = ((size_t)b * Lmax + kv_len[b] + s) * row;
+            const size_t src = ((size_t)b * T + t) * row;
+            memcpy((char *)k_cache + dst, (const char *)k_tree + src, row);
+            memcpy((char *)v_cache + dst, (const char *)v_tree + src, row);
+        }
+    }
+    return 0;
+}
