@@ -1,0 +1,544 @@
+#!/usr/bin/env python3
+"""Benchmark of the tree-verification step on one GB300.
+
+A step = best-first tree build + every GDN layer's tree verify + every
+attention layer's tree verify + argmax/acceptance/commit, all through the
+C ABI on one stream, replayed as one CUDA graph.  The default workload is the
+single-request configuration: 8x16 lattice, N = 24 drafts, one GDN layer
+(16 q-k / 32 v heads of 128x128 fp32 state), one attention layer (32 q / 8 kv
+heads of 128, KV length 4096), vocabulary 151936, bf16 I/O; synthetic seeded
+inputs.  L2 is flushed (a 2 x L2 write) before every timed step.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from speculative_decoding_tree_best_gb300 import synth  # noqa: E402
+
+METRIC = "tree_nodes_per_s (verify step: tree build + GDN + attention + accept/commit)"
+UNIT = "nodes/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------- bytes model
+
+def algorithmic_bytes(s: synth.SpecConfig, mean_L: float, tau: float) -> dict:
+    """Bytes each phase must move at least once (fp32 state, io-typed rows)."""
+    e = 2 if s.io == "bf16" else 4
+    T = s.T
+    gdn_state = s.Hv * s.dk * s.dv * 4
+    gdn_rows = T * (2 * s.Hk * s.dk * e + s.Hv * s.dv * e + 2 * s.Hv * 4 + s.Hv * s.dv * e)
+    attn_kv = mean_L * s.Hkv * s.D * e * 2
+    attn_rows = T * (s.Hq * s.D * e * 2 + s.Hkv * s.D * e * 2)
+    per_req = dict(
+        tree=s.m * s.K * 8 + T * 36,
+        gdn=s.n_gdn * (gdn_state + gdn_rows),
+        attn=s.n_attn * (attn_kv + attn_rows),
+        logits=T * s.V * e,
+        commit=s.n_gdn * gdn_state + s.n_attn * tau * s.Hkv * s.D * e * 2,
+    )
+    out = {k: v * s.B for k, v in per_req.items()}
+    out["step"] = sum(out.values())
+    out["gdn_kernel"] = s.B * (gdn_state + gdn_rows)          # one layer, one launch
+    out["attn_kernel"] = s.B * (attn_kv + attn_rows)          # one layer
+    return out
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------- clocks (read only)
+
+class ClockSampler:
+    """Samples SM clock, power and clock-event reasons through NVML (read-only
+    queries) in a background thread; falls back to nvidia-smi."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, dev_index: int):
+        self.samples = []
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._nvml = None
+        self._proc = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError
+            h = ctypes.c_void_p()
+            uuid = None
+            try:
+                uuid = "GPU-" + str(torch.cuda.get_device_properties(dev_index).uuid)
+            except Exception:
+                pass
+            ok = uuid and nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0
+            if not ok and nv.nvmlDeviceGetHandleByIndex_v2(dev_index, ctypes.byref(h)) != 0:
+                raise OSError
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._nvml, self._h = nv, h
+            fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None)
+            self._reasons_fn = fn or nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        except OSError:
+            self._nvml = None
+
+    def _loop(self):
+        nv, h = self._nvml, self._h
+        mhz, r, mw = ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0:
+                self._reasons_fn(h, ctypes.byref(r))
+                nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw))
+                self.samples.append((mhz.value, int(r.value), mw.value / 1000.0))
+            time.sleep(0.002)
+
+    def start(self):
+        if self._nvml is not None:
+            self._t = threading.Thread(target=self._loop, daemon=True)
+            self._t.start()
+        else:
+            q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active")
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(dev_index_env())], stdout=subprocess.PIPE, text=True)
+
+    def stop(self) -> dict:
+        if self._nvml is not None:
+            self._stop.set()
+            self._t.join()
+        elif self._proc is not None:
+            self._proc.terminate()
+            out, _ = self._proc.communicate()
+            for line in out.strip().splitlines():
+                try:
+                    sm, mx, pw, rs = [x.strip() for x in line.split(",")]
+                    self.samples.append((int(sm), int(rs, 16), float(pw)))
+                    self.max_mhz = int(mx)
+                except ValueError:
+                    pass
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        reasons = 0
+        for _, r, _ in self.samples:
+            reasons |= r
+        return {"sm_mhz": statistics.median(s[0] for s in self.samples),
+                "sm_max_mhz": self.max_mhz,
+                "reasons": [n for b, n in self.REASONS.items() if reasons & b],
+                "power_w_max": max(s[2] for s in self.samples),
+                "samples": len(self.samples)}
+
+
+def dev_index_env() -> int:
+    v = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    try:
+        return int(v.split(",")[int(os.environ.get("LOCAL_RANK", "0"))])
+    except (ValueError, IndexError):
+        return int(os.environ.get("LOCAL_RANK", "0"))
+
+
+# ----------------------------------------------------------------- distributed (timing only)
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- CPU oracle timing
+
+def oracle_step(scfg, inp):
+    """One whole verify step of the CPU oracle."""
+    import oracle
+    tree = oracle.tree_build(inp["lat_tok"], inp["lat_score"], inp["root_tok"], scfg.N)
+    for lay in inp["gdn"]:
+        oracle.gdn_tree(tree, lay["h0"], lay["q"], lay["k"], lay["v"], lay["alpha"], lay["beta"])
+    for lay in inp["attn"]:
+        oracle.attn_tree(tree, lay["q"], lay["k_tree"], lay["v_tree"], lay["k_cache"],
+                         lay["v_cache"], inp["kv_len"])
+    am, _ = oracle.argmax(inp["logits"])
+    acc = oracle.accept(tree, am, scfg.m)
+    for lay in inp["gdn"]:
+        oracle.commit_gdn(acc, lay["h0"], lay["k"], lay["v"], lay["alpha"], lay["beta"])
+    for lay in inp["attn"]:
+        oracle.commit_kv(acc, lay["k_tree"], lay["v_tree"], lay["k_cache"], lay["v_cache"],
+                         inp["kv_len"])
+    return tree, acc
+
+
+def planted_inputs_cpu(scfg, seed):
+    import oracle
+    inp = synth.make_step_inputs(scfg, seed)
+    tree = oracle.tree_build(inp["lat_tok"], inp["lat_score"], inp["root_tok"], scfg.N)
+    synth.plant_logits(inp["logits"], inp["lat_tok"], inp["lat_score"], tree["node_depth"],
+                       tree["n_nodes"], scfg.p_plant, inp["plant_gen"])
+    return inp
+
+
+def cpu_baseline(scfg, seed, budget_s=12.0, max_steps=4):
+    """Full oracle verify steps, single-threaded, until ~budget_s of CPU work."""
+    inp = planted_inputs_cpu(scfg, seed)
+    times = []
+    t_all = time.perf_counter()
+    while len(times) < max_steps and (time.perf_counter() - t_all) < budget_s:
+        t0 = time.perf_counter()
+        oracle_step(scfg, inp)
+        times.append(time.perf_counter() - t0)
+    per_step = statistics.median(times)
+    return {"value": scfg.B * scfg.N / per_step, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{len(times)} full verify steps of the C oracle (single thread, float64) "
+                      f"on the '{scfg.name}' workload, median {per_step:.3f} s/step"}
+
+
+# ----------------------------------------------------------------- reference arm
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    scfg = synth.config(args.config)
+    inp = planted_inputs_cpu(scfg, args.seed)
+    G = scfg.Hq // scfg.Hkv
+    grp = scfg.Hv // scfg.Hk
+    # A bounded sample per step: the tree, one GDN v-head, one attention kv-head
+    # group, the full argmax/accept/commit; the sampled head work is scaled by
+    # the head count to a whole-step estimate.
+    def one(step):
+        j = step % scfg.Hv
+        g = step % scfg.Hkv
+        t0 = time.perf_counter()
+        oracle_step_sampled(scfg, inp, j, g)
+        t_sampled = time.perf_counter() - t0
+        return t_sampled
+    for w in range(args.warmup):
+        one(w)
+    per = []
+    for s in range(args.steps):
+        per.append(one(s))
+    # scale: head-parallel parts were done for 1/Hv (GDN) and 1/Hkv (attention)
+    est = statistics.median(per)
+    full = est_full_step(scfg, inp)
+    value = scfg.B * scfg.N / full
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": full * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{scfg.name}: B={scfg.B} m={scfg.m} K={scfg.K} N={scfg.N} "
+                                   f"KV={scfg.L} V={scfg.V}", "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{args.steps} sampled steps (tree, one GDN v-head, one "
+                                       f"attention kv-head group, argmax/accept/commit), median "
+                                       f"{est * 1e3:.1f} ms; whole step {full:.3f} s"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def oracle_step_sampled(scfg, inp, j, g):
+    import oracle
+    tree = oracle.tree_build(inp["lat_tok"], inp["lat_score"], inp["root_tok"], scfg.N)
+    grp, G = scfg.Hv // scfg.Hk, scfg.Hq // scfg.Hkv
+    i = j // grp
+    for lay in inp["gdn"]:
+        oracle.gdn_tree(tree, lay["h0"][:, j:j + 1].contiguous(), lay["q"][:, :, i:i + 1].contiguous(),
+                        lay["k"][:, :, i:i + 1].contiguous(), lay["v"][:, :, j:j + 1].contiguous(),
+                        lay["alpha"][:, :, j:j + 1].contiguous(), lay["beta"][:, :, j:j + 1].contiguous())
+    for lay in inp["attn"]:
+        oracle.attn_tree(tree, lay["q"][:, :, g * G:(g + 1) * G].contiguous(),
+                         lay["k_tree"][:, :, g:g + 1].contiguous(), lay["v_tree"][:, :, g:g + 1].contiguous(),
+                         lay["k_cache"][:, :, g:g + 1].contiguous(),
+                         lay["v_cache"][:, :, g:g + 1].contiguous(), inp["kv_len"])
+    am, _ = oracle.argmax(inp["logits"])
+    acc = oracle.accept(tree, am, scfg.m)
+    for lay in inp["gdn"]:
+        oracle.commit_gdn(acc, lay["h0"][:, j:j + 1].contiguous(), lay["k"][:, :, i:i + 1].contiguous(),
+                          lay["v"][:, :, j:j + 1].contiguous(), lay["alpha"][:, :, j:j + 1].contiguous(),
+                          lay["beta"][:, :, j:j + 1].contiguous())
+
+
+_FULL_CACHE = {}
+
+
+def est_full_step(scfg, inp):
+    """Whole-step oracle time from per-part timings of head slices (measured once)."""
+    key = scfg
+    if key in _FULL_CACHE:
+        return _FULL_CACHE[key]
+    import oracle
+    t0 = time.perf_counter()
+    tree = oracle.tree_build(inp["lat_tok"], inp["lat_score"], inp["root_tok"], scfg.N)
+    am, _ = oracle.argmax(inp["logits"])
+    acc = oracle.accept(tree, am, scfg.m)
+    t_fixed = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle_step_sampled(scfg, inp, 0, 0)
+    t_one = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    G = scfg.Hq // scfg.Hkv
+    for lay in inp["attn"]:
+        oracle.attn_tree(tree, lay["q"][:, :, 0:G].contiguous(), lay["k_tree"][:, :, 0:1].contiguous(),
+                         lay["v_tree"][:, :, 0:1].contiguous(), lay["k_cache"][:, :, 0:1].contiguous(),
+                         lay["v_cache"][:, :, 0:1].contiguous(), inp["kv_len"])
+    t_attn1 = time.perf_counter() - t0
+    t_gdn1 = max(t_one - t_fixed - t_attn1, 0.0)
+    full = t_fixed + scfg.Hv * t_gdn1 + scfg.Hkv * t_attn1
+    _FULL_CACHE[key] = full
+    return full
+
+
+# ----------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local):
+    from speculative_decoding_tree_best_gb300 import binding, build
+    from speculative_decoding_tree_best_gb300.step import VerifyStep, stack_inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    build.build()
+    binding.load()
+    scfg = synth.config(args.config)
+    inp = synth.make_step_inputs(scfg, args.seed + rank)
+    x = stack_inputs(inp, dev)
+    st = VerifyStep(scfg, x, dev)
+    stream = torch.cuda.current_stream()
+
+    # plant the target argmax along the tree the library builds (input synthesis)
+    st.build_tree()
+    torch.cuda.synchronize()
+    t_np = st.tree.to_numpy()
+    logits = inp["logits"].clone()
+    synth.plant_logits(logits, inp["lat_tok"], inp["lat_score"], t_np["node_depth"],
+                       t_np["n_nodes"], scfg.p_plant, inp["plant_gen"])
+    x["logits"].copy_(logits.to(dev))
+    kv0, root0 = x["kv_len"].clone(), x["root_tok"].clone()
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+
+    def reset():
+        x["kv_len"].copy_(kv0)
+        x["root_tok"].copy_(root0)
+
+    # eager warm-up (sets kernel attributes), then capture the step as one graph
+    for _ in range(3):
+        reset()
+        st.run()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+        st.run()
+    torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        reset()
+        graph.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K graph replays, L2 flushed before each -----------------------
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall = time.perf_counter()
+    taus = []
+    for i in range(args.steps):
+        flush.zero_()
+        reset()
+        ev[i][0].record(stream)
+        graph.replay()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    barrier(world)
+    per_ms = [a.elapsed_time(b) for a, b in ev]
+    ms_step = sum(per_ms) / len(per_ms)
+    ms_step_max = max_over_ranks(ms_step, world)
+    taus = st.acc.accept_len.float().mean().item()
+    mean_L = float(kv0.float().mean().item())
+
+    # ---- phase breakdown (eager, CUDA events on the launching stream) -------------------
+    R = max(10, min(args.steps, 50))
+    phase = {k: [] for k in ("tree", "gdn", "attn", "accept_commit")}
+    for _ in range(R):
+        flush.zero_()
+        reset()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        e[0].record(stream)
+        st.build_tree()
+        e[1].record(stream)
+        c = st.cfg
+        for l in range(c.n_gdn_layers):
+            binding.gdn_tree_verify(c, st.tree, x["gdn_h0"][l], x["gdn_q"][l], x["gdn_k"][l],
+                                    x["gdn_v"][l], x["gdn_alpha"][l], x["gdn_beta"][l],
+                                    st.gdn_o[l], None, st.ws)
+        e[2].record(stream)
+        for l in range(c.n_attn_layers):
+            binding.attn_tree_verify(c, st.tree, x["attn_q"][l], x["k_tree"][l], x["v_tree"][l],
+                                     x["k_cache"][l], x["v_cache"][l], x["kv_len"], st.attn_o[l],
+                                     st.ws)
+        e[3].record(stream)
+        st.accept_commit()
+        e[4].record(stream)
+        torch.cuda.synchronize()
+        for k, (a, b) in zip(phase, zip(e[:-1], e[1:])):
+            phase[k].append(a.elapsed_time(b))
+    ph_us = {k: 1e3 * statistics.median(v) for k, v in phase.items()}
+
+    # ---- end to end through the public API with host buffers ----------------------
+    host_in = {k: x[k].cpu().pin_memory() for k in
+               ("lat_tok", "lat_score", "gdn_q", "gdn_k", "gdn_v", "gdn_alpha", "gdn_beta",
+                "attn_q", "k_tree", "v_tree", "logits")}
+    host_out = {k: torch.empty_like(getattr(st.acc, k), device="cpu").pin_memory()
+                for k in ("accept_len", "out_tok")}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        reset()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k, t in host_in.items():
+            x[k].copy_(t, non_blocking=True)
+        st.run()
+        for k, t in host_out.items():
+            t.copy_(getattr(st.acc, k), non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_ms_step = max_over_ranks(sum(e2e_ms) / len(e2e_ms), world)
+
+    nodes_total = sum_over_ranks(scfg.B * scfg.N, world)
+    value = nodes_total / (ms_step_max * 1e-3)
+    byts = algorithmic_bytes(scfg, mean_L, taus)
+    peak, peak_kind = hbm_peak()
+    attn_us = ph_us["attn"] / max(scfg.n_attn, 1)
+    gdn_us = ph_us["gdn"] / max(scfg.n_gdn, 1)
+    ach_attn = byts["attn_kernel"] / (attn_us * 1e-6) / 1e9
+    ach_gdn = byts["gdn_kernel"] / (gdn_us * 1e-6) / 1e9
+    step_gbs = byts["step"] / (ms_step * 1e-3) / 1e9
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if scfg.io == "bf16" else "f32",
+        "data": "synthetic (seeded; shapes and value distributions of the paper's workloads)",
+        "config": {"workload": f"{scfg.name}: B={scfg.B} lattice {scfg.m}x{scfg.K} N={scfg.N} "
+                               f"GDN {scfg.n_gdn}x({scfg.Hk}qk/{scfg.Hv}v heads {scfg.dk}x{scfg.dv}) "
+                               f"attn {scfg.n_attn}x({scfg.Hq}q/{scfg.Hkv}kv heads D={scfg.D}) "
+                               f"KV={scfg.L} V={scfg.V}",
+                   "l2": "flushed before every timed step (2 x L2 write)",
+                   "launch": "one CUDA graph per step", "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "verify_step_us": ms_step_max * 1e3,
+        "tree_nodes_per_s": value,
+        "step_hbm_gbs": step_gbs,
+        "step_roofline_frac": step_gbs / peak,
+        "phases_us": ph_us,
+        "tau_mean": taus,
+        "roofline": {"bound": "hbm", "kernel": "attn_tree_verify (split-KV + merge)",
+                     "achieved": ach_attn, "peak": peak, "unit": "GB/s", "frac": ach_attn / peak,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+                     "algorithmic_bytes": byts["attn_kernel"], "traffic": None},
+        "gdn_roofline": {"bound": "hbm", "kernel": "gdn_tree_verify", "achieved": ach_gdn,
+                         "peak": peak, "unit": "GB/s", "frac": ach_gdn / peak,
+                         "algorithmic_bytes": byts["gdn_kernel"]},
+        "algorithmic_bytes": byts,
+        "clocks": clk,
+        "gpu_launches": st.launches_per_step * args.steps,
+        "e2e": {"value": nodes_total / (e2e_ms_step * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms_step},
+        "wall_s_timed_region": wall,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(scfg, args.seed)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=1, help="workload index (see synth.CONFIGS)")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,218 @@
+/*
+ * spec_tree.h -- C ABI of libspectree: the tree-verification step of lossless
+ * greedy speculative decoding on a hybrid Gated-DeltaNet / attention target,
+ * as hand-written CUDA kernels for one NVIDIA GB300 (sm_103a).
+ *
+ * The operations are those of the paper digest "SpecPilot: Autonomous
+ * Algorithm Discovery and Systems Optimization for Speculative Decoding"
+ * (rainbus.top); each entry point names the section it implements.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument is a DEVICE pointer to a caller-owned, contiguous,
+ *    row-major buffer in the layout stated next to it, unless it says "host".
+ *    The library allocates no memory and keeps no state between calls.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL means the legacy default stream).  Calls on different streams must
+ *    use different buffers and workspaces.
+ *  - Notation: B requests, m lattice positions, K candidates per position,
+ *    N draft nodes, T = N + 1 tree rows (the root, i.e. the pending bonus
+ *    token, plus N drafts).  Hk/Hv GDN q-k/v heads of dims dk/dv; Hq/Hkv
+ *    attention query/key-value heads of dim D; Lmax cache rows per request;
+ *    V vocabulary.  "io" below means the element type cfg->io_dtype selects:
+ *    bfloat16 (SPEC_IO_BF16) or float (SPEC_IO_F32).
+ *  - Limits (else ST_EINVAL): 1 <= B; 1 <= m <= 64; 1 <= K <= 32;
+ *    0 <= N <= 127; dk, dv in {64, 128}; Hv % Hk == 0; D in {64, 128};
+ *    Hq % Hkv == 0; 1 <= V; every pointer non-NULL and 16-byte aligned.
+ *  - Host return value: an ST_* code.  Errors found on the device while the
+ *    kernels run (cache overflow, a malformed lattice) are OR-ed into the
+ *    device status word at the start of the workspace; read it with
+ *    spec_status_read.
+ *  - The workspace `ws` is caller-owned device memory of at least
+ *    spec_workspace_bytes(cfg) bytes, zero-filled ONCE after allocation; every
+ *    call leaves its internal counters at zero again.  One workspace serves
+ *    one stream at a time.
+ */
+#ifndef SPEC_TREE_H
+#define SPEC_TREE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPEC_TREE_ABI_VERSION 1
+#define SPEC_ANC_WORDS 2     /* ancestor bitmask words per tree row (T <= 128) */
+#define SPEC_MAX_ROWS 128
+#define SPEC_MAX_K 32
+#define SPEC_MAX_M 64
+
+/* Host return codes. */
+enum {
+    ST_OK = 0,           /* launched */
+    ST_EINVAL = 1,       /* NULL or misaligned pointer, shape outside the limits */
+    ST_EUNSUPPORTED = 2, /* unsupported dtype or head dimension */
+    ST_ECUDA = 3,        /* a CUDA launch or copy failed (cudaGetLastError) */
+    ST_EOVERFLOW = 4,    /* device status: kv_len + tau > Lmax for some request */
+    ST_TIMEOUT = 5       /* device status: a bounded device-side wait gave up */
+};
+
+/* Bits of the device status word (uint32 at byte 0 of the workspace). */
+#define SPEC_DEV_OVERFLOW 0x1u  /* a request's commit was skipped: no room in the cache */
+#define SPEC_DEV_BADLAT   0x2u  /* a lattice position repeats a token or has a NaN score */
+#define SPEC_DEV_TIMEOUT  0x4u  /* a bounded device-side wait gave up */
+
+enum { SPEC_IO_F32 = 0, SPEC_IO_BF16 = 1 };
+
+/* Problem shape; passed by host pointer, read during the call only. */
+typedef struct spec_cfg {
+    int32_t B, m, K, N;
+    int32_t Hk, Hv, dk, dv;          /* GDN */
+    int32_t Hq, Hkv, D;              /* attention */
+    int32_t Lmax;                    /* KV cache rows per request */
+    int32_t V;                       /* vocabulary */
+    int32_t n_gdn_layers, n_attn_layers;
+    int32_t io_dtype;                /* SPEC_IO_BF16 or SPEC_IO_F32 */
+} spec_cfg;
+
+/* A draft tree per request, T = N + 1 rows in insertion order (a parent
+ * always precedes its children).  Rows n >= n_nodes[b] are padding:
+ * tok = parent = depth = rank = -1, score = 0, anc = 0. */
+typedef struct spec_tree {
+    int32_t *node_tok;      /* [B][T] token of the row (row 0: the root token) */
+    int32_t *node_parent;   /* [B][T] parent row, -1 for the root */
+    int32_t *node_depth;    /* [B][T] 0 for the root */
+    int32_t *node_rank;     /* [B][T] rank of the token among its position's candidates, -1 root */
+    float   *node_score;    /* [B][T] fp32 root-path sum of edge scores, 0 for the root */
+    uint64_t *node_anc;     /* [B][T][2] bit a set iff row a is the row or one of its ancestors */
+    int32_t *n_nodes;       /* [B] rows in use, 1 + min(N, sum_d K^d) */
+} spec_tree;
+
+/* Stacked per-layer buffers that accept_and_commit reads and updates.  Each
+ * is the concatenation over layers (layer outermost) of the buffer the
+ * matching verify call used for that layer. */
+typedef struct spec_commit_io {
+    float *h0;              /* [n_gdn][B][Hv][dk][dv] fp32 committed state, updated in place */
+    const void *gdn_k;      /* [n_gdn][B][T][Hk][dk] io */
+    const void *gdn_v;      /* [n_gdn][B][T][Hv][dv] io */
+    const float *alpha;     /* [n_gdn][B][T][Hv] */
+    const float *beta;      /* [n_gdn][B][T][Hv] */
+    const void *k_tree;     /* [n_attn][B][T][Hkv][D] io */
+    const void *v_tree;     /* [n_attn][B][T][Hkv][D] io */
+    void *k_cache;          /* [n_attn][B][Lmax][Hkv][D] io, rows appended */
+    void *v_cache;          /* [n_attn][B][Lmax][Hkv][D] io, rows appended */
+    int32_t *kv_len;        /* [B] valid cache rows, advanced by tau */
+    int32_t *root_tok;      /* [B] replaced by the bonus token */
+} spec_commit_io;
+
+/* Outputs of the acceptance. */
+typedef struct spec_accept {
+    int32_t *argmax;        /* [B][T] target argmax of each row, -1 on padding rows */
+    int32_t *accept_len;    /* [B] tau in [1, m+1]: accepted drafts + 1 */
+    int32_t *accept_nodes;  /* [B][m+1] accepted root path (row 0 first), -1 beyond tau */
+    int32_t *out_tok;       /* [B][m+1] emitted tokens: accepted drafts then the bonus, -1 beyond tau */
+} spec_accept;
+
+/* Bytes of device workspace the calls below need for `cfg` (0 on invalid cfg). */
+size_t spec_workspace_bytes(const spec_cfg *cfg);
+
+/*
+ * spec_tree_build -- best-first draft tree over the drafter's lattice.
+ * Digest: prerequisites / parallel drafter (per-position top-k candidates and
+ * scores form a lattice), prerequisites / draft-tree verification (nodes are
+ * added greedily by root-path log-prob up to N) and technical novelty,
+ * Figure 6 (best-first tree, edges scored log p(child | parent)).
+ *
+ * Candidates of each position are ordered by score (descending), then input
+ * index; a candidate's rank is its place in that order.  Row 0 is the root
+ * (token root_tok[b], depth 0, score 0).  A child (p, r) of an inserted row p
+ * of depth < m takes the rank-r candidate of lattice position depth(p) and the
+ * key fl32(score_p + edge score).  N times (or until no child is left) the
+ * child first in the order (key desc, depth asc, parent asc, rank asc) becomes
+ * the next row.  Scores must be finite; a position must not repeat a token
+ * (else SPEC_DEV_BADLAT is raised and that request's tree is unspecified).
+ *   lat_tok   [B][m][K] int32     lat_score [B][m][K] float
+ *   root_tok  [B] int32           out       tree buffers for T = N + 1 rows
+ */
+int spec_tree_build(const spec_cfg *cfg, const int32_t *lat_tok, const float *lat_score,
+                    const int32_t *root_tok, const spec_tree *out, void *ws, void *stream);
+
+/*
+ * gdn_tree_verify -- outputs of one Gated-DeltaNet layer for every tree row.
+ * Digest: prerequisites / hybrid recurrent target (gated delta rule
+ * h_t = alpha_t (I - beta_t k_t k_t^T) h_{t-1} + beta_t k_t v_t^T,
+ * o_t = h_t^T q_t) and technical novelty (each node's state is recomputed
+ * along its root path from the committed state, without per-node snapshots).
+ *
+ * For row n and v-head j (q-k head j / (Hv/Hk)): start from h0[b][j], apply
+ * the step of every row on n's root path (root first, n last) and output
+ * o[b][n][j] = h^T q_n.  Padding rows get 0.  No state is written.
+ *   h0    [B][Hv][dk][dv] float          q, k [B][T][Hk][dk] io
+ *   v     [B][T][Hv][dv] io              alpha, beta [B][T][Hv] float
+ *   o     [B][T][Hv][dv] io (output)
+ *   c_opt NULL, or [B][T][Hv][dv] float: per-row write vectors
+ *         c_n = beta_n v_n - alpha_n beta_n h_parent^T k_n (output)
+ */
+int gdn_tree_verify(const spec_cfg *cfg, const spec_tree *tree, const float *h0,
+                    const void *q, const void *k, const void *v, const float *alpha,
+                    const float *beta, void *o, float *c_opt, void *ws, void *stream);
+
+/*
+ * attn_tree_verify -- tree-ancestor-masked attention of one layer.
+ * Digest: prerequisites / draft-tree verification (every node sees only its
+ * ancestors).
+ *
+ * Row n, q-head h (kv-head h / (Hq/Hkv)) attends to cache rows
+ * [0, kv_len[b]) and to the tree rows that are n or its ancestors:
+ * o = softmax(q K^T / sqrt(D)) V, fp32 accumulation.  Padding rows get 0.
+ * Requires 0 <= kv_len[b] <= Lmax (checked against Lmax on the device).
+ *   q [B][T][Hq][D] io      k_tree, v_tree [B][T][Hkv][D] io
+ *   k_cache, v_cache [B][Lmax][Hkv][D] io     kv_len [B] int32
+ *   o [B][T][Hq][D] io (output)
+ */
+int attn_tree_verify(const spec_cfg *cfg, const spec_tree *tree, const void *q,
+                     const void *k_tree, const void *v_tree, const void *k_cache,
+                     const void *v_cache, const int32_t *kv_len, void *o, void *ws,
+                     void *stream);
+
+/*
+ * accept_and_commit -- greedy acceptance and commit of the accepted path.
+ * Digest: prerequisites / speculative decoding (accept the longest prefix equal
+ * to the target argmax plus one bonus token, tau in [1, m+1]) and draft-tree
+ * verification (the longest matching root path); the commit recomputes the
+ * state along the accepted root path (technical novelty).
+ *
+ * (i) argmax[b][n] = first index of the maximum of logits[b][n][:].
+ * (ii) From the root, move to the child whose token equals the current row's
+ * argmax (lowest row index on repeats) while one exists; tau = rows on the path.
+ * out_tok = tokens of the accepted drafts, then the bonus (argmax of the last
+ * accepted row).  (iii) Unless kv_len[b] + tau > Lmax (then SPEC_DEV_OVERFLOW
+ * is raised and request b is left uncommitted): every GDN layer's h0 advances
+ * over the tau path rows, every attention layer's cache rows
+ * [kv_len, kv_len + tau) receive the path rows' tree K/V, kv_len += tau and
+ * root_tok = bonus.
+ *   logits [B][T][V] io
+ */
+int accept_and_commit(const spec_cfg *cfg, const spec_tree *tree, const void *logits,
+                      const spec_commit_io *io, const spec_accept *out, void *ws,
+                      void *stream);
+
+/* Copy the device status word into *host_status (host pointer) and wait for
+ * `stream`.  Returns ST_OK, or ST_ECUDA if the copy failed. */
+int spec_status_read(const void *ws, uint32_t *host_status, void *stream);
+
+/* Zero the device status word on `stream`. */
+int spec_status_clear(void *ws, void *stream);
+
+/* Static description of an ST_* code (never NULL). */
+const char *spec_status_string(int code);
+
+/* SPEC_TREE_ABI_VERSION of the loaded library. */
+int spec_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEC_TREE_H */

@@ -1,0 +1,232 @@
+"""Thin ctypes binding of libspectree (include/spec_tree.h).
+
+The functions below carry the C entry points' names and do argument
+marshalling only: they check that tensors are CUDA, contiguous and of the
+expected dtype, then pass raw device pointers and the current CUDA stream.
+Every step of the computation runs in the library's kernels; there is no
+fallback, and loading fails loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libspectree.so")
+
+ST_OK, ST_EINVAL, ST_EUNSUPPORTED, ST_ECUDA, ST_EOVERFLOW, ST_TIMEOUT = range(6)
+SPEC_DEV_OVERFLOW, SPEC_DEV_BADLAT, SPEC_DEV_TIMEOUT = 0x1, 0x2, 0x4
+SPEC_IO_F32, SPEC_IO_BF16 = 0, 1
+EXPORTS = ("spec_workspace_bytes", "spec_tree_build", "gdn_tree_verify", "attn_tree_verify",
+           "accept_and_commit", "spec_status_read", "spec_status_clear", "spec_status_string",
+           "spec_abi_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SpecError(RuntimeError):
+    def __init__(self, fn, code, msg):
+        super().__init__(f"{fn} returned {code}: {msg}")
+        self.code = code
+
+
+class SpecCfg(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "B", "m", "K", "N", "Hk", "Hv", "dk", "dv", "Hq", "Hkv", "D", "Lmax", "V",
+        "n_gdn_layers", "n_attn_layers", "io_dtype")]
+
+
+class SpecTree(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "node_tok", "node_parent", "node_depth", "node_rank", "node_score", "node_anc", "n_nodes")]
+
+
+class SpecCommitIO(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "h0", "gdn_k", "gdn_v", "alpha", "beta", "k_tree", "v_tree", "k_cache", "v_cache",
+        "kv_len", "root_tok")]
+
+
+class SpecAccept(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("argmax", "accept_len", "accept_nodes", "out_tok")]
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libspectree.so (raises if it is missing: build it first)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(f"libspectree not built ({p} missing): run "
+                                   "`python -c 'import __graft_entry__ as g; g.build()'`")
+            lib = ctypes.CDLL(p)
+            vp, cfgp = ctypes.c_void_p, ctypes.POINTER(SpecCfg)
+            lib.spec_workspace_bytes.argtypes = [cfgp]
+            lib.spec_workspace_bytes.restype = ctypes.c_size_t
+            lib.spec_tree_build.argtypes = [cfgp, vp, vp, vp, ctypes.POINTER(SpecTree), vp, vp]
+            lib.gdn_tree_verify.argtypes = [cfgp, ctypes.POINTER(SpecTree)] + [vp] * 10
+            lib.attn_tree_verify.argtypes = [cfgp, ctypes.POINTER(SpecTree)] + [vp] * 9
+            lib.accept_and_commit.argtypes = [cfgp, ctypes.POINTER(SpecTree), vp,
+                                              ctypes.POINTER(SpecCommitIO),
+                                              ctypes.POINTER(SpecAccept), vp, vp]
+            lib.spec_status_read.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
+            lib.spec_status_clear.argtypes = [vp, vp]
+            lib.spec_status_string.argtypes = [ctypes.c_int]
+            lib.spec_status_string.restype = ctypes.c_char_p
+            for n in ("spec_tree_build", "gdn_tree_verify", "attn_tree_verify",
+                      "accept_and_commit", "spec_status_read", "spec_status_clear",
+                      "spec_abi_version"):
+                getattr(lib, n).restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+# ------------------------------------------------------------------ helpers
+
+def make_cfg(sc, **over) -> SpecCfg:
+    """SpecCfg from a synth.SpecConfig (or any object with the same fields)."""
+    d = dict(B=sc.B, m=sc.m, K=sc.K, N=sc.N, Hk=sc.Hk, Hv=sc.Hv, dk=sc.dk, dv=sc.dv, Hq=sc.Hq,
+             Hkv=sc.Hkv, D=sc.D, Lmax=sc.Lmax, V=sc.V, n_gdn_layers=sc.n_gdn,
+             n_attn_layers=sc.n_attn, io_dtype=SPEC_IO_BF16 if sc.io == "bf16" else SPEC_IO_F32)
+    d.update(over)
+    return SpecCfg(**d)
+
+
+def _io_dtype(cfg: SpecCfg):
+    return torch.bfloat16 if cfg.io_dtype == SPEC_IO_BF16 else torch.float32
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(fn, rc):
+    if rc != ST_OK:
+        raise SpecError(fn, rc, load().spec_status_string(rc).decode())
+
+
+class TreeBuffers:
+    """Device buffers of a spec_tree for B requests and T = N + 1 rows."""
+
+    def __init__(self, cfg: SpecCfg, device="cuda"):
+        B, T = cfg.B, cfg.N + 1
+        i32 = dict(dtype=torch.int32, device=device)
+        self.node_tok = torch.empty((B, T), **i32)
+        self.node_parent = torch.empty((B, T), **i32)
+        self.node_depth = torch.empty((B, T), **i32)
+        self.node_rank = torch.empty((B, T), **i32)
+        self.node_score = torch.empty((B, T), dtype=torch.float32, device=device)
+        self.node_anc = torch.empty((B, T, 2), dtype=torch.int64, device=device)
+        self.n_nodes = torch.empty((B,), **i32)
+
+    def c(self) -> SpecTree:
+        return SpecTree(*(t.data_ptr() for t in (
+            self.node_tok, self.node_parent, self.node_depth, self.node_rank, self.node_score,
+            self.node_anc, self.n_nodes)))
+
+    def to_numpy(self) -> dict:
+        import numpy as np
+        d = {k: getattr(self, k).cpu().numpy() for k in (
+            "node_tok", "node_parent", "node_depth", "node_rank", "node_score", "n_nodes")}
+        d["node_anc"] = self.node_anc.cpu().numpy().view(np.uint64)
+        return d
+
+
+class AcceptBuffers:
+    def __init__(self, cfg: SpecCfg, device="cuda"):
+        B, T, m = cfg.B, cfg.N + 1, cfg.m
+        i32 = dict(dtype=torch.int32, device=device)
+        self.argmax = torch.empty((B, T), **i32)
+        self.accept_len = torch.empty((B,), **i32)
+        self.accept_nodes = torch.empty((B, m + 1), **i32)
+        self.out_tok = torch.empty((B, m + 1), **i32)
+
+    def c(self) -> SpecAccept:
+        return SpecAccept(self.argmax.data_ptr(), self.accept_len.data_ptr(),
+                          self.accept_nodes.data_ptr(), self.out_tok.data_ptr())
+
+
+# ------------------------------------------------------------- entry points
+
+def spec_workspace_bytes(cfg: SpecCfg) -> int:
+    n = load().spec_workspace_bytes(ctypes.byref(cfg))
+    if n == 0:
+        raise SpecError("spec_workspace_bytes", ST_EINVAL, "invalid configuration")
+    return int(n)
+
+
+def alloc_workspace(cfg: SpecCfg, device="cuda") -> torch.Tensor:
+    """Zero-filled workspace of spec_workspace_bytes(cfg) bytes."""
+    return torch.zeros((spec_workspace_bytes(cfg),), dtype=torch.uint8, device=device)
+
+
+def spec_tree_build(cfg, lat_tok, lat_score, root_tok, tree: TreeBuffers, ws, stream=None):
+    _check("spec_tree_build", load().spec_tree_build(
+        ctypes.byref(cfg), _ptr(lat_tok, torch.int32, "lat_tok"),
+        _ptr(lat_score, torch.float32, "lat_score"), _ptr(root_tok, torch.int32, "root_tok"),
+        ctypes.byref(tree.c()), _ptr(ws, name="ws"), _stream(stream)))
+
+
+def gdn_tree_verify(cfg, tree: TreeBuffers, h0, q, k, v, alpha, beta, o, c=None, ws=None,
+                    stream=None):
+    dt = _io_dtype(cfg)
+    _check("gdn_tree_verify", load().gdn_tree_verify(
+        ctypes.byref(cfg), ctypes.byref(tree.c()), _ptr(h0, torch.float32, "h0"),
+        _ptr(q, dt, "q"), _ptr(k, dt, "k"), _ptr(v, dt, "v"), _ptr(alpha, torch.float32, "alpha"),
+        _ptr(beta, torch.float32, "beta"), _ptr(o, dt, "o"), _ptr(c, torch.float32, "c"),
+        _ptr(ws, name="ws"), _stream(stream)))
+
+
+def attn_tree_verify(cfg, tree: TreeBuffers, q, k_tree, v_tree, k_cache, v_cache, kv_len, o, ws,
+                     stream=None):
+    dt = _io_dtype(cfg)
+    _check("attn_tree_verify", load().attn_tree_verify(
+        ctypes.byref(cfg), ctypes.byref(tree.c()), _ptr(q, dt, "q"), _ptr(k_tree, dt, "k_tree"),
+        _ptr(v_tree, dt, "v_tree"), _ptr(k_cache, dt, "k_cache"), _ptr(v_cache, dt, "v_cache"),
+        _ptr(kv_len, torch.int32, "kv_len"), _ptr(o, dt, "o"), _ptr(ws, name="ws"),
+        _stream(stream)))
+
+
+def accept_and_commit(cfg, tree: TreeBuffers, logits, io: dict, out: AcceptBuffers, ws,
+                      stream=None):
+    """io: dict with stacked h0, gdn_k, gdn_v, alpha, beta, k_tree, v_tree,
+    k_cache, v_cache (None allowed where the layer count is 0), kv_len, root_tok."""
+    dt = _io_dtype(cfg)
+    f32, i32 = torch.float32, torch.int32
+    types = dict(h0=f32, gdn_k=dt, gdn_v=dt, alpha=f32, beta=f32, k_tree=dt, v_tree=dt,
+                 k_cache=dt, v_cache=dt, kv_len=i32, root_tok=i32)
+    cio = SpecCommitIO(*(_ptr(io.get(n), types[n], n) for n in types))
+    _check("accept_and_commit", load().accept_and_commit(
+        ctypes.byref(cfg), ctypes.byref(tree.c()), _ptr(logits, dt, "logits"), ctypes.byref(cio),
+        ctypes.byref(out.c()), _ptr(ws, name="ws"), _stream(stream)))
+
+
+def spec_status_read(ws, stream=None) -> int:
+    v = ctypes.c_uint32(0)
+    _check("spec_status_read", load().spec_status_read(_ptr(ws, name="ws"), ctypes.byref(v),
+                                                       _stream(stream)))
+    return int(v.value)
+
+
+def spec_status_clear(ws, stream=None):
+    _check("spec_status_clear", load().spec_status_clear(_ptr(ws, name="ws"), _stream(stream)))

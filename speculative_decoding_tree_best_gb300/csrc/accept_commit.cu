@@ -1,0 +1,283 @@
+// accept_commit.cu -- vocabulary argmax, greedy acceptance of the longest
+// matching root path plus the bonus token, and commit of the accepted path.
+//
+// Digest "SpecPilot ...": prerequisites / speculative decoding (greedy: accept
+// the longest prefix equal to the target argmax, plus one bonus token,
+// tau in [1, m+1]), prerequisites / draft-tree verification (longest matching
+// root path) and technical novelty (states recomputed along the root path).
+//
+// Three launches:
+//  1. argmax_partial: every logits row is cut into `argmax_split` segments;
+//     a CTA scans one segment with 16-byte loads and reduces (value desc,
+//     index asc) with warp shuffles.
+//  2. accept: one warp per request reduces the segments of each row, walks
+//     the tree with ballots over the children, writes the outputs, checks the
+//     cache room and advances kv_len / root_tok.
+//  3. commit: GDN blocks apply the accepted rows' gated-delta steps to 32
+//     columns of a state each (literal recurrence, fp32, the state slice held
+//     in registers); KV blocks copy the accepted tree K/V rows into the cache.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace spec {
+
+namespace {
+
+constexpr int NT = 256;
+
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+    return v > bv || (v == bv && i < bi);
+}
+
+template <int IO>
+__global__ void __launch_bounds__(NT)
+argmax_partial(spec_cfg c, const typename io_t<IO>::T* __restrict__ logits,
+               const int32_t* __restrict__ n_nodes, void* ws, WsLayout w) {
+    using E = typename io_t<IO>::T;
+    constexpr int VEC = 16 / sizeof(E);
+    const int sp = blockIdx.x, row = blockIdx.y;
+    const int T = c.N + 1, b = row / T, t = row % T;
+    if (t >= n_nodes[b] || t >= T) return;
+    const int V = c.V;
+    int seg = (V + w.argmax_split - 1) / w.argmax_split;
+    seg = (seg + VEC - 1) / VEC * VEC;
+    const int lo = sp * seg, hi = min(V, lo + seg);
+    const E* rp = logits + (size_t)row * V;
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    const bool vec_ok = (V % VEC) == 0 && ((reinterpret_cast<uintptr_t>(rp) & 15) == 0);
+    if (vec_ok) {
+        for (int e0 = lo + threadIdx.x * VEC; e0 < hi; e0 += NT * VEC) {
+            const uint4 u = *reinterpret_cast<const uint4*>(rp + e0);
+            const E* ev = reinterpret_cast<const E*>(&u);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                const float x = io_t<IO>::ld(ev, e);
+                if (e0 + e < hi && x > bv) { bv = x; bi = e0 + e; }
+            }
+        }
+    } else {
+        for (int e = lo + threadIdx.x; e < hi; e += NT) {
+            const float x = io_t<IO>::ld(rp, e);
+            if (x > bv) { bv = x; bi = e; }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+    }
+    __shared__ float sv[NT / 32];
+    __shared__ int si[NT / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) { sv[warp] = bv; si[warp] = bi; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int k = 1; k < NT / 32; ++k)
+            if (better(sv[k], si[k], bv, bi)) { bv = sv[k]; bi = si[k]; }
+        float2* out = ws_ptr<float2>(ws, w.argmax_off);
+        out[(size_t)row * kArgmaxSplit + sp] = make_float2(bv, __int_as_float(bi));
+    }
+}
+
+__global__ void __launch_bounds__(32)
+accept_kernel(spec_cfg c, spec_tree tree, spec_commit_io io, spec_accept out, void* ws, WsLayout w) {
+    extern __shared__ int sa[];
+    const int T = c.N + 1, m = c.m, b = blockIdx.x, lane = threadIdx.x;
+    int* am = sa;            // [T]
+    int* tok = am + T;       // [T]
+    int* par = tok + T;      // [T]
+    int* path = par + T;     // [m + 1]
+    int nn = tree.n_nodes[b];
+    nn = nn < 1 ? 1 : (nn > T ? T : nn);
+    const float2* part = ws_ptr<const float2>(ws, w.argmax_off);
+    for (int t = lane; t < T; t += 32) {
+        int a = -1;
+        if (t < nn) {
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
+            for (int sp = 0; sp < w.argmax_split; ++sp) {
+                const float2 p = part[((size_t)b * T + t) * kArgmaxSplit + sp];
+                const int pi = __float_as_int(p.y);
+                if (better(p.x, pi, bv, bi)) { bv = p.x; bi = pi; }
+            }
+            a = bi;
+        }
+        am[t] = a;
+        tok[t] = tree.node_tok[(size_t)b * T + t];
+        par[t] = tree.node_parent[(size_t)b * T + t];
+        out.argmax[(size_t)b * T + t] = a;
+    }
+    __syncwarp();
+
+    int cur = 0, len = 1;
+    if (lane == 0) path[0] = 0;
+    for (;;) {
+        const int target = am[cur];
+        int next = -1;
+        for (int base = 0; base < nn && next < 0; base += 32) {
+            const int x = base + lane;
+            const bool hit = x < nn && par[x] == cur && tok[x] == target;
+            const unsigned msk = __ballot_sync(0xffffffffu, hit);
+            if (msk) next = base + __ffs(msk) - 1;
+        }
+        if (next < 0 || len > m) break;
+        if (lane == 0) path[len] = next;
+        ++len;
+        cur = next;
+    }
+    __syncwarp();
+    const int bonus = am[cur];
+    for (int s = lane; s <= m; s += 32) {
+        out.accept_nodes[(size_t)b * (m + 1) + s] = s < len ? path[s] : -1;
+        int ot = -1;
+        if (s < len - 1) ot = tok[path[s + 1]];
+        else if (s == len - 1) ot = bonus;
+        out.out_tok[(size_t)b * (m + 1) + s] = ot;
+    }
+    if (lane == 0) {
+        out.accept_len[b] = len;
+        const int L = io.kv_len[b];
+        const bool ok = L >= 0 && L + len <= c.Lmax;
+        int32_t* plan = ws_ptr<int32_t>(ws, w.plan_off) + 4 * b;
+        plan[0] = ok ? len : 0;
+        plan[1] = L;
+        if (ok) {
+            io.kv_len[b] = L + len;
+            io.root_tok[b] = bonus;
+        } else {
+            raise_status(ws, SPEC_DEV_OVERFLOW);
+        }
+    }
+}
+
+template <int IO, int DK>
+__global__ void __launch_bounds__(NT)
+commit_kernel(spec_cfg c, spec_commit_io io, spec_accept acc, void* ws, WsLayout w, int gdn_blocks) {
+    using E = typename io_t<IO>::T;
+    extern __shared__ __align__(16) float sc[];
+    const int T = c.N + 1, m = c.m;
+    const int32_t* plan = ws_ptr<const int32_t>(ws, w.plan_off);
+    const int tid = threadIdx.x;
+    if ((int)blockIdx.x < gdn_blocks) {
+        constexpr int CB = 32, NG = NT / 32, RPT = DK / NG;
+        const int nb = c.dv / CB;
+        int id = blockIdx.x;
+        const int cb = id % nb; id /= nb;
+        const int j = id % c.Hv; id /= c.Hv;
+        const int b = id % c.B;
+        const int layer = id / c.B;
+        const int tau = plan[4 * b];
+        if (tau == 0) return;
+        const int ih = j / (c.Hv / c.Hk), c0 = cb * CB, col = tid & 31, grp = tid >> 5;
+        float* ks = sc;                     // [tau][DK]
+        float* vsm = ks + (m + 1) * DK;     // [tau][CB]
+        float* ab = vsm + (m + 1) * CB;     // [tau][2]
+        float* red = ab + 2 * (m + 1);      // [2][NG][CB]
+        const E* kl = static_cast<const E*>(io.gdn_k) + (size_t)layer * c.B * T * c.Hk * DK;
+        const E* vl = static_cast<const E*>(io.gdn_v) + (size_t)layer * c.B * T * c.Hv * c.dv;
+        const float* al = io.alpha + (size_t)layer * c.B * T * c.Hv;
+        const float* be = io.beta + (size_t)layer * c.B * T * c.Hv;
+        const int32_t* nodes = acc.accept_nodes + (size_t)b * (m + 1);
+        for (int idx = tid; idx < tau * DK; idx += NT) {
+            const int s = idx / DK, r = idx % DK, x = nodes[s];
+            ks[idx] = io_t<IO>::ld(kl, (((size_t)b * T + x) * c.Hk + ih) * DK + r);
+        }
+        for (int idx = tid; idx < tau * CB; idx += NT) {
+            const int s = idx / CB, cc = idx % CB, x = nodes[s];
+            vsm[idx] = io_t<IO>::ld(vl, (((size_t)b * T + x) * c.Hv + j) * c.dv + c0 + cc);
+        }
+        for (int s = tid; s < tau; s += NT) {
+            const int x = nodes[s];
+            ab[2 * s] = al[((size_t)b * T + x) * c.Hv + j];
+            ab[2 * s + 1] = be[((size_t)b * T + x) * c.Hv + j];
+        }
+        float* h = io.h0 + (size_t)layer * c.B * c.Hv * DK * c.dv + ((size_t)b * c.Hv + j) * DK * c.dv;
+        float hr[RPT];
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) hr[i] = h[(size_t)(grp * RPT + i) * c.dv + c0 + col];
+        __syncthreads();
+        for (int s = 0; s < tau; ++s) {
+            const float* kk = ks + s * DK + grp * RPT;
+            float part = 0.0f;
+#pragma unroll
+            for (int i = 0; i < RPT; ++i) part = fmaf(hr[i], kk[i], part);
+            float* rb = red + (s & 1) * NG * CB;
+            rb[grp * CB + col] = part;
+            __syncthreads();
+            float u = 0.0f;
+#pragma unroll
+            for (int g2 = 0; g2 < NG; ++g2) u += rb[g2 * CB + col];
+            const float a = ab[2 * s], bb = ab[2 * s + 1], vv = vsm[s * CB + col];
+#pragma unroll
+            for (int i = 0; i < RPT; ++i) hr[i] = a * (hr[i] - bb * kk[i] * u) + bb * kk[i] * vv;
+        }
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) h[(size_t)(grp * RPT + i) * c.dv + c0 + col] = hr[i];
+        return;
+    }
+    // ---- KV append: one block per (layer, request, path slot) ----
+    int id = blockIdx.x - gdn_blocks;
+    const int s = id % (m + 1); id /= (m + 1);
+    const int b = id % c.B;
+    const int layer = id / c.B;
+    const int tau = plan[4 * b];
+    if (s >= tau) return;
+    const int L = plan[4 * b + 1];
+    const int x = acc.accept_nodes[(size_t)b * (m + 1) + s];
+    const size_t row = (size_t)c.Hkv * c.D * sizeof(E);          // bytes, multiple of 16
+    const size_t src = (((size_t)layer * c.B + b) * T + x) * row;
+    const size_t dst = (((size_t)layer * c.B + b) * c.Lmax + L + s) * row;
+    const char* kt = static_cast<const char*>(io.k_tree);
+    const char* vt = static_cast<const char*>(io.v_tree);
+    char* kc = static_cast<char*>(io.k_cache);
+    char* vc = static_cast<char*>(io.v_cache);
+    for (size_t o = (size_t)tid * 16; o < row; o += NT * 16) {
+        *reinterpret_cast<uint4*>(kc + dst + o) = *reinterpret_cast<const uint4*>(kt + src + o);
+        *reinterpret_cast<uint4*>(vc + dst + o) = *reinterpret_cast<const uint4*>(vt + src + o);
+    }
+}
+
+template <int IO, int DK>
+cudaError_t launch_commit(const spec_cfg& c, const spec_commit_io& io, const spec_accept& out,
+                          void* ws, const WsLayout& w, cudaStream_t st) {
+    const int gdn_blocks = c.n_gdn_layers * c.B * c.Hv * (c.dv / 32);
+    const int kv_blocks = c.n_attn_layers * c.B * (c.m + 1);
+    if (gdn_blocks + kv_blocks == 0) return cudaSuccess;
+    const size_t smem = sizeof(float) * ((size_t)(c.m + 1) * (DK + 32 + 2) + 2 * 8 * 32);
+    auto kern = commit_kernel<IO, DK>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<gdn_blocks + kv_blocks, NT, smem, st>>>(c, io, out, ws, w, gdn_blocks);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_accept_commit(const spec_cfg& c, const spec_tree& t, const void* logits,
+                                 const spec_commit_io& io, const spec_accept& out, void* ws,
+                                 cudaStream_t st) {
+    const WsLayout w = ws_layout(c);
+    const int T = c.N + 1;
+    dim3 g1(w.argmax_split, c.B * T);
+    if (c.io_dtype == SPEC_IO_BF16)
+        argmax_partial<SPEC_IO_BF16><<<g1, NT, 0, st>>>(c, static_cast<const __nv_bfloat16*>(logits), t.n_nodes, ws, w);
+    else
+        argmax_partial<SPEC_IO_F32><<<g1, NT, 0, st>>>(c, static_cast<const float*>(logits), t.n_nodes, ws, w);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const size_t smem = sizeof(int) * (3 * (size_t)T + c.m + 1);
+    accept_kernel<<<c.B, 32, smem, st>>>(c, t, io, out, ws, w);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (c.io_dtype == SPEC_IO_BF16)
+        return c.dk == 128 ? launch_commit<SPEC_IO_BF16, 128>(c, io, out, ws, w, st)
+                           : launch_commit<SPEC_IO_BF16, 64>(c, io, out, ws, w, st);
+    return c.dk == 128 ? launch_commit<SPEC_IO_F32, 128>(c, io, out, ws, w, st)
+                       : launch_commit<SPEC_IO_F32, 64>(c, io, out, ws, w, st);
+}
+
+}  // namespace spec

@@ -1,0 +1,136 @@
+// api.cu -- the extern "C" boundary of libspectree (declared in spec_tree.h):
+// argument validation, workspace sizing and the kernel launches.
+#include <stdint.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+using spec::WsLayout;
+
+bool al16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_cfg(const spec_cfg* c) {
+    if (!c) return ST_EINVAL;
+    if (c->B < 1 || c->m < 1 || c->m > SPEC_MAX_M || c->K < 1 || c->K > SPEC_MAX_K) return ST_EINVAL;
+    if (c->N < 0 || c->N + 1 > SPEC_MAX_ROWS || c->V < 1 || c->Lmax < 0) return ST_EINVAL;
+    if (c->Hk < 1 || c->Hv < 1 || c->Hv % c->Hk != 0) return ST_EINVAL;
+    if (c->Hq < 1 || c->Hkv < 1 || c->Hq % c->Hkv != 0) return ST_EINVAL;
+    if ((c->dk != 64 && c->dk != 128) || (c->dv != 64 && c->dv != 128)) return ST_EINVAL;
+    if (c->D != 64 && c->D != 128) return ST_EINVAL;
+    if (c->n_gdn_layers < 0 || c->n_attn_layers < 0) return ST_EINVAL;
+    if (c->io_dtype != SPEC_IO_F32 && c->io_dtype != SPEC_IO_BF16) return ST_EUNSUPPORTED;
+    return ST_OK;
+}
+
+int check_tree(const spec_tree* t) {
+    if (!t) return ST_EINVAL;
+    if (!al16(t->node_tok) || !al16(t->node_parent) || !al16(t->node_depth) ||
+        !al16(t->node_rank) || !al16(t->node_score) || !al16(t->node_anc) || !al16(t->n_nodes))
+        return ST_EINVAL;
+    return ST_OK;
+}
+
+int cuda_rc(cudaError_t e) {
+    if (e == cudaSuccess) return ST_OK;
+    if (e == cudaErrorInvalidConfiguration) return ST_EUNSUPPORTED;
+    return ST_ECUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_abi_version(void) { return SPEC_TREE_ABI_VERSION; }
+
+const char* spec_status_string(int code) {
+    switch (code) {
+        case ST_OK: return "ok";
+        case ST_EINVAL: return "invalid argument (NULL or misaligned pointer, or shape outside the limits)";
+        case ST_EUNSUPPORTED: return "unsupported dtype or shape";
+        case ST_ECUDA: return "CUDA launch or copy failed";
+        case ST_EOVERFLOW: return "KV cache overflow: kv_len + tau > Lmax";
+        case ST_TIMEOUT: return "a bounded device-side wait gave up";
+        default: return "unknown status";
+    }
+}
+
+size_t spec_workspace_bytes(const spec_cfg* cfg) {
+    if (check_cfg(cfg) != ST_OK) return 0;
+    return spec::ws_layout(*cfg).total;
+}
+
+int spec_tree_build(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_score,
+                    const int32_t* root_tok, const spec_tree* out, void* ws, void* stream) {
+    int rc = check_cfg(cfg);
+    if (rc) return rc;
+    if ((rc = check_tree(out))) return rc;
+    if (!al16(lat_tok) || !al16(lat_score) || !al16(root_tok) || !al16(ws)) return ST_EINVAL;
+    return cuda_rc(spec::launch_tree_build(*cfg, lat_tok, lat_score, root_tok, *out, ws,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_tree_verify(const spec_cfg* cfg, const spec_tree* tree, const float* h0, const void* q,
+                    const void* k, const void* v, const float* alpha, const float* beta, void* o,
+                    float* c_opt, void* ws, void* stream) {
+    int rc = check_cfg(cfg);
+    if (rc) return rc;
+    if ((rc = check_tree(tree))) return rc;
+    if (!al16(h0) || !al16(q) || !al16(k) || !al16(v) || !al16(alpha) || !al16(beta) || !al16(o) ||
+        !al16(ws))
+        return ST_EINVAL;
+    if (c_opt && !al16(c_opt)) return ST_EINVAL;
+    return cuda_rc(spec::launch_gdn_tree(*cfg, *tree, h0, q, k, v, alpha, beta, o, c_opt,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+int attn_tree_verify(const spec_cfg* cfg, const spec_tree* tree, const void* q, const void* k_tree,
+                     const void* v_tree, const void* k_cache, const void* v_cache,
+                     const int32_t* kv_len, void* o, void* ws, void* stream) {
+    int rc = check_cfg(cfg);
+    if (rc) return rc;
+    if ((rc = check_tree(tree))) return rc;
+    if (!al16(q) || !al16(k_tree) || !al16(v_tree) || !al16(k_cache) || !al16(v_cache) ||
+        !al16(kv_len) || !al16(o) || !al16(ws))
+        return ST_EINVAL;
+    return cuda_rc(spec::launch_attn_tree(*cfg, *tree, q, k_tree, v_tree, k_cache, v_cache, kv_len,
+                                          o, ws, static_cast<cudaStream_t>(stream)));
+}
+
+int accept_and_commit(const spec_cfg* cfg, const spec_tree* tree, const void* logits,
+                      const spec_commit_io* io, const spec_accept* out, void* ws, void* stream) {
+    int rc = check_cfg(cfg);
+    if (rc) return rc;
+    if ((rc = check_tree(tree))) return rc;
+    if (!io || !out || !al16(logits) || !al16(ws)) return ST_EINVAL;
+    if (!al16(io->kv_len) || !al16(io->root_tok)) return ST_EINVAL;
+    if (cfg->n_gdn_layers > 0 && (!al16(io->h0) || !al16(io->gdn_k) || !al16(io->gdn_v) ||
+                                  !al16(io->alpha) || !al16(io->beta)))
+        return ST_EINVAL;
+    if (cfg->n_attn_layers > 0 && (!al16(io->k_tree) || !al16(io->v_tree) ||
+                                   !al16(io->k_cache) || !al16(io->v_cache)))
+        return ST_EINVAL;
+    if (!al16(out->argmax) || !al16(out->accept_len) || !al16(out->accept_nodes) ||
+        !al16(out->out_tok))
+        return ST_EINVAL;
+    return cuda_rc(spec::launch_accept_commit(*cfg, *tree, logits, *io, *out, ws,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+int spec_status_read(const void* ws, uint32_t* host_status, void* stream) {
+    if (!ws || !host_status) return ST_EINVAL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(host_status, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return ST_ECUDA;
+    return cudaStreamSynchronize(st) == cudaSuccess ? ST_OK : ST_ECUDA;
+}
+
+int spec_status_clear(void* ws, void* stream) {
+    if (!ws) return ST_EINVAL;
+    return cudaMemsetAsync(ws, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? ST_OK
+               : ST_ECUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,186 @@
+// attn_tree.cu -- tree-ancestor-masked attention of the tree rows over the KV
+// cache plus their tree ancestors (split-KV, then a merge).
+//
+// Digest "SpecPilot ...": prerequisites / draft-tree verification (one target
+// pass verifies the whole tree; every node sees only its ancestors).
+//
+// Work split.  The query rows of one (request, kv-head) are the G = Hq/Hkv
+// q-heads of that group times the tree rows, row r = node * G + head_in_group,
+// cut into 128-row tiles.  The keys are the cache rows [0, kv_len) cut into
+// fixed chunks plus one extra "tree chunk" holding the T tree rows, where a
+// key is visible to node x iff it is x or an ancestor of x.  Every
+// (request, kv-head, tile, chunk) produces an un-normalised partial
+// (O, running max, running sum); the merge rescales and sums the partials.
+// Only the tree chunk depends on the tree, so the cache chunks (all the KV
+// bytes) need nothing from spec_tree_build except n_nodes.
+//
+// This file holds the SIMT path (fp32 I/O, head dim 64, and the parity
+// baseline); attn_tree_tc.cu holds the tcgen05 path for bf16, head dim 128.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace spec {
+
+namespace {
+
+constexpr int NT = 256;
+constexpr int NW = NT / 32;
+
+template <int IO, int D>
+__global__ void __launch_bounds__(NT)
+attn_partial_simt(spec_cfg c, spec_tree tree, const typename io_t<IO>::T* __restrict__ q,
+                  const typename io_t<IO>::T* __restrict__ k_tree,
+                  const typename io_t<IO>::T* __restrict__ v_tree,
+                  const typename io_t<IO>::T* __restrict__ k_cache,
+                  const typename io_t<IO>::T* __restrict__ v_cache,
+                  const int32_t* __restrict__ kv_len, void* ws, WsLayout w) {
+    constexpr int EPL = D / 32;
+    const int ch = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int T = c.N + 1, G = c.Hq / c.Hkv, Hkv = c.Hkv;
+    int nn = tree.n_nodes[b];
+    nn = nn < 1 ? 1 : (nn > T ? T : nn);
+    int L = kv_len[b];
+    L = L < 0 ? 0 : (L > c.Lmax ? c.Lmax : L);
+    const bool tree_chunk = ch == w.n_split;
+    int k0 = 0, k1 = 0;
+    if (!tree_chunk) {
+        k0 = ch * w.chunk;
+        k1 = min(k0 + w.chunk, L);
+        if (k0 >= L) return;                 // no cache rows here: the merge skips it
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float scale = rsqrtf((float)D);
+    float* wO = ws_ptr<float>(ws, w.attn_o_off);
+    float2* wML = ws_ptr<float2>(ws, w.attn_ml_off);
+
+    for (int r = warp; r < G * nn; r += NW) {
+        const int x = r / G, h = g * G + r % G;
+        float qv[EPL], acc[EPL];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+            qv[e] = io_t<IO>::ld(q, (((size_t)b * T + x) * c.Hq + h) * D + lane + 32 * e);
+            acc[e] = 0.0f;
+        }
+        float mx = -INFINITY, sum = 0.0f;
+        const uint64_t a0 = tree.node_anc[2 * ((size_t)b * T + x)];
+        const uint64_t a1 = tree.node_anc[2 * ((size_t)b * T + x) + 1];
+        const int kend = tree_chunk ? nn : k1;
+        for (int key = tree_chunk ? 0 : k0; key < kend; ++key) {
+            size_t base;
+            const typename io_t<IO>::T *kp, *vp;
+            if (tree_chunk) {
+                const uint64_t word = key < 64 ? a0 : a1;
+                if (!((word >> (key & 63)) & 1ull)) continue;
+                base = (((size_t)b * T + key) * Hkv + g) * D;
+                kp = k_tree;
+                vp = v_tree;
+            } else {
+                base = (((size_t)b * c.Lmax + key) * Hkv + g) * D;
+                kp = k_cache;
+                vp = v_cache;
+            }
+            float s = 0.0f;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) s = fmaf(qv[e], io_t<IO>::ld(kp, base + lane + 32 * e), s);
+            s = warp_sum(s) * scale;
+            const float mn = fmaxf(mx, s);
+            const float corr = __expf(mx - mn);
+            const float p = __expf(s - mn);
+            sum = sum * corr + p;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e)
+                acc[e] = fmaf(p, io_t<IO>::ld(vp, base + lane + 32 * e), acc[e] * corr);
+            mx = mn;
+        }
+        const int mt = r / 128, rr = r % 128;
+        const size_t tile = (((size_t)b * Hkv + g) * w.n_mt + mt) * w.n_chunks + ch;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) wO[(tile * 128 + rr) * D + lane + 32 * e] = acc[e];
+        if (lane == 0) wML[tile * 128 + rr] = make_float2(mx, sum);
+    }
+}
+
+// One warp per query row: rescale the partials of every chunk that holds
+// visible keys to a common maximum and normalise.
+template <int IO, int D>
+__global__ void __launch_bounds__(NT)
+attn_merge(spec_cfg c, spec_tree tree, const int32_t* __restrict__ kv_len, void* ws, WsLayout w,
+           typename io_t<IO>::T* __restrict__ o) {
+    constexpr int EPL = D / 32;
+    const int mt = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int T = c.N + 1, G = c.Hq / c.Hkv;
+    int nn = tree.n_nodes[b];
+    nn = nn < 1 ? 1 : (nn > T ? T : nn);
+    int L = kv_len[b];
+    L = L < 0 ? 0 : (L > c.Lmax ? c.Lmax : L);
+    const int n_cache = (L + w.chunk - 1) / w.chunk;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float* wO = ws_ptr<const float>(ws, w.attn_o_off);
+    const float2* wML = ws_ptr<const float2>(ws, w.attn_ml_off);
+    for (int rr = warp; rr < 128; rr += NW) {
+        const int r = mt * 128 + rr;
+        if (r >= G * T) break;
+        const int x = r / G, h = g * G + r % G;
+        float acc[EPL];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] = 0.0f;
+        if (x < nn) {
+            const size_t tile0 = (((size_t)b * c.Hkv + g) * w.n_mt + mt) * w.n_chunks;
+            float M = -INFINITY;
+            for (int ch = 0; ch < w.n_chunks; ++ch) {
+                if (ch >= n_cache && ch != w.n_split) continue;
+                M = fmaxf(M, wML[(tile0 + ch) * 128 + rr].x);
+            }
+            float den = 0.0f;
+            for (int ch = 0; ch < w.n_chunks; ++ch) {
+                if (ch >= n_cache && ch != w.n_split) continue;
+                const float2 ml = wML[(tile0 + ch) * 128 + rr];
+                const float f = __expf(ml.x - M);
+                den = fmaf(ml.y, f, den);
+#pragma unroll
+                for (int e = 0; e < EPL; ++e)
+                    acc[e] = fmaf(wO[((tile0 + ch) * 128 + rr) * D + lane + 32 * e], f, acc[e]);
+            }
+            const float inv = 1.0f / den;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc[e] *= inv;
+        }
+#pragma unroll
+        for (int e = 0; e < EPL; ++e)
+            io_t<IO>::st(o, (((size_t)b * T + x) * c.Hq + h) * D + lane + 32 * e, acc[e]);
+    }
+}
+
+template <int IO, int D>
+cudaError_t launch_simt(const spec_cfg& c, const spec_tree& t, const void* q, const void* kt,
+                        const void* vt, const void* kc, const void* vc, const int32_t* kv_len,
+                        void* o, void* ws, cudaStream_t st) {
+    using E = typename io_t<IO>::T;
+    const WsLayout w = ws_layout(c);
+    attn_partial_simt<IO, D><<<dim3(w.n_chunks, c.Hkv, c.B), NT, 0, st>>>(
+        c, t, static_cast<const E*>(q), static_cast<const E*>(kt), static_cast<const E*>(vt),
+        static_cast<const E*>(kc), static_cast<const E*>(vc), kv_len, ws, w);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    attn_merge<IO, D><<<dim3(w.n_mt, c.Hkv, c.B), NT, 0, st>>>(c, t, kv_len, ws, w,
+                                                              static_cast<E*>(o));
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_tree(const spec_cfg& c, const spec_tree& t, const void* q,
+                             const void* k_tree, const void* v_tree, const void* k_cache,
+                             const void* v_cache, const int32_t* kv_len, void* o, void* ws,
+                             cudaStream_t st) {
+    if (c.io_dtype == SPEC_IO_BF16) {
+        return c.D == 128 ? launch_simt<SPEC_IO_BF16, 128>(c, t, q, k_tree, v_tree, k_cache, v_cache, kv_len, o, ws, st)
+                          : launch_simt<SPEC_IO_BF16, 64>(c, t, q, k_tree, v_tree, k_cache, v_cache, kv_len, o, ws, st);
+    }
+    return c.D == 128 ? launch_simt<SPEC_IO_F32, 128>(c, t, q, k_tree, v_tree, k_cache, v_cache, kv_len, o, ws, st)
+                      : launch_simt<SPEC_IO_F32, 64>(c, t, q, k_tree, v_tree, k_cache, v_cache, kv_len, o, ws, st);
+}
+
+}  // namespace spec

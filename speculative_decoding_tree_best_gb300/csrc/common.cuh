@@ -1,0 +1,104 @@
+// common.cuh -- shared device helpers and the workspace layout of libspectree.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "spec_tree.h"
+
+namespace spec {
+
+constexpr int kWarp = 32;
+
+// ---- element I/O ------------------------------------------------------------
+// IO = SPEC_IO_F32 or SPEC_IO_BF16; all arithmetic is fp32.
+template <int IO> struct io_t;
+template <> struct io_t<SPEC_IO_F32> {
+    using T = float;
+    static __device__ __forceinline__ float ld(const T* p, size_t i) { return p[i]; }
+    static __device__ __forceinline__ void st(T* p, size_t i, float x) { p[i] = x; }
+};
+template <> struct io_t<SPEC_IO_BF16> {
+    using T = __nv_bfloat16;
+    static __device__ __forceinline__ float ld(const T* p, size_t i) { return __bfloat162float(p[i]); }
+    static __device__ __forceinline__ void st(T* p, size_t i, float x) { p[i] = __float2bfloat16_rn(x); }
+};
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+__device__ __forceinline__ void raise_status(void* ws, uint32_t bits) {
+    atomicOr(reinterpret_cast<unsigned int*>(ws), bits);
+}
+
+// ---- workspace layout ---------------------------------------------------------
+// byte 0: device status word; then argmax partials, attention split-KV
+// partials, per-(request, kv-head, m-tile) merge tickets and the per-request
+// commit plan written by the acceptance kernel.
+constexpr int kArgmaxSplit = 8;          // CTAs per logits row (upper bound)
+constexpr int kAttnRowsMax = 128 * 2;    // query rows of one (request, kv-head) tile group
+
+struct WsLayout {
+    size_t argmax_off;     // float2 [B][T][kArgmaxSplit]: (value, index bits)
+    size_t attn_o_off;     // float  [B][Hkv][n_mt][n_chunks][128][D]
+    size_t attn_ml_off;    // float2 [B][Hkv][n_mt][n_chunks][128]: (max, sum)
+    size_t ticket_off;     // uint32 [B][Hkv][n_mt]
+    size_t plan_off;       // int32  [B][4]: committed tau (0 = skip), old kv_len
+    size_t total;
+    int n_split;           // cache chunks per (request, kv-head)
+    int chunk;             // cache rows per chunk
+    int n_chunks;          // n_split + 1 (the tree chunk)
+    int n_mt;              // 128-row query tiles per (request, kv-head)
+    int argmax_split;      // CTAs per logits row
+};
+
+static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Cache rows per chunk: enough chunks that B x Hkv x tiles x chunks fills the
+// 152 SMs about twice, each chunk a multiple of 128 rows.
+static inline WsLayout ws_layout(const spec_cfg& c, int num_sms = 152) {
+    WsLayout w{};
+    const int T = c.N + 1;
+    const int G = c.Hq / c.Hkv;
+    w.n_mt = (G * T + 127) / 128;
+    const long units = (long)c.B * c.Hkv * w.n_mt;
+    long want = (2L * num_sms + units - 1) / units;
+    if (want < 1) want = 1;
+    long chunk = (c.Lmax + want - 1) / want;
+    chunk = (chunk + 127) / 128 * 128;
+    if (chunk < 128) chunk = 128;
+    w.chunk = (int)chunk;
+    w.n_split = (int)((c.Lmax + chunk - 1) / chunk);
+    if (w.n_split < 1) w.n_split = 1;
+    w.n_chunks = w.n_split + 1;
+    const long rows = (long)c.B * T;
+    int split = (int)((2L * num_sms + rows - 1) / rows);
+    if (split > kArgmaxSplit) split = kArgmaxSplit;
+    if (split < 1) split = 1;
+    w.argmax_split = split;
+
+    size_t off = 256;                                   // status word + reserve
+    w.argmax_off = off;
+    off = align_up(off + sizeof(float) * 2 * (size_t)c.B * T * kArgmaxSplit, 256);
+    const size_t tiles = (size_t)c.B * c.Hkv * w.n_mt * w.n_chunks;
+    w.attn_o_off = off;
+    off = align_up(off + sizeof(float) * tiles * 128 * (size_t)c.D, 256);
+    w.attn_ml_off = off;
+    off = align_up(off + sizeof(float) * 2 * tiles * 128, 256);
+    w.ticket_off = off;
+    off = align_up(off + sizeof(uint32_t) * (size_t)c.B * c.Hkv * w.n_mt, 256);
+    w.plan_off = off;
+    off = align_up(off + sizeof(int32_t) * 4 * (size_t)c.B, 256);
+    w.total = off;
+    return w;
+}
+
+template <typename T> __host__ __device__ __forceinline__ T* ws_ptr(void* ws, size_t off) {
+    return reinterpret_cast<T*>(reinterpret_cast<char*>(ws) + off);
+}
+
+}  // namespace spec

@@ -1,0 +1,31 @@
+// kernels.h -- launchers shared between the kernel files and the C ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace spec {
+
+cudaError_t launch_tree_build(const spec_cfg& c, const int32_t* lat_tok, const float* lat_score,
+                              const int32_t* root_tok, const spec_tree& out, void* ws,
+                              cudaStream_t st);
+size_t tree_build_smem(const spec_cfg& c);
+
+// Returns cudaErrorInvalidConfiguration when the shape needs more shared memory
+// than one CTA can have.
+cudaError_t launch_gdn_tree(const spec_cfg& c, const spec_tree& t, const float* h0,
+                            const void* q, const void* k, const void* v, const float* alpha,
+                            const float* beta, void* o, float* c_out, cudaStream_t st);
+size_t gdn_tree_smem(const spec_cfg& c);
+
+cudaError_t launch_attn_tree(const spec_cfg& c, const spec_tree& t, const void* q,
+                             const void* k_tree, const void* v_tree, const void* k_cache,
+                             const void* v_cache, const int32_t* kv_len, void* o, void* ws,
+                             cudaStream_t st);
+
+cudaError_t launch_accept_commit(const spec_cfg& c, const spec_tree& t, const void* logits,
+                                 const spec_commit_io& io, const spec_accept& out, void* ws,
+                                 cudaStream_t st);
+
+}  // namespace spec

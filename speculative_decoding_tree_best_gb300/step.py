@@ -1,0 +1,85 @@
+"""One whole verify step on device buffers: tree build, every GDN layer, every
+attention layer, then acceptance and commit -- each a call through the C ABI.
+
+The driver owns the device buffers (stacked per layer, layer outermost, so
+the commit sees every layer through one pointer per tensor) and issues the
+calls on one stream.  It does no arithmetic of its own.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding
+from .synth import SpecConfig
+
+
+def stack_inputs(inp: dict, device="cuda") -> dict:
+    """Device copies of synth.make_step_inputs' output with layers stacked."""
+    d = {}
+    for k in ("lat_tok", "lat_score", "root_tok", "kv_len", "logits"):
+        if k in inp:
+            d[k] = inp[k].to(device).contiguous()
+    g, a = inp["gdn"], inp["attn"]
+    for src, dst in (("h0", "gdn_h0"), ("q", "gdn_q"), ("k", "gdn_k"), ("v", "gdn_v"),
+                     ("alpha", "gdn_alpha"), ("beta", "gdn_beta")):
+        d[dst] = torch.stack([lay[src] for lay in g]).to(device).contiguous() if g else None
+    for src, dst in (("q", "attn_q"), ("k_tree", "k_tree"), ("v_tree", "v_tree"),
+                     ("k_cache", "k_cache"), ("v_cache", "v_cache")):
+        d[dst] = torch.stack([lay[src] for lay in a]).to(device).contiguous() if a else None
+    return d
+
+
+class VerifyStep:
+    """Buffers and calls of one verify step for a synthetic workload."""
+
+    def __init__(self, scfg: SpecConfig, x: dict, device="cuda"):
+        self.scfg = scfg
+        self.cfg = binding.make_cfg(scfg)
+        self.x = x
+        self.device = device
+        c = self.cfg
+        T = c.N + 1
+        dt = torch.bfloat16 if scfg.io == "bf16" else torch.float32
+        self.tree = binding.TreeBuffers(c, device)
+        self.acc = binding.AcceptBuffers(c, device)
+        self.ws = binding.alloc_workspace(c, device)
+        self.gdn_o = torch.empty((c.n_gdn_layers, c.B, T, c.Hv, c.dv), dtype=dt, device=device)
+        self.attn_o = torch.empty((c.n_attn_layers, c.B, T, c.Hq, c.D), dtype=dt, device=device)
+
+    # the three phases ----------------------------------------------------------
+    def build_tree(self, stream=None):
+        x = self.x
+        binding.spec_tree_build(self.cfg, x["lat_tok"], x["lat_score"], x["root_tok"], self.tree,
+                                self.ws, stream)
+
+    def verify(self, stream=None):
+        x, c = self.x, self.cfg
+        for l in range(c.n_gdn_layers):
+            binding.gdn_tree_verify(c, self.tree, x["gdn_h0"][l], x["gdn_q"][l], x["gdn_k"][l],
+                                    x["gdn_v"][l], x["gdn_alpha"][l], x["gdn_beta"][l],
+                                    self.gdn_o[l], None, self.ws, stream)
+        for l in range(c.n_attn_layers):
+            binding.attn_tree_verify(c, self.tree, x["attn_q"][l], x["k_tree"][l], x["v_tree"][l],
+                                     x["k_cache"][l], x["v_cache"][l], x["kv_len"],
+                                     self.attn_o[l], self.ws, stream)
+
+    def commit_io(self) -> dict:
+        x = self.x
+        return dict(h0=x["gdn_h0"], gdn_k=x["gdn_k"], gdn_v=x["gdn_v"], alpha=x["gdn_alpha"],
+                    beta=x["gdn_beta"], k_tree=x["k_tree"], v_tree=x["v_tree"],
+                    k_cache=x["k_cache"], v_cache=x["v_cache"], kv_len=x["kv_len"],
+                    root_tok=x["root_tok"])
+
+    def accept_commit(self, stream=None):
+        binding.accept_and_commit(self.cfg, self.tree, self.x["logits"], self.commit_io(),
+                                  self.acc, self.ws, stream)
+
+    def run(self, stream=None):
+        self.build_tree(stream)
+        self.verify(stream)
+        self.accept_commit(stream)
+
+    @property
+    def launches_per_step(self) -> int:
+        c = self.cfg
+        return 1 + c.n_gdn_layers + 2 * c.n_attn_layers + 3

@@ -1,0 +1,92 @@
+"""GPU parity: the CUDA library, called through its C ABI, against the CPU
+oracle on the same seeded inputs (bit-exact on trees, argmax, acceptance and
+commits; rel-L2 <= 2e-3 on GDN/attention outputs and committed states)."""
+import pytest
+import torch
+
+from speculative_decoding_tree_best_gb300 import binding, synth
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from speculative_decoding_tree_best_gb300 import build
+    build.build()
+    binding.load()
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_tiny_fp32(seed):
+    r = parity.check_case(synth.config(0), seed)
+    assert r["gdn_rel_l2"] < 1e-5 and r["attn_rel_l2"] < 1e-5 and r["state_rel_l2"] < 1e-5
+    assert r["status"] == 0
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_single_request_full_size(seed):
+    r = parity.check_case(synth.config(1), seed)
+    assert r["status"] == 0
+
+
+def test_long_tree_full_size_sampled():
+    r = parity.check_case(synth.config(2), 0, attn_kv_heads=[0, 5])
+    assert max(r["tau"]) >= 1
+
+
+def test_batched_sampled():
+    r = parity.check_case(synth.config(3), 0, req=[0, 7, 23], attn_kv_heads=[2, 7])
+    assert r["status"] == 0
+
+
+# ---- edge cases ---------------------------------------------------------------------
+
+SMALL = synth.config(1).replace(m=4, K=4, N=12, L=300, V=4096)
+
+
+def test_single_row_tree():
+    parity.check_case(SMALL.replace(N=0), 1)
+
+
+def test_frontier_exhausted_padding_rows():
+    r = parity.check_case(SMALL.replace(m=2, K=2, N=20), 2)     # 6 drafts exist, 14 pad rows
+    assert r["status"] == 0
+
+
+def test_k1_chain_and_m1_star():
+    parity.check_case(SMALL.replace(K=1, N=6), 3)
+    parity.check_case(SMALL.replace(m=1, K=16, N=10), 4)
+
+
+def test_tied_lattice_scores():
+    def ties(inp):
+        inp["lat_score"] = (-0.5 * torch.randint(0, 3, inp["lat_score"].shape,
+                                                 generator=torch.Generator().manual_seed(0))
+                            ).float().contiguous()
+    parity.check_case(SMALL.replace(m=4, K=8, N=40), 5, lat_edit=ties)
+
+
+def test_empty_cache_and_ragged_lengths():
+    cfg = SMALL.replace(B=4, L=700, N=12)
+    parity.check_case(cfg, 6, kv_len=[0, 1, 129, 700])
+
+
+def test_cache_overflow_skips_commit():
+    cfg = SMALL.replace(B=2, L=200, headroom=0)
+    r = parity.check_case(cfg, 7, kv_len=[200, 10])
+    assert r["overflow"] == [True, False]
+    assert r["status"] & binding.SPEC_DEV_OVERFLOW
+
+
+def test_head_dim_64_bf16_and_deep_tree():
+    cfg = synth.config(1).replace(dk=64, dv=64, D=64, Hk=4, Hv=8, Hq=8, Hkv=2, m=16, K=4,
+                                  N=100, L=513, V=2000)
+    parity.check_case(cfg, 8)
+
+
+def test_multi_layer_stack_small():
+    cfg = synth.config(4).replace(B=2, n_gdn=3, n_attn=2, L=257, V=3000)
+    parity.check_case(cfg, 9)

@@ -1,0 +1,83 @@
+"""The C-ABI library builds, loads and exports every function spec_tree.h
+declares; host-side argument validation rejects bad input before any CUDA
+call.  Runs without a GPU (no kernel is launched here)."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+from speculative_decoding_tree_best_gb300 import binding, synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spec_tree.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    from speculative_decoding_tree_best_gb300 import build
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\([^;]*\)\s*;", src, re.M)))
+
+
+def test_header_declares_the_four_calls():
+    names = declared_functions()
+    for n in ("spec_tree_build", "gdn_tree_verify", "attn_tree_verify", "accept_and_commit",
+              "spec_workspace_bytes"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} declared in spec_tree.h but not exported"
+    assert set(binding.EXPORTS) <= set(declared_functions())
+
+
+def test_abi_version_and_strings(lib):
+    assert lib.spec_abi_version() == 1
+    for code in range(6):
+        assert lib.spec_status_string(code)
+
+
+def test_workspace_sizing_is_host_only(lib):
+    for i in range(5):
+        cfg = binding.make_cfg(synth.config(i))
+        n = binding.spec_workspace_bytes(cfg)
+        assert n > 256 and n % 256 == 0
+    bad = binding.make_cfg(synth.config(1), dk=96)
+    assert lib.spec_workspace_bytes(ctypes.byref(bad)) == 0
+
+
+@pytest.mark.parametrize("field,value", [("K", 33), ("N", 128), ("m", 0), ("Hv", 20),
+                                         ("Hq", 30), ("D", 256), ("io_dtype", 7)])
+def test_validation_rejects_before_launch(lib, field, value):
+    cfg = binding.make_cfg(synth.config(1), **{field: value})
+    tree = binding.SpecTree(*([16] * 7))
+    rc = lib.spec_tree_build(ctypes.byref(cfg), ctypes.c_void_p(16), ctypes.c_void_p(16),
+                             ctypes.c_void_p(16), ctypes.byref(tree), ctypes.c_void_p(16), None)
+    assert rc in (binding.ST_EINVAL, binding.ST_EUNSUPPORTED)
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    cfg = binding.make_cfg(synth.config(1))
+    tree = binding.SpecTree(*([16] * 7))
+    rc = lib.spec_tree_build(ctypes.byref(cfg), None, ctypes.c_void_p(16), ctypes.c_void_p(16),
+                             ctypes.byref(tree), ctypes.c_void_p(16), None)
+    assert rc == binding.ST_EINVAL
+    rc = lib.gdn_tree_verify(ctypes.byref(cfg), ctypes.byref(tree), *([ctypes.c_void_p(16)] * 7),
+                             ctypes.c_void_p(24), None, ctypes.c_void_p(16), None)
+    assert rc == binding.ST_EINVAL
+    rc = lib.attn_tree_verify(ctypes.byref(cfg), None, *([ctypes.c_void_p(16)] * 8), None)
+    assert rc == binding.ST_EINVAL
+    rc = lib.accept_and_commit(ctypes.byref(cfg), ctypes.byref(tree), ctypes.c_void_p(16), None,
+                               None, ctypes.c_void_p(16), None)
+    assert rc == binding.ST_EINVAL
