@@ -415,32 +415,44 @@ def run_ours(args, rank, world, local):
     taus = st.acc.accept_len.float().mean().item()
     mean_L = float(kv0.float().mean().item())
 
-    # ---- phase breakdown (eager, CUDA events on the launching stream) -------------------
-    R = max(10, min(args.steps, 50))
-    phase = {k: [] for k in ("tree", "gdn", "attn", "accept_commit")}
-    for _ in range(R):
-        flush.zero_()
-        reset()
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-        e[0].record(stream)
-        st.build_tree()
-        e[1].record(stream)
-        c = st.cfg
+    # ---- phase breakdown: each phase captured as its own graph, timed with
+    # CUDA events on the launching stream (L2 flushed before every replay) -----
+    c = st.cfg
+
+    def gdn_all():
         for l in range(c.n_gdn_layers):
             binding.gdn_tree_verify(c, st.tree, x["gdn_h0"][l], x["gdn_q"][l], x["gdn_k"][l],
                                     x["gdn_v"][l], x["gdn_alpha"][l], x["gdn_beta"][l],
                                     st.gdn_o[l], None, st.ws)
-        e[2].record(stream)
+
+    def attn_all():
         for l in range(c.n_attn_layers):
             binding.attn_tree_verify(c, st.tree, x["attn_q"][l], x["k_tree"][l], x["v_tree"][l],
                                      x["k_cache"][l], x["v_cache"][l], x["kv_len"], st.attn_o[l],
                                      st.ws)
-        e[3].record(stream)
-        st.accept_commit()
-        e[4].record(stream)
-        torch.cuda.synchronize()
-        for k, (a, b) in zip(phase, zip(e[:-1], e[1:])):
-            phase[k].append(a.elapsed_time(b))
+
+    phase_fns = {"tree": st.build_tree, "gdn": gdn_all, "attn": attn_all,
+                 "accept_commit": st.accept_commit}
+    phase_graphs = {}
+    for name, fn in phase_fns.items():
+        reset()
+        pg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(pg, capture_error_mode="thread_local"):
+            fn()
+        phase_graphs[name] = pg
+    torch.cuda.synchronize()
+    R = max(10, min(args.steps, 50))
+    phase = {k: [] for k in phase_graphs}
+    for _ in range(R):
+        for name, pg in phase_graphs.items():
+            flush.zero_()
+            reset()
+            a, bev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            pg.replay()
+            bev.record(stream)
+            torch.cuda.synchronize()
+            phase[name].append(a.elapsed_time(bev))
     ph_us = {k: 1e3 * statistics.median(v) for k, v in phase.items()}
 
     # ---- end to end through the public API with host buffers ----------------------

@@ -49,13 +49,24 @@ argmax_partial(spec_cfg c, const typename io_t<IO>::T* __restrict__ logits,
     int bi = 0x7fffffff;
     const bool vec_ok = (V % VEC) == 0 && ((reinterpret_cast<uintptr_t>(rp) & 15) == 0);
     if (vec_ok) {
-        for (int e0 = lo + threadIdx.x * VEC; e0 < hi; e0 += NT * VEC) {
-            const uint4 u = *reinterpret_cast<const uint4*>(rp + e0);
-            const E* ev = reinterpret_cast<const E*>(&u);
+        // four 16-byte loads in flight per thread per iteration
+        constexpr int U = 4;
+        for (int e0 = lo + threadIdx.x * VEC; e0 < hi; e0 += U * NT * VEC) {
+            uint4 u[U];
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const float x = io_t<IO>::ld(ev, e);
-                if (e0 + e < hi && x > bv) { bv = x; bi = e0 + e; }
+            for (int k = 0; k < U; ++k) {
+                const int ek = e0 + k * NT * VEC;
+                u[k] = ek < hi ? *reinterpret_cast<const uint4*>(rp + ek) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const int ek = e0 + k * NT * VEC;
+                const E* ev = reinterpret_cast<const E*>(&u[k]);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const float x = io_t<IO>::ld(ev, e);
+                    if (ek < hi && x > bv) { bv = x; bi = ek + e; }
+                }
             }
         }
     } else {

@@ -14,8 +14,8 @@
 // Only the tree chunk depends on the tree, so the cache chunks (all the KV
 // bytes) need nothing from spec_tree_build except n_nodes.
 //
-// This file holds the SIMT path (fp32 I/O, head dim 64, and the parity
-// baseline); attn_tree_tc.cu holds the tcgen05 path for bf16, head dim 128.
+// This file holds the SIMT partial (fp32 I/O and head dim 64) and the merge;
+// attn_tree_tc.cu holds the tcgen05 partial used for bf16 I/O, head dim 128.
 #include <math.h>
 
 #include "common.cuh"
@@ -60,7 +60,7 @@ attn_partial_simt(spec_cfg c, spec_tree tree, const typename io_t<IO>::T* __rest
         float qv[EPL], acc[EPL];
 #pragma unroll
         for (int e = 0; e < EPL; ++e) {
-            qv[e] = io_t<IO>::ld(q, (((size_t)b * T + x) * c.Hq + h) * D + lane + 32 * e);
+            qv[e] = io_t<IO>::ld(q, (((size_t)b * T + x) * c.Hq + h) * D + lane * EPL + e);
             acc[e] = 0.0f;
         }
         float mx = -INFINITY, sum = 0.0f;
@@ -83,7 +83,7 @@ attn_partial_simt(spec_cfg c, spec_tree tree, const typename io_t<IO>::T* __rest
             }
             float s = 0.0f;
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) s = fmaf(qv[e], io_t<IO>::ld(kp, base + lane + 32 * e), s);
+            for (int e = 0; e < EPL; ++e) s = fmaf(qv[e], io_t<IO>::ld(kp, base + lane * EPL + e), s);
             s = warp_sum(s) * scale;
             const float mn = fmaxf(mx, s);
             const float corr = __expf(mx - mn);
@@ -91,66 +91,80 @@ attn_partial_simt(spec_cfg c, spec_tree tree, const typename io_t<IO>::T* __rest
             sum = sum * corr + p;
 #pragma unroll
             for (int e = 0; e < EPL; ++e)
-                acc[e] = fmaf(p, io_t<IO>::ld(vp, base + lane + 32 * e), acc[e] * corr);
+                acc[e] = fmaf(p, io_t<IO>::ld(vp, base + lane * EPL + e), acc[e] * corr);
             mx = mn;
         }
         const int mt = r / 128, rr = r % 128;
         const size_t tile = (((size_t)b * Hkv + g) * w.n_mt + mt) * w.n_chunks + ch;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) wO[(tile * 128 + rr) * D + lane + 32 * e] = acc[e];
+        for (int e = 0; e < EPL; ++e) wO[(tile * 128 + rr) * D + lane * EPL + e] = acc[e];
         if (lane == 0) wML[tile * 128 + rr] = make_float2(mx, sum);
     }
 }
 
-// One warp per query row: rescale the partials of every chunk that holds
-// visible keys to a common maximum and normalise.
+// One warp per query row (8 rows per CTA).  Pass 1: lane i reads the (max,
+// sum) of chunk i and the warp reduces them to the common maximum and the
+// denominator.  Pass 2: lane i owns D/32 consecutive output columns and sums
+// the chunks' rescaled partial rows.
 template <int IO, int D>
 __global__ void __launch_bounds__(NT)
 attn_merge(spec_cfg c, spec_tree tree, const int32_t* __restrict__ kv_len, void* ws, WsLayout w,
            typename io_t<IO>::T* __restrict__ o) {
     constexpr int EPL = D / 32;
-    const int mt = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int g = blockIdx.y, b = blockIdx.z;
     const int T = c.N + 1, G = c.Hq / c.Hkv;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int r = blockIdx.x * NW + warp;
+    if (r >= G * T) return;
     int nn = tree.n_nodes[b];
     nn = nn < 1 ? 1 : (nn > T ? T : nn);
     int L = kv_len[b];
     L = L < 0 ? 0 : (L > c.Lmax ? c.Lmax : L);
     const int n_cache = (L + w.chunk - 1) / w.chunk;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const float* wO = ws_ptr<const float>(ws, w.attn_o_off);
-    const float2* wML = ws_ptr<const float2>(ws, w.attn_ml_off);
-    for (int rr = warp; rr < 128; rr += NW) {
-        const int r = mt * 128 + rr;
-        if (r >= G * T) break;
-        const int x = r / G, h = g * G + r % G;
-        float acc[EPL];
+    const int x = r / G, h = g * G + r % G, mt = r / 128, rr = r % 128;
+    float acc[EPL];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[e] = 0.0f;
-        if (x < nn) {
-            const size_t tile0 = (((size_t)b * c.Hkv + g) * w.n_mt + mt) * w.n_chunks;
-            float M = -INFINITY;
-            for (int ch = 0; ch < w.n_chunks; ++ch) {
-                if (ch >= n_cache && ch != w.n_split) continue;
-                M = fmaxf(M, wML[(tile0 + ch) * 128 + rr].x);
-            }
-            float den = 0.0f;
-            for (int ch = 0; ch < w.n_chunks; ++ch) {
-                if (ch >= n_cache && ch != w.n_split) continue;
-                const float2 ml = wML[(tile0 + ch) * 128 + rr];
-                const float f = __expf(ml.x - M);
-                den = fmaf(ml.y, f, den);
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.0f;
+    if (x < nn) {
+        const float* wO = ws_ptr<const float>(ws, w.attn_o_off);
+        const float2* wML = ws_ptr<const float2>(ws, w.attn_ml_off);
+        const size_t tile0 = (((size_t)b * c.Hkv + g) * w.n_mt + mt) * w.n_chunks;
+        // chunks holding keys: cache chunks [0, n_cache) and the tree chunk n_split
+        const int nch = n_cache + 1;
+        auto chunk_id = [&](int i) { return i < n_cache ? i : w.n_split; };
+        float M = -INFINITY;
+        for (int i = lane; i < nch; i += 32) M = fmaxf(M, wML[(tile0 + chunk_id(i)) * 128 + rr].x);
 #pragma unroll
-                for (int e = 0; e < EPL; ++e)
-                    acc[e] = fmaf(wO[((tile0 + ch) * 128 + rr) * D + lane + 32 * e], f, acc[e]);
-            }
-            const float inv = 1.0f / den;
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) acc[e] *= inv;
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float den = 0.0f;
+        for (int i = lane; i < nch; i += 32) {
+            const float2 ml = wML[(tile0 + chunk_id(i)) * 128 + rr];
+            den += ml.y * __expf(ml.x - M);
         }
+        den = warp_sum(den);
+#pragma unroll 6
+        for (int i = 0; i < nch; ++i) {
+            const size_t t = tile0 + chunk_id(i);
+            const float f = __expf(wML[t * 128 + rr].x - M);
+            const float* src = wO + (t * 128 + rr) * D + lane * EPL;
+            if constexpr (EPL == 4) {
+                const float4 v = *reinterpret_cast<const float4*>(src);
+                acc[0] = fmaf(v.x, f, acc[0]);
+                acc[1] = fmaf(v.y, f, acc[1]);
+                acc[2] = fmaf(v.z, f, acc[2]);
+                acc[3] = fmaf(v.w, f, acc[3]);
+            } else {
 #pragma unroll
-        for (int e = 0; e < EPL; ++e)
-            io_t<IO>::st(o, (((size_t)b * T + x) * c.Hq + h) * D + lane + 32 * e, acc[e]);
+                for (int e = 0; e < EPL; ++e) acc[e] = fmaf(src[e], f, acc[e]);
+            }
+        }
+        const float inv = 1.0f / den;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] *= inv;
     }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e)
+        io_t<IO>::st(o, (((size_t)b * T + x) * c.Hq + h) * D + lane * EPL + e, acc[e]);
 }
 
 template <int IO, int D>
@@ -159,13 +173,19 @@ cudaError_t launch_simt(const spec_cfg& c, const spec_tree& t, const void* q, co
                         void* o, void* ws, cudaStream_t st) {
     using E = typename io_t<IO>::T;
     const WsLayout w = ws_layout(c);
-    attn_partial_simt<IO, D><<<dim3(w.n_chunks, c.Hkv, c.B), NT, 0, st>>>(
-        c, t, static_cast<const E*>(q), static_cast<const E*>(kt), static_cast<const E*>(vt),
-        static_cast<const E*>(kc), static_cast<const E*>(vc), kv_len, ws, w);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e;
+    if (attn_tc_supported(c)) {
+        e = launch_attn_tc(c, t, q, kt, vt, kc, vc, kv_len, ws, w, st);
+    } else {
+        attn_partial_simt<IO, D><<<dim3(w.n_chunks, c.Hkv, c.B), NT, 0, st>>>(
+            c, t, static_cast<const E*>(q), static_cast<const E*>(kt), static_cast<const E*>(vt),
+            static_cast<const E*>(kc), static_cast<const E*>(vc), kv_len, ws, w);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
-    attn_merge<IO, D><<<dim3(w.n_mt, c.Hkv, c.B), NT, 0, st>>>(c, t, kv_len, ws, w,
-                                                              static_cast<E*>(o));
+    const int G = c.Hq / c.Hkv;
+    attn_merge<IO, D><<<dim3((G * (c.N + 1) + NW - 1) / NW, c.Hkv, c.B), NT, 0, st>>>(
+        c, t, kv_len, ws, w, static_cast<E*>(o));
     return cudaGetLastError();
 }
 

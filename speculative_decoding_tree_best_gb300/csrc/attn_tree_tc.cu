@@ -1,0 +1,416 @@
+// attn_tree_tc.cu -- tensor-core (tcgen05) split-KV partial for tree attention,
+// bf16 I/O, head dim 128.
+//
+// Digest "SpecPilot ...": prerequisites / draft-tree verification (one target
+// pass verifies the tree; every node sees only its ancestors).
+//
+// One CTA = one (request, kv-head, 128-row query tile, key chunk).  The query
+// tile holds the G = Hq/Hkv q-heads of the group for 128/G consecutive tree
+// rows (row r = node * G + head_in_group), loaded once by TMA.  The chunk's
+// keys stream through a two-stage ring of 128-key K/V blocks (TMA, 128-byte
+// swizzle).  Per block:
+//    S = Q K^T              tcgen05.mma, A and B K-major, fp32 in tensor memory
+//    P = exp2(S*c - m)      one thread per row reads S from tensor memory
+//    O += P_hi V + P_lo V   tcgen05.mma, V MN-major; P is split into two bf16
+//                           terms (P_hi = bf16(P), P_lo = bf16(P - P_hi)) so the
+//                           probabilities keep ~16 significant bits: a single
+//                           bf16 P would cost ~1.7e-3 relative error on O.
+// The running maximum is only raised (and O rescaled in tensor memory) when a
+// block's maximum exceeds it by more than 2^8, so P <= 256 and O is rarely
+// touched.  Warp roles: warp 0 issues TMA, warp 1 issues MMAs (one thread
+// each), warps 2-5 run the softmax (tensor-memory lane = query row).  The
+// partial (O, max, sum) goes to the workspace; attn_merge combines chunks.
+//
+// The cache chunks read nothing from the tree; only the tree chunk (the T
+// tree rows as keys, masked by the ancestor bitmasks) does.
+//
+// Every mbarrier wait is bounded (about one second): on timeout the CTA raises
+// SPEC_DEV_TIMEOUT, every role unwinds, and tensor memory is freed.
+#include <cuda.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_util.cuh"
+
+namespace spec {
+
+namespace {
+
+using namespace tc;
+
+constexpr int NB = 128;             // keys per block
+constexpr int BM = 128;             // query rows per tile
+constexpr int HD = 128;             // head dim
+constexpr int NTHREADS = 192;
+constexpr uint32_t TILE_BYTES = 128 * 128 * 2;   // one 128 x 128 bf16 tile (two 64-wide halves)
+constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;
+
+// shared-memory map (offsets from the 1024-aligned base)
+constexpr uint32_t OFF_Q = 0;
+constexpr uint32_t OFF_KV = OFF_Q + TILE_BYTES;                  // 2 stages x (K, V)
+constexpr uint32_t OFF_PHI = OFF_KV + 4 * TILE_BYTES;
+constexpr uint32_t OFF_PLO = OFF_PHI + TILE_BYTES;
+constexpr uint32_t OFF_BAR = OFF_PLO + TILE_BYTES;
+constexpr int NBARS = 11;
+constexpr uint32_t SMEM_BYTES = OFF_BAR + NBARS * 8 + 32 + 1024;  // + slack for alignment
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+
+enum { B_Q = 0, B_KF0, B_KF1, B_VF0, B_VF1, B_EMP0, B_EMP1, B_SFULL, B_SFREE, B_PFULL, B_PVDONE };
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+struct TcParams {
+    spec_cfg c;
+    spec_tree tree;
+    const int32_t* kv_len;
+    void* ws;
+    WsLayout w;
+};
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mkc,
+                const __grid_constant__ CUtensorMap mvc, const __grid_constant__ CUtensorMap mkt,
+                const __grid_constant__ CUtensorMap mvt, const TcParams prm) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + NBARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* issued = reinterpret_cast<int*>(tmem_slot + 2);         // K/V blocks the producer issued
+
+    const spec_cfg& c = prm.c;
+    const WsLayout& w = prm.w;
+    const int T = c.N + 1, G = c.Hq / c.Hkv;
+    const int ch = blockIdx.x, g = blockIdx.y % c.Hkv, mt = blockIdx.y / c.Hkv, b = blockIdx.z;
+    const bool tree_chunk = ch == w.n_split;
+    int L = prm.kv_len[b];
+    L = L < 0 ? 0 : (L > c.Lmax ? c.Lmax : L);
+    int k0 = 0, k1 = T;
+    if (!tree_chunk) {
+        k0 = ch * w.chunk;
+        if (k0 >= L) return;                       // whole CTA idle: nothing allocated yet
+        k1 = min(k0 + w.chunk, L);
+    }
+    const int nblk = (k1 - k0 + NB - 1) / NB;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bar[B_Q], 1);
+        mbar_init(&bar[B_KF0], 1);
+        mbar_init(&bar[B_KF1], 1);
+        mbar_init(&bar[B_VF0], 1);
+        mbar_init(&bar[B_VF1], 1);
+        mbar_init(&bar[B_EMP0], 1);
+        mbar_init(&bar[B_EMP1], 1);
+        mbar_init(&bar[B_SFULL], 1);
+        mbar_init(&bar[B_SFREE], 128);
+        mbar_init(&bar[B_PFULL], 128);
+        mbar_init(&bar[B_PVDONE], 1);
+        *abort_flag = 0;
+        *issued = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&mq);
+        tma_prefetch_desc(tree_chunk ? &mkt : &mkc);
+        tma_prefetch_desc(tree_chunk ? &mvt : &mvc);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, 256);
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tS = tmem, tO = tmem + 128;
+    bool ok = true;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bar[B_Q], TILE_BYTES);
+            const int node0 = mt * (BM / G);
+            for (int h = 0; h < 2; ++h)
+                tma_load_3d(sm + OFF_Q + h * HALF_BYTES, &mq, &bar[B_Q], h * 64, g * G,
+                            b * T + node0);
+            const CUtensorMap* mk = tree_chunk ? &mkt : &mkc;
+            const CUtensorMap* mv = tree_chunk ? &mvt : &mvc;
+            for (int j = 0; j < nblk && ok; ++j) {
+                const int s = j & 1;
+                if (j >= 2 && !mbar_wait(&bar[B_EMP0 + s], ((j >> 1) - 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int key0 = k0 + j * NB;
+                unsigned char* ks = sm + OFF_KV + s * 2 * TILE_BYTES;
+                unsigned char* vs = ks + TILE_BYTES;
+                mbar_arrive_expect_tx(&bar[B_KF0 + s], TILE_BYTES);
+                for (int h = 0; h < 2; ++h)
+                    tma_load_4d(ks + h * HALF_BYTES, mk, &bar[B_KF0 + s], h * 64, g, key0, b);
+                mbar_arrive_expect_tx(&bar[B_VF0 + s], TILE_BYTES);
+                for (int h = 0; h < 2; ++h)
+                    tma_load_4d(vs + h * HALF_BYTES, mv, &bar[B_VF0 + s], h * 64, g, key0, b);
+                *issued = j + 1;
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idS = idesc_bf16_f32(128, NB, false, false);
+            const uint32_t idPV = idesc_bf16_f32(128, HD, false, true);
+            const uint32_t q_s = smem_u32(sm + OFF_Q);
+            const uint32_t phi_s = smem_u32(sm + OFF_PHI), plo_s = smem_u32(sm + OFF_PLO);
+            ok = mbar_wait(&bar[B_Q], 0, abort_flag);
+            for (int j = 0; j < nblk && ok; ++j) {
+                const int s = j & 1;
+                const uint32_t ps = (j >> 1) & 1;
+                const uint32_t k_s = smem_u32(sm + OFF_KV + s * 2 * TILE_BYTES);
+                const uint32_t v_s = k_s + TILE_BYTES;
+                if (!mbar_wait(&bar[B_KF0 + s], ps, abort_flag)) { ok = false; break; }
+                if (j >= 1 && !mbar_wait(&bar[B_SFREE], (j - 1) & 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < HD / 16; ++k) {
+                    const uint32_t off = (k >> 2) * HALF_BYTES + (k & 3) * 32;
+                    mma_bf16(tS, sdesc_sw128(q_s + off, 16, 1024), sdesc_sw128(k_s + off, 16, 1024),
+                             idS, k > 0);
+                }
+                mma_commit(&bar[B_SFULL]);
+                if (!mbar_wait(&bar[B_PFULL], j & 1, abort_flag)) { ok = false; break; }
+                if (!mbar_wait(&bar[B_VF0 + s], ps, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < NB / 16; ++k) {
+                    const uint32_t offp = (k >> 2) * HALF_BYTES + (k & 3) * 32;
+                    mma_bf16(tO, sdesc_sw128(phi_s + offp, 16, 1024),
+                             sdesc_sw128(v_s + k * 2048, HALF_BYTES, 1024), idPV, (j > 0 || k > 0));
+                }
+#pragma unroll
+                for (int k = 0; k < NB / 16; ++k) {
+                    const uint32_t offp = (k >> 2) * HALF_BYTES + (k & 3) * 32;
+                    mma_bf16(tO, sdesc_sw128(plo_s + offp, 16, 1024),
+                             sdesc_sw128(v_s + k * 2048, HALF_BYTES, 1024), idPV, 1);
+                }
+                mma_commit(&bar[B_PVDONE]);
+                mma_commit(&bar[B_EMP0 + s]);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ softmax, one row per thread
+        const int lg = warp & 3;                         // tensor-memory lane group of this warp
+        const int row = lg * 32 + lane;
+        const int r = mt * BM + row;                     // query row within (request, kv-head)
+        const int x = r / G;
+        const uint32_t lane_addr = static_cast<uint32_t>(lg * 32) << 16;
+        uint64_t anc0 = 0, anc1 = 0;
+        int nn = T;
+        if (tree_chunk) {
+            nn = prm.tree.n_nodes[b];
+            nn = nn < 1 ? 1 : (nn > T ? T : nn);
+            if (x < nn) {
+                anc0 = prm.tree.node_anc[2 * ((size_t)b * T + x)];
+                anc1 = prm.tree.node_anc[2 * ((size_t)b * T + x) + 1];
+            }
+        }
+        const float sl2 = 1.4426950408889634f * rsqrtf((float)HD);   // log2(e) / sqrt(D)
+        float m_ref = -INFINITY, l = 0.0f;
+        unsigned char* phi = sm + OFF_PHI;
+        unsigned char* plo = sm + OFF_PLO;
+        float sv[NB];
+        for (int j = 0; j < nblk && ok; ++j) {
+            // results of waits are made warp-uniform: tcgen05.ld/st are warp-collective
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL], j & 1, abort_flag))) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < NB / 32; ++cc) tmem_ld32(tS + lane_addr + cc * 32, sv + cc * 32);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&bar[B_SFREE]);
+
+            const int key0 = k0 + j * NB;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < NB; ++i) {
+                bool vis;
+                if (tree_chunk) vis = i < nn && (((i < 64 ? anc0 : anc1) >> (i & 63)) & 1ull);
+                else vis = key0 + i < k1;
+                const float xv = vis ? sv[i] * sl2 : -INFINITY;
+                sv[i] = xv;
+                mx = fmaxf(mx, xv);
+            }
+            float factor = 1.0f;
+            bool rescale = false;
+            if (j == 0) {
+                m_ref = mx;
+            } else if (mx > m_ref + 8.0f) {
+                factor = (m_ref == -INFINITY) ? 0.0f : ex2(m_ref - mx);
+                m_ref = mx;
+                rescale = true;
+            }
+            const float mu = (m_ref == -INFINITY) ? 0.0f : m_ref;
+            l *= factor;
+            // P_j may only overwrite the P buffers once the PV MMAs of block j-1 are done
+            if (j >= 1) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&bar[B_PVDONE], (j - 1) & 1, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            if (__any_sync(0xffffffffu, rescale)) {
+                float ov[32];
+#pragma unroll
+                for (int cc = 0; cc < HD / 32; ++cc) {
+                    tmem_ld32(tO + lane_addr + cc * 32, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] *= factor;
+                    tmem_st32(tO + lane_addr + cc * 32, ov);
+                }
+                tmem_wait_st();
+            }
+#pragma unroll
+            for (int cb = 0; cb < NB / 8; ++cb) {          // 16-byte chunks of 8 keys
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float p0 = ex2(sv[cb * 8 + 2 * e] - mu);
+                    const float p1 = ex2(sv[cb * 8 + 2 * e + 1] - mu);
+                    l += p0 + p1;
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+                    const float2 hf = __bfloat1622float2(h2);
+                    const __nv_bfloat162 l2 = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
+                    hw[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                    lw[e] = *reinterpret_cast<const uint32_t*>(&l2);
+                }
+                const uint32_t off = (cb >> 3) * HALF_BYTES + sw128_offset(row, (cb & 7) * 8);
+                *reinterpret_cast<uint4*>(phi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(plo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bar[B_PFULL]);
+        }
+        if (ok && !__all_sync(0xffffffffu, mbar_wait(&bar[B_PVDONE], (nblk - 1) & 1, abort_flag)))
+            ok = false;
+        if (ok) {
+            tc_fence_after();
+            float* wO = ws_ptr<float>(prm.ws, w.attn_o_off);
+            float2* wML = ws_ptr<float2>(prm.ws, w.attn_ml_off);
+            const size_t tile = (((size_t)b * c.Hkv + g) * w.n_mt + mt) * w.n_chunks + ch;
+            float ov[32];
+#pragma unroll
+            for (int cc = 0; cc < HD / 32; ++cc) {
+                tmem_ld32(tO + lane_addr + cc * 32, ov);
+                tmem_wait_ld();
+                if (r < G * T) {
+                    float4* dst = reinterpret_cast<float4*>(wO + (tile * BM + row) * HD + cc * 32);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
+                }
+            }
+            if (r < G * T)
+                wML[tile * BM + row] = make_float2(m_ref * 0.6931471805599453f, l);
+        }
+    }
+
+    if (!ok) {
+        *abort_flag = 1;
+        raise_status(prm.ws, SPEC_DEV_TIMEOUT);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) {
+        // let the TMA copies still in flight land before the CTA's shared memory
+        // is released: wait (bounded) on the phases of the last issued blocks
+        int never = 0;
+        mbar_wait(&bar[B_Q], 0, &never);
+        for (int j = max(0, *issued - 2); j < *issued; ++j) {
+            mbar_wait(&bar[B_KF0 + (j & 1)], (j >> 1) & 1, &never);
+            mbar_wait(&bar[B_VF0 + (j & 1)], (j >> 1) & 1, &never);
+        }
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// bf16 tensor map over `rank` dims (innermost first), box {64, box1, box2, 1}.
+bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+              const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
+               strides_bytes, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool attn_tc_supported(const spec_cfg& c) {
+    const int G = c.Hq / c.Hkv;
+    return c.io_dtype == SPEC_IO_BF16 && c.D == HD && G >= 1 && G <= BM && (BM % G) == 0 &&
+           c.N + 1 <= NB && encode_fn() != nullptr;
+}
+
+cudaError_t launch_attn_tc(const spec_cfg& c, const spec_tree& t, const void* q,
+                           const void* k_tree, const void* v_tree, const void* k_cache,
+                           const void* v_cache, const int32_t* kv_len, void* ws,
+                           const WsLayout& w, cudaStream_t st) {
+    const int T = c.N + 1, G = c.Hq / c.Hkv;
+    const cuuint64_t e = 2;   // bytes per bf16
+    CUtensorMap mq, mkc, mvc, mkt, mvt;
+    {
+        cuuint64_t dims[3] = {(cuuint64_t)HD, (cuuint64_t)c.Hq, (cuuint64_t)c.B * T};
+        cuuint64_t str[2] = {HD * e, (cuuint64_t)c.Hq * HD * e};
+        cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(BM / G)};
+        if (!make_map(&mq, q, 3, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    {
+        cuuint64_t dims[4] = {(cuuint64_t)HD, (cuuint64_t)c.Hkv, (cuuint64_t)c.Lmax, (cuuint64_t)c.B};
+        cuuint64_t str[3] = {HD * e, (cuuint64_t)c.Hkv * HD * e, (cuuint64_t)c.Lmax * c.Hkv * HD * e};
+        cuuint32_t box[4] = {64, 1, NB, 1};
+        if (!make_map(&mkc, k_cache, 4, dims, str, box)) return cudaErrorInvalidValue;
+        if (!make_map(&mvc, v_cache, 4, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    {
+        cuuint64_t dims[4] = {(cuuint64_t)HD, (cuuint64_t)c.Hkv, (cuuint64_t)T, (cuuint64_t)c.B};
+        cuuint64_t str[3] = {HD * e, (cuuint64_t)c.Hkv * HD * e, (cuuint64_t)T * c.Hkv * HD * e};
+        cuuint32_t box[4] = {64, 1, NB, 1};
+        if (!make_map(&mkt, k_tree, 4, dims, str, box)) return cudaErrorInvalidValue;
+        if (!make_map(&mvt, v_tree, 4, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    TcParams prm{c, t, kv_len, ws, w};
+    cudaError_t err = cudaFuncSetAttribute(attn_tc_partial,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    dim3 grid(w.n_chunks, c.Hkv * w.n_mt, c.B);
+    attn_tc_partial<<<grid, NTHREADS, SMEM_BYTES, st>>>(mq, mkc, mvc, mkt, mvt, prm);
+    return cudaGetLastError();
+}
+
+}  // namespace spec

@@ -58,19 +58,20 @@ struct WsLayout {
 
 static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Cache rows per chunk: enough chunks that B x Hkv x tiles x chunks fills the
-// 152 SMs about twice, each chunk a multiple of 128 rows.
+// Cache rows per chunk: about one CTA per SM over B x Hkv x tiles x chunks
+// for small problems, chunks of 256 to 1024 rows (multiples of 128).
 static inline WsLayout ws_layout(const spec_cfg& c, int num_sms = 152) {
     WsLayout w{};
     const int T = c.N + 1;
     const int G = c.Hq / c.Hkv;
     w.n_mt = (G * T + 127) / 128;
     const long units = (long)c.B * c.Hkv * w.n_mt;
-    long want = (2L * num_sms + units - 1) / units;
+    long want = (num_sms + units - 1) / units;
     if (want < 1) want = 1;
     long chunk = (c.Lmax + want - 1) / want;
     chunk = (chunk + 127) / 128 * 128;
-    if (chunk < 128) chunk = 128;
+    if (chunk < 256) chunk = 256;
+    if (chunk > 1024) chunk = 1024;
     w.chunk = (int)chunk;
     w.n_split = (int)((c.Lmax + chunk - 1) / chunk);
     if (w.n_split < 1) w.n_split = 1;

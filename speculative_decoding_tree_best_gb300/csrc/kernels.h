@@ -24,6 +24,12 @@ cudaError_t launch_attn_tree(const spec_cfg& c, const spec_tree& t, const void* 
                              const void* v_cache, const int32_t* kv_len, void* o, void* ws,
                              cudaStream_t st);
 
+bool attn_tc_supported(const spec_cfg& c);
+cudaError_t launch_attn_tc(const spec_cfg& c, const spec_tree& t, const void* q,
+                           const void* k_tree, const void* v_tree, const void* k_cache,
+                           const void* v_cache, const int32_t* kv_len, void* ws,
+                           const WsLayout& w, cudaStream_t st);
+
 cudaError_t launch_accept_commit(const spec_cfg& c, const spec_tree& t, const void* logits,
                                  const spec_commit_io& io, const spec_accept& out, void* ws,
                                  cudaStream_t st);

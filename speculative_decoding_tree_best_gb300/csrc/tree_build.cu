@@ -53,16 +53,22 @@ tree_build_kernel(spec_cfg c, const int32_t* __restrict__ lat_tok,
     int32_t* n_rank = n_dep + T;
     int32_t* n_next = n_rank + T;                                  // next child rank to offer
     float* n_sc = reinterpret_cast<float*>(n_next + T);
+    int32_t* r_tok = reinterpret_cast<int32_t*>(n_sc + T);          // [m][K] as given
+    float* r_sc = reinterpret_cast<float*>(r_tok + m * K);          // [m][K] as given
 
-    // ---- 1. rank every position ----------------------------------------------
+    // ---- 1. stage the lattice (one round trip), then rank every position -------
+    for (int i = lane; i < m * K; i += kWarp) {
+        r_tok[i] = lat_tok[(size_t)b * m * K + i];
+        r_sc[i] = lat_score[(size_t)b * m * K + i];
+    }
+    __syncwarp();
     bool bad = false;
     for (int s = 0; s < m; ++s) {
-        const size_t base = ((size_t)b * m + s) * K;
         int tok = 0;
         float sc = 0.0f;
         if (lane < K) {
-            tok = lat_tok[base + lane];
-            sc = lat_score[base + lane];
+            tok = r_tok[s * K + lane];
+            sc = r_sc[s * K + lane];
             bad |= (sc != sc);
         }
         int rank = 0;
@@ -155,7 +161,7 @@ tree_build_kernel(spec_cfg c, const int32_t* __restrict__ lat_tok,
 
 size_t tree_build_smem(const spec_cfg& c) {
     const int T = c.N + 1;
-    return sizeof(uint64_t) * 2 * T + (sizeof(int32_t) + sizeof(float)) * (size_t)c.m * c.K +
+    return sizeof(uint64_t) * 2 * T + 2 * (sizeof(int32_t) + sizeof(float)) * (size_t)c.m * c.K +
            (5 * sizeof(int32_t) + sizeof(float)) * (size_t)T;
 }
 
