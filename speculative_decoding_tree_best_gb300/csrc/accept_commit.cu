@@ -6,14 +6,15 @@
 // tau in [1, m+1]), prerequisites / draft-tree verification (longest matching
 // root path) and technical novelty (states recomputed along the root path).
 //
-// Three launches:
-//  1. argmax_partial: every logits row is cut into `argmax_split` segments;
-//     a CTA scans one segment with 16-byte loads and reduces (value desc,
-//     index asc) with warp shuffles.
-//  2. accept: one warp per request reduces the segments of each row, walks
-//     the tree with ballots over the children, writes the outputs, checks the
-//     cache room and advances kv_len / root_tok.
-//  3. commit: GDN blocks apply the accepted rows' gated-delta steps to 32
+// Two launches:
+//  1. argmax_accept: every logits row is cut into `argmax_split` segments;
+//     a CTA scans one segment with 16-byte loads (eight in flight per thread)
+//     and reduces (value desc, index asc) with warp shuffles.  The last CTA to
+//     finish a request (atomic ticket) runs its acceptance with one warp:
+//     reduce the segments of each row, walk the tree with ballots over the
+//     children, write the outputs, check the cache room and advance kv_len /
+//     root_tok.
+//  2. commit: GDN blocks apply the accepted rows' gated-delta steps to 32
 //     columns of a state each (literal recurrence, fp32, the state slice held
 //     in registers); KV blocks copy the accepted tree K/V rows into the cache.
 #include <math.h>
@@ -31,73 +32,11 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
     return v > bv || (v == bv && i < bi);
 }
 
-template <int IO>
-__global__ void __launch_bounds__(NT)
-argmax_partial(spec_cfg c, const typename io_t<IO>::T* __restrict__ logits,
-               const int32_t* __restrict__ n_nodes, void* ws, WsLayout w) {
-    using E = typename io_t<IO>::T;
-    constexpr int VEC = 16 / sizeof(E);
-    const int sp = blockIdx.x, row = blockIdx.y;
-    const int T = c.N + 1, b = row / T, t = row % T;
-    if (t >= n_nodes[b] || t >= T) return;
-    const int V = c.V;
-    int seg = (V + w.argmax_split - 1) / w.argmax_split;
-    seg = (seg + VEC - 1) / VEC * VEC;
-    const int lo = sp * seg, hi = min(V, lo + seg);
-    const E* rp = logits + (size_t)row * V;
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    const bool vec_ok = (V % VEC) == 0 && ((reinterpret_cast<uintptr_t>(rp) & 15) == 0);
-    if (vec_ok) {
-        // four 16-byte loads in flight per thread per iteration
-        constexpr int U = 4;
-        for (int e0 = lo + threadIdx.x * VEC; e0 < hi; e0 += U * NT * VEC) {
-            uint4 u[U];
-#pragma unroll
-            for (int k = 0; k < U; ++k) {
-                const int ek = e0 + k * NT * VEC;
-                u[k] = ek < hi ? *reinterpret_cast<const uint4*>(rp + ek) : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int k = 0; k < U; ++k) {
-                const int ek = e0 + k * NT * VEC;
-                const E* ev = reinterpret_cast<const E*>(&u[k]);
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const float x = io_t<IO>::ld(ev, e);
-                    if (ek < hi && x > bv) { bv = x; bi = ek + e; }
-                }
-            }
-        }
-    } else {
-        for (int e = lo + threadIdx.x; e < hi; e += NT) {
-            const float x = io_t<IO>::ld(rp, e);
-            if (x > bv) { bv = x; bi = e; }
-        }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-    }
-    __shared__ float sv[NT / 32];
-    __shared__ int si[NT / 32];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (lane == 0) { sv[warp] = bv; si[warp] = bi; }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        for (int k = 1; k < NT / 32; ++k)
-            if (better(sv[k], si[k], bv, bi)) { bv = sv[k]; bi = si[k]; }
-        float2* out = ws_ptr<float2>(ws, w.argmax_off);
-        out[(size_t)row * kArgmaxSplit + sp] = make_float2(bv, __int_as_float(bi));
-    }
-}
-
-__global__ void __launch_bounds__(32)
-accept_kernel(spec_cfg c, spec_tree tree, spec_commit_io io, spec_accept out, void* ws, WsLayout w) {
-    extern __shared__ int sa[];
-    const int T = c.N + 1, m = c.m, b = blockIdx.x, lane = threadIdx.x;
+// Acceptance of request b by one warp (lanes 0-31 of the calling CTA).
+__device__ void accept_request(const spec_cfg& c, const spec_tree& tree, const spec_commit_io& io,
+                               const spec_accept& out, void* ws, const WsLayout& w, int b) {
+    __shared__ int sa[3 * SPEC_MAX_ROWS + SPEC_MAX_M + 1];
+    const int T = c.N + 1, m = c.m, lane = threadIdx.x;
     int* am = sa;            // [T]
     int* tok = am + T;       // [T]
     int* par = tok + T;      // [T]
@@ -165,6 +104,93 @@ accept_kernel(spec_cfg c, spec_tree tree, spec_commit_io io, spec_accept out, vo
     }
 }
 
+// (max, first index) of logits row `row` over the segment [lo, hi), reduced
+// over the CTA; valid in thread 0.
+template <int IO>
+__device__ void scan_segment(const typename io_t<IO>::T* __restrict__ rp, int V, int lo, int hi,
+                             float& bv, int& bi) {
+    using E = typename io_t<IO>::T;
+    constexpr int VEC = 16 / sizeof(E);
+    bv = -INFINITY;
+    bi = 0x7fffffff;
+    const bool vec_ok = (V % VEC) == 0 && ((reinterpret_cast<uintptr_t>(rp) & 15) == 0);
+    if (vec_ok) {
+        constexpr int U = 8;                  // 16-byte loads in flight per thread
+        for (int e0 = lo + threadIdx.x * VEC; e0 < hi; e0 += U * NT * VEC) {
+            uint4 u[U];
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const int ek = e0 + k * NT * VEC;
+                u[k] = ek < hi ? *reinterpret_cast<const uint4*>(rp + ek) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const int ek = e0 + k * NT * VEC;
+                const E* ev = reinterpret_cast<const E*>(&u[k]);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const float x = io_t<IO>::ld(ev, e);
+                    if (ek < hi && x > bv) { bv = x; bi = ek + e; }
+                }
+            }
+        }
+    } else {
+        for (int e = lo + threadIdx.x; e < hi; e += NT) {
+            const float x = io_t<IO>::ld(rp, e);
+            if (x > bv) { bv = x; bi = e; }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+    }
+    __shared__ float sv[NT / 32];
+    __shared__ int si[NT / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) { sv[warp] = bv; si[warp] = bi; }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        for (int k = 1; k < NT / 32; ++k)
+            if (better(sv[k], si[k], bv, bi)) { bv = sv[k]; bi = si[k]; }
+}
+
+template <int IO>
+__global__ void __launch_bounds__(NT)
+argmax_accept(spec_cfg c, const typename io_t<IO>::T* __restrict__ logits, spec_tree tree,
+              spec_commit_io io, spec_accept acc, void* ws, WsLayout w) {
+    using E = typename io_t<IO>::T;
+    constexpr int VEC = 16 / sizeof(E);
+    const int sp = blockIdx.x, row = blockIdx.y;
+    const int T = c.N + 1, b = row / T, t = row % T;
+    if (t < tree.n_nodes[b]) {                           // CTA-uniform
+        int seg = (c.V + w.argmax_split - 1) / w.argmax_split;
+        seg = (seg + VEC - 1) / VEC * VEC;
+        const int lo = sp * seg, hi = min(c.V, lo + seg);
+        float bv;
+        int bi;
+        scan_segment<IO>(logits + (size_t)row * c.V, c.V, lo, hi, bv, bi);
+        if (threadIdx.x == 0)
+            ws_ptr<float2>(ws, w.argmax_off)[(size_t)row * kArgmaxSplit + sp] =
+                make_float2(bv, __int_as_float(bi));
+    }
+    // Every CTA of the request takes a ticket; the last one runs the acceptance.
+    __shared__ bool last;
+    if (threadIdx.x == 0) {
+        __threadfence();
+        unsigned int* tk = ws_ptr<unsigned int>(ws, w.acc_ticket_off) + b;
+        const unsigned int done = atomicAdd(tk, 1u);
+        last = done == (unsigned int)(T * w.argmax_split) - 1u;
+        if (last) *tk = 0u;                 // leave the ticket at zero for the next call
+    }
+    __syncthreads();
+    if (last && threadIdx.x < 32) {
+        __threadfence();
+        accept_request(c, tree, io, acc, ws, w, b);
+    }
+}
+
 template <int IO, int DK>
 __global__ void __launch_bounds__(NT)
 commit_kernel(spec_cfg c, spec_commit_io io, spec_accept acc, void* ws, WsLayout w, int gdn_blocks) {
@@ -181,9 +207,14 @@ commit_kernel(spec_cfg c, spec_commit_io io, spec_accept acc, void* ws, WsLayout
         const int j = id % c.Hv; id /= c.Hv;
         const int b = id % c.B;
         const int layer = id / c.B;
+        const int ih = j / (c.Hv / c.Hk), c0 = cb * CB, col = tid & 31, grp = tid >> 5;
+        // the state slice does not depend on the acceptance: load it first
+        float* h = io.h0 + (size_t)layer * c.B * c.Hv * DK * c.dv + ((size_t)b * c.Hv + j) * DK * c.dv;
+        float hr[RPT];
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) hr[i] = h[(size_t)(grp * RPT + i) * c.dv + c0 + col];
         const int tau = plan[4 * b];
         if (tau == 0) return;
-        const int ih = j / (c.Hv / c.Hk), c0 = cb * CB, col = tid & 31, grp = tid >> 5;
         float* ks = sc;                     // [tau][DK]
         float* vsm = ks + (m + 1) * DK;     // [tau][CB]
         float* ab = vsm + (m + 1) * CB;     // [tau][2]
@@ -206,10 +237,6 @@ commit_kernel(spec_cfg c, spec_commit_io io, spec_accept acc, void* ws, WsLayout
             ab[2 * s] = al[((size_t)b * T + x) * c.Hv + j];
             ab[2 * s + 1] = be[((size_t)b * T + x) * c.Hv + j];
         }
-        float* h = io.h0 + (size_t)layer * c.B * c.Hv * DK * c.dv + ((size_t)b * c.Hv + j) * DK * c.dv;
-        float hr[RPT];
-#pragma unroll
-        for (int i = 0; i < RPT; ++i) hr[i] = h[(size_t)(grp * RPT + i) * c.dv + c0 + col];
         __syncthreads();
         for (int s = 0; s < tau; ++s) {
             const float* kk = ks + s * DK + grp * RPT;
@@ -275,14 +302,10 @@ cudaError_t launch_accept_commit(const spec_cfg& c, const spec_tree& t, const vo
     const int T = c.N + 1;
     dim3 g1(w.argmax_split, c.B * T);
     if (c.io_dtype == SPEC_IO_BF16)
-        argmax_partial<SPEC_IO_BF16><<<g1, NT, 0, st>>>(c, static_cast<const __nv_bfloat16*>(logits), t.n_nodes, ws, w);
+        argmax_accept<SPEC_IO_BF16><<<g1, NT, 0, st>>>(c, static_cast<const __nv_bfloat16*>(logits), t, io, out, ws, w);
     else
-        argmax_partial<SPEC_IO_F32><<<g1, NT, 0, st>>>(c, static_cast<const float*>(logits), t.n_nodes, ws, w);
+        argmax_accept<SPEC_IO_F32><<<g1, NT, 0, st>>>(c, static_cast<const float*>(logits), t, io, out, ws, w);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const size_t smem = sizeof(int) * (3 * (size_t)T + c.m + 1);
-    accept_kernel<<<c.B, 32, smem, st>>>(c, t, io, out, ws, w);
-    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (c.io_dtype == SPEC_IO_BF16)
         return c.dk == 128 ? launch_commit<SPEC_IO_BF16, 128>(c, io, out, ws, w, st)

@@ -16,6 +16,7 @@
 //
 // This file holds the SIMT partial (fp32 I/O and head dim 64) and the merge;
 // attn_tree_tc.cu holds the tcgen05 partial used for bf16 I/O, head dim 128.
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "common.cuh"
@@ -52,7 +53,8 @@ attn_partial_simt(spec_cfg c, spec_tree tree, const typename io_t<IO>::T* __rest
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float scale = rsqrtf((float)D);
-    float* wO = ws_ptr<float>(ws, w.attn_o_off);
+    using PT = typename io_t<IO>::PT;
+    PT* wO = ws_ptr<PT>(ws, w.attn_o_off);
     float2* wML = ws_ptr<float2>(ws, w.attn_ml_off);
 
     for (int r = warp; r < G * nn; r += NW) {
@@ -96,21 +98,47 @@ attn_partial_simt(spec_cfg c, spec_tree tree, const typename io_t<IO>::T* __rest
         }
         const int mt = r / 128, rr = r % 128;
         const size_t tile = (((size_t)b * Hkv + g) * w.n_mt + mt) * w.n_chunks + ch;
+        const float inv = sum > 0.0f ? 1.0f / sum : 0.0f;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) wO[(tile * 128 + rr) * D + lane * EPL + e] = acc[e];
+        for (int e = 0; e < EPL; ++e) wO[(tile * 128 + rr) * D + lane * EPL + e] = static_cast<PT>(acc[e] * inv);
         if (lane == 0) wML[tile * 128 + rr] = make_float2(mx, sum);
     }
 }
 
-// One warp per query row (8 rows per CTA).  Pass 1: lane i reads the (max,
-// sum) of chunk i and the warp reduces them to the common maximum and the
-// denominator.  Pass 2: lane i owns D/32 consecutive output columns and sums
-// the chunks' rescaled partial rows.
+// One warp per query row (8 rows per CTA).  Each chunk left a normalised
+// row O_c / l_c (fp16 for bf16 I/O, fp32 for fp32 I/O) and its (max m_c,
+// sum l_c).  Lane i reads chunk i's
+// (m, l); the warp forms the weights w_c = l_c exp(m_c - M) / sum and every
+// lane sums its D/32 output columns over the chunks, all loads in flight.
+// EPL consecutive partial elements -> floats (one 8- or 16-byte load).
+template <int EPL>
+__device__ __forceinline__ void load_partial(const __half* p, float* f) {
+    if constexpr (EPL == 4) {
+        const uint2 u = *reinterpret_cast<const uint2*>(p);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+        f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    } else {
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(p));
+        f[0] = a.x; f[1] = a.y;
+    }
+}
+template <int EPL>
+__device__ __forceinline__ void load_partial(const float* p, float* f) {
+    if constexpr (EPL == 4) {
+        const float4 a = *reinterpret_cast<const float4*>(p);
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    } else {
+        const float2 a = *reinterpret_cast<const float2*>(p);
+        f[0] = a.x; f[1] = a.y;
+    }
+}
+
 template <int IO, int D>
 __global__ void __launch_bounds__(NT)
 attn_merge(spec_cfg c, spec_tree tree, const int32_t* __restrict__ kv_len, void* ws, WsLayout w,
            typename io_t<IO>::T* __restrict__ o) {
-    constexpr int EPL = D / 32;
+    constexpr int EPL = D / 32;              // output columns per lane (2 or 4)
     const int g = blockIdx.y, b = blockIdx.z;
     const int T = c.N + 1, G = c.Hq / c.Hkv;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -126,39 +154,50 @@ attn_merge(spec_cfg c, spec_tree tree, const int32_t* __restrict__ kv_len, void*
 #pragma unroll
     for (int e = 0; e < EPL; ++e) acc[e] = 0.0f;
     if (x < nn) {
-        const float* wO = ws_ptr<const float>(ws, w.attn_o_off);
+        using PT = typename io_t<IO>::PT;
+        const PT* wO = ws_ptr<const PT>(ws, w.attn_o_off);
         const float2* wML = ws_ptr<const float2>(ws, w.attn_ml_off);
         const size_t tile0 = (((size_t)b * c.Hkv + g) * w.n_mt + mt) * w.n_chunks;
         // chunks holding keys: cache chunks [0, n_cache) and the tree chunk n_split
         const int nch = n_cache + 1;
-        auto chunk_id = [&](int i) { return i < n_cache ? i : w.n_split; };
-        float M = -INFINITY;
-        for (int i = lane; i < nch; i += 32) M = fmaxf(M, wML[(tile0 + chunk_id(i)) * 128 + rr].x);
+        float m_run = -INFINITY, den_run = 0.0f;
+        for (int base = 0; base < nch; base += 32) {           // rounds of 32 chunks
+            const int i = base + lane;
+            const int ci = i < n_cache ? i : w.n_split;
+            const float2 ml = i < nch ? wML[(tile0 + ci) * 128 + rr] : make_float2(-INFINITY, 0.0f);
+            float M = ml.x;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        float den = 0.0f;
-        for (int i = lane; i < nch; i += 32) {
-            const float2 ml = wML[(tile0 + chunk_id(i)) * 128 + rr];
-            den += ml.y * __expf(ml.x - M);
-        }
-        den = warp_sum(den);
-#pragma unroll 6
-        for (int i = 0; i < nch; ++i) {
-            const size_t t = tile0 + chunk_id(i);
-            const float f = __expf(wML[t * 128 + rr].x - M);
-            const float* src = wO + (t * 128 + rr) * D + lane * EPL;
-            if constexpr (EPL == 4) {
-                const float4 v = *reinterpret_cast<const float4*>(src);
-                acc[0] = fmaf(v.x, f, acc[0]);
-                acc[1] = fmaf(v.y, f, acc[1]);
-                acc[2] = fmaf(v.z, f, acc[2]);
-                acc[3] = fmaf(v.w, f, acc[3]);
-            } else {
+            for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+            const float f = i < nch ? ml.y * __expf(ml.x - M) : 0.0f;   // unnormalised weight
+            const float den_r = warp_sum(f);
+            const int cnt = min(32, nch - base);
+            float gacc[EPL];
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) acc[e] = fmaf(src[e], f, acc[e]);
+            for (int e = 0; e < EPL; ++e) gacc[e] = 0.0f;
+            // all rows of this round in flight: predicated, fully unrolled
+            float raw[32][EPL];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const int ck = base + k < n_cache ? base + k : w.n_split;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) raw[k][e] = 0.0f;
+                if (k < cnt) load_partial<EPL>(wO + ((tile0 + ck) * 128 + rr) * D + lane * EPL, raw[k]);
             }
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const float fk = __shfl_sync(0xffffffffu, f, k);
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) gacc[e] = fmaf(raw[k][e], fk, gacc[e]);
+            }
+            const float m_new = fmaxf(m_run, M);
+            const float s_old = m_run == -INFINITY ? 0.0f : __expf(m_run - m_new);
+            const float s_new = __expf(M - m_new);
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc[e] = acc[e] * s_old + gacc[e] * s_new;
+            den_run = den_run * s_old + den_r * s_new;
+            m_run = m_new;
         }
-        const float inv = 1.0f / den;
+        const float inv = 1.0f / den_run;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) acc[e] *= inv;
     }

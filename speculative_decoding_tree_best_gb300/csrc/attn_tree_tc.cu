@@ -17,9 +17,11 @@
 //                           bf16 P would cost ~1.7e-3 relative error on O.
 // The running maximum is only raised (and O rescaled in tensor memory) when a
 // block's maximum exceeds it by more than 2^8, so P <= 256 and O is rarely
-// touched.  Warp roles: warp 0 issues TMA, warp 1 issues MMAs (one thread
-// each), warps 2-5 run the softmax (tensor-memory lane = query row).  The
-// partial (O, max, sum) goes to the workspace; attn_merge combines chunks.
+// touched.  The chunk's output is stored normalised (O / sum) in fp16 with its
+// (max, sum); |V| must stay below the fp16 range (65504).  Warp roles: warp 0 issues TMA, warp 1 issues MMAs (one thread
+// each), warps 2-17 run the softmax: four threads per query row (tensor-memory
+// lane = row), each owning 32 of the 128 key columns.  The partial
+// (O, max, sum) goes to the workspace; attn_merge combines chunks.
 //
 // The cache chunks read nothing from the tree; only the tree chunk (the T
 // tree rows as keys, masked by the ancestor bitmasks) does.
@@ -27,6 +29,7 @@
 // Every mbarrier wait is bounded (about one second): on timeout the CTA raises
 // SPEC_DEV_TIMEOUT, every role unwinds, and tensor memory is freed.
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "common.cuh"
@@ -42,7 +45,10 @@ using namespace tc;
 constexpr int NB = 128;             // keys per block
 constexpr int BM = 128;             // query rows per tile
 constexpr int HD = 128;             // head dim
-constexpr int NTHREADS = 192;
+constexpr int NWG = 4;              // softmax warpgroups: thread (wg, row) owns 32 key columns
+constexpr int CPT = 128 / NWG;      // key (and output) columns per softmax thread
+constexpr int NSOFT = 128 * NWG;    // softmax threads
+constexpr int NTHREADS = 64 + NSOFT;  // warp 0 TMA, warp 1 MMA, then the softmax warps
 constexpr uint32_t TILE_BYTES = 128 * 128 * 2;   // one 128 x 128 bf16 tile (two 64-wide halves)
 constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;
 
@@ -50,13 +56,31 @@ constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_KV = OFF_Q + TILE_BYTES;                  // 2 stages x (K, V)
 constexpr uint32_t OFF_PHI = OFF_KV + 4 * TILE_BYTES;
-constexpr uint32_t OFF_PLO = OFF_PHI + TILE_BYTES;
-constexpr uint32_t OFF_BAR = OFF_PLO + TILE_BYTES;
+// P_lo of block j is written into the K buffer of block j: S_j has consumed it,
+// and the stage is only refilled after the PV MMAs of block j complete.
+constexpr uint32_t OFF_RED = OFF_PHI + TILE_BYTES;               // float [2][NWG][128] row maxima
+constexpr uint32_t OFF_REDL = OFF_RED + 2 * NWG * 128 * 4;       // float [NWG][128] row sums
+constexpr uint32_t OFF_BAR = OFF_REDL + NWG * 128 * 4;
 constexpr int NBARS = 11;
 constexpr uint32_t SMEM_BYTES = OFF_BAR + NBARS * 8 + 32 + 1024;  // + slack for alignment
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 enum { B_Q = 0, B_KF0, B_KF1, B_VF0, B_VF1, B_EMP0, B_EMP1, B_SFULL, B_SFREE, B_PFULL, B_PVDONE };
+
+// Barrier over `nthreads` threads with id `id` that also ANDs a predicate, so
+// a pair of warps leaves a loop together.
+__device__ __forceinline__ bool bar_and(int id, int nthreads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -109,8 +133,8 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         mbar_init(&bar[B_EMP0], 1);
         mbar_init(&bar[B_EMP1], 1);
         mbar_init(&bar[B_SFULL], 1);
-        mbar_init(&bar[B_SFREE], 128);
-        mbar_init(&bar[B_PFULL], 128);
+        mbar_init(&bar[B_SFREE], NSOFT);
+        mbar_init(&bar[B_PFULL], NSOFT);
         mbar_init(&bar[B_PVDONE], 1);
         *abort_flag = 0;
         *issued = 0;
@@ -162,7 +186,7 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
             const uint32_t idS = idesc_bf16_f32(128, NB, false, false);
             const uint32_t idPV = idesc_bf16_f32(128, HD, false, true);
             const uint32_t q_s = smem_u32(sm + OFF_Q);
-            const uint32_t phi_s = smem_u32(sm + OFF_PHI), plo_s = smem_u32(sm + OFF_PLO);
+            const uint32_t phi_s = smem_u32(sm + OFF_PHI);
             ok = mbar_wait(&bar[B_Q], 0, abort_flag);
             for (int j = 0; j < nblk && ok; ++j) {
                 const int s = j & 1;
@@ -191,7 +215,7 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
 #pragma unroll
                 for (int k = 0; k < NB / 16; ++k) {
                     const uint32_t offp = (k >> 2) * HALF_BYTES + (k & 3) * 32;
-                    mma_bf16(tO, sdesc_sw128(plo_s + offp, 16, 1024),
+                    mma_bf16(tO, sdesc_sw128(k_s + offp, 16, 1024),
                              sdesc_sw128(v_s + k * 2048, HALF_BYTES, 1024), idPV, 1);
                 }
                 mma_commit(&bar[B_PVDONE]);
@@ -199,122 +223,166 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
             }
         }
     } else {
-        // ------------------------------------------------------------ softmax, one row per thread
-        const int lg = warp & 3;                         // tensor-memory lane group of this warp
+        // ------------------------------------------------------------ softmax
+        // Softmax warp sw = warp - 2: warpgroup wg = sw / 4 owns key (and
+        // output) columns [CPT wg, CPT wg + CPT) of row lg * 32 + lane, where
+        // lg = warp % 4 is the tensor-memory lane group the warp may access.
+        // The NWG threads of a row swap partial maxima through shared memory
+        // under a named barrier over the NWG warps of that lane group.
+        const int wg = (warp - 2) >> 2;
+        const int lg = warp & 3;
         const int row = lg * 32 + lane;
         const int r = mt * BM + row;                     // query row within (request, kv-head)
         const int x = r / G;
         const uint32_t lane_addr = static_cast<uint32_t>(lg * 32) << 16;
-        uint64_t anc0 = 0, anc1 = 0;
-        int nn = T;
+        const int cb0 = wg * CPT;                        // first column of this thread
+        const int grp_bar = 1 + lg;
+        constexpr int GRP_THREADS = 32 * NWG;
+        float* red = reinterpret_cast<float*>(sm + OFF_RED);
+        float* redl = reinterpret_cast<float*>(sm + OFF_REDL);
+        uint32_t visbits = 0xffffffffu;                  // tree chunk: visible keys among my columns
         if (tree_chunk) {
-            nn = prm.tree.n_nodes[b];
+            int nn = prm.tree.n_nodes[b];
             nn = nn < 1 ? 1 : (nn > T ? T : nn);
+            visbits = 0u;
             if (x < nn) {
-                anc0 = prm.tree.node_anc[2 * ((size_t)b * T + x)];
-                anc1 = prm.tree.node_anc[2 * ((size_t)b * T + x) + 1];
+                const uint64_t a = prm.tree.node_anc[2 * ((size_t)b * T + x) + (cb0 >> 6)];
+                visbits = static_cast<uint32_t>(a >> (cb0 & 63));
+                if (cb0 + CPT > nn) visbits &= (nn - cb0 <= 0) ? 0u : (0xffffffffu >> (32 - (nn - cb0)));
             }
         }
         const float sl2 = 1.4426950408889634f * rsqrtf((float)HD);   // log2(e) / sqrt(D)
-        float m_ref = -INFINITY, l = 0.0f;
+        float m_ref = -INFINITY, l = 0.0f;                // m_ref in raw score units
         unsigned char* phi = sm + OFF_PHI;
-        unsigned char* plo = sm + OFF_PLO;
-        float sv[NB];
-        for (int j = 0; j < nblk && ok; ++j) {
-            // results of waits are made warp-uniform: tcgen05.ld/st are warp-collective
-            if (!__all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL], j & 1, abort_flag))) { ok = false; break; }
-            tc_fence_after();
+        float sv[CPT];
+        for (int j = 0; j < nblk; ++j) {
+            bool w_ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL], j & 1, abort_flag));
+            float pm0 = -INFINITY, pm1 = -INFINITY, pm2 = -INFINITY, pm3 = -INFINITY;
+            if (w_ok) {
+                tc_fence_after();
+                tmem_ld32(tS + lane_addr + cb0, sv);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&bar[B_SFREE]);
+                // visibility: all columns of a full cache block are visible
+                uint32_t vis = visbits;
+                if (!tree_chunk) {
+                    const int nvis = k1 - (k0 + j * NB + cb0);
+                    vis = nvis >= CPT ? 0xffffffffu : (nvis <= 0 ? 0u : (0xffffffffu >> (32 - nvis)));
+                }
+                if (vis != 0xffffffffu) {
 #pragma unroll
-            for (int cc = 0; cc < NB / 32; ++cc) tmem_ld32(tS + lane_addr + cc * 32, sv + cc * 32);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&bar[B_SFREE]);
-
-            const int key0 = k0 + j * NB;
-            float mx = -INFINITY;
+                    for (int i = 0; i < CPT; ++i) sv[i] = ((vis >> i) & 1u) ? sv[i] : -INFINITY;
+                }
 #pragma unroll
-            for (int i = 0; i < NB; ++i) {
-                bool vis;
-                if (tree_chunk) vis = i < nn && (((i < 64 ? anc0 : anc1) >> (i & 63)) & 1ull);
-                else vis = key0 + i < k1;
-                const float xv = vis ? sv[i] * sl2 : -INFINITY;
-                sv[i] = xv;
-                mx = fmaxf(mx, xv);
+                for (int i = 0; i < CPT; i += 4) {
+                    pm0 = fmaxf(pm0, sv[i]);
+                    pm1 = fmaxf(pm1, sv[i + 1]);
+                    pm2 = fmaxf(pm2, sv[i + 2]);
+                    pm3 = fmaxf(pm3, sv[i + 3]);
+                }
+                red[((j & 1) * NWG + wg) * 128 + row] = fmaxf(fmaxf(pm0, pm1), fmaxf(pm2, pm3));
             }
+            if (!bar_and(grp_bar, GRP_THREADS, w_ok)) { ok = false; break; }
+            float mx = red[((j & 1) * NWG) * 128 + row];
+#pragma unroll
+            for (int k = 1; k < NWG; ++k) mx = fmaxf(mx, red[((j & 1) * NWG + k) * 128 + row]);
             float factor = 1.0f;
             bool rescale = false;
             if (j == 0) {
                 m_ref = mx;
-            } else if (mx > m_ref + 8.0f) {
-                factor = (m_ref == -INFINITY) ? 0.0f : ex2(m_ref - mx);
+            } else if ((mx - m_ref) * sl2 > 8.0f) {
+                factor = (m_ref == -INFINITY) ? 0.0f : ex2((m_ref - mx) * sl2);
                 m_ref = mx;
                 rescale = true;
             }
-            const float mu = (m_ref == -INFINITY) ? 0.0f : m_ref;
+            const float mu = (m_ref == -INFINITY) ? 0.0f : m_ref * sl2;
             l *= factor;
             // P_j may only overwrite the P buffers once the PV MMAs of block j-1 are done
             if (j >= 1) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&bar[B_PVDONE], (j - 1) & 1, abort_flag))) {
-                    ok = false;
-                    break;
-                }
+                w_ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_PVDONE], (j - 1) & 1, abort_flag));
+                if (!bar_and(grp_bar, GRP_THREADS, w_ok)) { ok = false; break; }
                 tc_fence_after();
             }
             if (__any_sync(0xffffffffu, rescale)) {
                 float ov[32];
 #pragma unroll
-                for (int cc = 0; cc < HD / 32; ++cc) {
-                    tmem_ld32(tO + lane_addr + cc * 32, ov);
+                for (int cc = 0; cc < CPT / 32; ++cc) {
+                    tmem_ld32(tO + lane_addr + cb0 + cc * 32, ov);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) ov[i] *= factor;
-                    tmem_st32(tO + lane_addr + cc * 32, ov);
+                    tmem_st32(tO + lane_addr + cb0 + cc * 32, ov);
                 }
                 tmem_wait_st();
             }
+            unsigned char* plo = sm + OFF_KV + (j & 1) * 2 * TILE_BYTES;   // K_j's buffer
+            float l0 = 0.0f, l1 = 0.0f;
 #pragma unroll
-            for (int cb = 0; cb < NB / 8; ++cb) {          // 16-byte chunks of 8 keys
+            for (int cb = 0; cb < CPT / 8; ++cb) {         // 16-byte chunks of 8 keys
                 uint32_t hw[4], lw[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float p0 = ex2(sv[cb * 8 + 2 * e] - mu);
-                    const float p1 = ex2(sv[cb * 8 + 2 * e + 1] - mu);
-                    l += p0 + p1;
-                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-                    const float2 hf = __bfloat1622float2(h2);
-                    const __nv_bfloat162 l2 = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
-                    hw[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                    const float p0 = ex2(fmaf(sv[cb * 8 + 2 * e], sl2, -mu));
+                    const float p1 = ex2(fmaf(sv[cb * 8 + 2 * e + 1], sl2, -mu));
+                    l0 += p0;
+                    l1 += p1;
+                    // P_hi: p truncated to bf16 (exact), P_lo: bf16(p - P_hi)
+                    const uint32_t u0 = __float_as_uint(p0) & 0xffff0000u;
+                    const uint32_t u1 = __float_as_uint(p1) & 0xffff0000u;
+                    hw[e] = __byte_perm(u0, u1, 0x7632);
+                    const __nv_bfloat162 l2 =
+                        __floats2bfloat162_rn(p0 - __uint_as_float(u0), p1 - __uint_as_float(u1));
                     lw[e] = *reinterpret_cast<const uint32_t*>(&l2);
                 }
-                const uint32_t off = (cb >> 3) * HALF_BYTES + sw128_offset(row, (cb & 7) * 8);
+                const int col = cb0 + cb * 8;              // key column within the block
+                const uint32_t off = (col >> 6) * HALF_BYTES + sw128_offset(row, col & 63);
                 *reinterpret_cast<uint4*>(phi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                 *reinterpret_cast<uint4*>(plo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
+            l += l0 + l1;
             fence_async_smem();
             tc_fence_before();
             mbar_arrive(&bar[B_PFULL]);
         }
-        if (ok && !__all_sync(0xffffffffu, mbar_wait(&bar[B_PVDONE], (nblk - 1) & 1, abort_flag)))
-            ok = false;
+        if (ok) {
+            const bool w_ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_PVDONE], (nblk - 1) & 1, abort_flag));
+            ok = bar_and(grp_bar, GRP_THREADS, w_ok);
+        }
         if (ok) {
             tc_fence_after();
-            float* wO = ws_ptr<float>(prm.ws, w.attn_o_off);
+            __half* wO = ws_ptr<__half>(prm.ws, w.attn_o_off);
             float2* wML = ws_ptr<float2>(prm.ws, w.attn_ml_off);
             const size_t tile = (((size_t)b * c.Hkv + g) * w.n_mt + mt) * w.n_chunks + ch;
+            redl[wg * 128 + row] = l;
+            bar_and(grp_bar, GRP_THREADS, true);
+            float lt = 0.0f;
+#pragma unroll
+            for (int k = 0; k < NWG; ++k) lt += redl[k * 128 + row];
+            const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
             float ov[32];
 #pragma unroll
-            for (int cc = 0; cc < HD / 32; ++cc) {
-                tmem_ld32(tO + lane_addr + cc * 32, ov);
+            for (int cc = 0; cc < CPT / 32; ++cc) {
+                tmem_ld32(tO + lane_addr + cb0 + cc * 32, ov);
                 tmem_wait_ld();
                 if (r < G * T) {
-                    float4* dst = reinterpret_cast<float4*>(wO + (tile * BM + row) * HD + cc * 32);
+                    uint4* dst = reinterpret_cast<uint4*>(wO + (tile * BM + row) * HD + cb0 + cc * 32);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        dst[i] = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t hv[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const __half2 h2 = __floats2half2_rn(ov[8 * i + 2 * e] * inv,
+                                                                 ov[8 * i + 2 * e + 1] * inv);
+                            hv[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                        }
+                        dst[i] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                    }
                 }
             }
-            if (r < G * T)
-                wML[tile * BM + row] = make_float2(m_ref * 0.6931471805599453f, l);
+            if (wg == 0 && r < G * T)
+                // partial max in natural-log units of the scaled score s / sqrt(D)
+                wML[tile * BM + row] = make_float2(m_ref * rsqrtf((float)HD), lt);
         }
     }
 

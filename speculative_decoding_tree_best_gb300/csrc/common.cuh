@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -16,11 +17,13 @@ constexpr int kWarp = 32;
 template <int IO> struct io_t;
 template <> struct io_t<SPEC_IO_F32> {
     using T = float;
+    using PT = float;    // attention split-KV partial element
     static __device__ __forceinline__ float ld(const T* p, size_t i) { return p[i]; }
     static __device__ __forceinline__ void st(T* p, size_t i, float x) { p[i] = x; }
 };
 template <> struct io_t<SPEC_IO_BF16> {
     using T = __nv_bfloat16;
+    using PT = __half;   // attention split-KV partial element
     static __device__ __forceinline__ float ld(const T* p, size_t i) { return __bfloat162float(p[i]); }
     static __device__ __forceinline__ void st(T* p, size_t i, float x) { p[i] = __float2bfloat16_rn(x); }
 };
@@ -39,15 +42,17 @@ __device__ __forceinline__ void raise_status(void* ws, uint32_t bits) {
 // byte 0: device status word; then argmax partials, attention split-KV
 // partials, per-(request, kv-head, m-tile) merge tickets and the per-request
 // commit plan written by the acceptance kernel.
-constexpr int kArgmaxSplit = 8;          // CTAs per logits row (upper bound)
+constexpr int kArgmaxSplit = 16;         // CTAs per logits row (upper bound)
 constexpr int kAttnRowsMax = 128 * 2;    // query rows of one (request, kv-head) tile group
 
 struct WsLayout {
     size_t argmax_off;     // float2 [B][T][kArgmaxSplit]: (value, index bits)
-    size_t attn_o_off;     // float  [B][Hkv][n_mt][n_chunks][128][D]
+    size_t attn_o_off;     // PT     [B][Hkv][n_mt][n_chunks][128][D]: O / l of the chunk,
+                           // PT = fp16 for bf16 I/O, fp32 for fp32 I/O
     size_t attn_ml_off;    // float2 [B][Hkv][n_mt][n_chunks][128]: (max, sum)
     size_t ticket_off;     // uint32 [B][Hkv][n_mt]
     size_t plan_off;       // int32  [B][4]: committed tau (0 = skip), old kv_len
+    size_t acc_ticket_off; // uint32 [B]: argmax CTAs finished per request
     size_t total;
     int n_split;           // cache chunks per (request, kv-head)
     int chunk;             // cache rows per chunk
@@ -77,7 +82,7 @@ static inline WsLayout ws_layout(const spec_cfg& c, int num_sms = 152) {
     if (w.n_split < 1) w.n_split = 1;
     w.n_chunks = w.n_split + 1;
     const long rows = (long)c.B * T;
-    int split = (int)((2L * num_sms + rows - 1) / rows);
+    int split = (int)((3L * num_sms + rows - 1) / rows);
     if (split > kArgmaxSplit) split = kArgmaxSplit;
     if (split < 1) split = 1;
     w.argmax_split = split;
@@ -87,13 +92,15 @@ static inline WsLayout ws_layout(const spec_cfg& c, int num_sms = 152) {
     off = align_up(off + sizeof(float) * 2 * (size_t)c.B * T * kArgmaxSplit, 256);
     const size_t tiles = (size_t)c.B * c.Hkv * w.n_mt * w.n_chunks;
     w.attn_o_off = off;
-    off = align_up(off + sizeof(float) * tiles * 128 * (size_t)c.D, 256);
+    off = align_up(off + (c.io_dtype == SPEC_IO_BF16 ? 2 : 4) * tiles * 128 * (size_t)c.D, 256);
     w.attn_ml_off = off;
     off = align_up(off + sizeof(float) * 2 * tiles * 128, 256);
     w.ticket_off = off;
     off = align_up(off + sizeof(uint32_t) * (size_t)c.B * c.Hkv * w.n_mt, 256);
     w.plan_off = off;
     off = align_up(off + sizeof(int32_t) * 4 * (size_t)c.B, 256);
+    w.acc_ticket_off = off;
+    off = align_up(off + sizeof(uint32_t) * (size_t)c.B, 256);
     w.total = off;
     return w;
 }

@@ -31,12 +31,13 @@ namespace {
 constexpr int CB = 32;       // state columns per CTA
 constexpr int NT = 256;      // threads per CTA (8 warps)
 constexpr int NG = NT / 32;  // warps = row groups
+constexpr int kChainMax = 17;  // per-thread chains for root paths of up to 17 rows (m <= 16)
 
+// 16 bytes of I/O elements -> floats (8 bf16 or 4 fp32).
 template <int IO>
-__device__ __forceinline__ void ld8(const typename io_t<IO>::T* p, float* f);
+__device__ __forceinline__ void unpack16(const uint4& u, float* f);
 template <>
-__device__ __forceinline__ void ld8<SPEC_IO_BF16>(const __nv_bfloat16* p, float* f) {
-    const uint4 u = *reinterpret_cast<const uint4*>(p);
+__device__ __forceinline__ void unpack16<SPEC_IO_BF16>(const uint4& u, float* f) {
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -46,11 +47,11 @@ __device__ __forceinline__ void ld8<SPEC_IO_BF16>(const __nv_bfloat16* p, float*
     }
 }
 template <>
-__device__ __forceinline__ void ld8<SPEC_IO_F32>(const float* p, float* f) {
-    const float4 a = *reinterpret_cast<const float4*>(p);
-    const float4 b = *reinterpret_cast<const float4*>(p + 4);
-    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+__device__ __forceinline__ void unpack16<SPEC_IO_F32>(const uint4& u, float* f) {
+    f[0] = __uint_as_float(u.x);
+    f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z);
+    f[3] = __uint_as_float(u.w);
 }
 
 struct GdnSmem {
@@ -65,7 +66,7 @@ __host__ __device__ inline GdnSmem gdn_smem_layout(int T, int m, int DK) {
     L.S = S;
     int o = 0;
     L.hs = o;  o += DK * CB;
-    L.kq = o;  o += 2 * T * DK;
+    L.kq = o;  o += 2 * T * (DK + 4);     // rows padded by 16 B: no bank conflicts across rows
     L.P = o;   o += 2 * T * CB;
     L.cv = o;  o += T * CB;
     L.vs = o;  o += T * CB;
@@ -82,7 +83,9 @@ __host__ __device__ inline GdnSmem gdn_smem_layout(int T, int m, int DK) {
     return L;
 }
 
-template <int IO, int DK>
+// MAXD > 0: trees whose root paths hold at most MAXD rows use per-thread
+// chains; MAXD == 0: level-synchronous recursion for deeper trees.
+template <int IO, int DK, int MAXD>
 __global__ void __launch_bounds__(NT)
 gdn_tree_kernel(spec_cfg c, spec_tree tree, const float* __restrict__ h0,
                 const typename io_t<IO>::T* __restrict__ q, const typename io_t<IO>::T* __restrict__ k,
@@ -96,6 +99,7 @@ gdn_tree_kernel(spec_cfg c, spec_tree tree, const float* __restrict__ h0,
     const int tid = threadIdx.x, col = tid & 31, grp = tid >> 5;
     const GdnSmem L = gdn_smem_layout(T, c.m, DK);
     const int S = L.S;
+    constexpr int KQS = DK + 4;             // k/q row stride in floats
     float* hs = sm + L.hs;
     float* kq = sm + L.kq;
     float* P = sm + L.P;
@@ -115,38 +119,95 @@ gdn_tree_kernel(spec_cfg c, spec_tree tree, const float* __restrict__ h0,
     nn = nn < 1 ? 1 : (nn > T ? T : nn);     // a malformed tree must not index out of range
 
     // ---- stage: tree, gates, h0 slice, k/q rows, v slice ---------------------------
-    for (int x = tid; x < nn; x += NT) {
-        const int p = tree.node_parent[(size_t)b * T + x];
+    // Every global load of the first round is issued into registers before any
+    // shared-memory store, so the CTA pays one memory round trip, not one per
+    // loop iteration.
+    using E = typename io_t<IO>::T;
+    constexpr int HQ = DK * (CB / 4) / NT;           // h0 float4 per thread
+    constexpr int KQR = 8;                           // k/q 16-byte chunks per thread per round
+    constexpr int EPC = 16 / sizeof(E);              // elements per 16-byte chunk
+    constexpr int KQC = DK / EPC;                    // chunks per k/q row
+    constexpr int VC = CB / EPC;                     // chunks per v row slice
+    const float* hsrc = h0 + ((size_t)b * Hv + j) * DK * dv + c0;
+    float4 hreg[HQ];
+#pragma unroll
+    for (int i = 0; i < HQ; ++i) {
+        const int idx = tid + i * NT, r = idx / (CB / 4), q4 = idx % (CB / 4);
+        hreg[i] = *reinterpret_cast<const float4*>(hsrc + (size_t)r * dv + q4 * 4);
+    }
+    int t_par = -1, t_dep = 0;
+    float t_al = 0.f, t_be = 0.f;
+    if (tid < nn) {
+        t_par = tree.node_parent[(size_t)b * T + tid];
+        t_dep = tree.node_depth[(size_t)b * T + tid];
+        t_al = alpha[((size_t)b * T + tid) * Hv + j];
+        t_be = beta[((size_t)b * T + tid) * Hv + j];
+    }
+    uint4 vreg = make_uint4(0, 0, 0, 0);
+    const bool has_v = tid < nn * VC;
+    if (has_v) {
+        const int x = tid / VC, e0 = (tid % VC) * EPC;
+        vreg = *reinterpret_cast<const uint4*>(v + (((size_t)b * T + x) * Hv + j) * dv + c0 + e0);
+    }
+    const int nkq = 2 * nn * KQC;
+    for (int base = 0; base < nkq; base += NT * KQR) {
+        uint4 kreg[KQR];
+#pragma unroll
+        for (int i = 0; i < KQR; ++i) {
+            const int idx = base + tid + i * NT;
+            if (idx < nkq) {
+                const int row = idx / KQC, ch = idx % KQC;
+                const int x = row < nn ? row : row - nn;
+                kreg[i] = *reinterpret_cast<const uint4*>(
+                    (row < nn ? k : q) + (((size_t)b * T + x) * Hk + ih) * DK + ch * EPC);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < KQR; ++i) {
+            const int idx = base + tid + i * NT;
+            if (idx < nkq) {
+                const int row = idx / KQC, ch = idx % KQC;
+                float f[EPC];
+                unpack16<IO>(kreg[i], f);
+#pragma unroll
+                for (int e = 0; e < EPC; e += 4)
+                    *reinterpret_cast<float4*>(kq + row * KQS + ch * EPC + e) =
+                        make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < HQ; ++i) {
+        const int idx = tid + i * NT, r = idx / (CB / 4), q4 = idx % (CB / 4);
+        *reinterpret_cast<float4*>(hs + r * CB + q4 * 4) = hreg[i];
+    }
+    if (tid < nn) {
+        par[tid] = (t_par >= 0 && t_par < tid) ? t_par : -1;
+        dep[tid] = t_dep < 0 ? 0 : (t_dep >= S ? S - 1 : t_dep);
+        al[tid] = t_al;
+        be[tid] = t_be;
+    }
+    if (has_v) {
+        const int x = tid / VC, e0 = (tid % VC) * EPC;
+        float f[EPC];
+        unpack16<IO>(vreg, f);
+#pragma unroll
+        for (int e = 0; e < EPC; ++e) vs[x * CB + e0 + e] = f[e];
+    }
+    for (int x = NT + tid; x < nn; x += NT) {     // trees with more rows than threads
+        const int pp = tree.node_parent[(size_t)b * T + x];
         const int d = tree.node_depth[(size_t)b * T + x];
-        par[x] = (p >= 0 && p < x) ? p : -1;
+        par[x] = (pp >= 0 && pp < x) ? pp : -1;
         dep[x] = d < 0 ? 0 : (d >= S ? S - 1 : d);
         al[x] = alpha[((size_t)b * T + x) * Hv + j];
         be[x] = beta[((size_t)b * T + x) * Hv + j];
     }
-    {
-        const float* hsrc = h0 + ((size_t)b * Hv + j) * DK * dv + c0;
-        for (int idx = tid; idx < DK * (CB / 4); idx += NT) {
-            const int r = idx / (CB / 4), q4 = idx % (CB / 4);
-            *reinterpret_cast<float4*>(hs + r * CB + q4 * 4) =
-                *reinterpret_cast<const float4*>(hsrc + (size_t)r * dv + q4 * 4);
-        }
-    }
-    for (int idx = tid; idx < 2 * nn * (DK / 8); idx += NT) {
-        const int row = idx / (DK / 8), e8 = (idx % (DK / 8)) * 8;
-        const int x = row < nn ? row : row - nn;
-        const auto* src = (row < nn ? k : q) + (((size_t)b * T + x) * Hk + ih) * DK + e8;
-        float f[8];
-        ld8<IO>(src, f);
-        float4* dst = reinterpret_cast<float4*>(kq + row * DK + e8);
-        dst[0] = make_float4(f[0], f[1], f[2], f[3]);
-        dst[1] = make_float4(f[4], f[5], f[6], f[7]);
-    }
-    for (int idx = tid; idx < nn * (CB / 8); idx += NT) {
-        const int x = idx / (CB / 8), e8 = (idx % (CB / 8)) * 8;
-        float f[8];
-        ld8<IO>(v + (((size_t)b * T + x) * Hv + j) * dv + c0 + e8, f);
+    for (int idx = NT + tid; idx < nn * VC; idx += NT) {
+        const int x = idx / VC, e0 = (idx % VC) * EPC;
+        float f[EPC];
+        unpack16<IO>(*reinterpret_cast<const uint4*>(v + (((size_t)b * T + x) * Hv + j) * dv + c0 + e0), f);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) vs[x * CB + e8 + e] = f[e];
+        for (int e = 0; e < EPC; ++e) vs[x * CB + e0 + e] = f[e];
     }
     __syncthreads();
 
@@ -164,34 +225,27 @@ gdn_tree_kernel(spec_cfg c, spec_tree tree, const float* __restrict__ h0,
     }
     __syncthreads();
 
-    // ---- Gram weights: wo *= k_a . q_x, wu *= k_a . k_x (one warp per row) ------------
-    {
-        constexpr int EPL = DK / 32;  // elements per lane
-        for (int x = grp; x < nn; x += NG) {
-            float kx[EPL], qx[EPL];
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) {
-                kx[e] = kq[x * DK + col + 32 * e];
-                qx[e] = kq[(nn + x) * DK + col + 32 * e];
-            }
-            const int d = dep[x];
-            for (int s = 0; s <= d; ++s) {
-                const float* ka = kq + pidx[x * S + s] * DK;
-                float dq = 0.0f, dk = 0.0f;
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) {
-                    const float a = ka[col + 32 * e];
-                    dq = fmaf(a, qx[e], dq);
-                    dk = fmaf(a, kx[e], dk);
-                }
-                dq = warp_sum(dq);
-                dk = warp_sum(dk);
-                if (col == 0) {
-                    wo[x * S + s] *= dq;
-                    if (s < d) wu[x * S + s] *= dk;
-                }
-            }
+    // ---- Gram weights: wo *= k_a . q_x, wu *= k_a . k_x (one thread per pair) ---------
+    for (int idx = tid; idx < nn * S; idx += NT) {
+        const int x = idx / S, s = idx - x * S;
+        const int d = dep[x];
+        if (s > d) continue;
+        const float4* ka = reinterpret_cast<const float4*>(kq + pidx[x * S + s] * KQS);
+        const float4* kx = reinterpret_cast<const float4*>(kq + x * KQS);
+        const float4* qx = reinterpret_cast<const float4*>(kq + (nn + x) * KQS);
+        float dq0 = 0.f, dq1 = 0.f, dk0 = 0.f, dk1 = 0.f;
+#pragma unroll 8
+        for (int e = 0; e < DK / 4; e += 2) {
+            const float4 a0 = ka[e], a1 = ka[e + 1];
+            const float4 q0 = qx[e], q1 = qx[e + 1];
+            const float4 k0 = kx[e], k1 = kx[e + 1];
+            dq0 = fmaf(a0.x, q0.x, fmaf(a0.y, q0.y, fmaf(a0.z, q0.z, fmaf(a0.w, q0.w, dq0))));
+            dq1 = fmaf(a1.x, q1.x, fmaf(a1.y, q1.y, fmaf(a1.z, q1.z, fmaf(a1.w, q1.w, dq1))));
+            dk0 = fmaf(a0.x, k0.x, fmaf(a0.y, k0.y, fmaf(a0.z, k0.z, fmaf(a0.w, k0.w, dk0))));
+            dk1 = fmaf(a1.x, k1.x, fmaf(a1.y, k1.y, fmaf(a1.z, k1.z, fmaf(a1.w, k1.w, dk1))));
         }
+        wo[x * S + s] *= dq0 + dq1;
+        if (s < d) wu[x * S + s] *= dk0 + dk1;
     }
 
     // ---- P = h0_slice^T [K; Q]: rows t = grp + 8 i, column col ------------------------
@@ -206,7 +260,7 @@ gdn_tree_kernel(spec_cfg c, spec_tree tree, const float* __restrict__ h0,
             for (int i = 0; i < 8; ++i) {
                 const int t = t0 + grp + NG * i;
                 if (t < 2 * nn) {
-                    const float4 kk = *reinterpret_cast<const float4*>(kq + t * DK + r);
+                    const float4 kk = *reinterpret_cast<const float4*>(kq + t * KQS + r);
                     acc[i] = fmaf(h_0, kk.x, fmaf(h_1, kk.y, fmaf(h_2, kk.z, fmaf(h_3, kk.w, acc[i]))));
                 }
             }
@@ -218,6 +272,38 @@ gdn_tree_kernel(spec_cfg c, spec_tree tree, const float* __restrict__ h0,
         }
     }
     __syncthreads();
+
+    if constexpr (MAXD > 0) {
+        // ---- write vectors and outputs, one (row, column) chain per thread ------------
+        // Thread (x, col) walks x's root path y_0 = root .. y_d = x and rebuilds
+        // c_{y_s} = beta v - alpha beta (A_par Pk + sum_{s'<s} wu[y_s][s'] c_{y_s'})
+        // in registers; y_s's ancestors are y_0 .. y_{s-1}, so its weights are
+        // indexed by the same path positions.  Work is redundant across
+        // siblings (shorter than one barrier per tree level at these depths).
+        for (int x = grp; x < T; x += NG) {
+            float ox = 0.0f, cx = 0.0f;
+            if (x < nn) {
+                const int d = dep[x];
+                float cc[MAXD];
+                ox = A[x] * P[(nn + x) * CB + col];
+#pragma unroll
+                for (int s = 0; s < MAXD; ++s) {
+                    if (s > d) break;
+                    const int y = pidx[x * S + s];
+                    float u = Ap[y] * P[y * CB + col];
+#pragma unroll
+                    for (int s2 = 0; s2 < s; ++s2) u = fmaf(wu[y * S + s2], cc[s2], u);
+                    cc[s] = be[y] * vs[y * CB + col] - al[y] * be[y] * u;
+                    ox = fmaf(wo[x * S + s], cc[s], ox);
+                    cx = cc[s];
+                }
+            }
+            const size_t oi = (((size_t)b * T + x) * Hv + j) * dv + c0 + col;
+            io_t<IO>::st(o, oi, ox);
+            if (c_out) c_out[oi] = cx;
+        }
+        return;
+    }
 
     // ---- write vectors c_x, level by level (ancestors first) --------------------------
     const int maxd = c.m < nn - 1 ? c.m : nn - 1;
@@ -246,12 +332,12 @@ gdn_tree_kernel(spec_cfg c, spec_tree tree, const float* __restrict__ h0,
     }
 }
 
-template <int IO, int DK>
+template <int IO, int DK, int MAXD>
 cudaError_t launch_one(const spec_cfg& c, const spec_tree& t, const float* h0, const void* q,
                        const void* k, const void* v, const float* alpha, const float* beta,
                        void* o, float* c_out, size_t smem, cudaStream_t st) {
     using E = typename io_t<IO>::T;
-    auto kern = gdn_tree_kernel<IO, DK>;
+    auto kern = gdn_tree_kernel<IO, DK, MAXD>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(c.dv / CB, c.Hv, c.B);
@@ -271,12 +357,19 @@ cudaError_t launch_gdn_tree(const spec_cfg& c, const spec_tree& t, const float* 
                             const float* beta, void* o, float* c_out, cudaStream_t st) {
     const size_t smem = gdn_tree_smem(c);
     if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
+    const int T = c.N + 1;
+    const int S = (c.m < T - 1 ? c.m : T - 1) + 1;        // rows on the longest root path
+    const bool chains = S <= kChainMax;
+#define SPEC_GDN_LAUNCH(IO_, DK_)                                                              \
+    return chains ? launch_one<IO_, DK_, kChainMax>(c, t, h0, q, k, v, alpha, beta, o, c_out, smem, st) \
+                  : launch_one<IO_, DK_, 0>(c, t, h0, q, k, v, alpha, beta, o, c_out, smem, st)
     if (c.io_dtype == SPEC_IO_BF16) {
-        return c.dk == 128 ? launch_one<SPEC_IO_BF16, 128>(c, t, h0, q, k, v, alpha, beta, o, c_out, smem, st)
-                           : launch_one<SPEC_IO_BF16, 64>(c, t, h0, q, k, v, alpha, beta, o, c_out, smem, st);
+        if (c.dk == 128) { SPEC_GDN_LAUNCH(SPEC_IO_BF16, 128); }
+        SPEC_GDN_LAUNCH(SPEC_IO_BF16, 64);
     }
-    return c.dk == 128 ? launch_one<SPEC_IO_F32, 128>(c, t, h0, q, k, v, alpha, beta, o, c_out, smem, st)
-                       : launch_one<SPEC_IO_F32, 64>(c, t, h0, q, k, v, alpha, beta, o, c_out, smem, st);
+    if (c.dk == 128) { SPEC_GDN_LAUNCH(SPEC_IO_F32, 128); }
+    SPEC_GDN_LAUNCH(SPEC_IO_F32, 64);
+#undef SPEC_GDN_LAUNCH
 }
 
 }  // namespace spec

@@ -6,21 +6,28 @@
 // verification (nodes added greedily by root-path log-prob up to N) and
 // technical novelty, Figure 6 (best-first tree, edges log p(child | parent)).
 //
-// One warp builds one request's tree entirely in shared memory.
-//  1. Each lattice position is ranked in registers: lane r holds candidate r
-//     and counts the candidates that precede it (score desc, index asc).
+// One warp builds one request's tree.
+//  1. Every candidate is ranked in registers, 32 / K positions per warp pass:
+//     its rank is the number of candidates of its position that precede it
+//     (score desc, index asc), counted over shuffles within the position.
 //  2. Because a position's ranked scores are non-increasing and fp32 addition
-//     is monotone, the best remaining child of any inserted node is its
-//     lowest not-yet-inserted rank.  The frontier is therefore one candidate
-//     per inserted node ("next rank"), not K per node.
-//  3. Every lane caches the best candidate among the nodes it owns
-//     (row % 32 == lane); one iteration is two warp-wide REDUX max operations
-//     (score, then depth/parent among equal scores), one insertion by lane 0,
-//     and a re-scan by the two lanes whose nodes changed.
+//     is monotone, the best remaining child of an inserted node is its lowest
+//     not-yet-inserted rank, so the frontier is one candidate per inserted row.
+//  3. Row x lives in the registers of lane x % 32 (slot x / 32, T <= 128).
+//     Each lane caches its best candidate; one insertion is two warp-wide
+//     REDUX max operations (score, then depth/parent among equal scores), a
+//     few shuffles from the parent's lane to the new row's lane, and a
+//     re-scan of at most four slots by the two lanes whose rows changed.  The
+//     edge scores a row will need next are prefetched from shared memory after
+//     each insertion, so the chain from one insertion to the next has no
+//     shared-memory load.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace spec {
+
+namespace {
+
 
 // Order-preserving map of a finite float to uint32 (-0 folded into +0, since
 // the two compare equal).
@@ -35,6 +42,8 @@ __device__ __forceinline__ uint32_t tie_key(int depth, int parent) {
     return ((uint32_t)(255 - depth) << 8) | (uint32_t)(255 - parent);
 }
 
+// SLOTS = rows per lane (1 for trees of up to 32 rows, else 2 or 4).
+template <int SLOTS>
 __global__ void __launch_bounds__(32)
 tree_build_kernel(spec_cfg c, const int32_t* __restrict__ lat_tok,
                   const float* __restrict__ lat_score, const int32_t* __restrict__ root_tok,
@@ -43,133 +52,230 @@ tree_build_kernel(spec_cfg c, const int32_t* __restrict__ lat_tok,
     const int b = blockIdx.x;
     const int lane = threadIdx.x;
     const int m = c.m, K = c.K, T = c.N + 1;
+    const int MK = m * K;
 
-    uint64_t* n_anc = reinterpret_cast<uint64_t*>(smem);          // [T][2]
-    int32_t* s_tok = reinterpret_cast<int32_t*>(n_anc + 2 * T);    // [m][K] ranked tokens
-    float* s_sc = reinterpret_cast<float*>(s_tok + m * K);         // [m][K] ranked scores
-    int32_t* n_tok = reinterpret_cast<int32_t*>(s_sc + m * K);     // [T]
-    int32_t* n_par = n_tok + T;
-    int32_t* n_dep = n_par + T;
-    int32_t* n_rank = n_dep + T;
-    int32_t* n_next = n_rank + T;                                  // next child rank to offer
-    float* n_sc = reinterpret_cast<float*>(n_next + T);
-    int32_t* r_tok = reinterpret_cast<int32_t*>(n_sc + T);          // [m][K] as given
-    float* r_sc = reinterpret_cast<float*>(r_tok + m * K);          // [m][K] as given
+    int32_t* s_tok = reinterpret_cast<int32_t*>(smem);      // [m][K] ranked tokens
+    float* s_sc = reinterpret_cast<float*>(s_tok + MK);      // [m][K] ranked edge scores
+    int32_t* r_tok = reinterpret_cast<int32_t*>(s_sc + MK);  // [m][K] as given
+    float* r_sc = reinterpret_cast<float*>(r_tok + MK);      // [m][K] as given
 
-    // ---- 1. stage the lattice (one round trip), then rank every position -------
-    for (int i = lane; i < m * K; i += kWarp) {
-        r_tok[i] = lat_tok[(size_t)b * m * K + i];
-        r_sc[i] = lat_score[(size_t)b * m * K + i];
+    // ---- 1. stage (one round trip), then rank: 32 / K2 positions per warp pass --------
+    const int root = root_tok[b];
+    for (int i = lane; i < MK; i += 32) {
+        r_tok[i] = lat_tok[(size_t)b * MK + i];
+        r_sc[i] = lat_score[(size_t)b * MK + i];
     }
     __syncwarp();
+    int K2 = 1;
+    while (K2 < K) K2 <<= 1;
+    const int ppp = 32 / K2;                                 // positions per pass
+    const int sub = lane / K2, ci = lane % K2;
     bool bad = false;
-    for (int s = 0; s < m; ++s) {
-        int tok = 0;
-        float sc = 0.0f;
-        if (lane < K) {
-            tok = r_tok[s * K + lane];
-            sc = r_sc[s * K + lane];
-            bad |= (sc != sc);
-        }
+    for (int s0 = 0; s0 < m; s0 += ppp) {
+        const int s = s0 + sub;
+        const bool valid = s < m && ci < K;
+        const float sc = valid ? r_sc[s * K + ci] : 0.0f;
+        const int tk = valid ? r_tok[s * K + ci] : 0;
+        bad |= valid && (sc != sc);
         int rank = 0;
-        for (int j = 0; j < K; ++j) {
-            const float sj = __shfl_sync(0xffffffffu, sc, j);
-            const int tj = __shfl_sync(0xffffffffu, tok, j);
-            if (lane < K && j != lane) {
-                rank += (sj > sc || (sj == sc && j < lane)) ? 1 : 0;
-                bad |= (tj == tok);
-            }
+#pragma unroll 8
+        for (int jj = 0; jj < K; ++jj) {
+            const float sj = __shfl_sync(0xffffffffu, sc, jj, K2);
+            const int tj = __shfl_sync(0xffffffffu, tk, jj, K2);
+            rank += (sj > sc || (sj == sc && jj < ci)) ? 1 : 0;
+            bad |= valid && jj != ci && tj == tk;
         }
-        if (lane < K && rank < K) {
-            s_tok[s * K + rank] = tok;
+        if (valid && rank < K) {
+            s_tok[s * K + rank] = tk;
             s_sc[s * K + rank] = sc;
         }
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) raise_status(ws, SPEC_DEV_BADLAT);
-
-    // ---- 2./3. best-first insertion ------------------------------------------
-    if (lane == 0) {
-        n_tok[0] = root_tok[b];
-        n_par[0] = -1;
-        n_dep[0] = 0;
-        n_rank[0] = -1;
-        n_next[0] = 0;
-        n_sc[0] = 0.0f;
-        n_anc[0] = 1ull;
-        n_anc[1] = 0ull;
-    }
     __syncwarp();
 
-    uint32_t my_ord = 0, my_tie = 0;   // cached best candidate of this lane's nodes
-    auto rescan = [&](int count) {
-        my_ord = 0;
-        my_tie = 0;
-        for (int x = lane; x < count; x += kWarp) {
-            const int d = n_dep[x], r = n_next[x];
-            if (d < m && r < K) {
-                const uint32_t o = ord_f32(n_sc[x] + s_sc[d * K + r]);
-                const uint32_t t = tie_key(d + 1, x);
-                if (o > my_ord || (o == my_ord && t > my_tie)) {
-                    my_ord = o;
-                    my_tie = t;
+    // ---- 2./3. best-first insertion, rows in registers ----------------------------
+    // Per slot: depth nd, offered rank nx, score ns, offered child score cs and
+    // its order key co (0 = nothing offered), nxt = edge score of the rank after
+    // the offered one, fst = first edge score of the next position (the first
+    // child of any new child of this row); both prefetched off the critical path.
+    int nd[SLOTS], nx[SLOTS], ntk[SLOTS], npar[SLOTS], nrk[SLOTS];
+    float ns[SLOTS], cs[SLOTS], nxt[SLOTS], fst[SLOTS];
+    uint32_t co[SLOTS];
+    uint64_t a0[SLOTS], a1[SLOTS];
+#pragma unroll
+    for (int k = 0; k < SLOTS; ++k) {
+        nd[k] = m; nx[k] = K; ntk[k] = -1; npar[k] = -1; nrk[k] = -1;
+        ns[k] = 0.0f; cs[k] = 0.0f; nxt[k] = 0.0f; fst[k] = 0.0f; co[k] = 0u;
+        a0[k] = 0ull; a1[k] = 0ull;
+    }
+    auto prefetch = [&](int k) {
+        const int d = nd[k];
+        nxt[k] = (d < m && nx[k] + 1 < K) ? s_sc[d * K + nx[k] + 1] : 0.0f;
+        fst[k] = (d + 1 < m) ? s_sc[(d + 1) * K] : 0.0f;
+    };
+    uint32_t bo = 0, bt = 0;   // this lane's best candidate (ord, tie)
+    auto best_of_lane = [&]() {
+        bo = 0u;
+        bt = 0u;
+#pragma unroll
+        for (int k = 0; k < SLOTS; ++k) {
+            const uint32_t t = tie_key(nd[k] + 1, lane + 32 * k);
+            if (co[k] > bo || (co[k] == bo && co[k] != 0u && t > bt)) { bo = co[k]; bt = t; }
+        }
+    };
+    if (lane == 0) {   // row 0: the root
+        nd[0] = 0; nx[0] = 0; ntk[0] = root; ns[0] = 0.0f; a0[0] = 1ull;
+        if (m > 0 && K > 0) {
+            cs[0] = 0.0f + s_sc[0];
+            co[0] = ord_f32(cs[0]);
+        }
+        prefetch(0);
+    }
+    best_of_lane();
+    int count = 1;
+    if constexpr (SLOTS == 1) {
+        // Trees of up to 32 rows: row x lives in lane x, and an insertion is pure
+        // data movement by shuffles and selects (no divergent branch).
+        uint32_t bo1 = co[0];
+        uint32_t bt1 = tie_key(nd[0] + 1, lane);
+        while (count < T) {
+            const uint32_t best_ord = __reduce_max_sync(0xffffffffu, bo1);
+            if (best_ord == 0u) break;                              // frontier empty
+            const uint32_t best_tie = __reduce_max_sync(0xffffffffu, bo1 == best_ord ? bt1 : 0u);
+            const int p = 255 - (int)(best_tie & 0xffu);
+            const int n = count++;
+            const int d = __shfl_sync(0xffffffffu, nd[0], p);
+            const int r = __shfl_sync(0xffffffffu, nx[0], p);
+            const float sc = __shfl_sync(0xffffffffu, cs[0], p);
+            const float fe = __shfl_sync(0xffffffffu, fst[0], p);
+            const bool isp = lane == p, isn = lane == n;
+            const float cs_p = ns[0] + nxt[0];
+            const uint32_t co_p = (r + 1 < K) ? ord_f32(cs_p) : 0u;
+            const float cs_n = sc + fe;
+            const uint32_t co_n = (d + 1 < m) ? ord_f32(cs_n) : 0u;
+            nx[0] = isp ? r + 1 : (isn ? 0 : nx[0]);
+            nd[0] = isn ? d + 1 : nd[0];
+            ns[0] = isn ? sc : ns[0];
+            npar[0] = isn ? p : npar[0];
+            nrk[0] = isn ? r : nrk[0];
+            cs[0] = isp ? cs_p : (isn ? cs_n : cs[0]);
+            co[0] = isp ? co_p : (isn ? co_n : co[0]);
+            bo1 = co[0];
+            bt1 = tie_key(nd[0] + 1, lane);
+            // off the critical path: ancestors, token, prefetched edge scores
+            const uint64_t pa0 = __shfl_sync(0xffffffffu, a0[0], p);
+            const uint64_t pa1 = __shfl_sync(0xffffffffu, a1[0], p);
+            const int tkn = s_tok[d * K + r];
+            a0[0] = isn ? (pa0 | (n < 64 ? 1ull << n : 0ull)) : a0[0];
+            a1[0] = isn ? (pa1 | (n >= 64 ? 1ull << (n - 64) : 0ull)) : a1[0];
+            ntk[0] = isn ? tkn : ntk[0];
+            const int dd = nd[0];
+            const int i_nxt = (dd < m && nx[0] + 1 < K) ? dd * K + nx[0] + 1 : 0;
+            const int i_fst = (dd + 1 < m) ? (dd + 1) * K : 0;
+            nxt[0] = s_sc[i_nxt];
+            fst[0] = s_sc[i_fst];
+        }
+    } else {
+    while (count < T) {
+        const uint32_t best_ord = __reduce_max_sync(0xffffffffu, bo);
+        if (best_ord == 0u) break;                                  // frontier empty
+        const uint32_t best_tie = __reduce_max_sync(0xffffffffu, bo == best_ord ? bt : 0u);
+        const int p = 255 - (int)(best_tie & 0xffu);
+        const int n = count++;
+        const int pl = p & 31, pk = p >> 5;
+        // the parent's lane publishes depth, offered rank, child score, the first
+        // edge score below the child, and its ancestor mask
+        int d = 0, r = 0;
+        float sc = 0.0f, fe = 0.0f;
+        uint64_t pa0 = 0ull, pa1 = 0ull;
+#pragma unroll
+        for (int k = 0; k < SLOTS; ++k)
+            if (SLOTS == 1 || k == pk) { d = nd[k]; r = nx[k]; sc = cs[k]; fe = fst[k]; pa0 = a0[k]; pa1 = a1[k]; }
+        d = __shfl_sync(0xffffffffu, d, pl);
+        r = __shfl_sync(0xffffffffu, r, pl);
+        sc = __shfl_sync(0xffffffffu, sc, pl);
+        fe = __shfl_sync(0xffffffffu, fe, pl);
+        if (lane == pl) {
+#pragma unroll
+            for (int k = 0; k < SLOTS; ++k)
+                if (SLOTS == 1 || k == pk) {
+                    nx[k] = r + 1;
+                    if (r + 1 < K) { cs[k] = ns[k] + nxt[k]; co[k] = ord_f32(cs[k]); }
+                    else co[k] = 0u;
+                }
+        }
+        if (lane == (n & 31)) {
+            const int nk = n >> 5;
+#pragma unroll
+            for (int k = 0; k < SLOTS; ++k) {
+                if (SLOTS == 1 || k == nk) {
+                    nd[k] = d + 1; nx[k] = 0; ns[k] = sc; npar[k] = p; nrk[k] = r;
+                    if (d + 1 < m) { cs[k] = sc + fe; co[k] = ord_f32(cs[k]); }
+                    else co[k] = 0u;
                 }
             }
         }
-    };
-    int count = 1;
-    rescan(count);
-    while (count < T) {
-        const uint32_t best_ord = __reduce_max_sync(0xffffffffu, my_ord);
-        if (best_ord == 0u) break;                                  // frontier empty
-        const uint32_t best_tie =
-            __reduce_max_sync(0xffffffffu, my_ord == best_ord ? my_tie : 0u);
-        const int p = 255 - (int)(best_tie & 0xffu);
-        const int n = count;
-        if (lane == 0) {
-            const int d = n_dep[p], r = n_next[p];
-            n_tok[n] = s_tok[d * K + r];
-            n_par[n] = p;
-            n_dep[n] = d + 1;
-            n_rank[n] = r;
-            n_next[n] = 0;
-            n_sc[n] = n_sc[p] + s_sc[d * K + r];
-            n_anc[2 * n] = n_anc[2 * p];
-            n_anc[2 * n + 1] = n_anc[2 * p + 1];
-            n_anc[2 * n + (n >> 6)] |= 1ull << (n & 63);
-            n_next[p] = r + 1;
+        if (lane == pl || lane == (n & 31)) best_of_lane();
+        // off the critical path: ancestors, token, prefetches
+        pa0 = __shfl_sync(0xffffffffu, pa0, pl);
+        pa1 = __shfl_sync(0xffffffffu, pa1, pl);
+        if (lane == pl) {
+#pragma unroll
+            for (int k = 0; k < SLOTS; ++k)
+                if (SLOTS == 1 || k == pk) prefetch(k);
         }
-        __syncwarp();
-        ++count;
-        if ((p & 31) == lane || (n & 31) == lane) rescan(count);
+        if (lane == (n & 31)) {
+            const int nk = n >> 5;
+#pragma unroll
+            for (int k = 0; k < SLOTS; ++k) {
+                if (SLOTS == 1 || k == nk) {
+                    ntk[k] = s_tok[d * K + r];
+                    a0[k] = pa0 | (n < 64 ? 1ull << n : 0ull);
+                    a1[k] = pa1 | (n >= 64 ? 1ull << (n - 64) : 0ull);
+                    prefetch(k);
+                }
+            }
+        }
     }
-    __syncwarp();
+
+    }
 
     // ---- write the tree ----------------------------------------------------------
-    for (int x = lane; x < T; x += kWarp) {
-        const size_t o = (size_t)b * T + x;
-        const bool used = x < count;
-        out.node_tok[o] = used ? n_tok[x] : -1;
-        out.node_parent[o] = used ? n_par[x] : -1;
-        out.node_depth[o] = used ? n_dep[x] : -1;
-        out.node_rank[o] = used ? n_rank[x] : -1;
-        out.node_score[o] = used ? n_sc[x] : 0.0f;
-        out.node_anc[2 * o] = used ? n_anc[2 * x] : 0ull;
-        out.node_anc[2 * o + 1] = used ? n_anc[2 * x + 1] : 0ull;
+#pragma unroll
+    for (int k = 0; k < SLOTS; ++k) {
+        const int x = lane + 32 * k;
+        if (x < T) {
+            const size_t o = (size_t)b * T + x;
+            const bool used = x < count;
+            out.node_tok[o] = used ? ntk[k] : -1;
+            out.node_parent[o] = used ? npar[k] : -1;
+            out.node_depth[o] = used ? nd[k] : -1;
+            out.node_rank[o] = used ? nrk[k] : -1;
+            out.node_score[o] = used ? ns[k] : 0.0f;
+            out.node_anc[2 * o] = used ? a0[k] : 0ull;
+            out.node_anc[2 * o + 1] = used ? a1[k] : 0ull;
+        }
     }
     if (lane == 0) out.n_nodes[b] = count;
 }
 
+}  // namespace
+
 size_t tree_build_smem(const spec_cfg& c) {
-    const int T = c.N + 1;
-    return sizeof(uint64_t) * 2 * T + 2 * (sizeof(int32_t) + sizeof(float)) * (size_t)c.m * c.K +
-           (5 * sizeof(int32_t) + sizeof(float)) * (size_t)T;
+    return 2 * (sizeof(int32_t) + sizeof(float)) * (size_t)c.m * c.K;
 }
 
 cudaError_t launch_tree_build(const spec_cfg& c, const int32_t* lat_tok, const float* lat_score,
                               const int32_t* root_tok, const spec_tree& out, void* ws,
                               cudaStream_t st) {
     const size_t smem = tree_build_smem(c);
-    tree_build_kernel<<<c.B, 32, smem, st>>>(c, lat_tok, lat_score, root_tok, out, ws);
+    const int T = c.N + 1;
+    if (T <= 32)
+        tree_build_kernel<1><<<c.B, 32, smem, st>>>(c, lat_tok, lat_score, root_tok, out, ws);
+    else if (T <= 64)
+        tree_build_kernel<2><<<c.B, 32, smem, st>>>(c, lat_tok, lat_score, root_tok, out, ws);
+    else
+        tree_build_kernel<4><<<c.B, 32, smem, st>>>(c, lat_tok, lat_score, root_tok, out, ws);
     return cudaGetLastError();
 }
 
