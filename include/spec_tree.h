@@ -199,6 +199,33 @@ int accept_and_commit(const spec_cfg *cfg, const spec_tree *tree, const void *lo
                       const spec_commit_io *io, const spec_accept *out, void *ws,
                       void *stream);
 
+/* Per-layer verify buffers of a whole step, stacked with the layer outermost
+ * (layer l of gdn_q is the q that gdn_tree_verify would get for layer l). */
+typedef struct spec_step_io {
+    const void *gdn_q;      /* [n_gdn][B][T][Hk][dk] io */
+    void *gdn_o;            /* [n_gdn][B][T][Hv][dv] io (output) */
+    float *gdn_c;           /* NULL, or [n_gdn][B][T][Hv][dv] float (output) */
+    const void *attn_q;     /* [n_attn][B][T][Hq][D] io */
+    void *attn_o;           /* [n_attn][B][T][Hq][D] io (output) */
+} spec_step_io;
+
+/*
+ * spec_verify_step -- one whole verify step: spec_tree_build into `tree`,
+ * gdn_tree_verify for every GDN layer, attn_tree_verify for every attention
+ * layer, then accept_and_commit; the results equal those of the four calls
+ * made in that order on `stream`.  (Digest sections as for the four calls.)
+ *
+ * The kernels are launched in that fixed order with programmatic dependent
+ * launch, so each one stages the inputs that do not depend on its
+ * predecessor (state slices, cache blocks, logits) while the predecessor
+ * finishes.  Per-layer inputs come from `step` (q) and `io` (everything the
+ * commit also needs); outputs go to `step`, `tree`, `out` and the state in
+ * `io`.  Needs spec_workspace_bytes(cfg) of workspace like the other calls.
+ */
+int spec_verify_step(const spec_cfg *cfg, const int32_t *lat_tok, const float *lat_score,
+                     const spec_tree *tree, const spec_step_io *step, const void *logits,
+                     const spec_commit_io *io, const spec_accept *out, void *ws, void *stream);
+
 /* Copy the device status word into *host_status (host pointer) and wait for
  * `stream`.  Returns ST_OK, or ST_ECUDA if the copy failed. */
 int spec_status_read(const void *ws, uint32_t *host_status, void *stream);

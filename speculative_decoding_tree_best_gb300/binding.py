@@ -22,8 +22,8 @@ ST_OK, ST_EINVAL, ST_EUNSUPPORTED, ST_ECUDA, ST_EOVERFLOW, ST_TIMEOUT = range(6)
 SPEC_DEV_OVERFLOW, SPEC_DEV_BADLAT, SPEC_DEV_TIMEOUT = 0x1, 0x2, 0x4
 SPEC_IO_F32, SPEC_IO_BF16 = 0, 1
 EXPORTS = ("spec_workspace_bytes", "spec_tree_build", "gdn_tree_verify", "attn_tree_verify",
-           "accept_and_commit", "spec_status_read", "spec_status_clear", "spec_status_string",
-           "spec_abi_version")
+           "accept_and_commit", "spec_verify_step", "spec_status_read", "spec_status_clear",
+           "spec_status_string", "spec_abi_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -52,6 +52,10 @@ class SpecCommitIO(ctypes.Structure):
         "kv_len", "root_tok")]
 
 
+class SpecStepIO(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("gdn_q", "gdn_o", "gdn_c", "attn_q", "attn_o")]
+
+
 class SpecAccept(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("argmax", "accept_len", "accept_nodes", "out_tok")]
 
@@ -75,13 +79,17 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
             lib.accept_and_commit.argtypes = [cfgp, ctypes.POINTER(SpecTree), vp,
                                               ctypes.POINTER(SpecCommitIO),
                                               ctypes.POINTER(SpecAccept), vp, vp]
+            lib.spec_verify_step.argtypes = [cfgp, vp, vp, ctypes.POINTER(SpecTree),
+                                             ctypes.POINTER(SpecStepIO), vp,
+                                             ctypes.POINTER(SpecCommitIO),
+                                             ctypes.POINTER(SpecAccept), vp, vp]
             lib.spec_status_read.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
             lib.spec_status_clear.argtypes = [vp, vp]
             lib.spec_status_string.argtypes = [ctypes.c_int]
             lib.spec_status_string.restype = ctypes.c_char_p
             for n in ("spec_tree_build", "gdn_tree_verify", "attn_tree_verify",
-                      "accept_and_commit", "spec_status_read", "spec_status_clear",
-                      "spec_abi_version"):
+                      "accept_and_commit", "spec_verify_step", "spec_status_read",
+                      "spec_status_clear", "spec_abi_version"):
                 getattr(lib, n).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -207,18 +215,38 @@ def attn_tree_verify(cfg, tree: TreeBuffers, q, k_tree, v_tree, k_cache, v_cache
         _stream(stream)))
 
 
+def _commit_io(cfg, io: dict) -> SpecCommitIO:
+    dt = _io_dtype(cfg)
+    f32, i32 = torch.float32, torch.int32
+    types = dict(h0=f32, gdn_k=dt, gdn_v=dt, alpha=f32, beta=f32, k_tree=dt, v_tree=dt,
+                 k_cache=dt, v_cache=dt, kv_len=i32, root_tok=i32)
+    return SpecCommitIO(*(_ptr(io.get(n), types[n], n) for n in types))
+
+
 def accept_and_commit(cfg, tree: TreeBuffers, logits, io: dict, out: AcceptBuffers, ws,
                       stream=None):
     """io: dict with stacked h0, gdn_k, gdn_v, alpha, beta, k_tree, v_tree,
     k_cache, v_cache (None allowed where the layer count is 0), kv_len, root_tok."""
     dt = _io_dtype(cfg)
-    f32, i32 = torch.float32, torch.int32
-    types = dict(h0=f32, gdn_k=dt, gdn_v=dt, alpha=f32, beta=f32, k_tree=dt, v_tree=dt,
-                 k_cache=dt, v_cache=dt, kv_len=i32, root_tok=i32)
-    cio = SpecCommitIO(*(_ptr(io.get(n), types[n], n) for n in types))
+    cio = _commit_io(cfg, io)
     _check("accept_and_commit", load().accept_and_commit(
         ctypes.byref(cfg), ctypes.byref(tree.c()), _ptr(logits, dt, "logits"), ctypes.byref(cio),
         ctypes.byref(out.c()), _ptr(ws, name="ws"), _stream(stream)))
+
+
+def spec_verify_step(cfg, lat_tok, lat_score, tree: TreeBuffers, step: dict, logits, io: dict,
+                     out: AcceptBuffers, ws, stream=None):
+    """Whole verify step (tree, every GDN and attention layer, accept+commit).
+    step: dict with stacked gdn_q, gdn_o, gdn_c (or None), attn_q, attn_o."""
+    dt = _io_dtype(cfg)
+    sio = SpecStepIO(_ptr(step.get("gdn_q"), dt, "gdn_q"), _ptr(step.get("gdn_o"), dt, "gdn_o"),
+                     _ptr(step.get("gdn_c"), torch.float32, "gdn_c"),
+                     _ptr(step.get("attn_q"), dt, "attn_q"), _ptr(step.get("attn_o"), dt, "attn_o"))
+    _check("spec_verify_step", load().spec_verify_step(
+        ctypes.byref(cfg), _ptr(lat_tok, torch.int32, "lat_tok"),
+        _ptr(lat_score, torch.float32, "lat_score"), ctypes.byref(tree.c()), ctypes.byref(sio),
+        _ptr(logits, dt, "logits"), ctypes.byref(_commit_io(cfg, io)), ctypes.byref(out.c()),
+        _ptr(ws, name="ws"), _stream(stream)))
 
 
 def spec_status_read(ws, stream=None) -> int:

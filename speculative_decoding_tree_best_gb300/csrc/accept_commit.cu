@@ -175,6 +175,10 @@ argmax_accept(spec_cfg c, const typename io_t<IO>::T* __restrict__ logits, spec_
             ws_ptr<float2>(ws, w.argmax_off)[(size_t)row * kArgmaxSplit + sp] =
                 make_float2(bv, __int_as_float(bi));
     }
+    // The acceptance reads the tree and rewrites kv_len: everything before this
+    // launch must be done.
+    pdl_wait();
+    pdl_trigger();
     // Every CTA of the request takes a ticket; the last one runs the acceptance.
     __shared__ bool last;
     if (threadIdx.x == 0) {
@@ -213,6 +217,8 @@ commit_kernel(spec_cfg c, spec_commit_io io, spec_accept acc, void* ws, WsLayout
         float hr[RPT];
 #pragma unroll
         for (int i = 0; i < RPT; ++i) hr[i] = h[(size_t)(grp * RPT + i) * c.dv + c0 + col];
+        pdl_wait();
+        pdl_trigger();
         const int tau = plan[4 * b];
         if (tau == 0) return;
         float* ks = sc;                     // [tau][DK]
@@ -258,6 +264,8 @@ commit_kernel(spec_cfg c, spec_commit_io io, spec_accept acc, void* ws, WsLayout
         return;
     }
     // ---- KV append: one block per (layer, request, path slot) ----
+    pdl_wait();
+    pdl_trigger();
     int id = blockIdx.x - gdn_blocks;
     const int s = id % (m + 1); id /= (m + 1);
     const int b = id % c.B;
@@ -281,7 +289,7 @@ commit_kernel(spec_cfg c, spec_commit_io io, spec_accept acc, void* ws, WsLayout
 
 template <int IO, int DK>
 cudaError_t launch_commit(const spec_cfg& c, const spec_commit_io& io, const spec_accept& out,
-                          void* ws, const WsLayout& w, cudaStream_t st) {
+                          void* ws, const WsLayout& w, cudaStream_t st, bool pdl) {
     const int gdn_blocks = c.n_gdn_layers * c.B * c.Hv * (c.dv / 32);
     const int kv_blocks = c.n_attn_layers * c.B * (c.m + 1);
     if (gdn_blocks + kv_blocks == 0) return cudaSuccess;
@@ -289,29 +297,29 @@ cudaError_t launch_commit(const spec_cfg& c, const spec_commit_io& io, const spe
     auto kern = commit_kernel<IO, DK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<gdn_blocks + kv_blocks, NT, smem, st>>>(c, io, out, ws, w, gdn_blocks);
-    return cudaGetLastError();
+    return launch_k(pdl, kern, dim3(gdn_blocks + kv_blocks), dim3(NT), smem, st, c, io, out, ws, w,
+                    gdn_blocks);
 }
 
 }  // namespace
 
 cudaError_t launch_accept_commit(const spec_cfg& c, const spec_tree& t, const void* logits,
                                  const spec_commit_io& io, const spec_accept& out, void* ws,
-                                 cudaStream_t st) {
+                                 cudaStream_t st, bool pdl) {
     const WsLayout w = ws_layout(c);
     const int T = c.N + 1;
     dim3 g1(w.argmax_split, c.B * T);
-    if (c.io_dtype == SPEC_IO_BF16)
-        argmax_accept<SPEC_IO_BF16><<<g1, NT, 0, st>>>(c, static_cast<const __nv_bfloat16*>(logits), t, io, out, ws, w);
-    else
-        argmax_accept<SPEC_IO_F32><<<g1, NT, 0, st>>>(c, static_cast<const float*>(logits), t, io, out, ws, w);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = c.io_dtype == SPEC_IO_BF16
+        ? launch_k(pdl, argmax_accept<SPEC_IO_BF16>, g1, dim3(NT), 0, st, c,
+                   static_cast<const __nv_bfloat16*>(logits), t, io, out, ws, w)
+        : launch_k(pdl, argmax_accept<SPEC_IO_F32>, g1, dim3(NT), 0, st, c,
+                   static_cast<const float*>(logits), t, io, out, ws, w);
     if (e != cudaSuccess) return e;
     if (c.io_dtype == SPEC_IO_BF16)
-        return c.dk == 128 ? launch_commit<SPEC_IO_BF16, 128>(c, io, out, ws, w, st)
-                           : launch_commit<SPEC_IO_BF16, 64>(c, io, out, ws, w, st);
-    return c.dk == 128 ? launch_commit<SPEC_IO_F32, 128>(c, io, out, ws, w, st)
-                       : launch_commit<SPEC_IO_F32, 64>(c, io, out, ws, w, st);
+        return c.dk == 128 ? launch_commit<SPEC_IO_BF16, 128>(c, io, out, ws, w, st, pdl)
+                           : launch_commit<SPEC_IO_BF16, 64>(c, io, out, ws, w, st, pdl);
+    return c.dk == 128 ? launch_commit<SPEC_IO_F32, 128>(c, io, out, ws, w, st, pdl)
+                       : launch_commit<SPEC_IO_F32, 64>(c, io, out, ws, w, st, pdl);
 }
 
 }  // namespace spec

@@ -118,6 +118,56 @@ int accept_and_commit(const spec_cfg* cfg, const spec_tree* tree, const void* lo
                                               static_cast<cudaStream_t>(stream)));
 }
 
+int spec_verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_score,
+                     const spec_tree* tree, const spec_step_io* step, const void* logits,
+                     const spec_commit_io* io, const spec_accept* out, void* ws, void* stream) {
+    int rc = check_cfg(cfg);
+    if (rc) return rc;
+    if ((rc = check_tree(tree))) return rc;
+    if (!step || !io || !out) return ST_EINVAL;
+    if (!al16(lat_tok) || !al16(lat_score) || !al16(logits) || !al16(ws)) return ST_EINVAL;
+    if (!al16(io->kv_len) || !al16(io->root_tok)) return ST_EINVAL;
+    const spec_cfg& c = *cfg;
+    if (c.n_gdn_layers > 0 && (!al16(io->h0) || !al16(io->gdn_k) || !al16(io->gdn_v) ||
+                               !al16(io->alpha) || !al16(io->beta) || !al16(step->gdn_q) ||
+                               !al16(step->gdn_o) || (step->gdn_c && !al16(step->gdn_c))))
+        return ST_EINVAL;
+    if (c.n_attn_layers > 0 && (!al16(io->k_tree) || !al16(io->v_tree) || !al16(io->k_cache) ||
+                                !al16(io->v_cache) || !al16(step->attn_q) || !al16(step->attn_o)))
+        return ST_EINVAL;
+    if (!al16(out->argmax) || !al16(out->accept_len) || !al16(out->accept_nodes) ||
+        !al16(out->out_tok))
+        return ST_EINVAL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t esz = c.io_dtype == SPEC_IO_BF16 ? 2 : 4;
+    const size_t T = (size_t)c.N + 1, B = (size_t)c.B;
+    auto at = [](const void* p, size_t bytes) {
+        return static_cast<const char*>(p) + bytes;
+    };
+    cudaError_t e = spec::launch_tree_build(c, lat_tok, lat_score, io->root_tok, *tree, ws, st, true);
+    for (int l = 0; l < c.n_gdn_layers && e == cudaSuccess; ++l) {
+        const size_t state = (size_t)l * B * c.Hv * c.dk * c.dv;
+        const size_t kq = (size_t)l * B * T * c.Hk * c.dk * esz;
+        const size_t vo = (size_t)l * B * T * c.Hv * c.dv;
+        const size_t gate = (size_t)l * B * T * c.Hv;
+        e = spec::launch_gdn_tree(c, *tree, io->h0 + state, at(step->gdn_q, kq), at(io->gdn_k, kq),
+                                  at(io->gdn_v, vo * esz), io->alpha + gate, io->beta + gate,
+                                  const_cast<char*>(at(step->gdn_o, vo * esz)),
+                                  step->gdn_c ? step->gdn_c + vo : nullptr, st, true);
+    }
+    for (int l = 0; l < c.n_attn_layers && e == cudaSuccess; ++l) {
+        const size_t qo = (size_t)l * B * T * c.Hq * c.D * esz;
+        const size_t tr = (size_t)l * B * T * c.Hkv * c.D * esz;
+        const size_t ca = (size_t)l * B * c.Lmax * c.Hkv * c.D * esz;
+        e = spec::launch_attn_tree(c, *tree, at(step->attn_q, qo), at(io->k_tree, tr),
+                                   at(io->v_tree, tr), at(io->k_cache, ca), at(io->v_cache, ca),
+                                   io->kv_len, const_cast<char*>(at(step->attn_o, qo)), ws, st,
+                                   true, l & 1);
+    }
+    if (e == cudaSuccess) e = spec::launch_accept_commit(c, *tree, logits, *io, *out, ws, st, true);
+    return cuda_rc(e);
+}
+
 int spec_status_read(const void* ws, uint32_t* host_status, void* stream) {
     if (!ws || !host_status) return ST_EINVAL;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

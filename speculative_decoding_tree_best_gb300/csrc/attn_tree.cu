@@ -40,6 +40,8 @@ attn_partial_simt(spec_cfg c, spec_tree tree, const typename io_t<IO>::T* __rest
     constexpr int EPL = D / 32;
     const int ch = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int T = c.N + 1, G = c.Hq / c.Hkv, Hkv = c.Hkv;
+    pdl_wait();
+    pdl_trigger();
     int nn = tree.n_nodes[b];
     nn = nn < 1 ? 1 : (nn > T ? T : nn);
     int L = kv_len[b];
@@ -143,6 +145,8 @@ attn_merge(spec_cfg c, spec_tree tree, const int32_t* __restrict__ kv_len, void*
     const int T = c.N + 1, G = c.Hq / c.Hkv;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int r = blockIdx.x * NW + warp;
+    pdl_wait();
+    pdl_trigger();
     if (r >= G * T) return;
     int nn = tree.n_nodes[b];
     nn = nn < 1 ? 1 : (nn > T ? T : nn);
@@ -207,25 +211,24 @@ attn_merge(spec_cfg c, spec_tree tree, const int32_t* __restrict__ kv_len, void*
 }
 
 template <int IO, int D>
-cudaError_t launch_simt(const spec_cfg& c, const spec_tree& t, const void* q, const void* kt,
+cudaError_t launch_attn(const spec_cfg& c, const spec_tree& t, const void* q, const void* kt,
                         const void* vt, const void* kc, const void* vc, const int32_t* kv_len,
-                        void* o, void* ws, cudaStream_t st) {
+                        void* o, void* ws, cudaStream_t st, bool pdl, int part_buf) {
     using E = typename io_t<IO>::T;
-    const WsLayout w = ws_layout(c);
+    const WsLayout w = with_attn_buf(ws_layout(c), part_buf);
     cudaError_t e;
     if (attn_tc_supported(c)) {
-        e = launch_attn_tc(c, t, q, kt, vt, kc, vc, kv_len, ws, w, st);
+        e = launch_attn_tc(c, t, q, kt, vt, kc, vc, kv_len, ws, w, st, pdl);
     } else {
-        attn_partial_simt<IO, D><<<dim3(w.n_chunks, c.Hkv, c.B), NT, 0, st>>>(
-            c, t, static_cast<const E*>(q), static_cast<const E*>(kt), static_cast<const E*>(vt),
-            static_cast<const E*>(kc), static_cast<const E*>(vc), kv_len, ws, w);
-        e = cudaGetLastError();
+        e = launch_k(pdl, attn_partial_simt<IO, D>, dim3(w.n_chunks, c.Hkv, c.B), dim3(NT), 0, st,
+                     c, t, static_cast<const E*>(q), static_cast<const E*>(kt),
+                     static_cast<const E*>(vt), static_cast<const E*>(kc),
+                     static_cast<const E*>(vc), kv_len, ws, w);
     }
     if (e != cudaSuccess) return e;
     const int G = c.Hq / c.Hkv;
-    attn_merge<IO, D><<<dim3((G * (c.N + 1) + NW - 1) / NW, c.Hkv, c.B), NT, 0, st>>>(
-        c, t, kv_len, ws, w, static_cast<E*>(o));
-    return cudaGetLastError();
+    return launch_k(pdl, attn_merge<IO, D>, dim3((G * (c.N + 1) + NW - 1) / NW, c.Hkv, c.B),
+                    dim3(NT), 0, st, c, t, kv_len, ws, w, static_cast<E*>(o));
 }
 
 }  // namespace
@@ -233,13 +236,13 @@ cudaError_t launch_simt(const spec_cfg& c, const spec_tree& t, const void* q, co
 cudaError_t launch_attn_tree(const spec_cfg& c, const spec_tree& t, const void* q,
                              const void* k_tree, const void* v_tree, const void* k_cache,
                              const void* v_cache, const int32_t* kv_len, void* o, void* ws,
-                             cudaStream_t st) {
+                             cudaStream_t st, bool pdl, int part_buf) {
     if (c.io_dtype == SPEC_IO_BF16) {
-        return c.D == 128 ? launch_simt<SPEC_IO_BF16, 128>(c, t, q, k_tree, v_tree, k_cache, v_cache, kv_len, o, ws, st)
-                          : launch_simt<SPEC_IO_BF16, 64>(c, t, q, k_tree, v_tree, k_cache, v_cache, kv_len, o, ws, st);
+        return c.D == 128 ? launch_attn<SPEC_IO_BF16, 128>(c, t, q, k_tree, v_tree, k_cache, v_cache, kv_len, o, ws, st, pdl, part_buf)
+                          : launch_attn<SPEC_IO_BF16, 64>(c, t, q, k_tree, v_tree, k_cache, v_cache, kv_len, o, ws, st, pdl, part_buf);
     }
-    return c.D == 128 ? launch_simt<SPEC_IO_F32, 128>(c, t, q, k_tree, v_tree, k_cache, v_cache, kv_len, o, ws, st)
-                      : launch_simt<SPEC_IO_F32, 64>(c, t, q, k_tree, v_tree, k_cache, v_cache, kv_len, o, ws, st);
+    return c.D == 128 ? launch_attn<SPEC_IO_F32, 128>(c, t, q, k_tree, v_tree, k_cache, v_cache, kv_len, o, ws, st, pdl, part_buf)
+                      : launch_attn<SPEC_IO_F32, 64>(c, t, q, k_tree, v_tree, k_cache, v_cache, kv_len, o, ws, st, pdl, part_buf);
 }
 
 }  // namespace spec

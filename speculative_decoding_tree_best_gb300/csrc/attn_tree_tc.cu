@@ -242,6 +242,7 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         float* redl = reinterpret_cast<float*>(sm + OFF_REDL);
         uint32_t visbits = 0xffffffffu;                  // tree chunk: visible keys among my columns
         if (tree_chunk) {
+            pdl_wait();          // the tree may come from the launch just before
             int nn = prm.tree.n_nodes[b];
             nn = nn < 1 ? 1 : (nn > T ? T : nn);
             visbits = 0u;
@@ -392,6 +393,8 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
     }
     tc_fence_before();
     __syncthreads();
+    pdl_wait();
+    pdl_trigger();
     if (*abort_flag && threadIdx.x == 0) {
         // let the TMA copies still in flight land before the CTA's shared memory
         // is released: wait (bounded) on the phases of the last issued blocks
@@ -448,7 +451,7 @@ bool attn_tc_supported(const spec_cfg& c) {
 cudaError_t launch_attn_tc(const spec_cfg& c, const spec_tree& t, const void* q,
                            const void* k_tree, const void* v_tree, const void* k_cache,
                            const void* v_cache, const int32_t* kv_len, void* ws,
-                           const WsLayout& w, cudaStream_t st) {
+                           const WsLayout& w, cudaStream_t st, bool pdl) {
     const int T = c.N + 1, G = c.Hq / c.Hkv;
     const cuuint64_t e = 2;   // bytes per bf16
     CUtensorMap mq, mkc, mvc, mkt, mvt;
@@ -477,8 +480,8 @@ cudaError_t launch_attn_tc(const spec_cfg& c, const spec_tree& t, const void* q,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (err != cudaSuccess) return err;
     dim3 grid(w.n_chunks, c.Hkv * w.n_mt, c.B);
-    attn_tc_partial<<<grid, NTHREADS, SMEM_BYTES, st>>>(mq, mkc, mvc, mkt, mvt, prm);
-    return cudaGetLastError();
+    return launch_k(pdl, attn_tc_partial, grid, dim3(NTHREADS), SMEM_BYTES, st, mq, mkc, mvc, mkt,
+                    mvt, prm);
 }
 
 }  // namespace spec

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "spec_tree.h"
 
 namespace spec {
@@ -34,6 +36,36 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+// spec_verify_step launches every kernel of a step with programmatic stream
+// serialization, in a fixed order.  Each kernel follows one rule: code before
+// pdl_wait() reads only data that kernels two or more launches earlier in
+// that order wrote (or inputs no kernel of the step writes), and
+// pdl_trigger() comes after pdl_wait().  So when kernel N+1 starts, kernels
+// up to N-1 have completed and kernel N+1 stages its inputs while kernel N
+// finishes.  The four single-operation entry points launch conventionally
+// (pdl = false), where pdl_wait() returns at once: they are safe in any order.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+static inline cudaError_t launch_k(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                                   size_t smem, cudaStream_t st, Args&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 __device__ __forceinline__ void raise_status(void* ws, uint32_t bits) {
     atomicOr(reinterpret_cast<unsigned int*>(ws), bits);
 }
@@ -50,6 +82,7 @@ struct WsLayout {
     size_t attn_o_off;     // PT     [B][Hkv][n_mt][n_chunks][128][D]: O / l of the chunk,
                            // PT = fp16 for bf16 I/O, fp32 for fp32 I/O
     size_t attn_ml_off;    // float2 [B][Hkv][n_mt][n_chunks][128]: (max, sum)
+    size_t attn_o_off1, attn_ml_off1;  // a second partial buffer: attention layer l uses l % 2
     size_t ticket_off;     // uint32 [B][Hkv][n_mt]
     size_t plan_off;       // int32  [B][4]: committed tau (0 = skip), old kv_len
     size_t acc_ticket_off; // uint32 [B]: argmax CTAs finished per request
@@ -95,6 +128,15 @@ static inline WsLayout ws_layout(const spec_cfg& c, int num_sms = 152) {
     off = align_up(off + (c.io_dtype == SPEC_IO_BF16 ? 2 : 4) * tiles * 128 * (size_t)c.D, 256);
     w.attn_ml_off = off;
     off = align_up(off + sizeof(float) * 2 * tiles * 128, 256);
+    if (c.n_attn_layers > 1) {
+        w.attn_o_off1 = off;
+        off = align_up(off + (w.attn_ml_off - w.attn_o_off), 256);
+        w.attn_ml_off1 = off;
+        off = align_up(off + sizeof(float) * 2 * tiles * 128, 256);
+    } else {
+        w.attn_o_off1 = w.attn_o_off;
+        w.attn_ml_off1 = w.attn_ml_off;
+    }
     w.ticket_off = off;
     off = align_up(off + sizeof(uint32_t) * (size_t)c.B * c.Hkv * w.n_mt, 256);
     w.plan_off = off;
@@ -102,6 +144,15 @@ static inline WsLayout ws_layout(const spec_cfg& c, int num_sms = 152) {
     w.acc_ticket_off = off;
     off = align_up(off + sizeof(uint32_t) * (size_t)c.B, 256);
     w.total = off;
+    return w;
+}
+
+// The layout with attention partial buffer `buf` (0 or 1) selected.
+static inline WsLayout with_attn_buf(WsLayout w, int buf) {
+    if (buf & 1) {
+        w.attn_o_off = w.attn_o_off1;
+        w.attn_ml_off = w.attn_ml_off1;
+    }
     return w;
 }
 

@@ -115,13 +115,11 @@ gdn_tree_kernel(spec_cfg c, spec_tree tree, const float* __restrict__ h0,
     float* wu = sm + L.wu;
     float* wo = sm + L.wo;
 
-    int nn = tree.n_nodes[b];
-    nn = nn < 1 ? 1 : (nn > T ? T : nn);     // a malformed tree must not index out of range
-
-    // ---- stage: tree, gates, h0 slice, k/q rows, v slice ---------------------------
-    // Every global load of the first round is issued into registers before any
-    // shared-memory store, so the CTA pays one memory round trip, not one per
-    // loop iteration.
+    // ---- before the tree exists: stage h0 slice, k/q/v rows and gates of all T
+    // rows, then P = h0_slice^T [K; Q].  (Rows beyond the tree are padding and
+    // their results are never used.)  Every global load of the first round is
+    // issued into registers before any shared-memory store, so the CTA pays one
+    // memory round trip, not one per loop iteration.
     using E = typename io_t<IO>::T;
     constexpr int HQ = DK * (CB / 4) / NT;           // h0 float4 per thread
     constexpr int KQR = 8;                           // k/q 16-byte chunks per thread per round
@@ -135,21 +133,18 @@ gdn_tree_kernel(spec_cfg c, spec_tree tree, const float* __restrict__ h0,
         const int idx = tid + i * NT, r = idx / (CB / 4), q4 = idx % (CB / 4);
         hreg[i] = *reinterpret_cast<const float4*>(hsrc + (size_t)r * dv + q4 * 4);
     }
-    int t_par = -1, t_dep = 0;
     float t_al = 0.f, t_be = 0.f;
-    if (tid < nn) {
-        t_par = tree.node_parent[(size_t)b * T + tid];
-        t_dep = tree.node_depth[(size_t)b * T + tid];
+    if (tid < T) {
         t_al = alpha[((size_t)b * T + tid) * Hv + j];
         t_be = beta[((size_t)b * T + tid) * Hv + j];
     }
     uint4 vreg = make_uint4(0, 0, 0, 0);
-    const bool has_v = tid < nn * VC;
+    const bool has_v = tid < T * VC;
     if (has_v) {
         const int x = tid / VC, e0 = (tid % VC) * EPC;
         vreg = *reinterpret_cast<const uint4*>(v + (((size_t)b * T + x) * Hv + j) * dv + c0 + e0);
     }
-    const int nkq = 2 * nn * KQC;
+    const int nkq = 2 * T * KQC;
     for (int base = 0; base < nkq; base += NT * KQR) {
         uint4 kreg[KQR];
 #pragma unroll
@@ -157,9 +152,9 @@ gdn_tree_kernel(spec_cfg c, spec_tree tree, const float* __restrict__ h0,
             const int idx = base + tid + i * NT;
             if (idx < nkq) {
                 const int row = idx / KQC, ch = idx % KQC;
-                const int x = row < nn ? row : row - nn;
+                const int x = row < T ? row : row - T;
                 kreg[i] = *reinterpret_cast<const uint4*>(
-                    (row < nn ? k : q) + (((size_t)b * T + x) * Hk + ih) * DK + ch * EPC);
+                    (row < T ? k : q) + (((size_t)b * T + x) * Hk + ih) * DK + ch * EPC);
             }
         }
 #pragma unroll
@@ -181,9 +176,7 @@ gdn_tree_kernel(spec_cfg c, spec_tree tree, const float* __restrict__ h0,
         const int idx = tid + i * NT, r = idx / (CB / 4), q4 = idx % (CB / 4);
         *reinterpret_cast<float4*>(hs + r * CB + q4 * 4) = hreg[i];
     }
-    if (tid < nn) {
-        par[tid] = (t_par >= 0 && t_par < tid) ? t_par : -1;
-        dep[tid] = t_dep < 0 ? 0 : (t_dep >= S ? S - 1 : t_dep);
+    if (tid < T) {
         al[tid] = t_al;
         be[tid] = t_be;
     }
@@ -194,20 +187,53 @@ gdn_tree_kernel(spec_cfg c, spec_tree tree, const float* __restrict__ h0,
 #pragma unroll
         for (int e = 0; e < EPC; ++e) vs[x * CB + e0 + e] = f[e];
     }
-    for (int x = NT + tid; x < nn; x += NT) {     // trees with more rows than threads
-        const int pp = tree.node_parent[(size_t)b * T + x];
-        const int d = tree.node_depth[(size_t)b * T + x];
-        par[x] = (pp >= 0 && pp < x) ? pp : -1;
-        dep[x] = d < 0 ? 0 : (d >= S ? S - 1 : d);
+    for (int x = NT + tid; x < T; x += NT) {       // more rows than threads
         al[x] = alpha[((size_t)b * T + x) * Hv + j];
         be[x] = beta[((size_t)b * T + x) * Hv + j];
     }
-    for (int idx = NT + tid; idx < nn * VC; idx += NT) {
+    for (int idx = NT + tid; idx < T * VC; idx += NT) {
         const int x = idx / VC, e0 = (idx % VC) * EPC;
         float f[EPC];
         unpack16<IO>(*reinterpret_cast<const uint4*>(v + (((size_t)b * T + x) * Hv + j) * dv + c0 + e0), f);
 #pragma unroll
         for (int e = 0; e < EPC; ++e) vs[x * CB + e0 + e] = f[e];
+    }
+    __syncthreads();
+
+    // ---- P = h0_slice^T [K; Q]: rows t = grp + 8 i, column col ------------------------
+    for (int t0 = 0; t0 < 2 * T; t0 += 8 * NG) {
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        for (int r = 0; r < DK; r += 4) {
+            const float h_0 = hs[(r + 0) * CB + col], h_1 = hs[(r + 1) * CB + col];
+            const float h_2 = hs[(r + 2) * CB + col], h_3 = hs[(r + 3) * CB + col];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int t = t0 + grp + NG * i;
+                if (t < 2 * T) {
+                    const float4 kk = *reinterpret_cast<const float4*>(kq + t * KQS + r);
+                    acc[i] = fmaf(h_0, kk.x, fmaf(h_1, kk.y, fmaf(h_2, kk.z, fmaf(h_3, kk.w, acc[i]))));
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int t = t0 + grp + NG * i;
+            if (t < 2 * T) P[t * CB + col] = acc[i];
+        }
+    }
+
+    // ---- the tree (written by the previous launch) from here on ----------------------
+    pdl_wait();
+    pdl_trigger();
+    int nn = tree.n_nodes[b];
+    nn = nn < 1 ? 1 : (nn > T ? T : nn);     // a malformed tree must not index out of range
+    for (int x = tid; x < nn; x += NT) {
+        const int pp = tree.node_parent[(size_t)b * T + x];
+        const int d = tree.node_depth[(size_t)b * T + x];
+        par[x] = (pp >= 0 && pp < x) ? pp : -1;
+        dep[x] = d < 0 ? 0 : (d >= S ? S - 1 : d);
     }
     __syncthreads();
 
@@ -232,7 +258,7 @@ gdn_tree_kernel(spec_cfg c, spec_tree tree, const float* __restrict__ h0,
         if (s > d) continue;
         const float4* ka = reinterpret_cast<const float4*>(kq + pidx[x * S + s] * KQS);
         const float4* kx = reinterpret_cast<const float4*>(kq + x * KQS);
-        const float4* qx = reinterpret_cast<const float4*>(kq + (nn + x) * KQS);
+        const float4* qx = reinterpret_cast<const float4*>(kq + (T + x) * KQS);
         float dq0 = 0.f, dq1 = 0.f, dk0 = 0.f, dk1 = 0.f;
 #pragma unroll 8
         for (int e = 0; e < DK / 4; e += 2) {
@@ -248,29 +274,6 @@ gdn_tree_kernel(spec_cfg c, spec_tree tree, const float* __restrict__ h0,
         if (s < d) wu[x * S + s] *= dk0 + dk1;
     }
 
-    // ---- P = h0_slice^T [K; Q]: rows t = grp + 8 i, column col ------------------------
-    for (int t0 = 0; t0 < 2 * nn; t0 += 8 * NG) {
-        float acc[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-        for (int r = 0; r < DK; r += 4) {
-            const float h_0 = hs[(r + 0) * CB + col], h_1 = hs[(r + 1) * CB + col];
-            const float h_2 = hs[(r + 2) * CB + col], h_3 = hs[(r + 3) * CB + col];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int t = t0 + grp + NG * i;
-                if (t < 2 * nn) {
-                    const float4 kk = *reinterpret_cast<const float4*>(kq + t * KQS + r);
-                    acc[i] = fmaf(h_0, kk.x, fmaf(h_1, kk.y, fmaf(h_2, kk.z, fmaf(h_3, kk.w, acc[i]))));
-                }
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int t = t0 + grp + NG * i;
-            if (t < 2 * nn) P[t * CB + col] = acc[i];
-        }
-    }
     __syncthreads();
 
     if constexpr (MAXD > 0) {
@@ -285,7 +288,7 @@ gdn_tree_kernel(spec_cfg c, spec_tree tree, const float* __restrict__ h0,
             if (x < nn) {
                 const int d = dep[x];
                 float cc[MAXD];
-                ox = A[x] * P[(nn + x) * CB + col];
+                ox = A[x] * P[(T + x) * CB + col];
 #pragma unroll
                 for (int s = 0; s < MAXD; ++s) {
                     if (s > d) break;
@@ -321,7 +324,7 @@ gdn_tree_kernel(spec_cfg c, spec_tree tree, const float* __restrict__ h0,
     for (int x = grp; x < T; x += NG) {
         float ox = 0.0f, cx = 0.0f;
         if (x < nn) {
-            ox = A[x] * P[(nn + x) * CB + col];
+            ox = A[x] * P[(T + x) * CB + col];
             const int d = dep[x];
             for (int s = 0; s <= d; ++s) ox = fmaf(wo[x * S + s], cv[pidx[x * S + s] * CB + col], ox);
             cx = cv[x * CB + col];
@@ -335,15 +338,15 @@ gdn_tree_kernel(spec_cfg c, spec_tree tree, const float* __restrict__ h0,
 template <int IO, int DK, int MAXD>
 cudaError_t launch_one(const spec_cfg& c, const spec_tree& t, const float* h0, const void* q,
                        const void* k, const void* v, const float* alpha, const float* beta,
-                       void* o, float* c_out, size_t smem, cudaStream_t st) {
+                       void* o, float* c_out, size_t smem, cudaStream_t st, bool pdl) {
     using E = typename io_t<IO>::T;
     auto kern = gdn_tree_kernel<IO, DK, MAXD>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(c.dv / CB, c.Hv, c.B);
-    kern<<<grid, NT, smem, st>>>(c, t, h0, static_cast<const E*>(q), static_cast<const E*>(k),
-                                 static_cast<const E*>(v), alpha, beta, static_cast<E*>(o), c_out);
-    return cudaGetLastError();
+    return launch_k(pdl, kern, grid, dim3(NT), smem, st, c, t, h0, static_cast<const E*>(q),
+                      static_cast<const E*>(k), static_cast<const E*>(v), alpha, beta,
+                      static_cast<E*>(o), c_out);
 }
 
 }  // namespace
@@ -354,15 +357,16 @@ size_t gdn_tree_smem(const spec_cfg& c) {
 
 cudaError_t launch_gdn_tree(const spec_cfg& c, const spec_tree& t, const float* h0,
                             const void* q, const void* k, const void* v, const float* alpha,
-                            const float* beta, void* o, float* c_out, cudaStream_t st) {
+                            const float* beta, void* o, float* c_out, cudaStream_t st,
+                            bool pdl) {
     const size_t smem = gdn_tree_smem(c);
     if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
     const int T = c.N + 1;
     const int S = (c.m < T - 1 ? c.m : T - 1) + 1;        // rows on the longest root path
     const bool chains = S <= kChainMax;
 #define SPEC_GDN_LAUNCH(IO_, DK_)                                                              \
-    return chains ? launch_one<IO_, DK_, kChainMax>(c, t, h0, q, k, v, alpha, beta, o, c_out, smem, st) \
-                  : launch_one<IO_, DK_, 0>(c, t, h0, q, k, v, alpha, beta, o, c_out, smem, st)
+    return chains ? launch_one<IO_, DK_, kChainMax>(c, t, h0, q, k, v, alpha, beta, o, c_out, smem, st, pdl) \
+                  : launch_one<IO_, DK_, 0>(c, t, h0, q, k, v, alpha, beta, o, c_out, smem, st, pdl)
     if (c.io_dtype == SPEC_IO_BF16) {
         if (c.dk == 128) { SPEC_GDN_LAUNCH(SPEC_IO_BF16, 128); }
         SPEC_GDN_LAUNCH(SPEC_IO_BF16, 64);

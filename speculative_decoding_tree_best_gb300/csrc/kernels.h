@@ -7,31 +7,33 @@
 
 namespace spec {
 
+// pdl: launch with programmatic stream serialization (spec_verify_step only).
 cudaError_t launch_tree_build(const spec_cfg& c, const int32_t* lat_tok, const float* lat_score,
                               const int32_t* root_tok, const spec_tree& out, void* ws,
-                              cudaStream_t st);
+                              cudaStream_t st, bool pdl = false);
 size_t tree_build_smem(const spec_cfg& c);
 
 // Returns cudaErrorInvalidConfiguration when the shape needs more shared memory
 // than one CTA can have.
 cudaError_t launch_gdn_tree(const spec_cfg& c, const spec_tree& t, const float* h0,
                             const void* q, const void* k, const void* v, const float* alpha,
-                            const float* beta, void* o, float* c_out, cudaStream_t st);
+                            const float* beta, void* o, float* c_out, cudaStream_t st,
+                            bool pdl = false);
 size_t gdn_tree_smem(const spec_cfg& c);
 
 cudaError_t launch_attn_tree(const spec_cfg& c, const spec_tree& t, const void* q,
                              const void* k_tree, const void* v_tree, const void* k_cache,
                              const void* v_cache, const int32_t* kv_len, void* o, void* ws,
-                             cudaStream_t st);
+                             cudaStream_t st, bool pdl = false, int part_buf = 0);
 
 bool attn_tc_supported(const spec_cfg& c);
 cudaError_t launch_attn_tc(const spec_cfg& c, const spec_tree& t, const void* q,
                            const void* k_tree, const void* v_tree, const void* k_cache,
                            const void* v_cache, const int32_t* kv_len, void* ws,
-                           const WsLayout& w, cudaStream_t st);
+                           const WsLayout& w, cudaStream_t st, bool pdl);
 
 cudaError_t launch_accept_commit(const spec_cfg& c, const spec_tree& t, const void* logits,
                                  const spec_commit_io& io, const spec_accept& out, void* ws,
-                                 cudaStream_t st);
+                                 cudaStream_t st, bool pdl = false);
 
 }  // namespace spec

@@ -60,6 +60,8 @@ tree_build_kernel(spec_cfg c, const int32_t* __restrict__ lat_tok,
     float* r_sc = reinterpret_cast<float*>(r_tok + MK);      // [m][K] as given
 
     // ---- 1. stage (one round trip), then rank: 32 / K2 positions per warp pass --------
+    pdl_wait();          // the previous step's acceptance wrote root_tok
+    pdl_trigger();
     const int root = root_tok[b];
     for (int i = lane; i < MK; i += 32) {
         r_tok[i] = lat_tok[(size_t)b * MK + i];
@@ -267,16 +269,14 @@ size_t tree_build_smem(const spec_cfg& c) {
 
 cudaError_t launch_tree_build(const spec_cfg& c, const int32_t* lat_tok, const float* lat_score,
                               const int32_t* root_tok, const spec_tree& out, void* ws,
-                              cudaStream_t st) {
+                              cudaStream_t st, bool pdl) {
     const size_t smem = tree_build_smem(c);
     const int T = c.N + 1;
     if (T <= 32)
-        tree_build_kernel<1><<<c.B, 32, smem, st>>>(c, lat_tok, lat_score, root_tok, out, ws);
-    else if (T <= 64)
-        tree_build_kernel<2><<<c.B, 32, smem, st>>>(c, lat_tok, lat_score, root_tok, out, ws);
-    else
-        tree_build_kernel<4><<<c.B, 32, smem, st>>>(c, lat_tok, lat_score, root_tok, out, ws);
-    return cudaGetLastError();
+        return launch_k(pdl, tree_build_kernel<1>, dim3(c.B), dim3(32), smem, st, c, lat_tok, lat_score, root_tok, out, ws);
+    if (T <= 64)
+        return launch_k(pdl, tree_build_kernel<2>, dim3(c.B), dim3(32), smem, st, c, lat_tok, lat_score, root_tok, out, ws);
+    return launch_k(pdl, tree_build_kernel<4>, dim3(c.B), dim3(32), smem, st, c, lat_tok, lat_score, root_tok, out, ws);
 }
 
 }  // namespace spec

@@ -74,10 +74,20 @@ class VerifyStep:
         binding.accept_and_commit(self.cfg, self.tree, self.x["logits"], self.commit_io(),
                                   self.acc, self.ws, stream)
 
-    def run(self, stream=None):
+    def run_calls(self, stream=None):
+        """The step as the four single-operation calls."""
         self.build_tree(stream)
         self.verify(stream)
         self.accept_commit(stream)
+
+    def run(self, stream=None):
+        """The step as one spec_verify_step call (programmatic dependent launch)."""
+        x = self.x
+        step = dict(gdn_q=x["gdn_q"], gdn_o=self.gdn_o if self.cfg.n_gdn_layers else None,
+                    gdn_c=None, attn_q=x["attn_q"],
+                    attn_o=self.attn_o if self.cfg.n_attn_layers else None)
+        binding.spec_verify_step(self.cfg, x["lat_tok"], x["lat_score"], self.tree, step,
+                                 x["logits"], self.commit_io(), self.acc, self.ws, stream)
 
     @property
     def launches_per_step(self) -> int:

@@ -48,10 +48,15 @@ def prepare(scfg: synth.SpecConfig, seed: int, kv_len=None, lat_edit=None):
     return inp, tree
 
 
-def run_gpu(scfg, inp):
+def run_gpu(scfg, inp, calls=False):
+    """One step on the GPU: one spec_verify_step call, or (calls=True) the four
+    single-operation calls."""
     x = stack_inputs(inp, "cuda")
     st = VerifyStep(scfg, x)
-    st.run()
+    if calls:
+        st.run_calls()
+    else:
+        st.run()
     torch.cuda.synchronize()
     return st
 
@@ -174,8 +179,9 @@ def compare(scfg, inp, tree_o, st, req=None, attn_kv_heads=None, gdn_layers=None
 def check_case(scfg, seed, **kw):
     kv_len = kw.pop("kv_len", None)
     lat_edit = kw.pop("lat_edit", None)
+    calls = kw.pop("calls", False)
     inp, tree_o = prepare(scfg, seed, kv_len=kv_len, lat_edit=lat_edit)
-    st = run_gpu(scfg, inp)
+    st = run_gpu(scfg, inp, calls=calls)
     res = compare(scfg, inp, tree_o, st, **kw)
     res["status"] = __import__("speculative_decoding_tree_best_gb300.binding",
                                fromlist=["x"]).spec_status_read(st.ws)
