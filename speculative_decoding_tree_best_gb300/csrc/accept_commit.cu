@@ -47,12 +47,18 @@ __device__ void accept_request(const spec_cfg& c, const spec_tree& tree, const s
     for (int t = lane; t < T; t += 32) {
         int a = -1;
         if (t < nn) {
+            // all segment partials of the row in flight, then reduced
+            float2 pp[kArgmaxSplit];
+#pragma unroll
+            for (int sp = 0; sp < kArgmaxSplit; ++sp)
+                pp[sp] = sp < w.argmax_split ? part[((size_t)b * T + t) * kArgmaxSplit + sp]
+                                             : make_float2(-INFINITY, __int_as_float(0x7fffffff));
             float bv = -INFINITY;
             int bi = 0x7fffffff;
-            for (int sp = 0; sp < w.argmax_split; ++sp) {
-                const float2 p = part[((size_t)b * T + t) * kArgmaxSplit + sp];
-                const int pi = __float_as_int(p.y);
-                if (better(p.x, pi, bv, bi)) { bv = p.x; bi = pi; }
+#pragma unroll
+            for (int sp = 0; sp < kArgmaxSplit; ++sp) {
+                const int pi = __float_as_int(pp[sp].y);
+                if (better(pp[sp].x, pi, bv, bi)) { bv = pp[sp].x; bi = pi; }
             }
             a = bi;
         }
@@ -195,78 +201,68 @@ argmax_accept(spec_cfg c, const typename io_t<IO>::T* __restrict__ logits, spec_
     }
 }
 
+// Gated-delta steps of the accepted rows on 32 state columns (rows split over
+// the CTA's 8 warps, held in registers), written back in place.
 template <int IO, int DK>
-__global__ void __launch_bounds__(NT)
-commit_kernel(spec_cfg c, spec_commit_io io, spec_accept acc, void* ws, WsLayout w, int gdn_blocks) {
+__device__ __forceinline__ void commit_state(const spec_cfg& c, const spec_commit_io& io,
+                                             const spec_accept& acc, const int32_t* plan,
+                                             float* hr, float* h, int b, int j, int layer, int cb,
+                                             float* sc) {
     using E = typename io_t<IO>::T;
-    extern __shared__ __align__(16) float sc[];
-    const int T = c.N + 1, m = c.m;
-    const int32_t* plan = ws_ptr<const int32_t>(ws, w.plan_off);
-    const int tid = threadIdx.x;
-    if ((int)blockIdx.x < gdn_blocks) {
-        constexpr int CB = 32, NG = NT / 32, RPT = DK / NG;
-        const int nb = c.dv / CB;
-        int id = blockIdx.x;
-        const int cb = id % nb; id /= nb;
-        const int j = id % c.Hv; id /= c.Hv;
-        const int b = id % c.B;
-        const int layer = id / c.B;
-        const int ih = j / (c.Hv / c.Hk), c0 = cb * CB, col = tid & 31, grp = tid >> 5;
-        // the state slice does not depend on the acceptance: load it first
-        float* h = io.h0 + (size_t)layer * c.B * c.Hv * DK * c.dv + ((size_t)b * c.Hv + j) * DK * c.dv;
-        float hr[RPT];
-#pragma unroll
-        for (int i = 0; i < RPT; ++i) hr[i] = h[(size_t)(grp * RPT + i) * c.dv + c0 + col];
-        pdl_wait();
-        pdl_trigger();
-        const int tau = plan[4 * b];
-        if (tau == 0) return;
-        float* ks = sc;                     // [tau][DK]
-        float* vsm = ks + (m + 1) * DK;     // [tau][CB]
-        float* ab = vsm + (m + 1) * CB;     // [tau][2]
-        float* red = ab + 2 * (m + 1);      // [2][NG][CB]
-        const E* kl = static_cast<const E*>(io.gdn_k) + (size_t)layer * c.B * T * c.Hk * DK;
-        const E* vl = static_cast<const E*>(io.gdn_v) + (size_t)layer * c.B * T * c.Hv * c.dv;
-        const float* al = io.alpha + (size_t)layer * c.B * T * c.Hv;
-        const float* be = io.beta + (size_t)layer * c.B * T * c.Hv;
-        const int32_t* nodes = acc.accept_nodes + (size_t)b * (m + 1);
-        for (int idx = tid; idx < tau * DK; idx += NT) {
-            const int s = idx / DK, r = idx % DK, x = nodes[s];
-            ks[idx] = io_t<IO>::ld(kl, (((size_t)b * T + x) * c.Hk + ih) * DK + r);
-        }
-        for (int idx = tid; idx < tau * CB; idx += NT) {
-            const int s = idx / CB, cc = idx % CB, x = nodes[s];
-            vsm[idx] = io_t<IO>::ld(vl, (((size_t)b * T + x) * c.Hv + j) * c.dv + c0 + cc);
-        }
-        for (int s = tid; s < tau; s += NT) {
-            const int x = nodes[s];
-            ab[2 * s] = al[((size_t)b * T + x) * c.Hv + j];
-            ab[2 * s + 1] = be[((size_t)b * T + x) * c.Hv + j];
-        }
-        __syncthreads();
-        for (int s = 0; s < tau; ++s) {
-            const float* kk = ks + s * DK + grp * RPT;
-            float part = 0.0f;
-#pragma unroll
-            for (int i = 0; i < RPT; ++i) part = fmaf(hr[i], kk[i], part);
-            float* rb = red + (s & 1) * NG * CB;
-            rb[grp * CB + col] = part;
-            __syncthreads();
-            float u = 0.0f;
-#pragma unroll
-            for (int g2 = 0; g2 < NG; ++g2) u += rb[g2 * CB + col];
-            const float a = ab[2 * s], bb = ab[2 * s + 1], vv = vsm[s * CB + col];
-#pragma unroll
-            for (int i = 0; i < RPT; ++i) hr[i] = a * (hr[i] - bb * kk[i] * u) + bb * kk[i] * vv;
-        }
-#pragma unroll
-        for (int i = 0; i < RPT; ++i) h[(size_t)(grp * RPT + i) * c.dv + c0 + col] = hr[i];
-        return;
+    constexpr int CB = 32, NG = NT / 32, RPT = DK / NG;
+    const int T = c.N + 1, m = c.m, tid = threadIdx.x;
+    const int ih = j / (c.Hv / c.Hk), c0 = cb * CB, col = tid & 31, grp = tid >> 5;
+    const int tau = plan[4 * b];
+    if (tau == 0) return;
+    float* ks = sc;                     // [tau][DK]
+    float* vsm = ks + (m + 1) * DK;     // [tau][CB]
+    float* ab = vsm + (m + 1) * CB;     // [tau][2]
+    float* red = ab + 2 * (m + 1);      // [2][NG][CB]
+    const E* kl = static_cast<const E*>(io.gdn_k) + (size_t)layer * c.B * T * c.Hk * DK;
+    const E* vl = static_cast<const E*>(io.gdn_v) + (size_t)layer * c.B * T * c.Hv * c.dv;
+    const float* al = io.alpha + (size_t)layer * c.B * T * c.Hv;
+    const float* be = io.beta + (size_t)layer * c.B * T * c.Hv;
+    const int32_t* nodes = acc.accept_nodes + (size_t)b * (m + 1);
+    for (int idx = tid; idx < tau * DK; idx += NT) {
+        const int s = idx / DK, r = idx % DK, x = nodes[s];
+        ks[idx] = io_t<IO>::ld(kl, (((size_t)b * T + x) * c.Hk + ih) * DK + r);
     }
-    // ---- KV append: one block per (layer, request, path slot) ----
-    pdl_wait();
-    pdl_trigger();
-    int id = blockIdx.x - gdn_blocks;
+    for (int idx = tid; idx < tau * CB; idx += NT) {
+        const int s = idx / CB, cc = idx % CB, x = nodes[s];
+        vsm[idx] = io_t<IO>::ld(vl, (((size_t)b * T + x) * c.Hv + j) * c.dv + c0 + cc);
+    }
+    for (int s = tid; s < tau; s += NT) {
+        const int x = nodes[s];
+        ab[2 * s] = al[((size_t)b * T + x) * c.Hv + j];
+        ab[2 * s + 1] = be[((size_t)b * T + x) * c.Hv + j];
+    }
+    __syncthreads();
+    for (int s = 0; s < tau; ++s) {
+        const float* kk = ks + s * DK + grp * RPT;
+        float part = 0.0f;
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) part = fmaf(hr[i], kk[i], part);
+        float* rb = red + (s & 1) * NG * CB;
+        rb[grp * CB + col] = part;
+        __syncthreads();
+        float u = 0.0f;
+#pragma unroll
+        for (int g2 = 0; g2 < NG; ++g2) u += rb[g2 * CB + col];
+        const float a = ab[2 * s], bb = ab[2 * s + 1], vv = vsm[s * CB + col];
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) hr[i] = a * (hr[i] - bb * kk[i] * u) + bb * kk[i] * vv;
+    }
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) h[(size_t)(grp * RPT + i) * c.dv + c0 + col] = hr[i];
+}
+
+// Copy the tree K/V row of accepted path slot s of (layer, request) into the
+// cache; block id encodes (layer, request, slot).
+template <int IO>
+__device__ __forceinline__ void append_kv(const spec_cfg& c, const spec_commit_io& io,
+                                          const spec_accept& acc, const int32_t* plan, int id) {
+    using E = typename io_t<IO>::T;
+    const int T = c.N + 1, m = c.m, tid = threadIdx.x;
     const int s = id % (m + 1); id /= (m + 1);
     const int b = id % c.B;
     const int layer = id / c.B;
@@ -287,9 +283,51 @@ commit_kernel(spec_cfg c, spec_commit_io io, spec_accept acc, void* ws, WsLayout
     }
 }
 
+// early: the acceptance, or a GDN layer that still reads h0, may be the launch
+// just before this one, so wait before anything else; otherwise both are at
+// least two launches back and the wait moves to the end.
 template <int IO, int DK>
-cudaError_t launch_commit(const spec_cfg& c, const spec_commit_io& io, const spec_accept& out,
-                          void* ws, const WsLayout& w, cudaStream_t st, bool pdl) {
+__global__ void __launch_bounds__(NT)
+commit_kernel(spec_cfg c, spec_commit_io io, spec_accept acc, void* ws, WsLayout w, int gdn_blocks,
+              bool early) {
+    extern __shared__ __align__(16) float sc[];
+    const int32_t* plan = ws_ptr<const int32_t>(ws, w.plan_off);
+    const int tid = threadIdx.x;
+    if ((int)blockIdx.x < gdn_blocks) {
+        constexpr int CB = 32, NG = NT / 32, RPT = DK / NG;
+        const int nb = c.dv / CB;
+        int id = blockIdx.x;
+        const int cb = id % nb; id /= nb;
+        const int j = id % c.Hv; id /= c.Hv;
+        const int b = id % c.B;
+        const int layer = id / c.B;
+        const int c0 = cb * CB, col = tid & 31, grp = tid >> 5;
+        // the state slice does not depend on the acceptance: load it first
+        float* h = io.h0 + (size_t)layer * c.B * c.Hv * DK * c.dv + ((size_t)b * c.Hv + j) * DK * c.dv;
+        float hr[RPT];
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) hr[i] = h[(size_t)(grp * RPT + i) * c.dv + c0 + col];
+        if (early) {
+            pdl_wait();
+            pdl_trigger();
+        }
+        commit_state<IO, DK>(c, io, acc, plan, hr, h, b, j, layer, cb, sc);
+    } else {
+        if (early) {
+            pdl_wait();
+            pdl_trigger();
+        }
+        append_kv<IO>(c, io, acc, plan, blockIdx.x - gdn_blocks);
+    }
+    if (!early) {
+        pdl_wait();
+        pdl_trigger();
+    }
+}
+
+template <int IO, int DK>
+cudaError_t launch_commit_k(const spec_cfg& c, const spec_commit_io& io, const spec_accept& out,
+                            void* ws, const WsLayout& w, cudaStream_t st, bool pdl, bool early) {
     const int gdn_blocks = c.n_gdn_layers * c.B * c.Hv * (c.dv / 32);
     const int kv_blocks = c.n_attn_layers * c.B * (c.m + 1);
     if (gdn_blocks + kv_blocks == 0) return cudaSuccess;
@@ -298,28 +336,39 @@ cudaError_t launch_commit(const spec_cfg& c, const spec_commit_io& io, const spe
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_k(pdl, kern, dim3(gdn_blocks + kv_blocks), dim3(NT), smem, st, c, io, out, ws, w,
-                    gdn_blocks);
+                    gdn_blocks, early);
 }
 
 }  // namespace
 
-cudaError_t launch_accept_commit(const spec_cfg& c, const spec_tree& t, const void* logits,
+cudaError_t launch_argmax_accept(const spec_cfg& c, const spec_tree& t, const void* logits,
                                  const spec_commit_io& io, const spec_accept& out, void* ws,
                                  cudaStream_t st, bool pdl) {
     const WsLayout w = ws_layout(c);
-    const int T = c.N + 1;
-    dim3 g1(w.argmax_split, c.B * T);
-    cudaError_t e = c.io_dtype == SPEC_IO_BF16
+    dim3 g1(w.argmax_split, c.B * (c.N + 1));
+    return c.io_dtype == SPEC_IO_BF16
         ? launch_k(pdl, argmax_accept<SPEC_IO_BF16>, g1, dim3(NT), 0, st, c,
                    static_cast<const __nv_bfloat16*>(logits), t, io, out, ws, w)
         : launch_k(pdl, argmax_accept<SPEC_IO_F32>, g1, dim3(NT), 0, st, c,
                    static_cast<const float*>(logits), t, io, out, ws, w);
-    if (e != cudaSuccess) return e;
+}
+
+cudaError_t launch_commit(const spec_cfg& c, const spec_commit_io& io, const spec_accept& out,
+                          void* ws, cudaStream_t st, bool pdl, bool early) {
+    const WsLayout w = ws_layout(c);
     if (c.io_dtype == SPEC_IO_BF16)
-        return c.dk == 128 ? launch_commit<SPEC_IO_BF16, 128>(c, io, out, ws, w, st, pdl)
-                           : launch_commit<SPEC_IO_BF16, 64>(c, io, out, ws, w, st, pdl);
-    return c.dk == 128 ? launch_commit<SPEC_IO_F32, 128>(c, io, out, ws, w, st, pdl)
-                       : launch_commit<SPEC_IO_F32, 64>(c, io, out, ws, w, st, pdl);
+        return c.dk == 128 ? launch_commit_k<SPEC_IO_BF16, 128>(c, io, out, ws, w, st, pdl, early)
+                           : launch_commit_k<SPEC_IO_BF16, 64>(c, io, out, ws, w, st, pdl, early);
+    return c.dk == 128 ? launch_commit_k<SPEC_IO_F32, 128>(c, io, out, ws, w, st, pdl, early)
+                       : launch_commit_k<SPEC_IO_F32, 64>(c, io, out, ws, w, st, pdl, early);
+}
+
+cudaError_t launch_accept_commit(const spec_cfg& c, const spec_tree& t, const void* logits,
+                                 const spec_commit_io& io, const spec_accept& out, void* ws,
+                                 cudaStream_t st, bool pdl) {
+    cudaError_t e = launch_argmax_accept(c, t, logits, io, out, ws, st, pdl);
+    if (e != cudaSuccess) return e;
+    return launch_commit(c, io, out, ws, st, pdl, true);
 }
 
 }  // namespace spec

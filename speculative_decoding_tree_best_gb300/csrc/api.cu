@@ -144,8 +144,39 @@ int spec_verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* l
     auto at = [](const void* p, size_t bytes) {
         return static_cast<const char*>(p) + bytes;
     };
+    // Launch order (each kernel's wait placement relies on it; see common.cuh):
+    //   tree -> attention partials (layer l, merge of l-1 between) -> argmax +
+    //   acceptance -> GDN layers -> merge of the last attention layer -> commit.
+    // Attention starts with the tree (its cache blocks do not need it); the
+    // acceptance follows the last attention layer, which is the last reader of
+    // kv_len; the GDN layers and the last merge then run before their waits.
+    const int na = c.n_attn_layers, ng = c.n_gdn_layers;
+    auto attn_args = [&](int l, const void*& q, const void*& kt, const void*& vt, const void*& kc,
+                         const void*& vc, void*& o) {
+        const size_t qo = (size_t)l * B * T * c.Hq * c.D * esz;
+        const size_t tr = (size_t)l * B * T * c.Hkv * c.D * esz;
+        const size_t ca = (size_t)l * B * c.Lmax * c.Hkv * c.D * esz;
+        q = at(step->attn_q, qo);
+        kt = at(io->k_tree, tr);
+        vt = at(io->v_tree, tr);
+        kc = at(io->k_cache, ca);
+        vc = at(io->v_cache, ca);
+        o = const_cast<char*>(at(step->attn_o, qo));
+    };
     cudaError_t e = spec::launch_tree_build(c, lat_tok, lat_score, io->root_tok, *tree, ws, st, true);
-    for (int l = 0; l < c.n_gdn_layers && e == cudaSuccess; ++l) {
+    for (int l = 0; l < na && e == cudaSuccess; ++l) {
+        const void *q, *kt, *vt, *kc, *vc;
+        void* o;
+        if (l > 0) {
+            attn_args(l - 1, q, kt, vt, kc, vc, o);
+            e = spec::launch_attn_merge(c, *tree, o, ws, st, true, (l - 1) & 1, true);
+            if (e != cudaSuccess) break;
+        }
+        attn_args(l, q, kt, vt, kc, vc, o);
+        e = spec::launch_attn_partial(c, *tree, q, kt, vt, kc, vc, io->kv_len, ws, st, true, l & 1);
+    }
+    if (e == cudaSuccess) e = spec::launch_argmax_accept(c, *tree, logits, *io, *out, ws, st, true);
+    for (int l = 0; l < ng && e == cudaSuccess; ++l) {
         const size_t state = (size_t)l * B * c.Hv * c.dk * c.dv;
         const size_t kq = (size_t)l * B * T * c.Hk * c.dk * esz;
         const size_t vo = (size_t)l * B * T * c.Hv * c.dv;
@@ -153,18 +184,18 @@ int spec_verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* l
         e = spec::launch_gdn_tree(c, *tree, io->h0 + state, at(step->gdn_q, kq), at(io->gdn_k, kq),
                                   at(io->gdn_v, vo * esz), io->alpha + gate, io->beta + gate,
                                   const_cast<char*>(at(step->gdn_o, vo * esz)),
-                                  step->gdn_c ? step->gdn_c + vo : nullptr, st, true);
+                                  step->gdn_c ? step->gdn_c + vo : nullptr, st, true,
+                                  /*early=*/false);
     }
-    for (int l = 0; l < c.n_attn_layers && e == cudaSuccess; ++l) {
-        const size_t qo = (size_t)l * B * T * c.Hq * c.D * esz;
-        const size_t tr = (size_t)l * B * T * c.Hkv * c.D * esz;
-        const size_t ca = (size_t)l * B * c.Lmax * c.Hkv * c.D * esz;
-        e = spec::launch_attn_tree(c, *tree, at(step->attn_q, qo), at(io->k_tree, tr),
-                                   at(io->v_tree, tr), at(io->k_cache, ca), at(io->v_cache, ca),
-                                   io->kv_len, const_cast<char*>(at(step->attn_o, qo)), ws, st,
-                                   true, l & 1);
+    if (na > 0 && e == cudaSuccess) {
+        const void *q, *kt, *vt, *kc, *vc;
+        void* o;
+        attn_args(na - 1, q, kt, vt, kc, vc, o);
+        e = spec::launch_attn_merge(c, *tree, o, ws, st, true, (na - 1) & 1, /*early=*/false);
     }
-    if (e == cudaSuccess) e = spec::launch_accept_commit(c, *tree, logits, *io, *out, ws, st, true);
+    // the commit may skip its early wait only when a merge sits between it and
+    // the last GDN layer / the acceptance
+    if (e == cudaSuccess) e = spec::launch_commit(c, *io, *out, ws, st, true, /*early=*/na == 0);
     return cuda_rc(e);
 }
 

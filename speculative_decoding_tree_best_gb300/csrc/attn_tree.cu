@@ -51,7 +51,14 @@ attn_partial_simt(spec_cfg c, spec_tree tree, const typename io_t<IO>::T* __rest
     if (!tree_chunk) {
         k0 = ch * w.chunk;
         k1 = min(k0 + w.chunk, L);
-        if (k0 >= L) return;                 // no cache rows here: the merge skips it
+        if (k0 >= L) {                       // no cache rows here: an empty partial
+            float2* wML = ws_ptr<float2>(ws, w.attn_ml_off);
+            for (int r = threadIdx.x; r < G * T; r += NT) {
+                const size_t tile = (((size_t)b * Hkv + g) * w.n_mt + r / 128) * w.n_chunks + ch;
+                wML[tile * 128 + r % 128] = make_float2(-INFINITY, 0.0f);
+            }
+            return;
+        }
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float scale = rsqrtf((float)D);
@@ -137,22 +144,38 @@ __device__ __forceinline__ void load_partial(const float* p, float* f) {
 }
 
 template <int IO, int D>
+__device__ __forceinline__ void merge_row(const spec_cfg& c, const spec_tree& tree, void* ws,
+                                          const WsLayout& w, typename io_t<IO>::T* __restrict__ o,
+                                          int r, int g, int b, int lane);
+
+template <int IO, int D>
 __global__ void __launch_bounds__(NT)
-attn_merge(spec_cfg c, spec_tree tree, const int32_t* __restrict__ kv_len, void* ws, WsLayout w,
-           typename io_t<IO>::T* __restrict__ o) {
-    constexpr int EPL = D / 32;              // output columns per lane (2 or 4)
+attn_merge(spec_cfg c, spec_tree tree, void* ws, WsLayout w, typename io_t<IO>::T* __restrict__ o,
+           bool early) {
     const int g = blockIdx.y, b = blockIdx.z;
     const int T = c.N + 1, G = c.Hq / c.Hkv;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int r = blockIdx.x * NW + warp;
-    pdl_wait();
-    pdl_trigger();
-    if (r >= G * T) return;
+    // early: the partials may come from the launch just before this one
+    if (early) {
+        pdl_wait();
+        pdl_trigger();
+    }
+    if (r < G * T) merge_row<IO, D>(c, tree, ws, w, o, r, g, b, lane);
+    if (!early) {
+        pdl_wait();
+        pdl_trigger();
+    }
+}
+
+template <int IO, int D>
+__device__ __forceinline__ void merge_row(const spec_cfg& c, const spec_tree& tree, void* ws,
+                                          const WsLayout& w, typename io_t<IO>::T* __restrict__ o,
+                                          int r, int g, int b, int lane) {
+    constexpr int EPL = D / 32;
+    const int T = c.N + 1, G = c.Hq / c.Hkv;
     int nn = tree.n_nodes[b];
     nn = nn < 1 ? 1 : (nn > T ? T : nn);
-    int L = kv_len[b];
-    L = L < 0 ? 0 : (L > c.Lmax ? c.Lmax : L);
-    const int n_cache = (L + w.chunk - 1) / w.chunk;
     const int x = r / G, h = g * G + r % G, mt = r / 128, rr = r % 128;
     float acc[EPL];
 #pragma unroll
@@ -162,17 +185,16 @@ attn_merge(spec_cfg c, spec_tree tree, const int32_t* __restrict__ kv_len, void*
         const PT* wO = ws_ptr<const PT>(ws, w.attn_o_off);
         const float2* wML = ws_ptr<const float2>(ws, w.attn_ml_off);
         const size_t tile0 = (((size_t)b * c.Hkv + g) * w.n_mt + mt) * w.n_chunks;
-        // chunks holding keys: cache chunks [0, n_cache) and the tree chunk n_split
-        const int nch = n_cache + 1;
+        // every chunk; chunks without keys left (max -inf, sum 0) and weigh 0
+        const int nch = w.n_chunks;
         float m_run = -INFINITY, den_run = 0.0f;
         for (int base = 0; base < nch; base += 32) {           // rounds of 32 chunks
             const int i = base + lane;
-            const int ci = i < n_cache ? i : w.n_split;
-            const float2 ml = i < nch ? wML[(tile0 + ci) * 128 + rr] : make_float2(-INFINITY, 0.0f);
+            const float2 ml = i < nch ? wML[(tile0 + i) * 128 + rr] : make_float2(-INFINITY, 0.0f);
             float M = ml.x;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-            const float f = i < nch ? ml.y * __expf(ml.x - M) : 0.0f;   // unnormalised weight
+            const float f = ml.y > 0.0f ? ml.y * __expf(ml.x - M) : 0.0f;  // unnormalised weight
             const float den_r = warp_sum(f);
             const int cnt = min(32, nch - base);
             float gacc[EPL];
@@ -182,10 +204,11 @@ attn_merge(spec_cfg c, spec_tree tree, const int32_t* __restrict__ kv_len, void*
             float raw[32][EPL];
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
-                const int ck = base + k < n_cache ? base + k : w.n_split;
 #pragma unroll
                 for (int e = 0; e < EPL; ++e) raw[k][e] = 0.0f;
-                if (k < cnt) load_partial<EPL>(wO + ((tile0 + ck) * 128 + rr) * D + lane * EPL, raw[k]);
+                const bool has = __shfl_sync(0xffffffffu, f, k) > 0.0f;   // empty chunks: no load
+                if (k < cnt && has)
+                    load_partial<EPL>(wO + ((tile0 + base + k) * 128 + rr) * D + lane * EPL, raw[k]);
             }
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
@@ -211,38 +234,57 @@ attn_merge(spec_cfg c, spec_tree tree, const int32_t* __restrict__ kv_len, void*
 }
 
 template <int IO, int D>
-cudaError_t launch_attn(const spec_cfg& c, const spec_tree& t, const void* q, const void* kt,
-                        const void* vt, const void* kc, const void* vc, const int32_t* kv_len,
-                        void* o, void* ws, cudaStream_t st, bool pdl, int part_buf) {
+cudaError_t launch_partial(const spec_cfg& c, const spec_tree& t, const void* q, const void* kt,
+                           const void* vt, const void* kc, const void* vc, const int32_t* kv_len,
+                           void* ws, cudaStream_t st, bool pdl, int part_buf) {
     using E = typename io_t<IO>::T;
     const WsLayout w = with_attn_buf(ws_layout(c), part_buf);
-    cudaError_t e;
-    if (attn_tc_supported(c)) {
-        e = launch_attn_tc(c, t, q, kt, vt, kc, vc, kv_len, ws, w, st, pdl);
-    } else {
-        e = launch_k(pdl, attn_partial_simt<IO, D>, dim3(w.n_chunks, c.Hkv, c.B), dim3(NT), 0, st,
-                     c, t, static_cast<const E*>(q), static_cast<const E*>(kt),
-                     static_cast<const E*>(vt), static_cast<const E*>(kc),
-                     static_cast<const E*>(vc), kv_len, ws, w);
-    }
-    if (e != cudaSuccess) return e;
+    if (attn_tc_supported(c)) return launch_attn_tc(c, t, q, kt, vt, kc, vc, kv_len, ws, w, st, pdl);
+    return launch_k(pdl, attn_partial_simt<IO, D>, dim3(w.n_chunks, c.Hkv, c.B), dim3(NT), 0, st,
+                    c, t, static_cast<const E*>(q), static_cast<const E*>(kt),
+                    static_cast<const E*>(vt), static_cast<const E*>(kc),
+                    static_cast<const E*>(vc), kv_len, ws, w);
+}
+
+template <int IO, int D>
+cudaError_t launch_merge(const spec_cfg& c, const spec_tree& t, void* o, void* ws, cudaStream_t st,
+                         bool pdl, int part_buf, bool early) {
+    using E = typename io_t<IO>::T;
+    const WsLayout w = with_attn_buf(ws_layout(c), part_buf);
     const int G = c.Hq / c.Hkv;
     return launch_k(pdl, attn_merge<IO, D>, dim3((G * (c.N + 1) + NW - 1) / NW, c.Hkv, c.B),
-                    dim3(NT), 0, st, c, t, kv_len, ws, w, static_cast<E*>(o));
+                    dim3(NT), 0, st, c, t, ws, w, static_cast<E*>(o), early);
 }
 
 }  // namespace
+
+#define SPEC_ATTN_DISPATCH(FN, ...)                                                      \
+    if (c.io_dtype == SPEC_IO_BF16)                                                      \
+        return c.D == 128 ? FN<SPEC_IO_BF16, 128>(__VA_ARGS__) : FN<SPEC_IO_BF16, 64>(__VA_ARGS__); \
+    return c.D == 128 ? FN<SPEC_IO_F32, 128>(__VA_ARGS__) : FN<SPEC_IO_F32, 64>(__VA_ARGS__)
+
+cudaError_t launch_attn_partial(const spec_cfg& c, const spec_tree& t, const void* q,
+                                const void* k_tree, const void* v_tree, const void* k_cache,
+                                const void* v_cache, const int32_t* kv_len, void* ws,
+                                cudaStream_t st, bool pdl, int part_buf) {
+    SPEC_ATTN_DISPATCH(launch_partial, c, t, q, k_tree, v_tree, k_cache, v_cache, kv_len, ws, st,
+                       pdl, part_buf);
+}
+
+cudaError_t launch_attn_merge(const spec_cfg& c, const spec_tree& t, void* o, void* ws,
+                              cudaStream_t st, bool pdl, int part_buf, bool early) {
+    SPEC_ATTN_DISPATCH(launch_merge, c, t, o, ws, st, pdl, part_buf, early);
+}
+#undef SPEC_ATTN_DISPATCH
 
 cudaError_t launch_attn_tree(const spec_cfg& c, const spec_tree& t, const void* q,
                              const void* k_tree, const void* v_tree, const void* k_cache,
                              const void* v_cache, const int32_t* kv_len, void* o, void* ws,
                              cudaStream_t st, bool pdl, int part_buf) {
-    if (c.io_dtype == SPEC_IO_BF16) {
-        return c.D == 128 ? launch_attn<SPEC_IO_BF16, 128>(c, t, q, k_tree, v_tree, k_cache, v_cache, kv_len, o, ws, st, pdl, part_buf)
-                          : launch_attn<SPEC_IO_BF16, 64>(c, t, q, k_tree, v_tree, k_cache, v_cache, kv_len, o, ws, st, pdl, part_buf);
-    }
-    return c.D == 128 ? launch_attn<SPEC_IO_F32, 128>(c, t, q, k_tree, v_tree, k_cache, v_cache, kv_len, o, ws, st, pdl, part_buf)
-                      : launch_attn<SPEC_IO_F32, 64>(c, t, q, k_tree, v_tree, k_cache, v_cache, kv_len, o, ws, st, pdl, part_buf);
+    cudaError_t e = launch_attn_partial(c, t, q, k_tree, v_tree, k_cache, v_cache, kv_len, ws, st,
+                                        pdl, part_buf);
+    if (e != cudaSuccess) return e;
+    return launch_attn_merge(c, t, o, ws, st, pdl, part_buf, true);
 }
 
 }  // namespace spec

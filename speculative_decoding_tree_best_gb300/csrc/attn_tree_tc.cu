@@ -118,7 +118,15 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
     int k0 = 0, k1 = T;
     if (!tree_chunk) {
         k0 = ch * w.chunk;
-        if (k0 >= L) return;                       // whole CTA idle: nothing allocated yet
+        if (k0 >= L) {
+            // no cache rows here: leave an empty partial (max -inf, sum 0) so the
+            // merge needs no kv_len, and exit (nothing allocated yet)
+            float2* wML = ws_ptr<float2>(prm.ws, w.attn_ml_off);
+            const size_t tile = (((size_t)b * c.Hkv + g) * w.n_mt + mt) * w.n_chunks + ch;
+            for (int row = threadIdx.x; row < BM; row += NTHREADS)
+                if (mt * BM + row < G * T) wML[tile * BM + row] = make_float2(-INFINITY, 0.0f);
+            return;
+        }
         k1 = min(k0 + w.chunk, L);
     }
     const int nblk = (k1 - k0 + NB - 1) / NB;

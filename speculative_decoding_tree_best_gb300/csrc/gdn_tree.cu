@@ -91,7 +91,7 @@ gdn_tree_kernel(spec_cfg c, spec_tree tree, const float* __restrict__ h0,
                 const typename io_t<IO>::T* __restrict__ q, const typename io_t<IO>::T* __restrict__ k,
                 const typename io_t<IO>::T* __restrict__ v, const float* __restrict__ alpha,
                 const float* __restrict__ beta, typename io_t<IO>::T* __restrict__ o,
-                float* __restrict__ c_out) {
+                float* __restrict__ c_out, bool early) {
     extern __shared__ __align__(16) float sm[];
     const int T = c.N + 1, Hv = c.Hv, Hk = c.Hk, dv = c.dv;
     const int c0 = blockIdx.x * CB, j = blockIdx.y, b = blockIdx.z;
@@ -224,9 +224,13 @@ gdn_tree_kernel(spec_cfg c, spec_tree tree, const float* __restrict__ h0,
         }
     }
 
-    // ---- the tree (written by the previous launch) from here on ----------------------
-    pdl_wait();
-    pdl_trigger();
+    // ---- the tree from here on.  early: it may come from the launch just before
+    // this one; otherwise it is at least two launches back and no wait is needed
+    // until the end.
+    if (early) {
+        pdl_wait();
+        pdl_trigger();
+    }
     int nn = tree.n_nodes[b];
     nn = nn < 1 ? 1 : (nn > T ? T : nn);     // a malformed tree must not index out of range
     for (int x = tid; x < nn; x += NT) {
@@ -305,6 +309,10 @@ gdn_tree_kernel(spec_cfg c, spec_tree tree, const float* __restrict__ h0,
             io_t<IO>::st(o, oi, ox);
             if (c_out) c_out[oi] = cx;
         }
+        if (!early) {
+            pdl_wait();
+            pdl_trigger();
+        }
         return;
     }
 
@@ -333,12 +341,17 @@ gdn_tree_kernel(spec_cfg c, spec_tree tree, const float* __restrict__ h0,
         io_t<IO>::st(o, oi, ox);
         if (c_out) c_out[oi] = cx;
     }
+    if (!early) {
+        pdl_wait();
+        pdl_trigger();
+    }
 }
 
 template <int IO, int DK, int MAXD>
 cudaError_t launch_one(const spec_cfg& c, const spec_tree& t, const float* h0, const void* q,
                        const void* k, const void* v, const float* alpha, const float* beta,
-                       void* o, float* c_out, size_t smem, cudaStream_t st, bool pdl) {
+                       void* o, float* c_out, size_t smem, cudaStream_t st, bool pdl,
+                       bool early) {
     using E = typename io_t<IO>::T;
     auto kern = gdn_tree_kernel<IO, DK, MAXD>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -346,7 +359,7 @@ cudaError_t launch_one(const spec_cfg& c, const spec_tree& t, const float* h0, c
     dim3 grid(c.dv / CB, c.Hv, c.B);
     return launch_k(pdl, kern, grid, dim3(NT), smem, st, c, t, h0, static_cast<const E*>(q),
                       static_cast<const E*>(k), static_cast<const E*>(v), alpha, beta,
-                      static_cast<E*>(o), c_out);
+                      static_cast<E*>(o), c_out, early);
 }
 
 }  // namespace
@@ -358,15 +371,15 @@ size_t gdn_tree_smem(const spec_cfg& c) {
 cudaError_t launch_gdn_tree(const spec_cfg& c, const spec_tree& t, const float* h0,
                             const void* q, const void* k, const void* v, const float* alpha,
                             const float* beta, void* o, float* c_out, cudaStream_t st,
-                            bool pdl) {
+                            bool pdl, bool early) {
     const size_t smem = gdn_tree_smem(c);
     if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
     const int T = c.N + 1;
     const int S = (c.m < T - 1 ? c.m : T - 1) + 1;        // rows on the longest root path
     const bool chains = S <= kChainMax;
 #define SPEC_GDN_LAUNCH(IO_, DK_)                                                              \
-    return chains ? launch_one<IO_, DK_, kChainMax>(c, t, h0, q, k, v, alpha, beta, o, c_out, smem, st, pdl) \
-                  : launch_one<IO_, DK_, 0>(c, t, h0, q, k, v, alpha, beta, o, c_out, smem, st, pdl)
+    return chains ? launch_one<IO_, DK_, kChainMax>(c, t, h0, q, k, v, alpha, beta, o, c_out, smem, st, pdl, early) \
+                  : launch_one<IO_, DK_, 0>(c, t, h0, q, k, v, alpha, beta, o, c_out, smem, st, pdl, early)
     if (c.io_dtype == SPEC_IO_BF16) {
         if (c.dk == 128) { SPEC_GDN_LAUNCH(SPEC_IO_BF16, 128); }
         SPEC_GDN_LAUNCH(SPEC_IO_BF16, 64);

@@ -18,7 +18,7 @@ size_t tree_build_smem(const spec_cfg& c);
 cudaError_t launch_gdn_tree(const spec_cfg& c, const spec_tree& t, const float* h0,
                             const void* q, const void* k, const void* v, const float* alpha,
                             const float* beta, void* o, float* c_out, cudaStream_t st,
-                            bool pdl = false);
+                            bool pdl = false, bool early = true);
 size_t gdn_tree_smem(const spec_cfg& c);
 
 cudaError_t launch_attn_tree(const spec_cfg& c, const spec_tree& t, const void* q,
@@ -26,12 +26,30 @@ cudaError_t launch_attn_tree(const spec_cfg& c, const spec_tree& t, const void* 
                              const void* v_cache, const int32_t* kv_len, void* o, void* ws,
                              cudaStream_t st, bool pdl = false, int part_buf = 0);
 
+// The two halves of attn_tree_verify: split-KV partials, then the merge.
+// early = false lets the merge run before its pdl_wait (only valid when the
+// partials are at least two launches back).
+cudaError_t launch_attn_partial(const spec_cfg& c, const spec_tree& t, const void* q,
+                                const void* k_tree, const void* v_tree, const void* k_cache,
+                                const void* v_cache, const int32_t* kv_len, void* ws,
+                                cudaStream_t st, bool pdl, int part_buf);
+cudaError_t launch_attn_merge(const spec_cfg& c, const spec_tree& t, void* o, void* ws,
+                              cudaStream_t st, bool pdl, int part_buf, bool early);
+
 bool attn_tc_supported(const spec_cfg& c);
 cudaError_t launch_attn_tc(const spec_cfg& c, const spec_tree& t, const void* q,
                            const void* k_tree, const void* v_tree, const void* k_cache,
                            const void* v_cache, const int32_t* kv_len, void* ws,
                            const WsLayout& w, cudaStream_t st, bool pdl);
 
+// accept_and_commit = argmax/accept, then the commit.  early = false lets the
+// commit run before its pdl_wait (only valid when no GDN layer is the launch
+// just before it).
+cudaError_t launch_argmax_accept(const spec_cfg& c, const spec_tree& t, const void* logits,
+                                 const spec_commit_io& io, const spec_accept& out, void* ws,
+                                 cudaStream_t st, bool pdl);
+cudaError_t launch_commit(const spec_cfg& c, const spec_commit_io& io, const spec_accept& out,
+                          void* ws, cudaStream_t st, bool pdl, bool early);
 cudaError_t launch_accept_commit(const spec_cfg& c, const spec_tree& t, const void* logits,
                                  const spec_commit_io& io, const spec_accept& out, void* ws,
                                  cudaStream_t st, bool pdl = false);
