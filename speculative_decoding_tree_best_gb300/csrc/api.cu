@@ -81,7 +81,7 @@ int gdn_tree_verify(const spec_cfg* cfg, const spec_tree* tree, const float* h0,
         !al16(ws))
         return ST_EINVAL;
     if (c_opt && !al16(c_opt)) return ST_EINVAL;
-    return cuda_rc(spec::launch_gdn_tree(*cfg, *tree, h0, q, k, v, alpha, beta, o, c_opt,
+    return cuda_rc(spec::launch_gdn_tree(*cfg, *tree, h0, q, k, v, alpha, beta, o, c_opt, ws,
                                          static_cast<cudaStream_t>(stream)));
 }
 
@@ -184,7 +184,7 @@ int spec_verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* l
         e = spec::launch_gdn_tree(c, *tree, io->h0 + state, at(step->gdn_q, kq), at(io->gdn_k, kq),
                                   at(io->gdn_v, vo * esz), io->alpha + gate, io->beta + gate,
                                   const_cast<char*>(at(step->gdn_o, vo * esz)),
-                                  step->gdn_c ? step->gdn_c + vo : nullptr, st, true,
+                                  step->gdn_c ? step->gdn_c + vo : nullptr, ws, st, true,
                                   /*early=*/false);
     }
     if (na > 0 && e == cudaSuccess) {
