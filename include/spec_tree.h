@@ -56,7 +56,9 @@ enum {
     ST_EUNSUPPORTED = 2, /* unsupported dtype or head dimension */
     ST_ECUDA = 3,        /* a CUDA launch or copy failed (cudaGetLastError) */
     ST_EOVERFLOW = 4,    /* device status: kv_len + tau > Lmax for some request */
-    ST_TIMEOUT = 5       /* device status: a bounded device-side wait gave up */
+    ST_TIMEOUT = 5,      /* device status: a bounded device-side wait gave up */
+    ST_ESCRATCH = 6      /* shape needs more than the fixed static scratch of
+                            attn_tree_verify_noalloc */
 };
 
 /* Bits of the device status word (uint32 at byte 0 of the workspace). */
@@ -238,6 +240,38 @@ const char *spec_status_string(int code);
 
 /* SPEC_TREE_ABI_VERSION of the loaded library. */
 int spec_abi_version(void);
+
+/*
+ * attn_tree_verify_noalloc -- attn_tree_verify without a caller workspace.
+ * The pages describe no such call (their method has no counterpart): it is a
+ * library convenience for callers that own no device allocator where they
+ * launch the op (a custom op inside a host runtime that owns all device
+ * memory, a serving loop that must not call into an allocator).  Neither the
+ * call nor anything it calls allocates device or host memory.
+ *
+ * Arguments, layouts and results are those of attn_tree_verify (the same
+ * kernels run), except:
+ *   - the scratch (status word + split-KV partials) is a static device array
+ *     of SPEC_NOALLOC_SCRATCH_BYTES inside the library, one per device; a
+ *     shape whose partials do not fit returns ST_ESCRATCH before any device
+ *     work (with Hkv = 8, D = 128, bf16: one request up to Lmax ~ 19K, or up to
+ *     4 requests at Lmax = 4096);
+ *   - dev_status: NULL, or a 4-byte-aligned device word the call ORs its
+ *     SPEC_DEV_* bits into (the caller zeroes it when it wants); the scratch
+ *     status word itself starts at zero and every call leaves it at zero.
+ * Returns ST_EINVAL on an invalid cfg or a NULL/misaligned pointer.
+ * The first call on a device (with that device current) sets up: it looks up
+ * the array's address and clears its status word synchronously, so make it
+ * before any stream capture or latency-critical section.  All calls on one
+ * device share the one scratch array: calls that overlap in time (other
+ * streams, other host threads, other layers in flight) race on it and give
+ * wrong results; order them on one stream or serialise them.
+ */
+#define SPEC_NOALLOC_SCRATCH_BYTES (8u << 20)
+int attn_tree_verify_noalloc(const spec_cfg *cfg, const spec_tree *tree, const void *q,
+                             const void *k_tree, const void *v_tree, const void *k_cache,
+                             const void *v_cache, const int32_t *kv_len, void *o,
+                             uint32_t *dev_status, void *stream);
 
 #ifdef __cplusplus
 }

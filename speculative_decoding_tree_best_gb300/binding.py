@@ -18,12 +18,13 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libspectree.so")
 
-ST_OK, ST_EINVAL, ST_EUNSUPPORTED, ST_ECUDA, ST_EOVERFLOW, ST_TIMEOUT = range(6)
+ST_OK, ST_EINVAL, ST_EUNSUPPORTED, ST_ECUDA, ST_EOVERFLOW, ST_TIMEOUT, ST_ESCRATCH = range(7)
+NOALLOC_SCRATCH_BYTES = 8 << 20
 SPEC_DEV_OVERFLOW, SPEC_DEV_BADLAT, SPEC_DEV_TIMEOUT = 0x1, 0x2, 0x4
 SPEC_IO_F32, SPEC_IO_BF16 = 0, 1
 EXPORTS = ("spec_workspace_bytes", "spec_tree_build", "gdn_tree_verify", "attn_tree_verify",
            "accept_and_commit", "spec_verify_step", "spec_status_read", "spec_status_clear",
-           "spec_status_string", "spec_abi_version")
+           "spec_status_string", "spec_abi_version", "attn_tree_verify_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -87,7 +88,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
             lib.spec_status_clear.argtypes = [vp, vp]
             lib.spec_status_string.argtypes = [ctypes.c_int]
             lib.spec_status_string.restype = ctypes.c_char_p
+            lib.attn_tree_verify_noalloc.argtypes = [cfgp, ctypes.POINTER(SpecTree)] + [vp] * 9
             for n in ("spec_tree_build", "gdn_tree_verify", "attn_tree_verify",
+                      "attn_tree_verify_noalloc",
                       "accept_and_commit", "spec_verify_step", "spec_status_read",
                       "spec_status_clear", "spec_abi_version"):
                 getattr(lib, n).restype = ctypes.c_int
@@ -213,6 +216,20 @@ def attn_tree_verify(cfg, tree: TreeBuffers, q, k_tree, v_tree, k_cache, v_cache
         _ptr(v_tree, dt, "v_tree"), _ptr(k_cache, dt, "k_cache"), _ptr(v_cache, dt, "v_cache"),
         _ptr(kv_len, torch.int32, "kv_len"), _ptr(o, dt, "o"), _ptr(ws, name="ws"),
         _stream(stream)))
+
+
+def attn_tree_verify_noalloc(cfg, tree: TreeBuffers, q, k_tree, v_tree, k_cache, v_cache, kv_len,
+                             o, dev_status=None, stream=None):
+    """attn_tree_verify with the library's static scratch (no workspace);
+    dev_status: None or a CUDA uint32/int32 word that receives SPEC_DEV_* bits."""
+    dt = _io_dtype(cfg)
+    if dev_status is not None and dev_status.dtype not in (torch.int32, torch.uint32):
+        raise TypeError("dev_status: expected an int32 or uint32 CUDA tensor")
+    _check("attn_tree_verify_noalloc", load().attn_tree_verify_noalloc(
+        ctypes.byref(cfg), ctypes.byref(tree.c()), _ptr(q, dt, "q"), _ptr(k_tree, dt, "k_tree"),
+        _ptr(v_tree, dt, "v_tree"), _ptr(k_cache, dt, "k_cache"), _ptr(v_cache, dt, "v_cache"),
+        _ptr(kv_len, torch.int32, "kv_len"), _ptr(o, dt, "o"),
+        _ptr(dev_status, name="dev_status"), _stream(stream)))
 
 
 def _commit_io(cfg, io: dict) -> SpecCommitIO:

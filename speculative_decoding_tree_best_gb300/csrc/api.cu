@@ -52,6 +52,7 @@ const char* spec_status_string(int code) {
         case ST_ECUDA: return "CUDA launch or copy failed";
         case ST_EOVERFLOW: return "KV cache overflow: kv_len + tau > Lmax";
         case ST_TIMEOUT: return "a bounded device-side wait gave up";
+        case ST_ESCRATCH: return "shape needs more than the static scratch of the no-allocation call";
         default: return "unknown status";
     }
 }
