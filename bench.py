@@ -202,6 +202,13 @@ def sum_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
+def whole_job(nodes_local: float, ms_local: float, world: int):
+    """(nodes of all ranks, slowest rank's ms per step, whole-job nodes/s)."""
+    nodes = sum_over_ranks(nodes_local, world)
+    ms = max_over_ranks(ms_local, world)
+    return nodes, ms, nodes / (ms * 1e-3)
+
+
 # ----------------------------------------------------------------- CPU oracle timing
 
 def oracle_step(scfg, inp):
@@ -250,30 +257,27 @@ def cpu_baseline(scfg, seed, budget_s=12.0, max_steps=4):
 # ----------------------------------------------------------------- reference arm
 
 def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle as it stands.  Under torchrun only rank
+    0 works and prints; the other ranks return at once."""
     if rank != 0:
         return
     scfg = synth.config(args.config)
     inp = planted_inputs_cpu(scfg, args.seed)
-    G = scfg.Hq // scfg.Hkv
-    grp = scfg.Hv // scfg.Hk
-    # A bounded sample per step: the tree, one GDN v-head, one attention kv-head
-    # group, the full argmax/accept/commit; the sampled head work is scaled by
-    # the head count to a whole-step estimate.
+
+    # A bounded sample per step: the tree, argmax, acceptance (whole), plus one
+    # GDN v-head (verify + commit) and one attention kv-head group, each timed
+    # on its own and scaled by its head count to a whole-step time.
     def one(step):
-        j = step % scfg.Hv
-        g = step % scfg.Hkv
-        t0 = time.perf_counter()
-        oracle_step_sampled(scfg, inp, j, g)
-        t_sampled = time.perf_counter() - t0
-        return t_sampled
+        t = oracle_step_parts(scfg, inp, step % scfg.Hv, step % scfg.Hkv)
+        return t["fixed"] + scfg.Hv * t["gdn_head"] + scfg.Hkv * t["attn_group"], t
     for w in range(args.warmup):
         one(w)
-    per = []
+    per, sampled = [], []
     for s in range(args.steps):
-        per.append(one(s))
-    # scale: head-parallel parts were done for 1/Hv (GDN) and 1/Hkv (attention)
-    est = statistics.median(per)
-    full = est_full_step(scfg, inp)
+        full, t = one(s)
+        per.append(full)
+        sampled.append(sum(t.values()))
+    full = statistics.median(per)
     value = scfg.B * scfg.N / full
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -282,63 +286,46 @@ def run_reference(args, rank, world):
             "config": {"workload": f"{scfg.name}: B={scfg.B} m={scfg.m} K={scfg.K} N={scfg.N} "
                                    f"KV={scfg.L} V={scfg.V}", "l2": "n/a (CPU)"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"{args.steps} sampled steps (tree, one GDN v-head, one "
-                                       f"attention kv-head group, argmax/accept/commit), median "
-                                       f"{est * 1e3:.1f} ms; whole step {full:.3f} s"},
+                             "sample": f"{args.steps} sampled steps (tree, argmax, acceptance, "
+                                       f"one GDN v-head of {scfg.Hv}, one attention kv-head group "
+                                       f"of {scfg.Hkv}), median {statistics.median(sampled) * 1e3:.1f} "
+                                       f"ms sampled; scaled whole step {full:.3f} s"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def oracle_step_sampled(scfg, inp, j, g):
+def oracle_step_parts(scfg, inp, j, g):
+    """Times (s) of one oracle step's parts: 'fixed' (tree, argmax, acceptance,
+    KV commit), 'gdn_head' (every GDN layer's verify + commit of v-head j) and
+    'attn_group' (every attention layer for kv-head group g)."""
     import oracle
-    tree = oracle.tree_build(inp["lat_tok"], inp["lat_score"], inp["root_tok"], scfg.N)
     grp, G = scfg.Hv // scfg.Hk, scfg.Hq // scfg.Hkv
     i = j // grp
-    for lay in inp["gdn"]:
-        oracle.gdn_tree(tree, lay["h0"][:, j:j + 1].contiguous(), lay["q"][:, :, i:i + 1].contiguous(),
-                        lay["k"][:, :, i:i + 1].contiguous(), lay["v"][:, :, j:j + 1].contiguous(),
-                        lay["alpha"][:, :, j:j + 1].contiguous(), lay["beta"][:, :, j:j + 1].contiguous())
-    for lay in inp["attn"]:
-        oracle.attn_tree(tree, lay["q"][:, :, g * G:(g + 1) * G].contiguous(),
-                         lay["k_tree"][:, :, g:g + 1].contiguous(), lay["v_tree"][:, :, g:g + 1].contiguous(),
-                         lay["k_cache"][:, :, g:g + 1].contiguous(),
-                         lay["v_cache"][:, :, g:g + 1].contiguous(), inp["kv_len"])
-    am, _ = oracle.argmax(inp["logits"])
-    acc = oracle.accept(tree, am, scfg.m)
-    for lay in inp["gdn"]:
-        oracle.commit_gdn(acc, lay["h0"][:, j:j + 1].contiguous(), lay["k"][:, :, i:i + 1].contiguous(),
-                          lay["v"][:, :, j:j + 1].contiguous(), lay["alpha"][:, :, j:j + 1].contiguous(),
-                          lay["beta"][:, :, j:j + 1].contiguous())
-
-
-_FULL_CACHE = {}
-
-
-def est_full_step(scfg, inp):
-    """Whole-step oracle time from per-part timings of head slices (measured once)."""
-    key = scfg
-    if key in _FULL_CACHE:
-        return _FULL_CACHE[key]
-    import oracle
     t0 = time.perf_counter()
     tree = oracle.tree_build(inp["lat_tok"], inp["lat_score"], inp["root_tok"], scfg.N)
     am, _ = oracle.argmax(inp["logits"])
     acc = oracle.accept(tree, am, scfg.m)
-    t_fixed = time.perf_counter() - t0
-    t0 = time.perf_counter()
-    oracle_step_sampled(scfg, inp, 0, 0)
-    t_one = time.perf_counter() - t0
-    t0 = time.perf_counter()
-    G = scfg.Hq // scfg.Hkv
+    t1 = time.perf_counter()
+    for lay in inp["gdn"]:
+        sl = dict(h0=lay["h0"][:, j:j + 1], q=lay["q"][:, :, i:i + 1], k=lay["k"][:, :, i:i + 1],
+                  v=lay["v"][:, :, j:j + 1], alpha=lay["alpha"][:, :, j:j + 1],
+                  beta=lay["beta"][:, :, j:j + 1])
+        sl = {k: v.contiguous() for k, v in sl.items()}
+        oracle.gdn_tree(tree, sl["h0"], sl["q"], sl["k"], sl["v"], sl["alpha"], sl["beta"])
+        oracle.commit_gdn(acc, sl["h0"], sl["k"], sl["v"], sl["alpha"], sl["beta"])
+    t2 = time.perf_counter()
     for lay in inp["attn"]:
-        oracle.attn_tree(tree, lay["q"][:, :, 0:G].contiguous(), lay["k_tree"][:, :, 0:1].contiguous(),
-                         lay["v_tree"][:, :, 0:1].contiguous(), lay["k_cache"][:, :, 0:1].contiguous(),
-                         lay["v_cache"][:, :, 0:1].contiguous(), inp["kv_len"])
-    t_attn1 = time.perf_counter() - t0
-    t_gdn1 = max(t_one - t_fixed - t_attn1, 0.0)
-    full = t_fixed + scfg.Hv * t_gdn1 + scfg.Hkv * t_attn1
-    _FULL_CACHE[key] = full
-    return full
+        oracle.attn_tree(tree, lay["q"][:, :, g * G:(g + 1) * G].contiguous(),
+                         lay["k_tree"][:, :, g:g + 1].contiguous(),
+                         lay["v_tree"][:, :, g:g + 1].contiguous(),
+                         lay["k_cache"][:, :, g:g + 1].contiguous(),
+                         lay["v_cache"][:, :, g:g + 1].contiguous(), inp["kv_len"])
+    t3 = time.perf_counter()
+    for lay in inp["attn"]:
+        oracle.commit_kv(acc, lay["k_tree"], lay["v_tree"], lay["k_cache"], lay["v_cache"],
+                         inp["kv_len"])
+    t4 = time.perf_counter()
+    return {"fixed": (t1 - t0) + (t4 - t3), "gdn_head": t2 - t1, "attn_group": t3 - t2}
 
 
 # ----------------------------------------------------------------- our arm
@@ -411,7 +398,6 @@ def run_ours(args, rank, world, local):
     barrier(world)
     per_ms = [a.elapsed_time(b) for a, b in ev]
     ms_step = sum(per_ms) / len(per_ms)
-    ms_step_max = max_over_ranks(ms_step, world)
     taus = st.acc.accept_len.float().mean().item()
     mean_L = float(kv0.float().mean().item())
 
@@ -480,8 +466,7 @@ def run_ours(args, rank, world, local):
             e2e_ms.append(a.elapsed_time(b))
     e2e_ms_step = max_over_ranks(sum(e2e_ms) / len(e2e_ms), world)
 
-    nodes_total = sum_over_ranks(scfg.B * scfg.N, world)
-    value = nodes_total / (ms_step_max * 1e-3)
+    nodes_total, ms_step_max, value = whole_job(scfg.B * scfg.N, ms_step, world)
     byts = algorithmic_bytes(scfg, mean_L, taus)
     peak, peak_kind = hbm_peak()
     attn_us = ph_us["attn"] / max(scfg.n_attn, 1)

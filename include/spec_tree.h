@@ -242,6 +242,19 @@ const char *spec_status_string(int code);
 int spec_abi_version(void);
 
 /*
+ * spec_wait_probe -- diagnostic; the pages describe no such call.  Launches one
+ * CTA that waits on a shared-memory mbarrier with the same bounded wait the
+ * tensor-core kernels use.  With satisfy = 0 nothing ever arrives, so after
+ * about limit_us microseconds (SM cycles at the 2070 MHz maximum clock) the
+ * wait gives up and ORs SPEC_DEV_TIMEOUT into the status word of `ws`; with
+ * satisfy != 0 the barrier completes first and the status is untouched.
+ * Either way the kernel returns normally and the context stays usable.
+ *   limit_us in [1, 1000000]; ws as for the other calls (only its status word
+ *   is touched).  Returns ST_EINVAL on a bad limit or NULL/misaligned ws.
+ */
+int spec_wait_probe(uint32_t limit_us, int satisfy, void *ws, void *stream);
+
+/*
  * attn_tree_verify_noalloc -- attn_tree_verify without a caller workspace.
  * The pages describe no such call (their method has no counterpart): it is a
  * library convenience for callers that own no device allocator where they

@@ -24,7 +24,8 @@ SPEC_DEV_OVERFLOW, SPEC_DEV_BADLAT, SPEC_DEV_TIMEOUT = 0x1, 0x2, 0x4
 SPEC_IO_F32, SPEC_IO_BF16 = 0, 1
 EXPORTS = ("spec_workspace_bytes", "spec_tree_build", "gdn_tree_verify", "attn_tree_verify",
            "accept_and_commit", "spec_verify_step", "spec_status_read", "spec_status_clear",
-           "spec_status_string", "spec_abi_version", "attn_tree_verify_noalloc")
+           "spec_status_string", "spec_abi_version", "attn_tree_verify_noalloc",
+           "spec_wait_probe")
 
 _lock = threading.Lock()
 _lib = None
@@ -89,8 +90,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
             lib.spec_status_string.argtypes = [ctypes.c_int]
             lib.spec_status_string.restype = ctypes.c_char_p
             lib.attn_tree_verify_noalloc.argtypes = [cfgp, ctypes.POINTER(SpecTree)] + [vp] * 9
+            lib.spec_wait_probe.argtypes = [ctypes.c_uint32, ctypes.c_int, vp, vp]
             for n in ("spec_tree_build", "gdn_tree_verify", "attn_tree_verify",
-                      "attn_tree_verify_noalloc",
+                      "attn_tree_verify_noalloc", "spec_wait_probe",
                       "accept_and_commit", "spec_verify_step", "spec_status_read",
                       "spec_status_clear", "spec_abi_version"):
                 getattr(lib, n).restype = ctypes.c_int
@@ -271,6 +273,12 @@ def spec_status_read(ws, stream=None) -> int:
     _check("spec_status_read", load().spec_status_read(_ptr(ws, name="ws"), ctypes.byref(v),
                                                        _stream(stream)))
     return int(v.value)
+
+
+def spec_wait_probe(limit_us: int, satisfy: bool, ws, stream=None):
+    """One bounded device wait (diagnostic): SPEC_DEV_TIMEOUT when unsatisfied."""
+    _check("spec_wait_probe", load().spec_wait_probe(int(limit_us), int(bool(satisfy)),
+                                                     _ptr(ws, name="ws"), _stream(stream)))
 
 
 def spec_status_clear(ws, stream=None):

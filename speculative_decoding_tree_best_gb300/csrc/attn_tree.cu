@@ -28,6 +28,7 @@ namespace {
 
 constexpr int NT = 256;
 constexpr int NW = NT / 32;
+constexpr int kMergeGroup = 8;   // merge: chunk partials loaded per round trip
 
 template <int IO, int D>
 __global__ void __launch_bounds__(NT)
@@ -149,7 +150,7 @@ __device__ __forceinline__ void merge_row(const spec_cfg& c, const spec_tree& tr
                                           int r, int g, int b, int lane);
 
 template <int IO, int D>
-__global__ void __launch_bounds__(NT)
+__global__ void __launch_bounds__(NT, 3)
 attn_merge(spec_cfg c, spec_tree tree, void* ws, WsLayout w, typename io_t<IO>::T* __restrict__ o,
            bool early) {
     const int g = blockIdx.y, b = blockIdx.z;
@@ -200,21 +201,26 @@ __device__ __forceinline__ void merge_row(const spec_cfg& c, const spec_tree& tr
             float gacc[EPL];
 #pragma unroll
             for (int e = 0; e < EPL; ++e) gacc[e] = 0.0f;
-            // all rows of this round in flight: predicated, fully unrolled
-            float raw[32][EPL];
+            // groups of 8 chunks, the group's loads all in flight (predicated;
+            // empty chunks load nothing); few registers, so many warps per SM
+            // hide the two dependent round trips (weights, then partials)
+            for (int k0 = 0; k0 < cnt; k0 += kMergeGroup) {
+                float raw[kMergeGroup][EPL];
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
+                for (int k = 0; k < kMergeGroup; ++k) {
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) raw[k][e] = 0.0f;
-                const bool has = __shfl_sync(0xffffffffu, f, k) > 0.0f;   // empty chunks: no load
-                if (k < cnt && has)
-                    load_partial<EPL>(wO + ((tile0 + base + k) * 128 + rr) * D + lane * EPL, raw[k]);
-            }
+                    for (int e = 0; e < EPL; ++e) raw[k][e] = 0.0f;
+                    const bool has = __shfl_sync(0xffffffffu, f, k0 + k) > 0.0f;
+                    if (k0 + k < cnt && has)
+                        load_partial<EPL>(wO + ((tile0 + base + k0 + k) * 128 + rr) * D + lane * EPL,
+                                          raw[k]);
+                }
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                const float fk = __shfl_sync(0xffffffffu, f, k);
+                for (int k = 0; k < kMergeGroup; ++k) {
+                    const float fk = __shfl_sync(0xffffffffu, f, k0 + k);
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) gacc[e] = fmaf(raw[k][e], fk, gacc[e]);
+                    for (int e = 0; e < EPL; ++e) gacc[e] = fmaf(raw[k][e], fk, gacc[e]);
+                }
             }
             const float m_new = fmaxf(m_run, M);
             const float s_old = m_run == -INFINITY ? 0.0f : __expf(m_run - m_new);

@@ -7,21 +7,28 @@
 // One CTA = one (request, kv-head, 128-row query tile, key chunk).  The query
 // tile holds the G = Hq/Hkv q-heads of the group for 128/G consecutive tree
 // rows (row r = node * G + head_in_group), loaded once by TMA.  The chunk's
-// keys stream through a two-stage ring of 128-key K/V blocks (TMA, 128-byte
-// swizzle).  Per block:
-//    S = Q K^T              tcgen05.mma, A and B K-major, fp32 in tensor memory
-//    P = exp2(S*c - m)      one thread per row reads S from tensor memory
-//    O += P_hi V + P_lo V   tcgen05.mma, V MN-major; P is split into two bf16
-//                           terms (P_hi = bf16(P), P_lo = bf16(P - P_hi)) so the
-//                           probabilities keep ~16 significant bits: a single
-//                           bf16 P would cost ~1.7e-3 relative error on O.
-// The running maximum is only raised (and O rescaled in tensor memory) when a
-// block's maximum exceeds it by more than 2^8, so P <= 256 and O is rarely
-// touched.  The chunk's output is stored normalised (O / sum) in fp16 with its
-// (max, sum); |V| must stay below the fp16 range (65504).  Warp roles: warp 0 issues TMA, warp 1 issues MMAs (one thread
-// each), warps 2-17 run the softmax: four threads per query row (tensor-memory
-// lane = row), each owning 32 of the 128 key columns.  The partial
-// (O, max, sum) goes to the workspace; attn_merge combines chunks.
+// keys stream through two-stage rings of 128-key K and V blocks (TMA, 128-byte
+// swizzle); a K stage is refilled as soon as its S product is done, a V stage
+// once its PV product is done.  Per block j:
+//    S_j = Q K_j^T          tcgen05.mma (bf16, exact products), fp32 in tensor
+//                           memory, two S buffers so S_{j+1} is ready while
+//                           the softmax works on S_j
+//    P_j = exp2(S_j c - m)  one thread per (row, 32 keys), written as fp16
+//                           (11 significant bits; a bf16 P would cost ~1.7e-3
+//                           relative error on O)
+//    V_j -> fp16            the softmax threads convert V_j in place (the same
+//                           swizzled layout), so PV runs as kind::f16 with f16
+//                           operands
+//    O += P_j V_j           tcgen05.mma, fp32 in tensor memory
+// The MMA order is S_0, S_1, PV_0, S_2, PV_1, ...  The running maximum is only
+// raised (and O rescaled in tensor memory) when a block's maximum exceeds it by
+// more than 2^8, so P <= 256.  The chunk's output is stored normalised
+// (O / sum) in fp16 with its (max, sum); |V| must stay below the fp16 range
+// (65504).  Warp roles: warp 0 loads Q and the K ring, warp 1 issues the MMAs
+// (one thread each), warp 2 loads the V ring, warps 3-18 run the softmax: four
+// threads per query row (tensor-memory lane = row), each owning 32 of the 128
+// key columns.  The partial (O, max, sum) goes to the workspace; attn_merge
+// combines chunks.
 //
 // The cache chunks read nothing from the tree; only the tree chunk (the T
 // tree rows as keys, masked by the ancestor bitmasks) does.
@@ -48,24 +55,24 @@ constexpr int HD = 128;             // head dim
 constexpr int NWG = 4;              // softmax warpgroups: thread (wg, row) owns 32 key columns
 constexpr int CPT = 128 / NWG;      // key (and output) columns per softmax thread
 constexpr int NSOFT = 128 * NWG;    // softmax threads
-constexpr int NTHREADS = 64 + NSOFT;  // warp 0 TMA, warp 1 MMA, then the softmax warps
-constexpr uint32_t TILE_BYTES = 128 * 128 * 2;   // one 128 x 128 bf16 tile (two 64-wide halves)
+constexpr int NROLE = 3;            // warps 0-2: K loads, MMA issue, V loads
+constexpr int NTHREADS = 32 * NROLE + NSOFT;
+constexpr uint32_t TILE_BYTES = 128 * 128 * 2;   // one 128 x 128 16-bit tile (two 64-wide halves)
 constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;
+constexpr uint32_t TMEM_COLS = 512;              // S0, S1, O (128 columns each), rounded up
 
 // shared-memory map (offsets from the 1024-aligned base)
 constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_KV = OFF_Q + TILE_BYTES;                  // 2 stages x (K, V)
-constexpr uint32_t OFF_PHI = OFF_KV + 4 * TILE_BYTES;
-// P_lo of block j is written into the K buffer of block j: S_j has consumed it,
-// and the stage is only refilled after the PV MMAs of block j complete.
-constexpr uint32_t OFF_RED = OFF_PHI + TILE_BYTES;               // float [2][NWG][128] row maxima
+constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;                   // 2 stages
+constexpr uint32_t OFF_V = OFF_K + 2 * TILE_BYTES;               // 2 stages
+constexpr uint32_t OFF_P = OFF_V + 2 * TILE_BYTES;               // fp16 P, K-major
+constexpr uint32_t OFF_RED = OFF_P + TILE_BYTES;                 // float [2][NWG][128] row maxima
 constexpr uint32_t OFF_REDL = OFF_RED + 2 * NWG * 128 * 4;       // float [NWG][128] row sums
 constexpr uint32_t OFF_BAR = OFF_REDL + NWG * 128 * 4;
-constexpr int NBARS = 11;
+enum { B_Q = 0, B_KF, B_VF = B_KF + 2, B_KE = B_VF + 2, B_VE = B_KE + 2, B_SFULL = B_VE + 2,
+       B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_PVDONE, NBARS };
 constexpr uint32_t SMEM_BYTES = OFF_BAR + NBARS * 8 + 32 + 1024;  // + slack for alignment
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-
-enum { B_Q = 0, B_KF0, B_KF1, B_VF0, B_VF1, B_EMP0, B_EMP1, B_SFULL, B_SFREE, B_PFULL, B_PVDONE };
 
 // Barrier over `nthreads` threads with id `id` that also ANDs a predicate, so
 // a pair of warps leaves a loop together.
@@ -88,6 +95,18 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Eight bf16 (one 16-byte chunk) to eight fp16, in place.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+        const __half2 h = __floats2half2_rn(lo, hi);
+        w[e] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 struct TcParams {
     spec_cfg c;
     spec_tree tree;
@@ -106,7 +125,8 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int* issued = reinterpret_cast<int*>(tmem_slot + 2);         // K/V blocks the producer issued
+    int* issued_k = reinterpret_cast<int*>(tmem_slot + 2);       // K blocks the producer issued
+    int* issued_v = reinterpret_cast<int*>(tmem_slot + 3);       // V blocks the producer issued
 
     const spec_cfg& c = prm.c;
     const WsLayout& w = prm.w;
@@ -134,18 +154,19 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
 
     if (threadIdx.x == 0) {
         mbar_init(&bar[B_Q], 1);
-        mbar_init(&bar[B_KF0], 1);
-        mbar_init(&bar[B_KF1], 1);
-        mbar_init(&bar[B_VF0], 1);
-        mbar_init(&bar[B_VF1], 1);
-        mbar_init(&bar[B_EMP0], 1);
-        mbar_init(&bar[B_EMP1], 1);
-        mbar_init(&bar[B_SFULL], 1);
-        mbar_init(&bar[B_SFREE], NSOFT);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bar[B_KF + s], 1);
+            mbar_init(&bar[B_VF + s], 1);
+            mbar_init(&bar[B_KE + s], 1);
+            mbar_init(&bar[B_VE + s], 1);
+            mbar_init(&bar[B_SFULL + s], 1);
+            mbar_init(&bar[B_SFREE + s], NSOFT);
+        }
         mbar_init(&bar[B_PFULL], NSOFT);
         mbar_init(&bar[B_PVDONE], 1);
         *abort_flag = 0;
-        *issued = 0;
+        *issued_k = 0;
+        *issued_v = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -153,91 +174,109 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         tma_prefetch_desc(tree_chunk ? &mkt : &mkc);
         tma_prefetch_desc(tree_chunk ? &mvt : &mvc);
     }
-    if (warp == 1) tmem_alloc(tmem_slot, 256);
+    if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem, tO = tmem + 128;
+    const uint32_t tO = tmem + 256;                  // S buffers at +0 and +128
     bool ok = true;
+    const CUtensorMap* mk = tree_chunk ? &mkt : &mkc;
+    const CUtensorMap* mv = tree_chunk ? &mvt : &mvc;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------ Q and the K ring
         if (lane == 0) {
             mbar_arrive_expect_tx(&bar[B_Q], TILE_BYTES);
             const int node0 = mt * (BM / G);
             for (int h = 0; h < 2; ++h)
                 tma_load_3d(sm + OFF_Q + h * HALF_BYTES, &mq, &bar[B_Q], h * 64, g * G,
                             b * T + node0);
-            const CUtensorMap* mk = tree_chunk ? &mkt : &mkc;
-            const CUtensorMap* mv = tree_chunk ? &mvt : &mvc;
-            for (int j = 0; j < nblk && ok; ++j) {
+            for (int j = 0; j < nblk; ++j) {
                 const int s = j & 1;
-                if (j >= 2 && !mbar_wait(&bar[B_EMP0 + s], ((j >> 1) - 1) & 1, abort_flag)) {
+                // stage s is free once S_{j-2} is done
+                if (j >= 2 && !mbar_wait(&bar[B_KE + s], ((j >> 1) - 1) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
-                const int key0 = k0 + j * NB;
-                unsigned char* ks = sm + OFF_KV + s * 2 * TILE_BYTES;
-                unsigned char* vs = ks + TILE_BYTES;
-                mbar_arrive_expect_tx(&bar[B_KF0 + s], TILE_BYTES);
+                mbar_arrive_expect_tx(&bar[B_KF + s], TILE_BYTES);
                 for (int h = 0; h < 2; ++h)
-                    tma_load_4d(ks + h * HALF_BYTES, mk, &bar[B_KF0 + s], h * 64, g, key0, b);
-                mbar_arrive_expect_tx(&bar[B_VF0 + s], TILE_BYTES);
+                    tma_load_4d(sm + OFF_K + s * TILE_BYTES + h * HALF_BYTES, mk, &bar[B_KF + s],
+                                h * 64, g, k0 + j * NB, b);
+                *issued_k = j + 1;
+            }
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ the V ring
+        if (lane == 0) {
+            for (int j = 0; j < nblk; ++j) {
+                const int s = j & 1;
+                // stage s is free once PV_{j-2} is done
+                if (j >= 2 && !mbar_wait(&bar[B_VE + s], ((j >> 1) - 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&bar[B_VF + s], TILE_BYTES);
                 for (int h = 0; h < 2; ++h)
-                    tma_load_4d(vs + h * HALF_BYTES, mv, &bar[B_VF0 + s], h * 64, g, key0, b);
-                *issued = j + 1;
+                    tma_load_4d(sm + OFF_V + s * TILE_BYTES + h * HALF_BYTES, mv, &bar[B_VF + s],
+                                h * 64, g, k0 + j * NB, b);
+                *issued_v = j + 1;
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idS = idesc_bf16_f32(128, NB, false, false);
-            const uint32_t idPV = idesc_bf16_f32(128, HD, false, true);
+            const uint32_t idPV = idesc_f16_f32(128, HD, false, true);
             const uint32_t q_s = smem_u32(sm + OFF_Q);
-            const uint32_t phi_s = smem_u32(sm + OFF_PHI);
-            ok = mbar_wait(&bar[B_Q], 0, abort_flag);
-            for (int j = 0; j < nblk && ok; ++j) {
-                const int s = j & 1;
-                const uint32_t ps = (j >> 1) & 1;
-                const uint32_t k_s = smem_u32(sm + OFF_KV + s * 2 * TILE_BYTES);
-                const uint32_t v_s = k_s + TILE_BYTES;
-                if (!mbar_wait(&bar[B_KF0 + s], ps, abort_flag)) { ok = false; break; }
-                if (j >= 1 && !mbar_wait(&bar[B_SFREE], (j - 1) & 1, abort_flag)) { ok = false; break; }
+            const uint32_t p_s = smem_u32(sm + OFF_P);
+            // S_i = Q K_i^T into S buffer i & 1
+            auto issue_s = [&](int i) -> bool {
+                const int s = i & 1;
+                if (!mbar_wait(&bar[B_KF + s], (i >> 1) & 1, abort_flag)) return false;
+                // the softmax has read S_{i-2} out of this buffer
+                if (i >= 2 && !mbar_wait(&bar[B_SFREE + s], ((i >> 1) - 1) & 1, abort_flag))
+                    return false;
                 tc_fence_after();
+                const uint32_t k_s = smem_u32(sm + OFF_K + s * TILE_BYTES);
 #pragma unroll
                 for (int k = 0; k < HD / 16; ++k) {
                     const uint32_t off = (k >> 2) * HALF_BYTES + (k & 3) * 32;
-                    mma_bf16(tS, sdesc_sw128(q_s + off, 16, 1024), sdesc_sw128(k_s + off, 16, 1024),
-                             idS, k > 0);
+                    mma_bf16(tmem + s * 128, sdesc_sw128(q_s + off, 16, 1024),
+                             sdesc_sw128(k_s + off, 16, 1024), idS, k > 0);
                 }
-                mma_commit(&bar[B_SFULL]);
+                mma_commit(&bar[B_SFULL + s]);
+                mma_commit(&bar[B_KE + s]);
+                return true;
+            };
+            ok = mbar_wait(&bar[B_Q], 0, abort_flag);
+            if (ok) ok = issue_s(0);
+            if (ok && nblk > 1) ok = issue_s(1);
+            for (int j = 0; j < nblk && ok; ++j) {
+                const int s = j & 1;
+                // P_j written and V_j converted to fp16 by the softmax threads
                 if (!mbar_wait(&bar[B_PFULL], j & 1, abort_flag)) { ok = false; break; }
-                if (!mbar_wait(&bar[B_VF0 + s], ps, abort_flag)) { ok = false; break; }
                 tc_fence_after();
+                const uint32_t v_s = smem_u32(sm + OFF_V + s * TILE_BYTES);
 #pragma unroll
                 for (int k = 0; k < NB / 16; ++k) {
                     const uint32_t offp = (k >> 2) * HALF_BYTES + (k & 3) * 32;
-                    mma_bf16(tO, sdesc_sw128(phi_s + offp, 16, 1024),
-                             sdesc_sw128(v_s + k * 2048, HALF_BYTES, 1024), idPV, (j > 0 || k > 0));
-                }
-#pragma unroll
-                for (int k = 0; k < NB / 16; ++k) {
-                    const uint32_t offp = (k >> 2) * HALF_BYTES + (k & 3) * 32;
-                    mma_bf16(tO, sdesc_sw128(k_s + offp, 16, 1024),
-                             sdesc_sw128(v_s + k * 2048, HALF_BYTES, 1024), idPV, 1);
+                    mma_f16(tO, sdesc_sw128(p_s + offp, 16, 1024),
+                            sdesc_sw128(v_s + k * 2048, HALF_BYTES, 1024), idPV, (j > 0 || k > 0));
                 }
                 mma_commit(&bar[B_PVDONE]);
-                mma_commit(&bar[B_EMP0 + s]);
+                mma_commit(&bar[B_VE + s]);
+                if (j + 2 < nblk) ok = issue_s(j + 2);
             }
         }
     } else {
         // ------------------------------------------------------------ softmax
-        // Softmax warp sw = warp - 2: warpgroup wg = sw / 4 owns key (and
+        // Softmax warp sw = warp - NROLE: warpgroup wg = sw / 4 owns key (and
         // output) columns [CPT wg, CPT wg + CPT) of row lg * 32 + lane, where
         // lg = warp % 4 is the tensor-memory lane group the warp may access.
         // The NWG threads of a row swap partial maxima through shared memory
         // under a named barrier over the NWG warps of that lane group.
-        const int wg = (warp - 2) >> 2;
+        const int st = threadIdx.x - 32 * NROLE;           // 0 .. NSOFT-1
+        const int wg = (warp - NROLE) >> 2;
         const int lg = warp & 3;
         const int row = lg * 32 + lane;
         const int r = mt * BM + row;                     // query row within (request, kv-head)
@@ -262,17 +301,18 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         }
         const float sl2 = 1.4426950408889634f * rsqrtf((float)HD);   // log2(e) / sqrt(D)
         float m_ref = -INFINITY, l = 0.0f;                // m_ref in raw score units
-        unsigned char* phi = sm + OFF_PHI;
+        unsigned char* pbuf = sm + OFF_P;
         float sv[CPT];
         for (int j = 0; j < nblk; ++j) {
-            bool w_ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL], j & 1, abort_flag));
+            const int s = j & 1;
+            bool w_ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL + s], (j >> 1) & 1, abort_flag));
             float pm0 = -INFINITY, pm1 = -INFINITY, pm2 = -INFINITY, pm3 = -INFINITY;
             if (w_ok) {
                 tc_fence_after();
-                tmem_ld32(tS + lane_addr + cb0, sv);
+                tmem_ld32(tmem + s * 128 + lane_addr + cb0, sv);
                 tmem_wait_ld();
                 tc_fence_before();
-                mbar_arrive(&bar[B_SFREE]);
+                mbar_arrive(&bar[B_SFREE + s]);
                 // visibility: all columns of a full cache block are visible
                 uint32_t vis = visbits;
                 if (!tree_chunk) {
@@ -307,12 +347,31 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
             }
             const float mu = (m_ref == -INFINITY) ? 0.0f : m_ref * sl2;
             l *= factor;
-            // P_j may only overwrite the P buffers once the PV MMAs of block j-1 are done
-            if (j >= 1) {
-                w_ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_PVDONE], (j - 1) & 1, abort_flag));
-                if (!bar_and(grp_bar, GRP_THREADS, w_ok)) { ok = false; break; }
-                tc_fence_after();
+            float l0 = 0.0f, l1 = 0.0f;
+#pragma unroll
+            for (int i = 0; i < CPT; i += 2) {
+                sv[i] = ex2(fmaf(sv[i], sl2, -mu));
+                sv[i + 1] = ex2(fmaf(sv[i + 1], sl2, -mu));
+                l0 += sv[i];
+                l1 += sv[i + 1];
             }
+            l += l0 + l1;
+            // V_j to fp16 in place: 16 bytes x 4 per thread
+            w_ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_VF + s], (j >> 1) & 1, abort_flag));
+            if (w_ok) {
+                uint4* vs = reinterpret_cast<uint4*>(sm + OFF_V + s * TILE_BYTES);
+                uint4 vv[TILE_BYTES / 16 / NSOFT];
+#pragma unroll
+                for (int i = 0; i < TILE_BYTES / 16 / NSOFT; ++i) vv[i] = vs[st + i * NSOFT];
+#pragma unroll
+                for (int i = 0; i < TILE_BYTES / 16 / NSOFT; ++i)
+                    vs[st + i * NSOFT] = bf16x8_to_f16x8(vv[i]);
+            }
+            // P_j may only overwrite the P buffer once PV_{j-1} is done
+            if (j >= 1 && w_ok)
+                w_ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_PVDONE], (j - 1) & 1, abort_flag));
+            if (!bar_and(grp_bar, GRP_THREADS, w_ok)) { ok = false; break; }
+            if (j >= 1) tc_fence_after();
             if (__any_sync(0xffffffffu, rescale)) {
                 float ov[32];
 #pragma unroll
@@ -325,31 +384,18 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
                 }
                 tmem_wait_st();
             }
-            unsigned char* plo = sm + OFF_KV + (j & 1) * 2 * TILE_BYTES;   // K_j's buffer
-            float l0 = 0.0f, l1 = 0.0f;
 #pragma unroll
             for (int cb = 0; cb < CPT / 8; ++cb) {         // 16-byte chunks of 8 keys
-                uint32_t hw[4], lw[4];
+                uint32_t hw[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float p0 = ex2(fmaf(sv[cb * 8 + 2 * e], sl2, -mu));
-                    const float p1 = ex2(fmaf(sv[cb * 8 + 2 * e + 1], sl2, -mu));
-                    l0 += p0;
-                    l1 += p1;
-                    // P_hi: p truncated to bf16 (exact), P_lo: bf16(p - P_hi)
-                    const uint32_t u0 = __float_as_uint(p0) & 0xffff0000u;
-                    const uint32_t u1 = __float_as_uint(p1) & 0xffff0000u;
-                    hw[e] = __byte_perm(u0, u1, 0x7632);
-                    const __nv_bfloat162 l2 =
-                        __floats2bfloat162_rn(p0 - __uint_as_float(u0), p1 - __uint_as_float(u1));
-                    lw[e] = *reinterpret_cast<const uint32_t*>(&l2);
+                    const __half2 h2 = __floats2half2_rn(sv[cb * 8 + 2 * e], sv[cb * 8 + 2 * e + 1]);
+                    hw[e] = *reinterpret_cast<const uint32_t*>(&h2);
                 }
                 const int col = cb0 + cb * 8;              // key column within the block
                 const uint32_t off = (col >> 6) * HALF_BYTES + sw128_offset(row, col & 63);
-                *reinterpret_cast<uint4*>(phi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4*>(plo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             }
-            l += l0 + l1;
             fence_async_smem();
             tc_fence_before();
             mbar_arrive(&bar[B_PFULL]);
@@ -408,14 +454,14 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         // is released: wait (bounded) on the phases of the last issued blocks
         int never = 0;
         mbar_wait(&bar[B_Q], 0, &never);
-        for (int j = max(0, *issued - 2); j < *issued; ++j) {
-            mbar_wait(&bar[B_KF0 + (j & 1)], (j >> 1) & 1, &never);
-            mbar_wait(&bar[B_VF0 + (j & 1)], (j >> 1) & 1, &never);
-        }
+        for (int j = max(0, *issued_k - 2); j < *issued_k; ++j)
+            mbar_wait(&bar[B_KF + (j & 1)], (j >> 1) & 1, &never);
+        for (int j = max(0, *issued_v - 2); j < *issued_v; ++j)
+            mbar_wait(&bar[B_VF + (j & 1)], (j >> 1) & 1, &never);
     }
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, TMEM_COLS);
     }
 }
 

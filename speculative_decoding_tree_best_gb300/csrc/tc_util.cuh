@@ -47,15 +47,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Wait for the phase with the given parity to complete; false on timeout or
-// when *abort becomes non-zero (another role of the CTA gave up).
+// Wait for the phase with the given parity to complete; false after `limit`
+// SM cycles or when *abort becomes non-zero (another role of the CTA gave up).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort) {
+                                          volatile int* abort,
+                                          long long limit = kWaitCycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
         if (*abort) return false;
-        if (clock64() - t0 > kWaitCycles) return false;
+        if (clock64() - t0 > limit) return false;
     }
     return true;
 }
@@ -157,6 +158,12 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// kind::f16 takes its operand type (bf16 or f16, the same for A and B) from the
+// instruction descriptor; this name marks the f16 uses.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    mma_bf16(d_tmem, a_desc, b_desc, idesc, accumulate);
+}
 // Arrive on *bar once every previously issued tcgen05.mma of this thread has
 // completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -189,6 +196,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
     return (1u << 4)                               // D format: f32
            | (1u << 7)                             // A format: bf16
            | (1u << 10)                            // B format: bf16
+           | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16)
+           | ((uint32_t)(N >> 3) << 17)            // N / 8
+           | ((uint32_t)(M >> 4) << 24);           // M / 16
+}
+
+// Instruction descriptor: kind::f16 with f16 A and B, fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4)                               // D format: f32 (A, B format 0: f16)
            | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16)
            | ((uint32_t)(N >> 3) << 17)            // N / 8
            | ((uint32_t)(M >> 4) << 24);           // M / 16
