@@ -228,6 +228,10 @@ int spec_verify_step(const spec_cfg *cfg, const int32_t *lat_tok, const float *l
                      const spec_tree *tree, const spec_step_io *step, const void *logits,
                      const spec_commit_io *io, const spec_accept *out, void *ws, void *stream);
 
+/* Number of kernel launches one spec_verify_step(cfg) call makes (host only;
+ * -1 on an invalid cfg): for sizing graphs and counting launches. */
+int spec_step_launches(const spec_cfg *cfg);
+
 /* Copy the device status word into *host_status (host pointer) and wait for
  * `stream`.  Returns ST_OK, or ST_ECUDA if the copy failed. */
 int spec_status_read(const void *ws, uint32_t *host_status, void *stream);

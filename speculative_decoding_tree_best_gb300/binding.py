@@ -25,7 +25,7 @@ SPEC_IO_F32, SPEC_IO_BF16 = 0, 1
 EXPORTS = ("spec_workspace_bytes", "spec_tree_build", "gdn_tree_verify", "attn_tree_verify",
            "accept_and_commit", "spec_verify_step", "spec_status_read", "spec_status_clear",
            "spec_status_string", "spec_abi_version", "attn_tree_verify_noalloc",
-           "spec_wait_probe")
+           "spec_wait_probe", "spec_step_launches")
 
 _lock = threading.Lock()
 _lib = None
@@ -91,8 +91,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
             lib.spec_status_string.restype = ctypes.c_char_p
             lib.attn_tree_verify_noalloc.argtypes = [cfgp, ctypes.POINTER(SpecTree)] + [vp] * 9
             lib.spec_wait_probe.argtypes = [ctypes.c_uint32, ctypes.c_int, vp, vp]
+            lib.spec_step_launches.argtypes = [cfgp]
             for n in ("spec_tree_build", "gdn_tree_verify", "attn_tree_verify",
-                      "attn_tree_verify_noalloc", "spec_wait_probe",
+                      "attn_tree_verify_noalloc", "spec_wait_probe", "spec_step_launches",
                       "accept_and_commit", "spec_verify_step", "spec_status_read",
                       "spec_status_clear", "spec_abi_version"):
                 getattr(lib, n).restype = ctypes.c_int
@@ -273,6 +274,14 @@ def spec_status_read(ws, stream=None) -> int:
     _check("spec_status_read", load().spec_status_read(_ptr(ws, name="ws"), ctypes.byref(v),
                                                        _stream(stream)))
     return int(v.value)
+
+
+def spec_step_launches(cfg) -> int:
+    """Kernel launches one spec_verify_step call makes (host only)."""
+    n = load().spec_step_launches(ctypes.byref(cfg))
+    if n < 0:
+        raise SpecError("spec_step_launches", ST_EINVAL, "invalid cfg")
+    return n
 
 
 def spec_wait_probe(limit_us: int, satisfy: bool, ws, stream=None):

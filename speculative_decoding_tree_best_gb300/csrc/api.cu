@@ -200,6 +200,13 @@ int spec_verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* l
     return cuda_rc(e);
 }
 
+int spec_step_launches(const spec_cfg* cfg) {
+    if (check_cfg(cfg) != ST_OK) return -1;
+    const int na = cfg->n_attn_layers, ng = cfg->n_gdn_layers;
+    const int commit = (na + ng) > 0 ? 1 : 0;
+    return 1 + 2 * na + 1 + ng + commit;    // tree, partials + merges, argmax, GDN, commit
+}
+
 int spec_status_read(const void* ws, uint32_t* host_status, void* stream) {
     if (!ws || !host_status) return ST_EINVAL;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

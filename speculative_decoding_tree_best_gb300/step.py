@@ -91,5 +91,4 @@ class VerifyStep:
 
     @property
     def launches_per_step(self) -> int:
-        c = self.cfg
-        return 1 + c.n_gdn_layers + 2 * c.n_attn_layers + 2
+        return binding.spec_step_launches(self.cfg)

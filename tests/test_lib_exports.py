@@ -57,6 +57,14 @@ def test_workspace_sizing_is_host_only(lib):
     assert lib.spec_workspace_bytes(ctypes.byref(bad)) == 0
 
 
+def test_step_launch_count_is_host_only(lib):
+    # tree, attention partials + merge, argmax/accept, GDN, commit
+    assert binding.spec_step_launches(binding.make_cfg(synth.config(0))) == 6
+    assert binding.spec_step_launches(binding.make_cfg(synth.config(4))) == 1 + 32 + 1 + 48 + 1
+    bad = binding.make_cfg(synth.config(1), dk=96)
+    assert lib.spec_step_launches(ctypes.byref(bad)) == -1
+
+
 @pytest.mark.parametrize("field,value", [("K", 33), ("N", 128), ("m", 0), ("Hv", 20),
                                          ("Hq", 30), ("D", 256), ("io_dtype", 7)])
 def test_validation_rejects_before_launch(lib, field, value):
