@@ -61,6 +61,29 @@ def algorithmic_bytes(s: synth.SpecConfig, mean_L: float, tau: float) -> dict:
     return out
 
 
+# DRAM bytes per launch of the attention pair (split-KV partial + merge) from
+# ncu captures (dram__bytes_read.sum + dram__bytes_write.sum, caches flushed
+# between kernels), keyed by workload, with the SHA-256 of the two kernel
+# sources they were taken on: once the kernels change, the figure is dropped.
+ATTN_SOURCES = ("speculative_decoding_tree_best_gb300/csrc/attn_tree_tc.cu",
+                "speculative_decoding_tree_best_gb300/csrc/attn_tree.cu")
+ATTN_TRAFFIC_SHA256 = "1ad6bfffb056df6e92a631de108d7e6abca57b4f0fb30a5c9a5ffbe1ae261feb"
+ATTN_TRAFFIC_BYTES = {"single": 17128448 + 0 + 3627520 + 0,
+                      "long": 71257600 + 3963136 + 9381376 + 0,
+                      "batched": 440023808 + 24915712 + 30205696 + 2816}
+
+
+def attn_traffic(name: str):
+    import hashlib
+    h = hashlib.sha256()
+    for f in ATTN_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest() != ATTN_TRAFFIC_SHA256:
+        return None
+    return ATTN_TRAFFIC_BYTES.get(name)
+
+
 def hbm_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -496,7 +519,7 @@ def run_ours(args, rank, world, local):
         "roofline": {"bound": "hbm", "kernel": "attn_tree_verify (split-KV + merge)",
                      "achieved": ach_attn, "peak": peak, "unit": "GB/s", "frac": ach_attn / peak,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
-                     "algorithmic_bytes": byts["attn_kernel"], "traffic": None},
+                     "algorithmic_bytes": byts["attn_kernel"], "traffic": attn_traffic(scfg.name)},
         "gdn_roofline": {"bound": "hbm", "kernel": "gdn_tree_verify", "achieved": ach_gdn,
                          "peak": peak, "unit": "GB/s", "frac": ach_gdn / peak,
                          "algorithmic_bytes": byts["gdn_kernel"]},
