@@ -15,11 +15,13 @@
 //  1. threads read the fp32 state once and write it as two bf16 terms
 //     (h = hi + lo, hi = bf16(h), lo = bf16(h - hi): ~16 significant bits, the
 //     product keeps fp32 accuracy to ~2^-17) in the MN-major 128-byte-swizzled
-//     layout; TMA brings the K and Q rows of the q-k head (K-major, 32 rows
-//     each) and the v rows of the head;
-//  2. one thread issues 2 x 8 tcgen05.mma for P (M = 128 state columns,
-//     N = 64 rows of [K; Q], K = 16) and 8 more for the Gram rows [K; Q] K^T;
-//     both accumulate in tensor memory;
+//     layout, one half of the d_k rows at a time through one 32 KB buffer (the
+//     second half's lines are prefetched into L2 meanwhile); TMA brings the K
+//     and Q rows of the q-k head (K-major, 32 rows each) and the v rows;
+//  2. one thread issues 2 x 4 tcgen05.mma for P per half (M = 128 state
+//     columns, N = 64 rows of [K; Q], K = 16) and 8 more for the Gram rows
+//     [K; Q] K^T; both accumulate in tensor memory.  66 KB of shared memory
+//     per CTA: three CTAs share an SM;
 //  3. P and the Gram rows move to shared memory (over the dead state terms);
 //     with the tree, one thread per row turns its ancestor mask into dense
 //     weight rows (decay x Gram entry on the root path, zero elsewhere); one
@@ -43,16 +45,17 @@ using namespace tc;
 constexpr int DKV = 128;                 // d_k = d_v
 constexpr int NT = 256;
 constexpr int NG = NT / 128;             // column groups of 128 threads
-constexpr uint32_t A_PART = DKV * DKV * 2;   // one bf16 state term: 32 KB
+constexpr uint32_t A_PART = DKV * DKV;       // one bf16 term of half the state rows: 16 KB
 
 // Trees of up to 32 rows (TP = 32 padded rows): N = 2 TP = 64 rows of [K; Q].
 constexpr int TPM = 32;
 constexpr int NM = 2 * TPM;
 
 struct TcGdnLayout {
-    // byte offsets from the 1024-aligned shared-memory base.  After the MMAs,
-    // the state terms' space holds P [N][128] and the Gram rows G [N][TP]
-    // (fp32).
+    // byte offsets from the 1024-aligned shared-memory base.  The state goes
+    // through the tensor cores in two halves of d_k rows, each as two bf16
+    // terms (hi, lo).  After the MMAs the terms' space holds P [N][128] and
+    // the dead K/Q tile the Gram rows G [N][TP] (fp32).
     uint32_t a_hi, a_lo, p, g, b, v, nodes, bar, total;
 };
 
@@ -61,19 +64,19 @@ __host__ __device__ inline TcGdnLayout tcgdn_layout() {
     uint32_t o = 0;
     L.a_hi = o; o += A_PART;
     L.a_lo = o; o += A_PART;
-    L.p = 0;
-    L.g = L.p + NM * DKV * 4;                            // after P (32 KB)
+    L.p = 0;                                             // P: 32 KB over both terms
     L.b = o;    o += 2u * NM * 128;                      // [2 halves][64 rows][64] bf16, swizzled
+    L.g = L.b;                                           // G: 8 KB over the K/Q tile
     L.v = o;    o += 2u * TPM * 128;                     // [2 halves][32 rows][64] bf16
     L.nodes = o;
     o += 4u * (4 * TPM + 2 * TPM * TPM);                 // al be A Ap | Wu Wo [TP][TP]
     L.bar = (o + 7) / 8 * 8;
-    o = L.bar + 16 + 16;
+    o = L.bar + 24 + 16;                                 // 3 mbarriers, TMEM slot, abort flag
     L.total = o + 1024;                                  // alignment slack
     return L;
 }
 
-__global__ void __launch_bounds__(NT)
+__global__ void __launch_bounds__(NT, 3)
 gdn_tc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mq,
               const __grid_constant__ CUtensorMap mv, spec_cfg c, spec_tree tree,
               const float* __restrict__ h0, const float* __restrict__ alpha,
@@ -87,9 +90,10 @@ gdn_tc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CU
     const int ih = j / (Hv / Hk);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const TcGdnLayout L = tcgdn_layout();
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L.bar);      // [0] TMA, [1] MMA
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 2);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L.bar);      // [0] TMA, [1] MMA, [2] first half
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 3);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* issued = reinterpret_cast<volatile int*>(tmem_slot + 2);   // halves issued
     float* nodes = reinterpret_cast<float*>(sm + L.nodes);
     float* al = nodes;
     float* be = al + TPM;
@@ -102,7 +106,9 @@ gdn_tc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CU
     if (tid == 0) {
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
+        mbar_init(&bar[2], 1);
         *abort_flag = 0;
+        *issued = 0;
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
@@ -120,19 +126,22 @@ gdn_tc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CU
             tma_load_3d(sm + L.v + h * TPM * 128, &mv, &bar[0], h * 64, j, b * T);
         }
     }
-    // ---- 1. the state as two bf16 terms, MN-major, 128-byte swizzle -----------------
-    {
-        const float* hsrc = h0 + ((size_t)b * Hv + j) * DKV * DKV;
-        // 16-byte chunk = 8 consecutive columns of one row r; 2048 chunks, 8 per
-        // thread, all 16 loads in flight before any conversion
-        constexpr int CPT = DKV * 16 / NT;
-        float4 xr[2 * CPT];
+    // ---- 1./2. the state as two bf16 terms, MN-major, 128-byte swizzle, one half of
+    // the d_k rows at a time; the tensor cores form P = h0^T [K; Q] half by half
+    // (two bf16 terms of h0) and the Gram rows G = [K; Q] K^T (exact bf16 products).
+    const float* hsrc = h0 + ((size_t)b * Hv + j) * DKV * DKV;
+    // 16-byte chunk = 8 consecutive columns of one row; 1024 chunks per half,
+    // 4 per thread: chunk i of half hh is row 64 hh + (tid + i NT) / 16
+    constexpr int CPT = DKV * 8 / NT;
+    auto load_half = [&](int hh, float4* xr) {
 #pragma unroll
         for (int i = 0; i < CPT; ++i) {
-            const int idx = tid + i * NT, r = idx >> 4, ch = idx & 15;
+            const int idx = tid + i * NT, r = 64 * hh + (idx >> 4), ch = idx & 15;
             xr[2 * i] = *reinterpret_cast<const float4*>(hsrc + r * DKV + ch * 8);
             xr[2 * i + 1] = *reinterpret_cast<const float4*>(hsrc + r * DKV + ch * 8 + 4);
         }
+    };
+    auto store_half = [&](const float4* xr) {
 #pragma unroll
         for (int i = 0; i < CPT; ++i) {
             const int idx = tid + i * NT, r = idx >> 4, ch = idx & 15;
@@ -151,50 +160,75 @@ gdn_tc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CU
             *reinterpret_cast<uint4*>(sm + L.a_hi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             *reinterpret_cast<uint4*>(sm + L.a_lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
-    }
-    if (tid < T) {
-        al[tid] = alpha[((size_t)b * T + tid) * Hv + j];
-        be[tid] = beta[((size_t)b * T + tid) * Hv + j];
-    }
-    fence_async_smem();
-    __syncthreads();
-
-    // ---- 2. tensor cores: P = h0^T [K; Q] (two bf16 terms of h0), and the Gram rows
-    // G = [K; Q] K^T (exact bf16 products) ----------------------------------------------
-    bool ok = true;
-    if (warp == 1 && lane == 0) {
-        ok = mbar_wait(&bar[0], 0, abort_flag);
-        if (ok) {
-            tc_fence_after();
-            const uint32_t idP = idesc_bf16_f32(128, NM, /*a_mn=*/true, /*b_mn=*/false);
-            const uint32_t idG = idesc_bf16_f32(128, TPM, false, false);
-            const uint32_t b_s = smem_u32(sm + L.b);
+    };
+    // the MMAs of half hh (and, after the second, the Gram rows); one thread
+    auto issue_half = [&](int hh) {
+        const uint32_t idP = idesc_bf16_f32(128, NM, /*a_mn=*/true, /*b_mn=*/false);
+        const uint32_t b_s = smem_u32(sm + L.b);
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                const uint32_t a_s = smem_u32(sm + (part ? L.a_lo : L.a_hi));
+        for (int part = 0; part < 2; ++part) {
+            const uint32_t a_s = smem_u32(sm + (part ? L.a_lo : L.a_hi));
 #pragma unroll
-                for (int ks = 0; ks < DKV / 16; ++ks) {
-                    const uint64_t ad = sdesc_sw128(a_s + ks * 2048, A_PART / 2, 1024);
-                    const uint64_t bd = sdesc_sw128(b_s + (ks >> 2) * NM * 128 + (ks & 3) * 32, 16, 1024);
-                    mma_bf16(tmem, ad, bd, idP, (part | ks) != 0);
-                }
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = sdesc_sw128(a_s + kk * 2048, A_PART / 2, 1024);
+                const uint64_t bd = sdesc_sw128(b_s + hh * NM * 128 + kk * 32, 16, 1024);
+                mma_bf16(tmem, ad, bd, idP, (hh | part | kk) != 0);
             }
-            // Gram: A = the [K; Q] rows (M = 128 rows read, the first 64 meaningful),
-            // B = the K rows (N = 32); both K-major over d_k
+        }
+        if (hh == 1) {
+            // Gram: A = the [K; Q] rows (M = 128 rows read, the first 64
+            // meaningful), B = the K rows (N = 32); both K-major over d_k
+            const uint32_t idG = idesc_bf16_f32(128, TPM, false, false);
 #pragma unroll
             for (int ks = 0; ks < DKV / 16; ++ks) {
                 const uint32_t off = (ks >> 2) * NM * 128 + (ks & 3) * 32;
                 mma_bf16(tmem + NM, sdesc_sw128(b_s + off, 16, 1024),
                          sdesc_sw128(b_s + off, 16, 1024), idG, ks != 0);
             }
-            mma_commit(&bar[1]);
+        }
+        mma_commit(&bar[hh ? 1 : 2]);
+        *issued = hh + 1;
+    };
+    float4 xr[2 * CPT];
+    load_half(0, xr);
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) {          // the second half's lines on their way to L2
+        const int idx = tid + i * NT;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(hsrc + (64 + (idx >> 4)) * DKV + (idx & 15) * 8));
+    }
+    store_half(xr);
+    if (tid < T) {
+        al[tid] = alpha[((size_t)b * T + tid) * Hv + j];
+        be[tid] = beta[((size_t)b * T + tid) * Hv + j];
+    }
+    fence_async_smem();
+    __syncthreads();
+    bool ok = true;
+    if (warp == 1 && lane == 0) {
+        ok = mbar_wait(&bar[0], 0, abort_flag);
+        if (ok) {
+            tc_fence_after();
+            issue_half(0);
+        }
+    }
+    load_half(1, xr);
+    // the first half's MMAs have read the terms: write the second half over them
+    if (!__syncthreads_and(ok && mbar_wait(&bar[2], 0, abort_flag))) {
+        ok = false;
+    } else {
+        store_half(xr);
+        fence_async_smem();
+        __syncthreads();
+        if (warp == 1 && lane == 0) {
+            tc_fence_after();
+            issue_half(1);
         }
     }
     // P -> smem [64][128] and G -> smem [64][32] (over the dead state terms); warp
     // w < 4 owns tensor-memory lanes 32w..32w+31
     float* P = reinterpret_cast<float*>(sm + L.p);
     float* Gs = reinterpret_cast<float*>(sm + L.g);
-    if (warp < 4) {
+    if (warp < 4 && ok) {
         const bool w_ok = __all_sync(0xffffffffu, mbar_wait(&bar[1], 0, abort_flag));
         if (w_ok) {
             tc_fence_after();
@@ -229,9 +263,11 @@ gdn_tc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CU
         tmem_dealloc(tmem, kTmemCols);
     }
     if (*abort_flag) {
-        if (tid == 0) {          // let the TMA copies land before leaving
+        if (tid == 0) {          // let the TMA copies and issued MMAs land before leaving
             int never = 0;
             mbar_wait(&bar[0], 0, &never);
+            if (*issued >= 1) mbar_wait(&bar[2], 0, &never);
+            if (*issued >= 2) mbar_wait(&bar[1], 0, &never);
         }
         pdl_wait();
         pdl_trigger();
