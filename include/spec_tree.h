@@ -271,8 +271,8 @@ int spec_wait_probe(uint32_t limit_us, int satisfy, void *ws, void *stream);
  *   - the scratch (status word + split-KV partials) is a static device array
  *     of SPEC_NOALLOC_SCRATCH_BYTES inside the library, one per device; a
  *     shape whose partials do not fit returns ST_ESCRATCH before any device
- *     work (with Hkv = 8, D = 128, bf16: one request up to Lmax ~ 19K, or up to
- *     4 requests at Lmax = 4096);
+ *     work (with Hkv = 8, D = 128, bf16, T <= 32: one request up to Lmax ~ 61K,
+ *     two up to ~ 28K, four up to ~ 12K);
  *   - dev_status: NULL, or a 4-byte-aligned device word the call ORs its
  *     SPEC_DEV_* bits into (the caller zeroes it when it wants); the scratch
  *     status word itself starts at zero and every call leaves it at zero.
