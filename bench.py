@@ -66,11 +66,12 @@ def algorithmic_bytes(s: synth.SpecConfig, mean_L: float, tau: float) -> dict:
 # between kernels), keyed by workload, with the SHA-256 of the two kernel
 # sources they were taken on: once the kernels change, the figure is dropped.
 ATTN_SOURCES = ("speculative_decoding_tree_best_gb300/csrc/attn_tree_tc.cu",
-                "speculative_decoding_tree_best_gb300/csrc/attn_tree.cu")
-ATTN_TRAFFIC_SHA256 = "1ad6bfffb056df6e92a631de108d7e6abca57b4f0fb30a5c9a5ffbe1ae261feb"
-ATTN_TRAFFIC_BYTES = {"single": 17128448 + 0 + 3627520 + 0,
-                      "long": 71257600 + 3963136 + 9381376 + 0,
-                      "batched": 440023808 + 24915712 + 30205696 + 2816}
+                "speculative_decoding_tree_best_gb300/csrc/attn_tree.cu",
+                "speculative_decoding_tree_best_gb300/csrc/common.cuh")
+ATTN_TRAFFIC_SHA256 = "c90a50e0f6cddc32ced357912cc8bda85e8d25260e348b22a67e49c8ac5f72d2"
+ATTN_TRAFFIC_BYTES = {"single": 17128704 + 0 + 3628544 + 0,
+                      "long": 72053760 + 3496192 + 4983552 + 0,
+                      "batched": 440008192 + 16598528 + 19070720 + 0}
 
 
 def attn_traffic(name: str):
