@@ -191,33 +191,47 @@ __device__ __forceinline__ void merge_row(const spec_cfg& c, const spec_tree& tr
         float m_run = -INFINITY, den_run = 0.0f;
         for (int base = 0; base < nch; base += 32) {           // rounds of 32 chunks
             const int i = base + lane;
+            const int cnt = min(32, nch - base);
+            // the first group's partial rows go out with the (max, sum) pairs: one
+            // round trip.  Chunks without keys never wrote their rows; their
+            // weight is 0 and a select (not a product) drops whatever is there.
+            float raw[kMergeGroup][EPL];
+#pragma unroll
+            for (int k = 0; k < kMergeGroup; ++k) {
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) raw[k][e] = 0.0f;
+                if (k < cnt)
+                    load_partial<EPL>(wO + ((tile0 + base + k) * 128 + rr) * D + lane * EPL, raw[k]);
+            }
             const float2 ml = i < nch ? wML[(tile0 + i) * 128 + rr] : make_float2(-INFINITY, 0.0f);
             float M = ml.x;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
             const float f = ml.y > 0.0f ? ml.y * __expf(ml.x - M) : 0.0f;  // unnormalised weight
             const float den_r = warp_sum(f);
-            const int cnt = min(32, nch - base);
             float gacc[EPL];
 #pragma unroll
             for (int e = 0; e < EPL; ++e) gacc[e] = 0.0f;
-            // groups of 8 chunks, the group's loads all in flight (predicated;
-            // empty chunks load nothing); few registers, so many warps per SM
-            // hide the two dependent round trips (weights, then partials)
-            for (int k0 = 0; k0 < cnt; k0 += kMergeGroup) {
-                float raw[kMergeGroup][EPL];
+#pragma unroll
+            for (int k = 0; k < kMergeGroup; ++k) {
+                const float fk = __shfl_sync(0xffffffffu, f, k);
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) gacc[e] = fk > 0.0f ? fmaf(raw[k][e], fk, gacc[e]) : gacc[e];
+            }
+            // further groups (more than 8 chunks): loads only where the weight is non-zero
+            for (int k0 = kMergeGroup; k0 < cnt; k0 += kMergeGroup) {
 #pragma unroll
                 for (int k = 0; k < kMergeGroup; ++k) {
 #pragma unroll
                     for (int e = 0; e < EPL; ++e) raw[k][e] = 0.0f;
-                    const bool has = __shfl_sync(0xffffffffu, f, k0 + k) > 0.0f;
+                    const bool has = __shfl_sync(0xffffffffu, f, (k0 + k) & 31) > 0.0f;
                     if (k0 + k < cnt && has)
                         load_partial<EPL>(wO + ((tile0 + base + k0 + k) * 128 + rr) * D + lane * EPL,
                                           raw[k]);
                 }
 #pragma unroll
                 for (int k = 0; k < kMergeGroup; ++k) {
-                    const float fk = __shfl_sync(0xffffffffu, f, k0 + k);
+                    const float fk = __shfl_sync(0xffffffffu, f, (k0 + k) & 31);
 #pragma unroll
                     for (int e = 0; e < EPL; ++e) gacc[e] = fmaf(raw[k][e], fk, gacc[e]);
                 }
