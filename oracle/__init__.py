@@ -60,8 +60,9 @@ def _load():
         if _lib is None:
             path = build()
             lib = ctypes.CDLL(path)
-            for name in ("orc_tree_build", "orc_gdn_tree", "orc_attn_tree", "orc_argmax",
-                         "orc_accept", "orc_commit_gdn", "orc_commit_kv"):
+            for name in ("orc_tree_build", "orc_tree_build_ragged", "orc_gdn_tree",
+                         "orc_attn_tree", "orc_argmax", "orc_accept", "orc_commit_gdn",
+                         "orc_commit_kv"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -132,6 +133,36 @@ def tree_build(lat_tok, lat_score, root_tok, N: int) -> dict:
         _p(out["node_depth"]), _p(out["node_rank"]), _p(out["node_score"]), _p(out["node_anc"]),
         _p(out["n_nodes"]))
     _check(rc, "tree_build")
+    return out
+
+
+def tree_build_ragged(lat_tok, lat_score, root_tok, N: int, m_req, budget: int) -> dict:
+    """Best-first draft trees of a batch sharing a node budget.
+
+    Digest section: technical novelty, batching (a node budget shared by the
+    batch at the target GEMM's 192-node plateau; 16/12/8 draft positions
+    chosen per request), with the tree rules of tree_build.  Request b drafts
+    from its first m_req[b] lattice positions; draft nodes are inserted
+    best-first over all requests' frontiers together (score desc, request asc,
+    then depth, parent, rank), at most N per request, at most `budget` in all
+    (budget < 0: no shared budget).
+    """
+    tok = _np(lat_tok, np.int32)
+    sc = _np(lat_score, np.float32)
+    root = _np(root_tok, np.int32).reshape(-1)
+    mr = _np(m_req, np.int32).reshape(-1)
+    B, m, K = tok.shape
+    T = N + 1
+    out = dict(
+        node_tok=np.empty((B, T), np.int32), node_parent=np.empty((B, T), np.int32),
+        node_depth=np.empty((B, T), np.int32), node_rank=np.empty((B, T), np.int32),
+        node_score=np.empty((B, T), np.float32),
+        node_anc=np.empty((B, T, ANC_WORDS), np.uint64), n_nodes=np.empty((B,), np.int32))
+    rc = _load().orc_tree_build_ragged(
+        B, m, K, N, _p(mr), int(budget), _p(tok), _p(sc), _p(root), _p(out["node_tok"]),
+        _p(out["node_parent"]), _p(out["node_depth"]), _p(out["node_rank"]),
+        _p(out["node_score"]), _p(out["node_anc"]), _p(out["n_nodes"]))
+    _check(rc, "tree_build_ragged")
     return out
 
 

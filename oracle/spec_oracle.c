@@ -23,7 +23,10 @@
  *           o_t = h_t^T q_t;
  *   [NOV]   technical novelty + Figure 6 ("Best-first tree on a hybrid
  *           target") -- best-first tree with edges scored log p(child|parent);
- *           node states recomputed along root paths, no per-node snapshots.
+ *           node states recomputed along root paths, no per-node snapshots;
+ *   [BATCH] technical novelty, batching -- a node budget shared by the batch
+ *           (the target GEMM's 192-node plateau) and the number of draft
+ *           positions chosen per request (16/12/8).
  *
  * Precision: every floating-point result is accumulated in double from the
  * exact values of the (bf16 or fp32) inputs.  The one exception is the tree
@@ -41,6 +44,11 @@
  *   R8  Attention scale 1/sqrt(D); q-head h reads kv-head h / (Hq / Hkv).
  *   R9  Commit: the state after the last accepted node becomes the committed
  *       state; the tree K/V rows of the accepted path are appended.
+ *   R12 Shared budget: request b drafts from its first m_b lattice positions;
+ *       the batch's draft nodes are inserted best-first over the frontiers of
+ *       all requests together (key: score desc, then request index asc, then
+ *       the R3 order), each request holding at most N drafts, until the budget
+ *       is spent or every frontier is empty.
  *
  * Layouts (all row-major, outermost first):
  *   lattice     tok int32 [B][m][K], score f32 [B][m][K]
@@ -197,6 +205,118 @@ int orc_tree_build(int B, int m, int K, int N,
     }
     free(order);
     free(front);
+    return rc;
+}
+
+/*
+ * orc_tree_build_ragged: best-first draft trees of a batch that shares a node
+ * budget [BATCH][TREE][NOV], reading R12.
+ *
+ * m_req[b] in [1, m] lattice positions per request; budget = total draft
+ * nodes over the batch (budget < 0: no shared budget, every request up to N).
+ * The frontier is one list over all requests; the entry first in the order
+ * (score desc, request asc, depth asc, parent asc, rank asc) becomes the next
+ * node of its request, unless that request already holds N drafts, in which
+ * case the entry is dropped.  Outputs and padding rows as orc_tree_build.
+ * Returns -1 on bad sizes or m_req, -2 on a repeated token, -3 on allocation.
+ */
+int orc_tree_build_ragged(int B, int m, int K, int N, const int32_t *m_req, int budget,
+                          const int32_t *lat_tok, const float *lat_score,
+                          const int32_t *root_tok,
+                          int32_t *node_tok, int32_t *node_parent, int32_t *node_depth,
+                          int32_t *node_rank, float *node_score, uint64_t *node_anc,
+                          int32_t *n_nodes)
+{
+    if (B < 0 || m < 1 || K < 1 || N < 0 || N + 1 > ORC_MAX_ROWS) return -1;
+    for (int b = 0; b < B; ++b)
+        if (m_req[b] < 1 || m_req[b] > m) return -1;
+    const int T = N + 1;
+    int *order = (int *)malloc(sizeof(int) * (size_t)(B > 0 ? B : 1) * m * K);
+    orc_cand *front = (orc_cand *)malloc(sizeof(orc_cand) * (size_t)(B > 0 ? B : 1) * (T * K + K));
+    int *front_req = (int *)malloc(sizeof(int) * (size_t)(B > 0 ? B : 1) * (T * K + K));
+    if (!order || !front || !front_req) { free(order); free(front); free(front_req); return -3; }
+    int rc = 0, nfront = 0;
+
+    for (int b = 0; b < B && rc == 0; ++b) {
+        const int32_t *tok = lat_tok + (size_t)b * m * K;
+        const float *sc = lat_score + (size_t)b * m * K;
+        for (int s = 0; s < m; ++s) {            /* canonical order per position */
+            int *o = order + ((size_t)b * m + s) * K;
+            for (int i = 0; i < K; ++i) {
+                int j = i;
+                while (j > 0 && sc[s * K + i] > sc[s * K + o[j - 1]]) {
+                    o[j] = o[j - 1];
+                    --j;
+                }
+                o[j] = i;
+            }
+            for (int i = 0; i < K; ++i)
+                for (int j = i + 1; j < K; ++j)
+                    if (tok[s * K + i] == tok[s * K + j]) rc = -2;
+        }
+        int32_t *ntok = node_tok + (size_t)b * T, *npar = node_parent + (size_t)b * T;
+        int32_t *ndep = node_depth + (size_t)b * T, *nrank = node_rank + (size_t)b * T;
+        float *nsc = node_score + (size_t)b * T;
+        uint64_t *nanc = node_anc + (size_t)b * T * ORC_ANC_WORDS;
+        for (int n = 0; n < T; ++n) {
+            ntok[n] = -1; npar[n] = -1; ndep[n] = -1; nrank[n] = -1; nsc[n] = 0.0f;
+            for (int w = 0; w < ORC_ANC_WORDS; ++w) nanc[n * ORC_ANC_WORDS + w] = 0;
+        }
+        ntok[0] = root_tok[b]; ndep[0] = 0; nanc[0] = 1ull;
+        n_nodes[b] = 1;
+        for (int r = 0; r < K; ++r) {            /* children of the root */
+            orc_cand c = { 0, r, 1, sc[order[(size_t)b * m * K + r]] };
+            front_req[nfront] = b;
+            front[nfront++] = c;
+        }
+    }
+    int used = 0;
+    while (rc == 0 && nfront > 0 && (budget < 0 || used < budget)) {
+        int best = 0;
+        for (int i = 1; i < nfront; ++i) {
+            const orc_cand *a = &front[i], *c = &front[best];
+            int before;
+            if (a->score != c->score) before = a->score > c->score;
+            else if (front_req[i] != front_req[best]) before = front_req[i] < front_req[best];
+            else before = orc_cand_before(a, c);
+            if (before) best = i;
+        }
+        const orc_cand c = front[best];
+        const int b = front_req[best];
+        front[best] = front[nfront - 1];
+        front_req[best] = front_req[nfront - 1];
+        --nfront;
+        if (n_nodes[b] >= T) continue;           /* request full: drop the entry */
+
+        const int32_t *tok = lat_tok + (size_t)b * m * K;
+        const float *sc = lat_score + (size_t)b * m * K;
+        const int *ord = order + (size_t)b * m * K;
+        int32_t *ntok = node_tok + (size_t)b * T, *npar = node_parent + (size_t)b * T;
+        int32_t *ndep = node_depth + (size_t)b * T, *nrank = node_rank + (size_t)b * T;
+        float *nsc = node_score + (size_t)b * T;
+        uint64_t *nanc = node_anc + (size_t)b * T * ORC_ANC_WORDS;
+        const int n = n_nodes[b]++;
+        ++used;
+        const int s = c.depth - 1;
+        ntok[n] = tok[s * K + ord[s * K + c.rank]];
+        npar[n] = c.parent;
+        ndep[n] = c.depth;
+        nrank[n] = c.rank;
+        nsc[n] = c.score;
+        for (int w = 0; w < ORC_ANC_WORDS; ++w)
+            nanc[n * ORC_ANC_WORDS + w] = nanc[c.parent * ORC_ANC_WORDS + w];
+        nanc[n * ORC_ANC_WORDS + n / 64] |= 1ull << (n % 64);
+        if (c.depth < m_req[b]) {
+            for (int r = 0; r < K; ++r) {
+                orc_cand ch = { n, r, c.depth + 1, nsc[n] + sc[c.depth * K + ord[c.depth * K + r]] };
+                front_req[nfront] = b;
+                front[nfront++] = ch;
+            }
+        }
+    }
+    free(order);
+    free(front);
+    free(front_req);
     return rc;
 }
 

@@ -82,6 +82,48 @@ def brute_force_tree(tok, sc, root, N):
     return out
 
 
+def brute_force_ragged(tok, sc, root, N, m_req, budget):
+    """A batch sharing a node budget, by brute force: every root path of every
+    request (depth <= m_req[b]) sorted by (score desc, request asc, then the
+    recursive tree order); paths are taken in that order while their request
+    holds fewer than N drafts and fewer than `budget` drafts are taken in all.
+    tok int [B][m][K], sc f32 [B][m][K] -> dict of batched tree arrays."""
+    B = tok.shape[0]
+    per = []
+    for b in range(B):
+        t = brute_force_tree(tok[b][: m_req[b]], sc[b][: m_req[b]], root[b],
+                             sum(tok.shape[2] ** d for d in range(1, m_req[b] + 1)))
+        per.append(t)
+    # all draft nodes of all full trees, in the global order
+    allp = []
+    for b in range(B):
+        t = per[b]
+        for i in range(1, int(t["n_nodes"])):
+            allp.append((-float(t["node_score"][i]), b, i))
+    allp.sort()
+    take = [0] * B
+    used = 0
+    for _, b, i in allp:
+        if budget >= 0 and used >= budget:
+            break
+        if take[b] >= N:
+            continue
+        assert i == take[b] + 1, "a request's drafts are taken in its own order"
+        take[b] += 1
+        used += 1
+    T = N + 1
+    out = dict(node_tok=np.full((B, T), -1, np.int32), node_parent=np.full((B, T), -1, np.int32),
+               node_depth=np.full((B, T), -1, np.int32), node_rank=np.full((B, T), -1, np.int32),
+               node_score=np.zeros((B, T), np.float32), node_anc=np.zeros((B, T, 2), np.uint64),
+               n_nodes=np.zeros(B, np.int32))
+    for b in range(B):
+        n = take[b] + 1
+        for k in ("node_tok", "node_parent", "node_depth", "node_rank", "node_score", "node_anc"):
+            out[k][b, :n] = per[b][k][:n]
+        out["n_nodes"][b] = n
+    return out
+
+
 def root_path(parent, n):
     p = []
     while n >= 0:
