@@ -264,8 +264,8 @@ int orc_tree_build_ragged(int B, int m, int K, int N, const int32_t *m_req, int 
         }
         ntok[0] = root_tok[b]; ndep[0] = 0; nanc[0] = 1ull;
         n_nodes[b] = 1;
-        for (int r = 0; r < K; ++r) {            /* children of the root */
-            orc_cand c = { 0, r, 1, sc[order[(size_t)b * m * K + r]] };
+        for (int r = 0; r < K; ++r) {            /* children of the root: 0 + edge (R2) */
+            orc_cand c = { 0, r, 1, nsc[0] + sc[order[(size_t)b * m * K + r]] };
             front_req[nfront] = b;
             front[nfront++] = c;
         }

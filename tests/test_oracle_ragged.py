@@ -43,9 +43,11 @@ def test_shared_budget_equals_brute_force(ties):
         root = rng.integers(0, 60, size=B).astype(np.int32)
         t = oracle.tree_build_ragged(tok, sc, root, N, m_req, budget)
         bf = brute_force_ragged(tok, sc, root, N, m_req, budget)
-        for key in ("n_nodes", "node_tok", "node_parent", "node_depth", "node_rank", "node_score",
-                    "node_anc"):
+        for key in ("n_nodes", "node_tok", "node_parent", "node_depth", "node_rank", "node_anc"):
             np.testing.assert_array_equal(t[key], bf[key], err_msg=f"{key} trial {trial}")
+        # keys compared bit for bit (a -0.0 edge must give a +0.0 key: 0 + edge)
+        np.testing.assert_array_equal(t["node_score"].view(np.uint32),
+                                      bf["node_score"].view(np.uint32), err_msg=f"score bits {trial}")
 
 
 def test_no_budget_is_independent_trees_over_truncated_lattices():
