@@ -65,6 +65,7 @@ enum {
 #define SPEC_DEV_OVERFLOW 0x1u  /* a request's commit was skipped: no room in the cache */
 #define SPEC_DEV_BADLAT   0x2u  /* a lattice position repeats a token or has a NaN score */
 #define SPEC_DEV_TIMEOUT  0x4u  /* a bounded device-side wait gave up */
+#define SPEC_DEV_BADREQ   0x8u  /* a per-request position count was outside [1, m] (clamped) */
 
 enum { SPEC_IO_F32 = 0, SPEC_IO_BF16 = 1 };
 
@@ -227,6 +228,42 @@ typedef struct spec_step_io {
 int spec_verify_step(const spec_cfg *cfg, const int32_t *lat_tok, const float *lat_score,
                      const spec_tree *tree, const spec_step_io *step, const void *logits,
                      const spec_commit_io *io, const spec_accept *out, void *ws, void *stream);
+
+/*
+ * spec_tree_build_ragged -- best-first draft trees of a batch with per-request
+ * draft positions and a node budget shared by the batch.
+ * Digest: technical novelty, batching (one node budget shared across the
+ * batch, at the target GEMM's 192-node plateau; 16/12/8 draft positions chosen
+ * per request), with the tree rules of spec_tree_build.
+ *
+ * Request b drafts from its first m_req[b] lattice positions (its nodes have
+ * depth <= m_req[b]).  With node_budget >= 0 the batch keeps node_budget draft
+ * nodes in all: the ones first in the order (score desc, request asc, then the
+ * per-tree order), i.e. best-first over every request's frontier together,
+ * each request holding at most N; every request keeps a prefix of its own
+ * best-first order.  node_budget < 0: no shared budget (each request up to N).
+ *   m_req  NULL (all m) or device int32 [B], values in [1, m]; an out-of-range
+ *          value is clamped and sets SPEC_DEV_BADREQ.
+ * Other arguments, outputs and padding rows as spec_tree_build.  The budget
+ * step needs 4 (B (N + 1) + 2 B) bytes of shared memory in one CTA: more than
+ * 200 KB returns ST_EUNSUPPORTED.  One more launch than spec_tree_build when
+ * node_budget >= 0.
+ */
+int spec_tree_build_ragged(const spec_cfg *cfg, const int32_t *lat_tok, const float *lat_score,
+                           const int32_t *root_tok, const int32_t *m_req, int node_budget,
+                           const spec_tree *out, void *ws, void *stream);
+
+/*
+ * spec_verify_step_ragged -- spec_verify_step with the trees of
+ * spec_tree_build_ragged (per-request draft positions, shared node budget);
+ * the rest of the step treats the rows a request did not keep as padding rows.
+ * One more launch than spec_verify_step when node_budget >= 0.
+ */
+int spec_verify_step_ragged(const spec_cfg *cfg, const int32_t *lat_tok, const float *lat_score,
+                            const int32_t *m_req, int node_budget, const spec_tree *tree,
+                            const spec_step_io *step, const void *logits,
+                            const spec_commit_io *io, const spec_accept *out, void *ws,
+                            void *stream);
 
 /* Number of kernel launches one spec_verify_step(cfg) call makes (host only;
  * -1 on an invalid cfg): for sizing graphs and counting launches. */

@@ -20,12 +20,13 @@ LIB_PATH = os.path.join(_HERE, "libspectree.so")
 
 ST_OK, ST_EINVAL, ST_EUNSUPPORTED, ST_ECUDA, ST_EOVERFLOW, ST_TIMEOUT, ST_ESCRATCH = range(7)
 NOALLOC_SCRATCH_BYTES = 8 << 20
-SPEC_DEV_OVERFLOW, SPEC_DEV_BADLAT, SPEC_DEV_TIMEOUT = 0x1, 0x2, 0x4
+SPEC_DEV_OVERFLOW, SPEC_DEV_BADLAT, SPEC_DEV_TIMEOUT, SPEC_DEV_BADREQ = 0x1, 0x2, 0x4, 0x8
 SPEC_IO_F32, SPEC_IO_BF16 = 0, 1
 EXPORTS = ("spec_workspace_bytes", "spec_tree_build", "gdn_tree_verify", "attn_tree_verify",
            "accept_and_commit", "spec_verify_step", "spec_status_read", "spec_status_clear",
            "spec_status_string", "spec_abi_version", "attn_tree_verify_noalloc",
-           "spec_wait_probe", "spec_step_launches")
+           "spec_wait_probe", "spec_step_launches", "spec_tree_build_ragged",
+           "spec_verify_step_ragged")
 
 _lock = threading.Lock()
 _lib = None
@@ -85,6 +86,13 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                              ctypes.POINTER(SpecStepIO), vp,
                                              ctypes.POINTER(SpecCommitIO),
                                              ctypes.POINTER(SpecAccept), vp, vp]
+            lib.spec_tree_build_ragged.argtypes = [cfgp, vp, vp, vp, vp, ctypes.c_int,
+                                                   ctypes.POINTER(SpecTree), vp, vp]
+            lib.spec_verify_step_ragged.argtypes = [cfgp, vp, vp, vp, ctypes.c_int,
+                                                    ctypes.POINTER(SpecTree),
+                                                    ctypes.POINTER(SpecStepIO), vp,
+                                                    ctypes.POINTER(SpecCommitIO),
+                                                    ctypes.POINTER(SpecAccept), vp, vp]
             lib.spec_status_read.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
             lib.spec_status_clear.argtypes = [vp, vp]
             lib.spec_status_string.argtypes = [ctypes.c_int]
@@ -94,6 +102,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
             lib.spec_step_launches.argtypes = [cfgp]
             for n in ("spec_tree_build", "gdn_tree_verify", "attn_tree_verify",
                       "attn_tree_verify_noalloc", "spec_wait_probe", "spec_step_launches",
+                      "spec_tree_build_ragged", "spec_verify_step_ragged",
                       "accept_and_commit", "spec_verify_step", "spec_status_read",
                       "spec_status_clear", "spec_abi_version"):
                 getattr(lib, n).restype = ctypes.c_int
@@ -254,19 +263,48 @@ def accept_and_commit(cfg, tree: TreeBuffers, logits, io: dict, out: AcceptBuffe
         ctypes.byref(out.c()), _ptr(ws, name="ws"), _stream(stream)))
 
 
+def spec_tree_build_ragged(cfg, lat_tok, lat_score, root_tok, m_req, node_budget: int,
+                           tree: TreeBuffers, ws, stream=None):
+    """Trees with per-request draft positions (m_req: CUDA int32 [B] or None) and
+    a node budget shared by the batch (node_budget < 0: none)."""
+    _check("spec_tree_build_ragged", load().spec_tree_build_ragged(
+        ctypes.byref(cfg), _ptr(lat_tok, torch.int32, "lat_tok"),
+        _ptr(lat_score, torch.float32, "lat_score"), _ptr(root_tok, torch.int32, "root_tok"),
+        _ptr(m_req, torch.int32, "m_req"), int(node_budget), ctypes.byref(tree.c()),
+        _ptr(ws, name="ws"), _stream(stream)))
+
+
+def _step_io(cfg, step: dict) -> SpecStepIO:
+    dt = _io_dtype(cfg)
+    return SpecStepIO(_ptr(step.get("gdn_q"), dt, "gdn_q"), _ptr(step.get("gdn_o"), dt, "gdn_o"),
+                      _ptr(step.get("gdn_c"), torch.float32, "gdn_c"),
+                      _ptr(step.get("attn_q"), dt, "attn_q"), _ptr(step.get("attn_o"), dt, "attn_o"))
+
+
 def spec_verify_step(cfg, lat_tok, lat_score, tree: TreeBuffers, step: dict, logits, io: dict,
                      out: AcceptBuffers, ws, stream=None):
     """Whole verify step (tree, every GDN and attention layer, accept+commit).
     step: dict with stacked gdn_q, gdn_o, gdn_c (or None), attn_q, attn_o."""
     dt = _io_dtype(cfg)
-    sio = SpecStepIO(_ptr(step.get("gdn_q"), dt, "gdn_q"), _ptr(step.get("gdn_o"), dt, "gdn_o"),
-                     _ptr(step.get("gdn_c"), torch.float32, "gdn_c"),
-                     _ptr(step.get("attn_q"), dt, "attn_q"), _ptr(step.get("attn_o"), dt, "attn_o"))
+    sio = _step_io(cfg, step)
     _check("spec_verify_step", load().spec_verify_step(
         ctypes.byref(cfg), _ptr(lat_tok, torch.int32, "lat_tok"),
         _ptr(lat_score, torch.float32, "lat_score"), ctypes.byref(tree.c()), ctypes.byref(sio),
         _ptr(logits, dt, "logits"), ctypes.byref(_commit_io(cfg, io)), ctypes.byref(out.c()),
         _ptr(ws, name="ws"), _stream(stream)))
+
+
+def spec_verify_step_ragged(cfg, lat_tok, lat_score, m_req, node_budget: int, tree: TreeBuffers,
+                            step: dict, logits, io: dict, out: AcceptBuffers, ws, stream=None):
+    """spec_verify_step over the trees of spec_tree_build_ragged."""
+    dt = _io_dtype(cfg)
+    sio = _step_io(cfg, step)
+    _check("spec_verify_step_ragged", load().spec_verify_step_ragged(
+        ctypes.byref(cfg), _ptr(lat_tok, torch.int32, "lat_tok"),
+        _ptr(lat_score, torch.float32, "lat_score"), _ptr(m_req, torch.int32, "m_req"),
+        int(node_budget), ctypes.byref(tree.c()), ctypes.byref(sio), _ptr(logits, dt, "logits"),
+        ctypes.byref(_commit_io(cfg, io)), ctypes.byref(out.c()), _ptr(ws, name="ws"),
+        _stream(stream)))
 
 
 def spec_status_read(ws, stream=None) -> int:

@@ -119,9 +119,32 @@ int accept_and_commit(const spec_cfg* cfg, const spec_tree* tree, const void* lo
                                               static_cast<cudaStream_t>(stream)));
 }
 
-int spec_verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_score,
-                     const spec_tree* tree, const spec_step_io* step, const void* logits,
-                     const spec_commit_io* io, const spec_accept* out, void* ws, void* stream) {
+int spec_tree_build_ragged(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_score,
+                           const int32_t* root_tok, const int32_t* m_req, int node_budget,
+                           const spec_tree* out, void* ws, void* stream) {
+    int rc = check_cfg(cfg);
+    if (rc) return rc;
+    if ((rc = check_tree(out))) return rc;
+    if (!al16(lat_tok) || !al16(lat_score) || !al16(root_tok) || !al16(ws)) return ST_EINVAL;
+    if (m_req && !al16(m_req)) return ST_EINVAL;
+    if (node_budget >= 0 && spec::budget_select_smem(*cfg) > 200 * 1024) return ST_EUNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = spec::launch_tree_build(*cfg, lat_tok, lat_score, root_tok, *out, ws, st, false,
+                                            m_req);
+    if (e == cudaSuccess && node_budget >= 0)
+        e = spec::launch_budget_select(*cfg, *out, node_budget, st, false);
+    return cuda_rc(e);
+}
+
+}  // extern "C"
+
+namespace {
+
+// The fused step; m_req / node_budget as in spec_tree_build_ragged.
+int verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_score,
+                const int32_t* m_req, int node_budget, const spec_tree* tree,
+                const spec_step_io* step, const void* logits, const spec_commit_io* io,
+                const spec_accept* out, void* ws, void* stream) {
     int rc = check_cfg(cfg);
     if (rc) return rc;
     if ((rc = check_tree(tree))) return rc;
@@ -164,7 +187,13 @@ int spec_verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* l
         vc = at(io->v_cache, ca);
         o = const_cast<char*>(at(step->attn_o, qo));
     };
-    cudaError_t e = spec::launch_tree_build(c, lat_tok, lat_score, io->root_tok, *tree, ws, st, true);
+    if (m_req && !al16(m_req)) return ST_EINVAL;
+    if (node_budget >= 0 && spec::budget_select_smem(c) > 200 * 1024) return ST_EUNSUPPORTED;
+    cudaError_t e = spec::launch_tree_build(c, lat_tok, lat_score, io->root_tok, *tree, ws, st, true,
+                                            m_req);
+    // the shared budget trims the trees before anything reads them
+    if (e == cudaSuccess && node_budget >= 0)
+        e = spec::launch_budget_select(c, *tree, node_budget, st, true);
     for (int l = 0; l < na && e == cudaSuccess; ++l) {
         const void *q, *kt, *vt, *kc, *vc;
         void* o;
@@ -200,11 +229,30 @@ int spec_verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* l
     return cuda_rc(e);
 }
 
+}  // namespace
+
+extern "C" {
+
 int spec_step_launches(const spec_cfg* cfg) {
     if (check_cfg(cfg) != ST_OK) return -1;
     const int na = cfg->n_attn_layers, ng = cfg->n_gdn_layers;
     const int commit = (na + ng) > 0 ? 1 : 0;
     return 1 + 2 * na + 1 + ng + commit;    // tree, partials + merges, argmax, GDN, commit
+}
+
+int spec_verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_score,
+                     const spec_tree* tree, const spec_step_io* step, const void* logits,
+                     const spec_commit_io* io, const spec_accept* out, void* ws, void* stream) {
+    return verify_step(cfg, lat_tok, lat_score, nullptr, -1, tree, step, logits, io, out, ws,
+                       stream);
+}
+
+int spec_verify_step_ragged(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_score,
+                            const int32_t* m_req, int node_budget, const spec_tree* tree,
+                            const spec_step_io* step, const void* logits, const spec_commit_io* io,
+                            const spec_accept* out, void* ws, void* stream) {
+    return verify_step(cfg, lat_tok, lat_score, m_req, node_budget, tree, step, logits, io, out, ws,
+                       stream);
 }
 
 int spec_status_read(const void* ws, uint32_t* host_status, void* stream) {

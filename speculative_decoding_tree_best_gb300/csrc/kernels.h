@@ -8,9 +8,15 @@
 namespace spec {
 
 // pdl: launch with programmatic stream serialization (spec_verify_step only).
+// m_req: lattice positions per request (nullptr: all m).
 cudaError_t launch_tree_build(const spec_cfg& c, const int32_t* lat_tok, const float* lat_score,
                               const int32_t* root_tok, const spec_tree& out, void* ws,
-                              cudaStream_t st, bool pdl = false);
+                              cudaStream_t st, bool pdl = false, const int32_t* m_req = nullptr);
+// Keep the `budget` best drafts of the batch (trees from launch_tree_build).
+// cudaErrorInvalidConfiguration when the batch's scores do not fit one CTA.
+cudaError_t launch_budget_select(const spec_cfg& c, const spec_tree& out, int budget,
+                                 cudaStream_t st, bool pdl = false);
+size_t budget_select_smem(const spec_cfg& c);
 size_t tree_build_smem(const spec_cfg& c);
 
 // Returns cudaErrorInvalidConfiguration when the shape needs more shared memory

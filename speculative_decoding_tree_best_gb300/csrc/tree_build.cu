@@ -47,12 +47,21 @@ template <int SLOTS>
 __global__ void __launch_bounds__(32)
 tree_build_kernel(spec_cfg c, const int32_t* __restrict__ lat_tok,
                   const float* __restrict__ lat_score, const int32_t* __restrict__ root_tok,
-                  spec_tree out, void* ws) {
+                  spec_tree out, void* ws, const int32_t* __restrict__ m_req) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int b = blockIdx.x;
     const int lane = threadIdx.x;
     const int m = c.m, K = c.K, T = c.N + 1;
     const int MK = m * K;
+    // depth limit of this request: m_req[b] lattice positions (all m when absent)
+    int mb = m;
+    if (m_req != nullptr) {
+        mb = m_req[b];
+        if (mb < 1 || mb > m) {
+            if (lane == 0) raise_status(ws, SPEC_DEV_BADREQ);
+            mb = mb < 1 ? 1 : m;
+        }
+    }
 
     int32_t* s_tok = reinterpret_cast<int32_t*>(smem);      // [m][K] ranked tokens
     float* s_sc = reinterpret_cast<float*>(s_tok + MK);      // [m][K] ranked edge scores
@@ -112,8 +121,8 @@ tree_build_kernel(spec_cfg c, const int32_t* __restrict__ lat_tok,
     }
     auto prefetch = [&](int k) {
         const int d = nd[k];
-        nxt[k] = (d < m && nx[k] + 1 < K) ? s_sc[d * K + nx[k] + 1] : 0.0f;
-        fst[k] = (d + 1 < m) ? s_sc[(d + 1) * K] : 0.0f;
+        nxt[k] = (d < mb && nx[k] + 1 < K) ? s_sc[d * K + nx[k] + 1] : 0.0f;
+        fst[k] = (d + 1 < mb) ? s_sc[(d + 1) * K] : 0.0f;
     };
     uint32_t bo = 0, bt = 0;   // this lane's best candidate (ord, tie)
     auto best_of_lane = [&]() {
@@ -154,7 +163,7 @@ tree_build_kernel(spec_cfg c, const int32_t* __restrict__ lat_tok,
             const float cs_p = ns[0] + nxt[0];
             const uint32_t co_p = (r + 1 < K) ? ord_f32(cs_p) : 0u;
             const float cs_n = sc + fe;
-            const uint32_t co_n = (d + 1 < m) ? ord_f32(cs_n) : 0u;
+            const uint32_t co_n = (d + 1 < mb) ? ord_f32(cs_n) : 0u;
             nx[0] = isp ? r + 1 : (isn ? 0 : nx[0]);
             nd[0] = isn ? d + 1 : nd[0];
             ns[0] = isn ? sc : ns[0];
@@ -172,8 +181,8 @@ tree_build_kernel(spec_cfg c, const int32_t* __restrict__ lat_tok,
             a1[0] = isn ? (pa1 | (n >= 64 ? 1ull << (n - 64) : 0ull)) : a1[0];
             ntk[0] = isn ? tkn : ntk[0];
             const int dd = nd[0];
-            const int i_nxt = (dd < m && nx[0] + 1 < K) ? dd * K + nx[0] + 1 : 0;
-            const int i_fst = (dd + 1 < m) ? (dd + 1) * K : 0;
+            const int i_nxt = (dd < mb && nx[0] + 1 < K) ? dd * K + nx[0] + 1 : 0;
+            const int i_fst = (dd + 1 < mb) ? (dd + 1) * K : 0;
             nxt[0] = s_sc[i_nxt];
             fst[0] = s_sc[i_fst];
         }
@@ -212,7 +221,7 @@ tree_build_kernel(spec_cfg c, const int32_t* __restrict__ lat_tok,
             for (int k = 0; k < SLOTS; ++k) {
                 if (SLOTS == 1 || k == nk) {
                     nd[k] = d + 1; nx[k] = 0; ns[k] = sc; npar[k] = p; nrk[k] = r;
-                    if (d + 1 < m) { cs[k] = sc + fe; co[k] = ord_f32(cs[k]); }
+                    if (d + 1 < mb) { cs[k] = sc + fe; co[k] = ord_f32(cs[k]); }
                     else co[k] = 0u;
                 }
             }
@@ -261,6 +270,67 @@ tree_build_kernel(spec_cfg c, const int32_t* __restrict__ lat_tok,
     if (lane == 0) out.n_nodes[b] = count;
 }
 
+// A node budget shared by the batch (digest, technical novelty: batching
+// shares one node budget across requests).  Each request's tree was built
+// best-first up to N drafts; the batch keeps the `budget` drafts first in the
+// order (score desc, request asc, index asc), which is the best-first order
+// over all frontiers together, and every request keeps a prefix of its own
+// insertion order.  A draft's place in that order is its index within its
+// request plus, for every other request, the count of that request's drafts
+// that precede it (a binary search: a request's scores never increase along
+// its insertion order).  One CTA; rows past a request's kept drafts become
+// padding rows.
+__global__ void __launch_bounds__(1024)
+budget_select(spec_cfg c, spec_tree t, int budget) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int B = c.B, T = c.N + 1, N = c.N;
+    float* s_sc = reinterpret_cast<float*>(smem);               // [B][T] scores
+    int* s_n = reinterpret_cast<int*>(s_sc + (size_t)B * T);    // [B] rows built
+    int* s_keep = s_n + B;                                      // [B] drafts kept
+    pdl_wait();                  // the trees come from the launch just before
+    pdl_trigger();
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+        int n = t.n_nodes[b];
+        s_n[b] = n < 1 ? 1 : (n > T ? T : n);
+        s_keep[b] = 0;
+    }
+    for (int i = threadIdx.x; i < B * T; i += blockDim.x) s_sc[i] = t.node_score[i];
+    __syncthreads();
+    for (int cand = threadIdx.x; cand < B * N; cand += blockDim.x) {
+        const int b = cand / N, i = 1 + cand % N;
+        if (i >= s_n[b]) continue;
+        const float s = s_sc[b * T + i];
+        int rank = i - 1;
+        for (int b2 = 0; b2 < B && rank < budget; ++b2) {
+            if (b2 == b) continue;
+            // drafts of b2 before this one: score > s, or score == s when b2 < b
+            const float* a = s_sc + b2 * T;
+            int lo = 1, hi = s_n[b2];           // first j in [1, n) not preceding
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                const bool before = a[mid] > s || (a[mid] == s && b2 < b);
+                if (before) lo = mid + 1; else hi = mid;
+            }
+            rank += lo - 1;
+        }
+        if (rank < budget) atomicMax(&s_keep[b], i);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < B * T; i += blockDim.x) {
+        const int b = i / T, x = i % T;
+        if (x > s_keep[b] && x < s_n[b]) {
+            t.node_tok[i] = -1;
+            t.node_parent[i] = -1;
+            t.node_depth[i] = -1;
+            t.node_rank[i] = -1;
+            t.node_score[i] = 0.0f;
+            t.node_anc[2 * (size_t)i] = 0ull;
+            t.node_anc[2 * (size_t)i + 1] = 0ull;
+        }
+    }
+    for (int b = threadIdx.x; b < B; b += blockDim.x) t.n_nodes[b] = 1 + s_keep[b];
+}
+
 }  // namespace
 
 size_t tree_build_smem(const spec_cfg& c) {
@@ -269,14 +339,33 @@ size_t tree_build_smem(const spec_cfg& c) {
 
 cudaError_t launch_tree_build(const spec_cfg& c, const int32_t* lat_tok, const float* lat_score,
                               const int32_t* root_tok, const spec_tree& out, void* ws,
-                              cudaStream_t st, bool pdl) {
+                              cudaStream_t st, bool pdl, const int32_t* m_req) {
     const size_t smem = tree_build_smem(c);
     const int T = c.N + 1;
     if (T <= 32)
-        return launch_k(pdl, tree_build_kernel<1>, dim3(c.B), dim3(32), smem, st, c, lat_tok, lat_score, root_tok, out, ws);
+        return launch_k(pdl, tree_build_kernel<1>, dim3(c.B), dim3(32), smem, st, c, lat_tok,
+                        lat_score, root_tok, out, ws, m_req);
     if (T <= 64)
-        return launch_k(pdl, tree_build_kernel<2>, dim3(c.B), dim3(32), smem, st, c, lat_tok, lat_score, root_tok, out, ws);
-    return launch_k(pdl, tree_build_kernel<4>, dim3(c.B), dim3(32), smem, st, c, lat_tok, lat_score, root_tok, out, ws);
+        return launch_k(pdl, tree_build_kernel<2>, dim3(c.B), dim3(32), smem, st, c, lat_tok,
+                        lat_score, root_tok, out, ws, m_req);
+    return launch_k(pdl, tree_build_kernel<4>, dim3(c.B), dim3(32), smem, st, c, lat_tok,
+                    lat_score, root_tok, out, ws, m_req);
+}
+
+size_t budget_select_smem(const spec_cfg& c) {
+    return sizeof(float) * (size_t)c.B * (c.N + 1) + 2 * sizeof(int) * (size_t)c.B;
+}
+
+cudaError_t launch_budget_select(const spec_cfg& c, const spec_tree& out, int budget,
+                                 cudaStream_t st, bool pdl) {
+    const size_t smem = budget_select_smem(c);
+    if (smem > 200 * 1024) return cudaErrorInvalidConfiguration;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(budget_select,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_k(pdl, budget_select, dim3(1), dim3(1024), smem, st, c, out, budget);
 }
 
 }  // namespace spec

@@ -16,7 +16,7 @@ from .synth import SpecConfig
 def stack_inputs(inp: dict, device="cuda") -> dict:
     """Device copies of synth.make_step_inputs' output with layers stacked."""
     d = {}
-    for k in ("lat_tok", "lat_score", "root_tok", "kv_len", "logits"):
+    for k in ("lat_tok", "lat_score", "root_tok", "kv_len", "logits", "m_req"):
         if k in inp:
             d[k] = inp[k].to(device).contiguous()
     g, a = inp["gdn"], inp["attn"]
@@ -49,8 +49,13 @@ class VerifyStep:
     # the three phases ----------------------------------------------------------
     def build_tree(self, stream=None):
         x = self.x
-        binding.spec_tree_build(self.cfg, x["lat_tok"], x["lat_score"], x["root_tok"], self.tree,
-                                self.ws, stream)
+        if self.scfg.ragged:
+            binding.spec_tree_build_ragged(self.cfg, x["lat_tok"], x["lat_score"], x["root_tok"],
+                                           x.get("m_req"), self.scfg.budget, self.tree, self.ws,
+                                           stream)
+        else:
+            binding.spec_tree_build(self.cfg, x["lat_tok"], x["lat_score"], x["root_tok"],
+                                    self.tree, self.ws, stream)
 
     def verify(self, stream=None):
         x, c = self.x, self.cfg
@@ -86,9 +91,15 @@ class VerifyStep:
         step = dict(gdn_q=x["gdn_q"], gdn_o=self.gdn_o if self.cfg.n_gdn_layers else None,
                     gdn_c=None, attn_q=x["attn_q"],
                     attn_o=self.attn_o if self.cfg.n_attn_layers else None)
-        binding.spec_verify_step(self.cfg, x["lat_tok"], x["lat_score"], self.tree, step,
-                                 x["logits"], self.commit_io(), self.acc, self.ws, stream)
+        if self.scfg.ragged:
+            binding.spec_verify_step_ragged(self.cfg, x["lat_tok"], x["lat_score"], x.get("m_req"),
+                                            self.scfg.budget, self.tree, step, x["logits"],
+                                            self.commit_io(), self.acc, self.ws, stream)
+        else:
+            binding.spec_verify_step(self.cfg, x["lat_tok"], x["lat_score"], self.tree, step,
+                                     x["logits"], self.commit_io(), self.acc, self.ws, stream)
 
     @property
     def launches_per_step(self) -> int:
-        return binding.spec_step_launches(self.cfg)
+        # the shared budget adds one launch (the selection) to the step
+        return binding.spec_step_launches(self.cfg) + (1 if self.scfg.budget >= 0 else 0)

@@ -17,6 +17,9 @@ hybrid Gated-DeltaNet / attention target, a 151936-token vocabulary):
   long      1 request, 16x16 lattice, N=64, KV 16384, plant p=0.9
   batched   24 requests of 'single', KV length per request ~ U[1024, 8192]
   stack     8 requests of 'single', 48 GDN + 16 attention layers, KV 8192
+  ragged    24 requests, 16x16 lattices of which request b drafts from 16, 12
+            or 8 positions (cycled), a 192-node budget shared by the batch,
+            N = 24 per request, KV as 'batched'
 
 Value recipe: lattice scores are log-softmax over the K candidate logits
 ~ N(0, 2^2) of each position; candidate tokens are drawn uniformly without
@@ -63,6 +66,17 @@ class SpecConfig:
     io: str = "bf16"  # "bf16" or "f32"
     L_lo: Optional[int] = None   # per-request KV length ~ U[L_lo, L] when set
     headroom: int = 64           # cache rows beyond the longest KV length
+    m_cycle: Optional[tuple] = None   # draft positions per request, cycled over b
+    budget: int = -1             # draft nodes shared by the batch (< 0: none)
+
+    @property
+    def ragged(self) -> bool:
+        return self.m_cycle is not None or self.budget >= 0
+
+    def m_req(self) -> torch.Tensor:
+        """int32 [B]: lattice positions request b drafts from."""
+        cyc = self.m_cycle or (self.m,)
+        return torch.tensor([cyc[b % len(cyc)] for b in range(self.B)], dtype=torch.int32)
 
     @property
     def T(self) -> int:
@@ -90,6 +104,9 @@ CONFIGS = {
     3: SpecConfig("batched", B=24, m=8, K=16, N=24, L=8192, L_lo=1024, p_plant=0.85, **_BIG),
     4: SpecConfig("stack", B=8, m=8, K=16, N=24, L=8192, p_plant=0.85, n_gdn=48, n_attn=16,
                   **_BIG),
+    # batch sharing a 192-node budget, 16/12/8 draft positions per request
+    5: SpecConfig("ragged", B=24, m=16, K=16, N=24, L=8192, L_lo=1024, p_plant=0.85,
+                  m_cycle=(16, 12, 8), budget=192, **_BIG),
 }
 
 
@@ -253,6 +270,8 @@ def make_step_inputs(cfg: SpecConfig, seed: int, device="cpu", logits=True) -> d
     attn = [make_attn_layer(cfg, g) for _ in range(cfg.n_attn)]
     out = dict(cfg=cfg, seed=seed, lat_tok=lat_tok, lat_score=lat_score, root_tok=root,
                kv_len=kv_len, gdn=gdn, attn=attn)
+    if cfg.ragged:
+        out["m_req"] = cfg.m_req()
     if logits:
         out["logits"] = make_logits(cfg, g)
     out["plant_gen"] = g

@@ -42,7 +42,11 @@ def prepare(scfg: synth.SpecConfig, seed: int, kv_len=None, lat_edit=None):
         inp["kv_len"] = torch.as_tensor(kv_len, dtype=torch.int32).reshape(scfg.B)
     if lat_edit is not None:
         lat_edit(inp)
-    tree = oracle.tree_build(inp["lat_tok"], inp["lat_score"], inp["root_tok"], scfg.N)
+    if scfg.ragged:
+        tree = oracle.tree_build_ragged(inp["lat_tok"], inp["lat_score"], inp["root_tok"], scfg.N,
+                                        inp["m_req"], scfg.budget)
+    else:
+        tree = oracle.tree_build(inp["lat_tok"], inp["lat_score"], inp["root_tok"], scfg.N)
     synth.plant_logits(inp["logits"], inp["lat_tok"], inp["lat_score"], tree["node_depth"],
                        tree["n_nodes"], scfg.p_plant, inp["plant_gen"])
     return inp, tree

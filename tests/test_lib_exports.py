@@ -65,6 +65,17 @@ def test_step_launch_count_is_host_only(lib):
     assert lib.spec_step_launches(ctypes.byref(bad)) == -1
 
 
+def test_shared_budget_beyond_one_cta_is_unsupported(lib):
+    """The budget step holds every score of the batch in one CTA's shared
+    memory; larger batches are refused on the host before any launch."""
+    cfg = binding.make_cfg(synth.config(1), B=2000, N=127)
+    rc = lib.spec_tree_build_ragged(ctypes.byref(cfg), ctypes.c_void_p(16), ctypes.c_void_p(16),
+                                    ctypes.c_void_p(16), None, 100,
+                                    ctypes.byref(binding.SpecTree(*([16] * 7))),
+                                    ctypes.c_void_p(16), None)
+    assert rc == binding.ST_EUNSUPPORTED
+
+
 @pytest.mark.parametrize("field,value", [("K", 33), ("N", 128), ("m", 0), ("Hv", 20),
                                          ("Hq", 30), ("D", 256), ("io_dtype", 7)])
 def test_validation_rejects_before_launch(lib, field, value):
