@@ -39,10 +39,11 @@ FALLBACK_HBM_GBS = 6800.0
 
 # ----------------------------------------------------------------- bytes model
 
-def algorithmic_bytes(s: synth.SpecConfig, mean_L: float, tau: float) -> dict:
-    """Bytes each phase must move at least once (fp32 state, io-typed rows)."""
+def algorithmic_bytes(s: synth.SpecConfig, mean_L: float, tau: float, rows=None) -> dict:
+    """Bytes each phase must move at least once (fp32 state, io-typed rows).
+    rows: mean tree rows a request keeps (T unless a shared budget trims it)."""
     e = 2 if s.io == "bf16" else 4
-    T = s.T
+    T = s.T if rows is None else rows
     gdn_state = s.Hv * s.dk * s.dv * 4
     gdn_rows = T * (2 * s.Hk * s.dk * e + s.Hv * s.dv * e + 2 * s.Hv * 4 + s.Hv * s.dv * e)
     attn_kv = mean_L * s.Hkv * s.D * e * 2
@@ -235,10 +236,18 @@ def whole_job(nodes_local: float, ms_local: float, world: int):
 
 # ----------------------------------------------------------------- CPU oracle timing
 
+def oracle_tree(scfg, inp):
+    import oracle
+    if scfg.ragged:
+        return oracle.tree_build_ragged(inp["lat_tok"], inp["lat_score"], inp["root_tok"], scfg.N,
+                                        inp["m_req"], scfg.budget)
+    return oracle.tree_build(inp["lat_tok"], inp["lat_score"], inp["root_tok"], scfg.N)
+
+
 def oracle_step(scfg, inp):
     """One whole verify step of the CPU oracle."""
     import oracle
-    tree = oracle.tree_build(inp["lat_tok"], inp["lat_score"], inp["root_tok"], scfg.N)
+    tree = oracle_tree(scfg, inp)
     for lay in inp["gdn"]:
         oracle.gdn_tree(tree, lay["h0"], lay["q"], lay["k"], lay["v"], lay["alpha"], lay["beta"])
     for lay in inp["attn"]:
@@ -257,7 +266,7 @@ def oracle_step(scfg, inp):
 def planted_inputs_cpu(scfg, seed):
     import oracle
     inp = synth.make_step_inputs(scfg, seed)
-    tree = oracle.tree_build(inp["lat_tok"], inp["lat_score"], inp["root_tok"], scfg.N)
+    tree = oracle_tree(scfg, inp)
     synth.plant_logits(inp["logits"], inp["lat_tok"], inp["lat_score"], tree["node_depth"],
                        tree["n_nodes"], scfg.p_plant, inp["plant_gen"])
     return inp
@@ -326,7 +335,7 @@ def oracle_step_parts(scfg, inp, j, g):
     grp, G = scfg.Hv // scfg.Hk, scfg.Hq // scfg.Hkv
     i = j // grp
     t0 = time.perf_counter()
-    tree = oracle.tree_build(inp["lat_tok"], inp["lat_score"], inp["root_tok"], scfg.N)
+    tree = oracle_tree(scfg, inp)
     am, _ = oracle.argmax(inp["logits"])
     acc = oracle.accept(tree, am, scfg.m)
     t1 = time.perf_counter()
@@ -423,6 +432,9 @@ def run_ours(args, rank, world, local):
     per_ms = [a.elapsed_time(b) for a, b in ev]
     ms_step = sum(per_ms) / len(per_ms)
     taus = st.acc.accept_len.float().mean().item()
+    kept = st.tree.n_nodes.float()                       # rows each request keeps
+    drafts_per_step = int((kept - 1).sum().item())
+    mean_rows = float(kept.mean().item())
     mean_L = float(kv0.float().mean().item())
 
     # ---- phase breakdown: each phase captured as its own graph, timed with
@@ -468,7 +480,7 @@ def run_ours(args, rank, world, local):
     # ---- end to end through the public API with host buffers ----------------------
     host_in = {k: x[k].cpu().pin_memory() for k in
                ("lat_tok", "lat_score", "gdn_q", "gdn_k", "gdn_v", "gdn_alpha", "gdn_beta",
-                "attn_q", "k_tree", "v_tree", "logits")}
+                "attn_q", "k_tree", "v_tree", "logits", "m_req") if x.get(k) is not None}
     host_out = {k: torch.empty_like(getattr(st.acc, k), device="cpu").pin_memory()
                 for k in ("accept_len", "out_tok")}
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
@@ -490,8 +502,8 @@ def run_ours(args, rank, world, local):
             e2e_ms.append(a.elapsed_time(b))
     e2e_ms_step = max_over_ranks(sum(e2e_ms) / len(e2e_ms), world)
 
-    nodes_total, ms_step_max, value = whole_job(scfg.B * scfg.N, ms_step, world)
-    byts = algorithmic_bytes(scfg, mean_L, taus)
+    nodes_total, ms_step_max, value = whole_job(drafts_per_step, ms_step, world)
+    byts = algorithmic_bytes(scfg, mean_L, taus, rows=mean_rows if scfg.ragged else None)
     peak, peak_kind = hbm_peak()
     attn_us = ph_us["attn"] / max(scfg.n_attn, 1)
     gdn_us = ph_us["gdn"] / max(scfg.n_gdn, 1)
@@ -506,7 +518,10 @@ def run_ours(args, rank, world, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if scfg.io == "bf16" else "f32",
         "data": "synthetic (seeded; shapes and value distributions of the paper's workloads)",
         "config": {"workload": f"{scfg.name}: B={scfg.B} lattice {scfg.m}x{scfg.K} N={scfg.N} "
-                               f"GDN {scfg.n_gdn}x({scfg.Hk}qk/{scfg.Hv}v heads {scfg.dk}x{scfg.dv}) "
+                               + (f"positions/request {'/'.join(map(str, scfg.m_cycle))} "
+                                  f"shared budget {scfg.budget} drafts "
+                                  if scfg.ragged else "")
+                               + f"GDN {scfg.n_gdn}x({scfg.Hk}qk/{scfg.Hv}v heads {scfg.dk}x{scfg.dv}) "
                                f"attn {scfg.n_attn}x({scfg.Hq}q/{scfg.Hkv}kv heads D={scfg.D}) "
                                f"KV={scfg.L} V={scfg.V}",
                    "l2": "flushed before every timed step (2 x L2 write)",
