@@ -60,7 +60,8 @@ def _load():
         if _lib is None:
             path = build()
             lib = ctypes.CDLL(path)
-            for name in ("orc_tree_build", "orc_tree_build_ragged", "orc_gdn_tree",
+            for name in ("orc_tree_build", "orc_tree_build_ragged", "orc_tree_build_markov",
+                         "orc_markov_edges", "orc_exp32_log32", "orc_gdn_tree",
                          "orc_attn_tree", "orc_argmax", "orc_accept", "orc_commit_gdn",
                          "orc_commit_kv"):
                 getattr(lib, name).restype = ctypes.c_int
@@ -163,6 +164,59 @@ def tree_build_ragged(lat_tok, lat_score, root_tok, N: int, m_req, budget: int) 
         _p(out["node_parent"]), _p(out["node_depth"]), _p(out["node_rank"]),
         _p(out["node_score"]), _p(out["node_anc"]), _p(out["n_nodes"]))
     _check(rc, "tree_build_ragged")
+    return out
+
+
+def exp32_log32(x, z):
+    """The fp32 exp (x <= 0) and log (z >= 1) that fix the Markov edge scores to
+    the bit (Cody-Waite reduction + Taylor polynomial; exponent split + atanh
+    series).  Returns (exp32(x), log32(z)) as float32 arrays."""
+    xa = np.ascontiguousarray(x, np.float32).reshape(-1)
+    za = np.ascontiguousarray(z, np.float32).reshape(-1)
+    assert xa.size == za.size
+    ex = np.empty_like(xa)
+    lz = np.empty_like(za)
+    _check(_load().orc_exp32_log32(xa.size, _p(xa), _p(ex), _p(za), _p(lz)), "exp32_log32")
+    return ex, lz
+
+
+def markov_edges(x: int, tok, base, W1, W2) -> np.ndarray:
+    """Edge scores of one lattice position's K candidates under a parent with
+    token x: l = base + <W1[x], W2[y]>, minus their log-sum-exp (fp32, fixed
+    order).  Digest section: prerequisites / parallel drafter (DSpark's Markov
+    head l_s(y) = bases(y) + <W1[x_{s-1}], W2[y]>) and technical novelty (edges
+    scored log p(child | parent))."""
+    t = _np(tok, np.int32).reshape(-1)
+    bs = _np(base, np.float32).reshape(-1)
+    w1 = _np(W1, np.float32)
+    w2 = _np(W2, np.float32)
+    out = np.empty(t.size, np.float32)
+    _check(_load().orc_markov_edges(t.size, w1.shape[1], int(x), _p(t), _p(bs), _p(w1), _p(w2),
+                                    _p(out)), "markov_edges")
+    return out
+
+
+def tree_build_markov(lat_tok, lat_base, W1, W2, root_tok, N: int) -> dict:
+    """Best-first draft tree with parent-dependent (Markov-head) edge scores:
+    node n's children are ranked by markov_edges(token of n, its position).
+    Outputs as tree_build."""
+    tok = _np(lat_tok, np.int32)
+    bs = _np(lat_base, np.float32)
+    w1 = _np(W1, np.float32)
+    w2 = _np(W2, np.float32)
+    root = _np(root_tok, np.int32).reshape(-1)
+    B, m, K = tok.shape
+    T = N + 1
+    out = dict(
+        node_tok=np.empty((B, T), np.int32), node_parent=np.empty((B, T), np.int32),
+        node_depth=np.empty((B, T), np.int32), node_rank=np.empty((B, T), np.int32),
+        node_score=np.empty((B, T), np.float32),
+        node_anc=np.empty((B, T, ANC_WORDS), np.uint64), n_nodes=np.empty((B,), np.int32))
+    rc = _load().orc_tree_build_markov(
+        B, m, K, N, w1.shape[1], _p(tok), _p(bs), _p(w1), _p(w2), _p(root), _p(out["node_tok"]),
+        _p(out["node_parent"]), _p(out["node_depth"]), _p(out["node_rank"]),
+        _p(out["node_score"]), _p(out["node_anc"]), _p(out["n_nodes"]))
+    _check(rc, "tree_build_markov")
     return out
 
 

@@ -26,7 +26,10 @@
  *           node states recomputed along root paths, no per-node snapshots;
  *   [BATCH] technical novelty, batching -- a node budget shared by the batch
  *           (the target GEMM's 192-node plateau) and the number of draft
- *           positions chosen per request (16/12/8).
+ *           positions chosen per request (16/12/8);
+ *   [MARK]  prerequisites / parallel drafter -- DSpark's Markov head conditions
+ *           each position on the previous token:
+ *           l_s(y) = bases(y) + <W1[x_{s-1}], W2[y]>.
  *
  * Precision: every floating-point result is accumulated in double from the
  * exact values of the (bf16 or fp32) inputs.  The one exception is the tree
@@ -44,6 +47,14 @@
  *   R8  Attention scale 1/sqrt(D); q-head h reads kv-head h / (Hq / Hkv).
  *   R9  Commit: the state after the last accepted node becomes the committed
  *       state; the tree K/V rows of the accepted path are appended.
+ *   R14 Markov edges: a child y of a parent with token x at lattice position d
+ *       has l = base_d(y) + <W1[x], W2[y]> (fp32: the dot product as a chain
+ *       of fused multiply-adds in index order, then one add) and edge score
+ *       l - LSE, the log-sum-exp over the position's K candidates under the
+ *       same parent (fp32: M = max l, Z = sum in index order of exp32(l - M),
+ *       LSE = M + log32(Z)).  exp32 and log32 are the fp32 functions defined
+ *       below, so the scores are fixed to the bit.  Children of a parent are
+ *       ranked by (edge desc, candidate index asc).
  *   R12 Shared budget: request b drafts from its first m_b lattice positions;
  *       the batch's draft nodes are inserted best-first over the frontiers of
  *       all requests together (key: score desc, then request index asc, then
@@ -72,6 +83,8 @@
 #include <string.h>
 
 #define ORC_ANC_WORDS 2   /* trees hold at most 128 rows */
+#define ORC_LN2 0.69314718055994530941723212145818   /* ln 2 */
+#define ORC_SQRT2 1.4142135623730950488016887242097  /* sqrt 2 */
 #define ORC_MAX_ROWS 128
 
 /* ---- element access ---------------------------------------------------- */
@@ -317,6 +330,187 @@ int orc_tree_build_ragged(int B, int m, int K, int N, const int32_t *m_req, int 
     free(order);
     free(front);
     free(front_req);
+    return rc;
+}
+
+/* ---- R14: Markov-head edge scores [MARK][NOV] ----------------------------
+ *
+ * exp32(x), x <= 0: Cody-Waite reduction x = n ln2 + r with ln2 split into a
+ * 9-bit head 355/512 and the fp32 rounding of the rest, n = rint(x / ln2) (the
+ * product with fp32(1/ln2) rounded to fp32), e^r by its Taylor polynomial to
+ * degree 7 (Horner, fused multiply-adds, coefficients fp32(1/k!)), times 2^n;
+ * x < -86 gives 0.
+ * log32(z), z >= 1: z = f 2^e with f in [1, 2), halved (e + 1) when f > fp32
+ * (sqrt 2); log f = 2 atanh(s), s = (f - 1) / (f + 1), by the odd series to
+ * s^13 (Horner in s^2, coefficients fp32(1/k)); log z = e ln2 + log f.
+ */
+static float orc_exp32(float x)
+{
+    if (x < -86.0f) return 0.0f;
+    const float inv_ln2 = (float)(1.0 / ORC_LN2);
+    const float ln2_hi = 355.0f / 512.0f;
+    const float ln2_lo = (float)(ORC_LN2 - 355.0 / 512.0);
+    const float n = rintf(x * inv_ln2);
+    float r = fmaf(-n, ln2_hi, x);
+    r = fmaf(-n, ln2_lo, r);
+    float p = (float)(1.0 / 5040.0);
+    p = fmaf(p, r, (float)(1.0 / 720.0));
+    p = fmaf(p, r, (float)(1.0 / 120.0));
+    p = fmaf(p, r, (float)(1.0 / 24.0));
+    p = fmaf(p, r, (float)(1.0 / 6.0));
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    const uint32_t bits = (uint32_t)((int)n + 127) << 23;   /* 2^n, n in [-125, 0] */
+    float scale;
+    memcpy(&scale, &bits, sizeof scale);
+    return p * scale;
+}
+
+static float orc_log32(float z)
+{
+    uint32_t bits;
+    memcpy(&bits, &z, sizeof bits);
+    int e = (int)((bits >> 23) & 0xffu) - 127;
+    const uint32_t fb = (bits & 0x7fffffu) | 0x3f800000u;
+    float f;
+    memcpy(&f, &fb, sizeof f);
+    if (f > (float)ORC_SQRT2) { f = f * 0.5f; e += 1; }
+    const float s = (f - 1.0f) / (f + 1.0f);
+    const float s2 = s * s;
+    float t = (float)(1.0 / 13.0);
+    t = fmaf(t, s2, (float)(1.0 / 11.0));
+    t = fmaf(t, s2, (float)(1.0 / 9.0));
+    t = fmaf(t, s2, (float)(1.0 / 7.0));
+    t = fmaf(t, s2, (float)(1.0 / 5.0));
+    t = fmaf(t, s2, (float)(1.0 / 3.0));
+    t = fmaf(t, s2, 1.0f);
+    const float lf = (2.0f * s) * t;
+    const float ef = (float)e;
+    return fmaf(ef, 355.0f / 512.0f, fmaf(ef, (float)(ORC_LN2 - 355.0 / 512.0), lf));
+}
+
+/* Edge scores of the K candidates (tokens tok[K], bases base[K]) under a
+ * parent with token x (R14); W1, W2 f32 [V][R]. */
+static void orc_markov_edges_row(int K, int R, int x, const int32_t *tok, const float *base,
+                                 const float *W1, const float *W2, float *edge)
+{
+    float M = -INFINITY;
+    for (int i = 0; i < K; ++i) {
+        float dot = 0.0f;
+        for (int k = 0; k < R; ++k)
+            dot = fmaf(W1[(size_t)x * R + k], W2[(size_t)tok[i] * R + k], dot);
+        edge[i] = base[i] + dot;
+        if (edge[i] > M) M = edge[i];
+    }
+    float Z = 0.0f;
+    for (int i = 0; i < K; ++i) Z = Z + orc_exp32(edge[i] - M);
+    const float lse = M + orc_log32(Z);
+    for (int i = 0; i < K; ++i) edge[i] = edge[i] - lse;
+}
+
+/* Exported for the pins: exp32/log32 of n values, and one edge row. */
+int orc_exp32_log32(int n, const float *x, float *ex, const float *z, float *lz)
+{
+    for (int i = 0; i < n; ++i) { ex[i] = orc_exp32(x[i]); lz[i] = orc_log32(z[i]); }
+    return 0;
+}
+
+int orc_markov_edges(int K, int R, int x, const int32_t *tok, const float *base,
+                     const float *W1, const float *W2, float *edge)
+{
+    if (K < 1 || R < 0) return -1;
+    orc_markov_edges_row(K, R, x, tok, base, W1, W2, edge);
+    return 0;
+}
+
+/*
+ * orc_tree_build_markov: best-first draft tree whose edge scores depend on the
+ * parent's token [MARK][TREE][NOV], reading R14.
+ *
+ * lat_tok int32 [B][m][K], lat_base f32 [B][m][K] (the drafter's base logits),
+ * W1, W2 f32 [V][R].  When node n (token x, depth d < m) is inserted, its
+ * children are the K candidates of lattice position d with edge scores
+ * R14(x, d), ranked by (edge desc, index asc); the child of rank r has key
+ * fl32(score_n + edge).  Frontier order, padding rows and return codes as
+ * orc_tree_build.
+ */
+int orc_tree_build_markov(int B, int m, int K, int N, int R, const int32_t *lat_tok,
+                          const float *lat_base, const float *W1, const float *W2,
+                          const int32_t *root_tok,
+                          int32_t *node_tok, int32_t *node_parent, int32_t *node_depth,
+                          int32_t *node_rank, float *node_score, uint64_t *node_anc,
+                          int32_t *n_nodes)
+{
+    if (B < 0 || m < 1 || K < 1 || N < 0 || N + 1 > ORC_MAX_ROWS || R < 0) return -1;
+    const int T = N + 1;
+    float *cedge = (float *)malloc(sizeof(float) * (size_t)T * K);   /* [T][K] by rank */
+    int *cidx = (int *)malloc(sizeof(int) * (size_t)T * K);          /* [T][K] by rank */
+    float *row = (float *)malloc(sizeof(float) * (size_t)K);
+    orc_cand *front = (orc_cand *)malloc(sizeof(orc_cand) * (size_t)(T * K + K));
+    if (!cedge || !cidx || !row || !front) {
+        free(cedge); free(cidx); free(row); free(front);
+        return -3;
+    }
+    int rc = 0;
+    for (int b = 0; b < B && rc == 0; ++b) {
+        const int32_t *tok = lat_tok + (size_t)b * m * K;
+        const float *base = lat_base + (size_t)b * m * K;
+        for (int s = 0; s < m; ++s)
+            for (int i = 0; i < K; ++i)
+                for (int j = i + 1; j < K; ++j)
+                    if (tok[s * K + i] == tok[s * K + j]) rc = -2;
+        if (rc) break;
+        int32_t *ntok = node_tok + (size_t)b * T, *npar = node_parent + (size_t)b * T;
+        int32_t *ndep = node_depth + (size_t)b * T, *nrank = node_rank + (size_t)b * T;
+        float *nsc = node_score + (size_t)b * T;
+        uint64_t *nanc = node_anc + (size_t)b * T * ORC_ANC_WORDS;
+        for (int n = 0; n < T; ++n) {
+            ntok[n] = -1; npar[n] = -1; ndep[n] = -1; nrank[n] = -1; nsc[n] = 0.0f;
+            for (int w = 0; w < ORC_ANC_WORDS; ++w) nanc[n * ORC_ANC_WORDS + w] = 0;
+        }
+        ntok[0] = root_tok[b]; ndep[0] = 0; nanc[0] = 1ull;
+        int count = 1, nfront = 0;
+        /* the children of node n, ranked: edges R14(token of n, its depth) */
+        #define ORC_OFFER(n_)                                                              \
+            do {                                                                           \
+                const int d_ = ndep[n_];                                                   \
+                orc_markov_edges_row(K, R, ntok[n_], tok + d_ * K, base + d_ * K, W1, W2, row); \
+                int *o_ = cidx + (size_t)(n_) * K;                                         \
+                for (int i_ = 0; i_ < K; ++i_) {                                           \
+                    int j_ = i_;                                                           \
+                    while (j_ > 0 && row[i_] > row[o_[j_ - 1]]) { o_[j_] = o_[j_ - 1]; --j_; } \
+                    o_[j_] = i_;                                                           \
+                }                                                                          \
+                for (int r_ = 0; r_ < K; ++r_) {                                           \
+                    cedge[(size_t)(n_) * K + r_] = row[o_[r_]];                            \
+                    orc_cand c_ = { n_, r_, d_ + 1, nsc[n_] + row[o_[r_]] };               \
+                    front[nfront++] = c_;                                                  \
+                }                                                                          \
+            } while (0)
+        ORC_OFFER(0);
+        while (count < T && nfront > 0) {
+            int best = 0;
+            for (int i = 1; i < nfront; ++i)
+                if (orc_cand_before(&front[i], &front[best])) best = i;
+            orc_cand c = front[best];
+            front[best] = front[--nfront];
+            const int n = count++;
+            const int s = c.depth - 1;
+            ntok[n] = tok[s * K + cidx[(size_t)c.parent * K + c.rank]];
+            npar[n] = c.parent;
+            ndep[n] = c.depth;
+            nrank[n] = c.rank;
+            nsc[n] = c.score;
+            for (int w = 0; w < ORC_ANC_WORDS; ++w)
+                nanc[n * ORC_ANC_WORDS + w] = nanc[c.parent * ORC_ANC_WORDS + w];
+            nanc[n * ORC_ANC_WORDS + n / 64] |= 1ull << (n % 64);
+            if (c.depth < m) ORC_OFFER(n);
+        }
+        #undef ORC_OFFER
+        n_nodes[b] = count;
+    }
+    free(cedge); free(cidx); free(row); free(front);
     return rc;
 }
 

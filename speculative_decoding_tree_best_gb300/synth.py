@@ -175,6 +175,18 @@ def make_attn_layer(cfg: SpecConfig, gen: torch.Generator, device="cpu", batch=N
     return dict(q=q, k_tree=k_tree, v_tree=v_tree, k_cache=k_cache, v_cache=v_cache)
 
 
+def make_markov(cfg: SpecConfig, gen: torch.Generator, R: int = 32):
+    """Inputs of a drafter with a Markov head: per-candidate base logits
+    ~ N(0, 2^2) [B][m][K] (the logits whose log-softmax is the plain lattice's
+    score) and the two embedding tables W1, W2 [V][R] ~ N(0, R^-1/2), so the
+    Markov term <W1[x], W2[y]> has unit variance."""
+    base = (torch.randn((cfg.B, cfg.m, cfg.K), generator=gen) * 2.0).float().contiguous()
+    sd = R ** -0.25
+    W1 = (torch.randn((cfg.V, R), generator=gen) * sd).float().contiguous()
+    W2 = (torch.randn((cfg.V, R), generator=gen) * sd).float().contiguous()
+    return base, W1, W2
+
+
 def make_kv_len(cfg: SpecConfig, gen: torch.Generator) -> torch.Tensor:
     if cfg.L_lo is None:
         return torch.full((cfg.B,), cfg.L, dtype=torch.int32)

@@ -124,6 +124,69 @@ def brute_force_ragged(tok, sc, root, N, m_req, budget):
     return out
 
 
+def brute_force_markov(tok, base, W1, W2, root, N, edges):
+    """Best-first tree with parent-dependent edges, by brute force: every root
+    path (a sequence of ranks, each rank taken among the children of the path's
+    last node under that node's token), sorted by the recursive total order.
+    edges(x, d) -> fp32 edge scores of position d's candidates under token x.
+    tok int [m][K], base f32 [m][K]."""
+    m, K = tok.shape
+    paths = {}
+
+    def children(x, d):
+        e = edges(x, d)
+        order = sorted(range(K), key=lambda i: (-float(e[i]), i))
+        return [(int(tok[d][i]), np.float32(e[i])) for i in order]
+
+    def walk(prefix, x, score):
+        d = len(prefix)
+        if d == m:
+            return
+        for r, (t, e) in enumerate(children(x, d)):
+            s = np.float32(score + e)
+            p = prefix + (r,)
+            paths[p] = (s, t)
+            walk(p, t, s)
+
+    walk((), int(root), np.float32(0.0))
+
+    def cmp(a, b):
+        if a == b:
+            return 0
+        sa, sb = paths[a][0], paths[b][0]
+        if sa != sb:
+            return -1 if sa > sb else 1
+        if len(a) != len(b):
+            return -1 if len(a) < len(b) else 1
+        if a[:-1] != b[:-1]:
+            return cmp(a[:-1], b[:-1])
+        return -1 if a[-1] < b[-1] else 1
+
+    ordered = sorted(paths, key=functools.cmp_to_key(cmp))[:N]
+    index = {(): 0}
+    for i, p in enumerate(ordered):
+        index[p] = i + 1
+    T = N + 1
+    out = dict(node_tok=np.full(T, -1, np.int32), node_parent=np.full(T, -1, np.int32),
+               node_depth=np.full(T, -1, np.int32), node_rank=np.full(T, -1, np.int32),
+               node_score=np.zeros(T, np.float32), node_anc=np.zeros((T, 2), np.uint64))
+    out["node_tok"][0] = root
+    out["node_depth"][0] = 0
+    out["node_anc"][0, 0] = 1
+    for p in ordered:
+        n = index[p]
+        par = index[p[:-1]]
+        out["node_tok"][n] = paths[p][1]
+        out["node_parent"][n] = par
+        out["node_depth"][n] = len(p)
+        out["node_rank"][n] = p[-1]
+        out["node_score"][n] = paths[p][0]
+        out["node_anc"][n] = out["node_anc"][par]
+        out["node_anc"][n, n // 64] |= np.uint64(1) << np.uint64(n % 64)
+    out["n_nodes"] = len(ordered) + 1
+    return out
+
+
 def root_path(parent, n):
     p = []
     while n >= 0:
