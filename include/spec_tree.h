@@ -254,6 +254,35 @@ int spec_tree_build_ragged(const spec_cfg *cfg, const int32_t *lat_tok, const fl
                            const spec_tree *out, void *ws, void *stream);
 
 /*
+ * spec_tree_build_markov -- best-first draft tree whose edge scores depend on
+ * the parent's token (a drafter with a Markov head).
+ * Digest: prerequisites / parallel drafter (DSpark's Markov head:
+ * l_s(y) = bases(y) + <W1[x_{s-1}], W2[y]>) and technical novelty, Figure 6
+ * (edges scored log p(child | parent)).
+ *
+ * Candidate i of lattice position d under a parent with token x scores
+ *   l_i = base_i + W1[x] . W2[y_i]      (fp32: one fused multiply-add chain over
+ *                                        k = 0..R-1, then one add)
+ *   e_i = l_i - (M + log32(sum_i exp32(l_i - M))),  M = max_i l_i
+ * (the sum in index order; exp32 / log32 are fp32 functions fixed by their
+ * algorithm: Cody-Waite reduction by ln 2 split as 355/512 + fp32(ln 2 -
+ * 355/512), rint(x fp32(1/ln 2)), Taylor to degree 7 with coefficients
+ * fp32(1/k!) by fused multiply-adds, times 2^n; exponent split, f halved when
+ * above fp32(sqrt 2), s = (f - 1) / (f + 1), 2 s times the series in s^2 to
+ * s^12 with coefficients fp32(1/k), plus e ln 2 as two fused multiply-adds;
+ * exp32 is 0 below -86).  A parent's children are ranked by (e desc, index
+ * asc); a child's key is fl32(parent key + e); insertion as spec_tree_build.
+ *   lat_tok int32 [B][m][K]; lat_base f32 [B][m][K] the drafter's base logits;
+ *   W1, W2 f32 [V][R] the head's two tables (R <= 1024; NULL allowed when R=0);
+ *   root_tok, out, ws as spec_tree_build.  A NaN edge sets SPEC_DEV_BADLAT.
+ * Shared memory: 14 (1 + (m-1) K) K bytes of tables; more than 200 KB returns
+ * ST_EUNSUPPORTED.
+ */
+int spec_tree_build_markov(const spec_cfg *cfg, const int32_t *lat_tok, const float *lat_base,
+                           const float *W1, const float *W2, int R, const int32_t *root_tok,
+                           const spec_tree *out, void *ws, void *stream);
+
+/*
  * spec_verify_step_ragged -- spec_verify_step with the trees of
  * spec_tree_build_ragged (per-request draft positions, shared node budget);
  * the rest of the step treats the rows a request did not keep as padding rows.

@@ -26,7 +26,7 @@ EXPORTS = ("spec_workspace_bytes", "spec_tree_build", "gdn_tree_verify", "attn_t
            "accept_and_commit", "spec_verify_step", "spec_status_read", "spec_status_clear",
            "spec_status_string", "spec_abi_version", "attn_tree_verify_noalloc",
            "spec_wait_probe", "spec_step_launches", "spec_tree_build_ragged",
-           "spec_verify_step_ragged")
+           "spec_verify_step_ragged", "spec_tree_build_markov")
 
 _lock = threading.Lock()
 _lib = None
@@ -93,6 +93,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                                     ctypes.POINTER(SpecStepIO), vp,
                                                     ctypes.POINTER(SpecCommitIO),
                                                     ctypes.POINTER(SpecAccept), vp, vp]
+            lib.spec_tree_build_markov.argtypes = [cfgp, vp, vp, vp, vp, ctypes.c_int, vp,
+                                                   ctypes.POINTER(SpecTree), vp, vp]
             lib.spec_status_read.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
             lib.spec_status_clear.argtypes = [vp, vp]
             lib.spec_status_string.argtypes = [ctypes.c_int]
@@ -102,7 +104,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
             lib.spec_step_launches.argtypes = [cfgp]
             for n in ("spec_tree_build", "gdn_tree_verify", "attn_tree_verify",
                       "attn_tree_verify_noalloc", "spec_wait_probe", "spec_step_launches",
-                      "spec_tree_build_ragged", "spec_verify_step_ragged",
+                      "spec_tree_build_ragged", "spec_verify_step_ragged", "spec_tree_build_markov",
                       "accept_and_commit", "spec_verify_step", "spec_status_read",
                       "spec_status_clear", "spec_abi_version"):
                 getattr(lib, n).restype = ctypes.c_int
@@ -272,6 +274,16 @@ def spec_tree_build_ragged(cfg, lat_tok, lat_score, root_tok, m_req, node_budget
         _ptr(lat_score, torch.float32, "lat_score"), _ptr(root_tok, torch.int32, "root_tok"),
         _ptr(m_req, torch.int32, "m_req"), int(node_budget), ctypes.byref(tree.c()),
         _ptr(ws, name="ws"), _stream(stream)))
+
+
+def spec_tree_build_markov(cfg, lat_tok, lat_base, W1, W2, root_tok, tree: TreeBuffers, ws,
+                           stream=None):
+    """Best-first tree with Markov-head edge scores (W1, W2: CUDA f32 [V][R])."""
+    _check("spec_tree_build_markov", load().spec_tree_build_markov(
+        ctypes.byref(cfg), _ptr(lat_tok, torch.int32, "lat_tok"),
+        _ptr(lat_base, torch.float32, "lat_base"), _ptr(W1, torch.float32, "W1"),
+        _ptr(W2, torch.float32, "W2"), int(W1.shape[1]), _ptr(root_tok, torch.int32, "root_tok"),
+        ctypes.byref(tree.c()), _ptr(ws, name="ws"), _stream(stream)))
 
 
 def _step_io(cfg, step: dict) -> SpecStepIO:

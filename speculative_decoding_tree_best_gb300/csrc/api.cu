@@ -136,6 +136,19 @@ int spec_tree_build_ragged(const spec_cfg* cfg, const int32_t* lat_tok, const fl
     return cuda_rc(e);
 }
 
+int spec_tree_build_markov(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_base,
+                           const float* W1, const float* W2, int R, const int32_t* root_tok,
+                           const spec_tree* out, void* ws, void* stream) {
+    int rc = check_cfg(cfg);
+    if (rc) return rc;
+    if ((rc = check_tree(out))) return rc;
+    if (!al16(lat_tok) || !al16(lat_base) || !al16(root_tok) || !al16(ws)) return ST_EINVAL;
+    if (R < 0 || R > 1024 || (R > 0 && (!al16(W1) || !al16(W2)))) return ST_EINVAL;
+    if (spec::tree_markov_smem(*cfg) > 200 * 1024) return ST_EUNSUPPORTED;
+    return cuda_rc(spec::launch_tree_markov(*cfg, lat_tok, lat_base, W1, W2, R, root_tok, *out, ws,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"
 
 namespace {

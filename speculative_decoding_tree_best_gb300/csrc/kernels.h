@@ -17,6 +17,13 @@ cudaError_t launch_tree_build(const spec_cfg& c, const int32_t* lat_tok, const f
 cudaError_t launch_budget_select(const spec_cfg& c, const spec_tree& out, int budget,
                                  cudaStream_t st, bool pdl = false);
 size_t budget_select_smem(const spec_cfg& c);
+
+// Markov-head trees (edge scores depend on the parent's token); W1, W2 f32 [V][R].
+// cudaErrorInvalidConfiguration when the edge tables exceed shared memory.
+cudaError_t launch_tree_markov(const spec_cfg& c, const int32_t* lat_tok, const float* lat_base,
+                               const float* W1, const float* W2, int R, const int32_t* root_tok,
+                               const spec_tree& out, void* ws, cudaStream_t st, bool pdl = false);
+size_t tree_markov_smem(const spec_cfg& c);
 size_t tree_build_smem(const spec_cfg& c);
 
 // Returns cudaErrorInvalidConfiguration when the shape needs more shared memory

@@ -181,7 +181,7 @@ def make_markov(cfg: SpecConfig, gen: torch.Generator, R: int = 32):
     score) and the two embedding tables W1, W2 [V][R] ~ N(0, R^-1/2), so the
     Markov term <W1[x], W2[y]> has unit variance."""
     base = (torch.randn((cfg.B, cfg.m, cfg.K), generator=gen) * 2.0).float().contiguous()
-    sd = R ** -0.25
+    sd = R ** -0.25 if R > 0 else 1.0
     W1 = (torch.randn((cfg.V, R), generator=gen) * sd).float().contiguous()
     W2 = (torch.randn((cfg.V, R), generator=gen) * sd).float().contiguous()
     return base, W1, W2
