@@ -238,6 +238,9 @@ def whole_job(nodes_local: float, ms_local: float, world: int):
 
 def oracle_tree(scfg, inp):
     import oracle
+    if scfg.markov_R > 0:
+        return oracle.tree_build_markov(inp["lat_tok"], inp["lat_base"], inp["W1"], inp["W2"],
+                                        inp["root_tok"], scfg.N)
     if scfg.ragged:
         return oracle.tree_build_ragged(inp["lat_tok"], inp["lat_score"], inp["root_tok"], scfg.N,
                                         inp["m_req"], scfg.budget)
@@ -267,8 +270,10 @@ def planted_inputs_cpu(scfg, seed):
     import oracle
     inp = synth.make_step_inputs(scfg, seed)
     tree = oracle_tree(scfg, inp)
+    fc = (synth.first_child_tokens(tree["node_parent"], tree["node_rank"], tree["node_tok"],
+                                   tree["n_nodes"]) if scfg.markov_R > 0 else None)
     synth.plant_logits(inp["logits"], inp["lat_tok"], inp["lat_score"], tree["node_depth"],
-                       tree["n_nodes"], scfg.p_plant, inp["plant_gen"])
+                       tree["n_nodes"], scfg.p_plant, inp["plant_gen"], first_child=fc)
     return inp
 
 
@@ -382,8 +387,10 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     t_np = st.tree.to_numpy()
     logits = inp["logits"].clone()
+    fc = (synth.first_child_tokens(t_np["node_parent"], t_np["node_rank"], t_np["node_tok"],
+                                   t_np["n_nodes"]) if scfg.markov_R > 0 else None)
     synth.plant_logits(logits, inp["lat_tok"], inp["lat_score"], t_np["node_depth"],
-                       t_np["n_nodes"], scfg.p_plant, inp["plant_gen"])
+                       t_np["n_nodes"], scfg.p_plant, inp["plant_gen"], first_child=fc)
     x["logits"].copy_(logits.to(dev))
     kv0, root0 = x["kv_len"].clone(), x["root_tok"].clone()
 
@@ -480,7 +487,8 @@ def run_ours(args, rank, world, local):
     # ---- end to end through the public API with host buffers ----------------------
     host_in = {k: x[k].cpu().pin_memory() for k in
                ("lat_tok", "lat_score", "gdn_q", "gdn_k", "gdn_v", "gdn_alpha", "gdn_beta",
-                "attn_q", "k_tree", "v_tree", "logits", "m_req") if x.get(k) is not None}
+                "attn_q", "k_tree", "v_tree", "logits", "m_req", "lat_base")
+               if x.get(k) is not None}
     host_out = {k: torch.empty_like(getattr(st.acc, k), device="cpu").pin_memory()
                 for k in ("accept_len", "out_tok")}
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
@@ -521,6 +529,7 @@ def run_ours(args, rank, world, local):
                                + (f"positions/request {'/'.join(map(str, scfg.m_cycle))} "
                                   f"shared budget {scfg.budget} drafts "
                                   if scfg.ragged else "")
+                               + (f"Markov head rank {scfg.markov_R} " if scfg.markov_R else "")
                                + f"GDN {scfg.n_gdn}x({scfg.Hk}qk/{scfg.Hv}v heads {scfg.dk}x{scfg.dv}) "
                                f"attn {scfg.n_attn}x({scfg.Hq}q/{scfg.Hkv}kv heads D={scfg.D}) "
                                f"KV={scfg.L} V={scfg.V}",

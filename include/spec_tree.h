@@ -274,8 +274,12 @@ int spec_tree_build_ragged(const spec_cfg *cfg, const int32_t *lat_tok, const fl
  * asc); a child's key is fl32(parent key + e); insertion as spec_tree_build.
  *   lat_tok int32 [B][m][K]; lat_base f32 [B][m][K] the drafter's base logits;
  *   W1, W2 f32 [V][R] the head's two tables (R <= 1024; NULL allowed when R=0);
- *   root_tok, out, ws as spec_tree_build.  A NaN edge sets SPEC_DEV_BADLAT.
- * Shared memory: 14 (1 + (m-1) K) K bytes of tables; more than 200 KB returns
+ *   root_tok, out, ws as spec_tree_build.  A NaN edge, or a token (or root
+ *   token) outside [0, V), sets SPEC_DEV_BADLAT (such a token reads head row 0;
+ *   that request's tree is unspecified).
+ * Shared memory: 16 (1 + (m-1) K) K bytes of table entries plus
+ * 4 (2 m K + 1) (R + 4) of staged head rows (R + 1 when R is not a multiple
+ * of 4) plus 8 m K + 4 of tokens and bases; more than 200 KB returns
  * ST_EUNSUPPORTED.
  */
 int spec_tree_build_markov(const spec_cfg *cfg, const int32_t *lat_tok, const float *lat_base,
@@ -290,6 +294,17 @@ int spec_tree_build_markov(const spec_cfg *cfg, const int32_t *lat_tok, const fl
  */
 int spec_verify_step_ragged(const spec_cfg *cfg, const int32_t *lat_tok, const float *lat_score,
                             const int32_t *m_req, int node_budget, const spec_tree *tree,
+                            const spec_step_io *step, const void *logits,
+                            const spec_commit_io *io, const spec_accept *out, void *ws,
+                            void *stream);
+
+/*
+ * spec_verify_step_markov -- spec_verify_step with the tree of
+ * spec_tree_build_markov (lat_base: the drafter's base logits; W1, W2, R: its
+ * Markov head); the same number of launches as spec_verify_step.
+ */
+int spec_verify_step_markov(const spec_cfg *cfg, const int32_t *lat_tok, const float *lat_base,
+                            const float *W1, const float *W2, int R, const spec_tree *tree,
                             const spec_step_io *step, const void *logits,
                             const spec_commit_io *io, const spec_accept *out, void *ws,
                             void *stream);

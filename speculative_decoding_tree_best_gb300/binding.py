@@ -26,7 +26,7 @@ EXPORTS = ("spec_workspace_bytes", "spec_tree_build", "gdn_tree_verify", "attn_t
            "accept_and_commit", "spec_verify_step", "spec_status_read", "spec_status_clear",
            "spec_status_string", "spec_abi_version", "attn_tree_verify_noalloc",
            "spec_wait_probe", "spec_step_launches", "spec_tree_build_ragged",
-           "spec_verify_step_ragged", "spec_tree_build_markov")
+           "spec_verify_step_ragged", "spec_tree_build_markov", "spec_verify_step_markov")
 
 _lock = threading.Lock()
 _lib = None
@@ -95,6 +95,11 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                                     ctypes.POINTER(SpecAccept), vp, vp]
             lib.spec_tree_build_markov.argtypes = [cfgp, vp, vp, vp, vp, ctypes.c_int, vp,
                                                    ctypes.POINTER(SpecTree), vp, vp]
+            lib.spec_verify_step_markov.argtypes = [cfgp, vp, vp, vp, vp, ctypes.c_int,
+                                                    ctypes.POINTER(SpecTree),
+                                                    ctypes.POINTER(SpecStepIO), vp,
+                                                    ctypes.POINTER(SpecCommitIO),
+                                                    ctypes.POINTER(SpecAccept), vp, vp]
             lib.spec_status_read.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
             lib.spec_status_clear.argtypes = [vp, vp]
             lib.spec_status_string.argtypes = [ctypes.c_int]
@@ -105,6 +110,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
             for n in ("spec_tree_build", "gdn_tree_verify", "attn_tree_verify",
                       "attn_tree_verify_noalloc", "spec_wait_probe", "spec_step_launches",
                       "spec_tree_build_ragged", "spec_verify_step_ragged", "spec_tree_build_markov",
+                      "spec_verify_step_markov",
                       "accept_and_commit", "spec_verify_step", "spec_status_read",
                       "spec_status_clear", "spec_abi_version"):
                 getattr(lib, n).restype = ctypes.c_int
@@ -317,6 +323,19 @@ def spec_verify_step_ragged(cfg, lat_tok, lat_score, m_req, node_budget: int, tr
         int(node_budget), ctypes.byref(tree.c()), ctypes.byref(sio), _ptr(logits, dt, "logits"),
         ctypes.byref(_commit_io(cfg, io)), ctypes.byref(out.c()), _ptr(ws, name="ws"),
         _stream(stream)))
+
+
+def spec_verify_step_markov(cfg, lat_tok, lat_base, W1, W2, tree: TreeBuffers, step: dict, logits,
+                            io: dict, out: AcceptBuffers, ws, stream=None):
+    """spec_verify_step over the tree of spec_tree_build_markov."""
+    dt = _io_dtype(cfg)
+    sio = _step_io(cfg, step)
+    _check("spec_verify_step_markov", load().spec_verify_step_markov(
+        ctypes.byref(cfg), _ptr(lat_tok, torch.int32, "lat_tok"),
+        _ptr(lat_base, torch.float32, "lat_base"), _ptr(W1, torch.float32, "W1"),
+        _ptr(W2, torch.float32, "W2"), int(W1.shape[1]), ctypes.byref(tree.c()),
+        ctypes.byref(sio), _ptr(logits, dt, "logits"), ctypes.byref(_commit_io(cfg, io)),
+        ctypes.byref(out.c()), _ptr(ws, name="ws"), _stream(stream)))
 
 
 def spec_status_read(ws, stream=None) -> int:

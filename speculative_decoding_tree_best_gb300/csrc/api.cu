@@ -144,7 +144,7 @@ int spec_tree_build_markov(const spec_cfg* cfg, const int32_t* lat_tok, const fl
     if ((rc = check_tree(out))) return rc;
     if (!al16(lat_tok) || !al16(lat_base) || !al16(root_tok) || !al16(ws)) return ST_EINVAL;
     if (R < 0 || R > 1024 || (R > 0 && (!al16(W1) || !al16(W2)))) return ST_EINVAL;
-    if (spec::tree_markov_smem(*cfg) > 200 * 1024) return ST_EUNSUPPORTED;
+    if (spec::tree_markov_smem(*cfg, R) > 200 * 1024) return ST_EUNSUPPORTED;
     return cuda_rc(spec::launch_tree_markov(*cfg, lat_tok, lat_base, W1, W2, R, root_tok, *out, ws,
                                             static_cast<cudaStream_t>(stream)));
 }
@@ -153,11 +153,19 @@ int spec_tree_build_markov(const spec_cfg* cfg, const int32_t* lat_tok, const fl
 
 namespace {
 
-// The fused step; m_req / node_budget as in spec_tree_build_ragged.
+// A drafter with a Markov head: lat_score then holds the base logits.
+struct MarkovHead {
+    const float* W1;
+    const float* W2;
+    int R;
+};
+
+// The fused step; m_req / node_budget as in spec_tree_build_ragged, markov as
+// in spec_tree_build_markov (NULL: the plain lattice).
 int verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_score,
-                const int32_t* m_req, int node_budget, const spec_tree* tree,
-                const spec_step_io* step, const void* logits, const spec_commit_io* io,
-                const spec_accept* out, void* ws, void* stream) {
+                const int32_t* m_req, int node_budget, const MarkovHead* markov,
+                const spec_tree* tree, const spec_step_io* step, const void* logits,
+                const spec_commit_io* io, const spec_accept* out, void* ws, void* stream) {
     int rc = check_cfg(cfg);
     if (rc) return rc;
     if ((rc = check_tree(tree))) return rc;
@@ -202,8 +210,14 @@ int verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_sc
     };
     if (m_req && !al16(m_req)) return ST_EINVAL;
     if (node_budget >= 0 && spec::budget_select_smem(c) > 200 * 1024) return ST_EUNSUPPORTED;
-    cudaError_t e = spec::launch_tree_build(c, lat_tok, lat_score, io->root_tok, *tree, ws, st, true,
-                                            m_req);
+    if (markov && (markov->R < 0 || markov->R > 1024 ||
+                   (markov->R > 0 && (!al16(markov->W1) || !al16(markov->W2)))))
+        return ST_EINVAL;
+    if (markov && spec::tree_markov_smem(c, markov->R) > 200 * 1024) return ST_EUNSUPPORTED;
+    cudaError_t e = markov
+        ? spec::launch_tree_markov(c, lat_tok, lat_score, markov->W1, markov->W2, markov->R,
+                                   io->root_tok, *tree, ws, st, true)
+        : spec::launch_tree_build(c, lat_tok, lat_score, io->root_tok, *tree, ws, st, true, m_req);
     // the shared budget trims the trees before anything reads them
     if (e == cudaSuccess && node_budget >= 0)
         e = spec::launch_budget_select(c, *tree, node_budget, st, true);
@@ -256,7 +270,16 @@ int spec_step_launches(const spec_cfg* cfg) {
 int spec_verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_score,
                      const spec_tree* tree, const spec_step_io* step, const void* logits,
                      const spec_commit_io* io, const spec_accept* out, void* ws, void* stream) {
-    return verify_step(cfg, lat_tok, lat_score, nullptr, -1, tree, step, logits, io, out, ws,
+    return verify_step(cfg, lat_tok, lat_score, nullptr, -1, nullptr, tree, step, logits, io, out,
+                       ws, stream);
+}
+
+int spec_verify_step_markov(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_base,
+                            const float* W1, const float* W2, int R, const spec_tree* tree,
+                            const spec_step_io* step, const void* logits, const spec_commit_io* io,
+                            const spec_accept* out, void* ws, void* stream) {
+    const MarkovHead head{W1, W2, R};
+    return verify_step(cfg, lat_tok, lat_base, nullptr, -1, &head, tree, step, logits, io, out, ws,
                        stream);
 }
 
@@ -264,8 +287,8 @@ int spec_verify_step_ragged(const spec_cfg* cfg, const int32_t* lat_tok, const f
                             const int32_t* m_req, int node_budget, const spec_tree* tree,
                             const spec_step_io* step, const void* logits, const spec_commit_io* io,
                             const spec_accept* out, void* ws, void* stream) {
-    return verify_step(cfg, lat_tok, lat_score, m_req, node_budget, tree, step, logits, io, out, ws,
-                       stream);
+    return verify_step(cfg, lat_tok, lat_score, m_req, node_budget, nullptr, tree, step, logits, io,
+                       out, ws, stream);
 }
 
 int spec_status_read(const void* ws, uint32_t* host_status, void* stream) {

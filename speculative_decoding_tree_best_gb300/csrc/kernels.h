@@ -23,7 +23,7 @@ size_t budget_select_smem(const spec_cfg& c);
 cudaError_t launch_tree_markov(const spec_cfg& c, const int32_t* lat_tok, const float* lat_base,
                                const float* W1, const float* W2, int R, const int32_t* root_tok,
                                const spec_tree& out, void* ws, cudaStream_t st, bool pdl = false);
-size_t tree_markov_smem(const spec_cfg& c);
+size_t tree_markov_smem(const spec_cfg& c, int R);
 size_t tree_build_smem(const spec_cfg& c);
 
 // Returns cudaErrorInvalidConfiguration when the shape needs more shared memory

@@ -16,19 +16,22 @@
 // to s^13), every operation an explicitly rounded intrinsic, so the scores are
 // fixed to the bit.  Children of a parent are ranked by (e desc, index asc).
 //
-// One CTA of 256 threads per request.
-//  A. All warps fill the tables.  A table row is (position d, parent): the
+// One CTA per request: 1024 threads (512 when T > 64).
+//  A. All warps stage the rows of W1 and W2 the tables need (every candidate's
+//     and the root's) in shared memory, every load in flight before the
+//     stores, then fill the tables.  A table row is (position d, parent): the
 //     root for d = 0, candidate p of position d-1 otherwise, so row
-//     rho = 0 or 1 + (d-1) K + p.  A group of lanes computes one row: lane i
-//     the dot product and l_i, the group the maximum, lane 0 the ordered sum
-//     and the log-sum-exp, each lane its edge and its rank.  Per entry
-//     (row, rank): edge, token, the row of that child's own children, and
-//     the first (best) edge among them.
+//     rho = 0 or 1 + (d-1) K + p.  A group of 16 or 32 lanes computes one row:
+//     lane i the dot product and l_i, the group the maximum, every lane the
+//     ordered sum (read back from shared memory in index order) and the
+//     log-sum-exp, each lane its edge and its rank.  Per entry (row, rank): edge, token, the row of that
+//     child's own children, and the first (best) edge among them.
 //  B. Warp 0 inserts nodes best-first exactly as tree_build.cu does, row x in
 //     lane x % 32, slot x / 32.  Each row offers its best remaining child; the
 //     offers are compared with two warp-wide max reductions (key, then depth
 //     and parent among equal keys).  The child lookups go through the row's
-//     table row instead of a position's ranked list.
+//     table row instead of a position's ranked list; both entries an insertion
+//     reads are loaded warp-wide before the (predicated) updates.
 #include <math.h>
 
 #include "common.cuh"
@@ -38,7 +41,9 @@ namespace spec {
 
 namespace {
 
-constexpr int kMarkovThreads = 256;
+// Threads per CTA: 1024 while the insertion's per-lane slots fit in 64
+// registers (T <= 64), else 512.
+constexpr int kMarkovThreadsMax = 1024;
 
 __device__ __forceinline__ float exp32(float x) {
     if (x < -86.0f) return 0.0f;
@@ -95,22 +100,121 @@ __device__ __forceinline__ uint32_t tie_rank(int child_depth, int parent) {
     return (static_cast<uint32_t>(255 - child_depth) << 8) | static_cast<uint32_t>(255 - parent);
 }
 
-struct MarkovTables {
-    float* edge;      // [rows][K] edge score by rank
-    int32_t* tok;     // [rows][K] token by rank
-    int16_t* crow;    // [rows][K] table row of that child's children (-1: none)
-    float* first;     // [rows][K] the first edge among that child's children (0: none)
+// One table entry (row, rank): 16 bytes, so that the insertion reads an entry
+// with one shared-memory load.
+struct MEnt {
+    float edge;       // edge score of the rank-th child
+    float first;      // the first (best) edge among that child's children (0: none)
+    int32_t tok;      // its token
+    int32_t crow;     // the table row of its children (-1: none)
 };
 
 __host__ __device__ inline size_t markov_rows(int m, int K) { return 1 + (size_t)(m - 1) * K; }
 
-__host__ __device__ inline size_t markov_smem(int m, int K) {
+// Row stride of the staged head rows in floats: R + 4 when R is a multiple of
+// 4 (16-byte loads; the 8 lanes of a load phase then start 4 banks apart),
+// else R + 1 (the lanes of a group, each reading its own W2 row at the same
+// k, hit distinct banks).
+__host__ __device__ inline int markov_stride(int R) { return (R & 3) == 0 ? R + 4 : R + 1; }
+
+// table entries, the staged head rows (W1 of every candidate and the root, W2
+// of every candidate), then the lattice's tokens (and the root) and bases
+__host__ __device__ inline size_t markov_smem(int m, int K, int R) {
     const size_t e = markov_rows(m, K) * K;
-    return e * (4 + 4 + 4) + ((e * 2 + 15) & ~size_t(15));
+    return sizeof(MEnt) * e + sizeof(float) * (size_t)(2 * m * K + 1) * markov_stride(R) +
+           sizeof(int32_t) * (size_t)(m * K + 1) + sizeof(float) * (size_t)m * K;
 }
 
-template <int SLOTS>
-__global__ void __launch_bounds__(kMarkovThreads)
+// Phase A for lane groups of G lanes (G >= K): fills every table row's entries
+// except `first`.  Returns true when an edge is NaN.
+// xs: 64 floats of scratch per warp (the group's exp terms, then its edges),
+// read back in index order with 16-byte broadcast loads.
+template <int G>
+__device__ __forceinline__ bool markov_fill(const spec_cfg& c, int R, int RP, int nthreads,
+                                            const float* w1s, const float* w2s,
+                                            const int32_t* tok_s, const float* base_s, MEnt* tb,
+                                            float* xs_all) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int m = c.m, K = c.K;
+    const int groups = (nthreads / 32) * (32 / G);
+    const int grp = warp * (32 / G) + lane / G, gl = lane % G;
+    float* xs = xs_all + warp * 64;
+    const int g0 = lane & ~(G - 1);          // the group's first lane
+    const int nrows = (int)markov_rows(m, K);
+    const bool vec = (RP & 3) == 0;
+    bool bad = false;
+    for (int rho0 = 0; rho0 < nrows; rho0 += groups) {
+        const int rho = rho0 + grp;
+        const bool act = rho < nrows && gl < K;
+        // row rho: position d under parent p (the root for rho = 0)
+        const int d = rho == 0 ? 0 : 1 + (rho - 1) / K;
+        const int p = rho == 0 ? 0 : rho - 1 - (d - 1) * K;
+        float l = -INFINITY;
+        int y = 0;
+        if (act) {
+            y = tok_s[d * K + gl];
+            const float* w1 = w1s + (size_t)(rho == 0 ? m * K : (d - 1) * K + p) * RP;
+            const float* w2 = w2s + (size_t)(d * K + gl) * RP;
+            float dot = 0.0f;
+            if (vec) {
+#pragma unroll 4
+                for (int k = 0; k < R; k += 4) {
+                    const float4 a = *reinterpret_cast<const float4*>(w1 + k);
+                    const float4 v = *reinterpret_cast<const float4*>(w2 + k);
+                    dot = __fmaf_rn(a.x, v.x, dot);
+                    dot = __fmaf_rn(a.y, v.y, dot);
+                    dot = __fmaf_rn(a.z, v.z, dot);
+                    dot = __fmaf_rn(a.w, v.w, dot);
+                }
+            } else {
+#pragma unroll 4
+                for (int k = 0; k < R; ++k) dot = __fmaf_rn(w1[k], w2[k], dot);
+            }
+            l = __fadd_rn(base_s[d * K + gl], dot);
+        }
+        float M = l;
+#pragma unroll
+        for (int o = G / 2; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o, G));
+        // lanes past K add +0, which leaves the ordered sum unchanged
+        xs[lane] = act ? exp32(__fsub_rn(l, M)) : 0.0f;
+        __syncwarp();
+        float Z = 0.0f;
+#pragma unroll
+        for (int j = 0; j < G; j += 4) {
+            const float4 q = *reinterpret_cast<const float4*>(xs + g0 + j);
+            Z = __fadd_rn(Z, q.x);
+            Z = __fadd_rn(Z, q.y);
+            Z = __fadd_rn(Z, q.z);
+            Z = __fadd_rn(Z, q.w);
+        }
+        const float e = __fsub_rn(l, __fadd_rn(M, log32(Z)));
+        xs[32 + lane] = e;
+        __syncwarp();
+        // lanes past K hold e = -inf and never outrank an active lane
+        int rank = 0;
+#pragma unroll
+        for (int j = 0; j < G; j += 4) {
+            const float4 q = *reinterpret_cast<const float4*>(xs + 32 + g0 + j);
+            rank += (q.x > e || (q.x == e && j < gl)) ? 1 : 0;
+            rank += (q.y > e || (q.y == e && j + 1 < gl)) ? 1 : 0;
+            rank += (q.z > e || (q.z == e && j + 2 < gl)) ? 1 : 0;
+            rank += (q.w > e || (q.w == e && j + 3 < gl)) ? 1 : 0;
+        }
+        __syncwarp();                        // the next pass rewrites xs
+        if (act) {
+            MEnt& t = tb[(size_t)rho * K + rank];
+            t.edge = e;
+            t.tok = y;
+            // the child's own children: row 1 + d K + (candidate index)
+            t.crow = d + 1 < m ? 1 + d * K + gl : -1;
+        }
+        bad |= act && !(e == e);           // a NaN base or weight
+    }
+    return bad;
+}
+
+template <int SLOTS, int NT>
+__global__ void __launch_bounds__(NT)
 tree_markov_kernel(spec_cfg c, int R, const int32_t* __restrict__ lat_tok,
                    const float* __restrict__ lat_base, const float* __restrict__ W1,
                    const float* __restrict__ W2, const int32_t* __restrict__ root_tok,
@@ -118,66 +222,76 @@ tree_markov_kernel(spec_cfg c, int R, const int32_t* __restrict__ lat_tok,
     extern __shared__ __align__(16) unsigned char smem[];
     const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int m = c.m, K = c.K, T = c.N + 1;
-    const size_t E = markov_rows(m, K) * K;
-    MarkovTables tb;
-    tb.edge = reinterpret_cast<float*>(smem);
-    tb.tok = reinterpret_cast<int32_t*>(tb.edge + E);
-    tb.first = reinterpret_cast<float*>(tb.tok + E);
-    tb.crow = reinterpret_cast<int16_t*>(tb.first + E);
-    const int32_t* tok_b = lat_tok + (size_t)b * m * K;
-    const float* base_b = lat_base + (size_t)b * m * K;
+    const int E = (int)markov_rows(m, K) * K;
+    MEnt* tb = reinterpret_cast<MEnt*>(smem);
+    __shared__ __align__(16) float xs[(NT / 32) * 64];
+    // staged head rows: w1s [m K + 1][RP] (candidate (d, i) at d K + i, the
+    // root last), w2s [m K][RP]
+    const int RP = markov_stride(R);
+    float* w1s = reinterpret_cast<float*>(tb + E);
+    float* w2s = w1s + (size_t)(m * K + 1) * RP;
+    int32_t* tok_s = reinterpret_cast<int32_t*>(w2s + (size_t)m * K * RP);  // [m K] + root
+    float* base_s = reinterpret_cast<float*>(tok_s + m * K + 1);          // [m K]
 
     pdl_wait();          // root_tok may come from the previous step's acceptance
     pdl_trigger();
-    const int root = root_tok[b];
-
-    // ---- A. tables: one row per lane group of G lanes ------------------------------
-    const int G = K <= 16 ? 16 : 32;
-    const int groups = (kMarkovThreads / 32) * (32 / G);
-    const int grp = warp * (32 / G) + lane / G, gl = lane % G;
-    const unsigned gmask = G == 32 ? 0xffffffffu : (0xffffu << (lane & 16));
-    const int nrows = (int)markov_rows(m, K);
     bool bad = false;
-    for (int rho0 = 0; rho0 < nrows; rho0 += groups) {
-        const int rho = rho0 + grp;
-        const bool live = rho < nrows;
-        const int d = rho == 0 ? 0 : 1 + (rho - 1) / K;
-        const int p = rho == 0 ? 0 : (rho - 1) % K;
-        const int x = rho == 0 ? root : (live ? tok_b[(d - 1) * K + p] : 0);
-        const bool act = live && gl < K;
-        const int y = act ? tok_b[d * K + gl] : 0;
-        float l = -INFINITY;
-        if (act) {
-            float dot = 0.0f;
-            const float* w1 = W1 + (size_t)x * R;
-            const float* w2 = W2 + (size_t)y * R;
-            for (int k = 0; k < R; ++k) dot = __fmaf_rn(w1[k], w2[k], dot);
-            l = __fadd_rn(base_b[d * K + gl], dot);
-        }
-        float M = l;
-        for (int o = G / 2; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(gmask, M, o, G));
-        const float ex = act ? exp32(__fsub_rn(l, M)) : 0.0f;
-        float Z = 0.0f;
-        for (int j = 0; j < K; ++j) Z = __fadd_rn(Z, __shfl_sync(gmask, ex, j, G));
-        const float lse = __fadd_rn(M, log32(Z));
-        const float e = __fsub_rn(l, lse);
-        int rank = 0;
-        for (int j = 0; j < K; ++j) {
-            const float ej = __shfl_sync(gmask, e, j, G);
-            rank += (ej > e || (ej == e && j < gl)) ? 1 : 0;
-        }
-        if (act) {
-            tb.edge[(size_t)rho * K + rank] = e;
-            tb.tok[(size_t)rho * K + rank] = y;
-            // the child's own children: row 1 + d K + (candidate index)
-            tb.crow[(size_t)rho * K + rank] = static_cast<int16_t>(d + 1 < m ? 1 + d * K + gl : -1);
-        }
-        bad |= act && !(e == e);           // a NaN base or weight
+    for (int i = tid; i <= m * K; i += NT) {
+        const int t = i < m * K ? lat_tok[(size_t)b * m * K + i] : root_tok[b];
+        tok_s[i] = t;
+        if (i < m * K) base_s[i] = lat_base[(size_t)b * m * K + i];
+        bad |= t < 0 || t >= c.V;          // such a token reads head row 0 below
     }
     __syncthreads();
-    for (size_t i = tid; i < E; i += kMarkovThreads) {
-        const int cr = tb.crow[i];
-        tb.first[i] = cr >= 0 ? tb.edge[(size_t)cr * K] : 0.0f;
+    const int root = tok_s[m * K];
+    // every row of W1 and W2 the tables need: each thread issues up to 4 loads
+    // before it stores any (16 bytes at a time when the rows allow it)
+    {
+        const int nw = 2 * m * K + 1;
+        const bool vec = (R & 3) == 0 &&
+            ((reinterpret_cast<uintptr_t>(W1) | reinterpret_cast<uintptr_t>(W2)) & 15u) == 0;
+        const int per_row = vec ? R >> 2 : R;       // loads per row
+        const int total = nw * per_row;
+        for (int i0 = tid; i0 < total; i0 += 4 * NT) {
+            float4 v[4];
+            float* dst[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * NT;
+                dst[u] = nullptr;
+                if (i < total) {
+                    const int row = i / per_row, k = i - row * per_row;
+                    const bool first = row < m * K + 1;
+                    int t = tok_s[first ? row : row - (m * K + 1)];
+                    t = (t >= 0 && t < c.V) ? t : 0;
+                    const float* src = (first ? W1 : W2) + (size_t)t * R;
+                    dst[u] = (first ? w1s + (size_t)row * RP : w2s + (size_t)(row - (m * K + 1)) * RP);
+                    if (vec) {
+                        v[u] = reinterpret_cast<const float4*>(src)[k];
+                        dst[u] += 4 * k;
+                    } else {
+                        v[u].x = src[k];
+                        dst[u] += k;
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (dst[u] == nullptr) continue;
+                if (vec) *reinterpret_cast<float4*>(dst[u]) = v[u];
+                else *dst[u] = v[u].x;
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- A. tables: one row per lane group ------------------------------------------
+    bad |= K <= 16 ? markov_fill<16>(c, R, RP, NT, w1s, w2s, tok_s, base_s, tb, xs)
+                   : markov_fill<32>(c, R, RP, NT, w1s, w2s, tok_s, base_s, tb, xs);
+    __syncthreads();
+    for (int i = tid; i < E; i += NT) {
+        const int cr = tb[i].crow;
+        tb[i].first = cr >= 0 ? tb[(size_t)cr * K].edge : 0.0f;
     }
     if (__syncthreads_or(bad) && tid == 0) raise_status(ws, SPEC_DEV_BADLAT);
     if (warp != 0) return;
@@ -194,7 +308,7 @@ tree_markov_kernel(spec_cfg c, int R, const int32_t* __restrict__ lat_tok,
     }
     if (lane == 0) {
         nrow[0] = 0; nx[0] = 0; ntk[0] = root; a0[0] = 1ull;
-        cs[0] = __fadd_rn(0.0f, tb.edge[0]);
+        cs[0] = __fadd_rn(0.0f, tb[0].edge);
         co[0] = ord_key(cs[0]);
     }
     int count = 1;
@@ -223,37 +337,29 @@ tree_markov_kernel(spec_cfg c, int R, const int32_t* __restrict__ lat_tok,
         sc = __shfl_sync(0xffffffffu, sc, pl);
         pa0 = __shfl_sync(0xffffffffu, pa0, pl);
         pa1 = __shfl_sync(0xffffffffu, pa1, pl);
-        const size_t ent = (size_t)rw * K + r;                      // the offered child
-        if (lane == pl) {                                           // the parent's next offer
+        // the offered child and the parent's next child: warp-uniform loads, both
+        // in flight before either update
+        const int ent = rw * K + r;
+        const bool more = r + 1 < K;
+        const MEnt ch = tb[ent];
+        const float nxt = tb[more ? ent + 1 : ent].edge;
+        const bool is_par = lane == pl, is_new = lane == (n & 31);
+        const int nk = n >> 5;
 #pragma unroll
-            for (int k = 0; k < SLOTS; ++k)
-                if (k == pk) {
-                    nx[k] = r + 1;
-                    if (r + 1 < K) {
-                        cs[k] = __fadd_rn(ns[k], tb.edge[ent + 1]);
-                        co[k] = ord_key(cs[k]);
-                    } else {
-                        co[k] = 0u;
-                    }
-                }
-        }
-        if (lane == (n & 31)) {                                     // the new row
-            const int nk = n >> 5;
-            const int crow = tb.crow[ent];
-#pragma unroll
-            for (int k = 0; k < SLOTS; ++k)
-                if (k == nk) {
-                    nd[k] = d + 1; nrow[k] = crow; nx[k] = 0; ns[k] = sc; npar[k] = pr; nrk[k] = r;
-                    ntk[k] = tb.tok[ent];
-                    a0[k] = pa0 | (n < 64 ? 1ull << n : 0ull);
-                    a1[k] = pa1 | (n >= 64 ? 1ull << (n - 64) : 0ull);
-                    if (crow >= 0) {
-                        cs[k] = __fadd_rn(sc, tb.first[ent]);
-                        co[k] = ord_key(cs[k]);
-                    } else {
-                        co[k] = 0u;
-                    }
-                }
+        for (int k = 0; k < SLOTS; ++k) {
+            if (is_par && k == pk) {                                // the parent's next offer
+                nx[k] = r + 1;
+                cs[k] = __fadd_rn(ns[k], nxt);
+                co[k] = more ? ord_key(cs[k]) : 0u;
+            }
+            if (is_new && k == nk) {                                // the new row
+                nd[k] = d + 1; nrow[k] = ch.crow; nx[k] = 0; ns[k] = sc; npar[k] = pr; nrk[k] = r;
+                ntk[k] = ch.tok;
+                a0[k] = pa0 | (n < 64 ? 1ull << n : 0ull);
+                a1[k] = pa1 | (n >= 64 ? 1ull << (n - 64) : 0ull);
+                cs[k] = __fadd_rn(sc, ch.first);
+                co[k] = ch.crow >= 0 ? ord_key(cs[k]) : 0u;
+            }
         }
     }
 #pragma unroll
@@ -276,24 +382,24 @@ tree_markov_kernel(spec_cfg c, int R, const int32_t* __restrict__ lat_tok,
 
 }  // namespace
 
-size_t tree_markov_smem(const spec_cfg& c) { return markov_smem(c.m, c.K); }
+size_t tree_markov_smem(const spec_cfg& c, int R) { return markov_smem(c.m, c.K, R); }
 
 cudaError_t launch_tree_markov(const spec_cfg& c, const int32_t* lat_tok, const float* lat_base,
                                const float* W1, const float* W2, int R, const int32_t* root_tok,
                                const spec_tree& out, void* ws, cudaStream_t st, bool pdl) {
-    const size_t smem = tree_markov_smem(c);
+    const size_t smem = tree_markov_smem(c, R);
     if (smem > 200 * 1024) return cudaErrorInvalidConfiguration;
     const int T = c.N + 1;
-    auto go = [&](auto kern) -> cudaError_t {
+    auto go = [&](auto kern, int nt) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
         if (e != cudaSuccess) return e;
-        return launch_k(pdl, kern, dim3(c.B), dim3(kMarkovThreads), smem, st, c, R, lat_tok,
-                        lat_base, W1, W2, root_tok, out, ws);
+        return launch_k(pdl, kern, dim3(c.B), dim3(nt), smem, st, c, R, lat_tok, lat_base, W1, W2,
+                        root_tok, out, ws);
     };
-    if (T <= 32) return go(tree_markov_kernel<1>);
-    if (T <= 64) return go(tree_markov_kernel<2>);
-    return go(tree_markov_kernel<4>);
+    if (T <= 32) return go(tree_markov_kernel<1, kMarkovThreadsMax>, kMarkovThreadsMax);
+    if (T <= 64) return go(tree_markov_kernel<2, kMarkovThreadsMax>, kMarkovThreadsMax);
+    return go(tree_markov_kernel<4, kMarkovThreadsMax / 2>, kMarkovThreadsMax / 2);
 }
 
 }  // namespace spec

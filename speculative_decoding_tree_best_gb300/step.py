@@ -16,7 +16,8 @@ from .synth import SpecConfig
 def stack_inputs(inp: dict, device="cuda") -> dict:
     """Device copies of synth.make_step_inputs' output with layers stacked."""
     d = {}
-    for k in ("lat_tok", "lat_score", "root_tok", "kv_len", "logits", "m_req"):
+    for k in ("lat_tok", "lat_score", "root_tok", "kv_len", "logits", "m_req", "lat_base", "W1",
+              "W2"):
         if k in inp:
             d[k] = inp[k].to(device).contiguous()
     g, a = inp["gdn"], inp["attn"]
@@ -49,7 +50,10 @@ class VerifyStep:
     # the three phases ----------------------------------------------------------
     def build_tree(self, stream=None):
         x = self.x
-        if self.scfg.ragged:
+        if self.scfg.markov_R > 0:
+            binding.spec_tree_build_markov(self.cfg, x["lat_tok"], x["lat_base"], x["W1"], x["W2"],
+                                           x["root_tok"], self.tree, self.ws, stream)
+        elif self.scfg.ragged:
             binding.spec_tree_build_ragged(self.cfg, x["lat_tok"], x["lat_score"], x["root_tok"],
                                            x.get("m_req"), self.scfg.budget, self.tree, self.ws,
                                            stream)
@@ -91,7 +95,11 @@ class VerifyStep:
         step = dict(gdn_q=x["gdn_q"], gdn_o=self.gdn_o if self.cfg.n_gdn_layers else None,
                     gdn_c=None, attn_q=x["attn_q"],
                     attn_o=self.attn_o if self.cfg.n_attn_layers else None)
-        if self.scfg.ragged:
+        if self.scfg.markov_R > 0:
+            binding.spec_verify_step_markov(self.cfg, x["lat_tok"], x["lat_base"], x["W1"], x["W2"],
+                                            self.tree, step, x["logits"], self.commit_io(), self.acc,
+                                            self.ws, stream)
+        elif self.scfg.ragged:
             binding.spec_verify_step_ragged(self.cfg, x["lat_tok"], x["lat_score"], x.get("m_req"),
                                             self.scfg.budget, self.tree, step, x["logits"],
                                             self.commit_io(), self.acc, self.ws, stream)

@@ -20,6 +20,8 @@ hybrid Gated-DeltaNet / attention target, a 151936-token vocabulary):
   ragged    24 requests, 16x16 lattices of which request b drafts from 16, 12
             or 8 positions (cycled), a 192-node budget shared by the batch,
             N = 24 per request, KV as 'batched'
+  markov    'single' with a Markov-head drafter: base logits ~ N(0, 2^2) and
+            two tables W1, W2 [V][32] ~ N(0, 32^-1/2)
 
 Value recipe: lattice scores are log-softmax over the K candidate logits
 ~ N(0, 2^2) of each position; candidate tokens are drawn uniformly without
@@ -68,6 +70,7 @@ class SpecConfig:
     headroom: int = 64           # cache rows beyond the longest KV length
     m_cycle: Optional[tuple] = None   # draft positions per request, cycled over b
     budget: int = -1             # draft nodes shared by the batch (< 0: none)
+    markov_R: int = 0            # > 0: a drafter with a Markov head of this rank
 
     @property
     def ragged(self) -> bool:
@@ -107,6 +110,8 @@ CONFIGS = {
     # batch sharing a 192-node budget, 16/12/8 draft positions per request
     5: SpecConfig("ragged", B=24, m=16, K=16, N=24, L=8192, L_lo=1024, p_plant=0.85,
                   m_cycle=(16, 12, 8), budget=192, **_BIG),
+    # 'single' drafted by a drafter with a Markov head (parent-dependent edges)
+    6: SpecConfig("markov", B=1, m=8, K=16, N=24, L=4096, p_plant=0.85, markov_R=32, **_BIG),
 }
 
 
@@ -207,13 +212,32 @@ def top_candidates(lat_tok: torch.Tensor, lat_score: torch.Tensor) -> torch.Tens
     return torch.gather(lat_tok, -1, best).squeeze(-1)
 
 
+def first_child_tokens(node_parent, node_rank, node_tok, n_nodes) -> torch.Tensor:
+    """[B][T] token of each row's rank-0 child in the tree, -1 where that child
+    is not in the tree (indexing only)."""
+    par = torch.as_tensor(node_parent).long()
+    rank = torch.as_tensor(node_rank).long()
+    tok = torch.as_tensor(node_tok).long()
+    B, T = par.shape
+    out = torch.full((B, T), -1, dtype=torch.long)
+    nn = torch.as_tensor(n_nodes).long()
+    for b in range(B):
+        for x in range(1, int(nn[b])):
+            if int(rank[b, x]) == 0:
+                out[b, par[b, x]] = tok[b, x]
+    return out
+
+
 def plant_logits(logits: torch.Tensor, lat_tok, lat_score, node_depth, n_nodes, p: float,
-                 gen: torch.Generator) -> torch.Tensor:
+                 gen: torch.Generator, first_child=None) -> torch.Tensor:
     """Plant the drafter's first choice as the argmax of tree rows (in place).
 
     node_depth [B][T] and n_nodes [B] describe the tree the logits belong to.
     One uniform draw per row decides, independently, whether that row is
-    planted (rows of depth m and padding rows never are).
+    planted (rows of depth m and padding rows never are).  The first choice is
+    the top candidate of the next lattice position, or, with first_child
+    ([B][T] from first_child_tokens: for drafters whose ranking depends on the
+    parent), the row's rank-0 child in the tree (no plant where it is absent).
     """
     B, T, V = logits.shape
     m = lat_tok.shape[1]
@@ -223,8 +247,13 @@ def plant_logits(logits: torch.Tensor, lat_tok, lat_score, node_depth, n_nodes, 
     nn = torch.as_tensor(n_nodes, device=dev).long()
     rows = torch.arange(T, device=dev).unsqueeze(0)
     ok = (u < p) & (rows < nn.unsqueeze(1)) & (depth >= 0) & (depth < m)
-    top = top_candidates(torch.as_tensor(lat_tok).to(dev), torch.as_tensor(lat_score).to(dev))
-    tok = torch.gather(top.long(), 1, depth.clamp(0, m - 1))
+    if first_child is None:
+        top = top_candidates(torch.as_tensor(lat_tok).to(dev), torch.as_tensor(lat_score).to(dev))
+        tok = torch.gather(top.long(), 1, depth.clamp(0, m - 1))
+    else:
+        tok = torch.as_tensor(first_child).long().to(dev)
+        ok = ok & (tok >= 0)
+        tok = tok.clamp(min=0)
     val = (logits.float().amax(dim=-1) + 1.0).to(logits.dtype)
     bi, ti = torch.nonzero(ok, as_tuple=True)
     logits[bi, ti, tok[bi, ti]] = val[bi, ti]
@@ -284,6 +313,8 @@ def make_step_inputs(cfg: SpecConfig, seed: int, device="cpu", logits=True) -> d
                kv_len=kv_len, gdn=gdn, attn=attn)
     if cfg.ragged:
         out["m_req"] = cfg.m_req()
+    if cfg.markov_R > 0:
+        out["lat_base"], out["W1"], out["W2"] = make_markov(cfg, g, cfg.markov_R)
     if logits:
         out["logits"] = make_logits(cfg, g)
     out["plant_gen"] = g

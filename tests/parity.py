@@ -42,13 +42,18 @@ def prepare(scfg: synth.SpecConfig, seed: int, kv_len=None, lat_edit=None):
         inp["kv_len"] = torch.as_tensor(kv_len, dtype=torch.int32).reshape(scfg.B)
     if lat_edit is not None:
         lat_edit(inp)
-    if scfg.ragged:
+    if scfg.markov_R > 0:
+        tree = oracle.tree_build_markov(inp["lat_tok"], inp["lat_base"], inp["W1"], inp["W2"],
+                                        inp["root_tok"], scfg.N)
+    elif scfg.ragged:
         tree = oracle.tree_build_ragged(inp["lat_tok"], inp["lat_score"], inp["root_tok"], scfg.N,
                                         inp["m_req"], scfg.budget)
     else:
         tree = oracle.tree_build(inp["lat_tok"], inp["lat_score"], inp["root_tok"], scfg.N)
+    fc = (synth.first_child_tokens(tree["node_parent"], tree["node_rank"], tree["node_tok"],
+                                   tree["n_nodes"]) if scfg.markov_R > 0 else None)
     synth.plant_logits(inp["logits"], inp["lat_tok"], inp["lat_score"], tree["node_depth"],
-                       tree["n_nodes"], scfg.p_plant, inp["plant_gen"])
+                       tree["n_nodes"], scfg.p_plant, inp["plant_gen"], first_child=fc)
     return inp, tree
 
 

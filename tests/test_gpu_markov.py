@@ -70,3 +70,15 @@ def test_batched_requests():
 def test_zero_head_and_tied_bases():
     _check(SMALL.replace(K=8), 5, R=4, zero=True, ties=True)
     _check(SMALL, 6, R=0)
+
+
+def test_fused_step_with_markov_head():
+    from tests import parity
+    scfg = synth.config(6).replace(V=3000, L=500)
+    assert parity.check_case(scfg, 0)["status"] == 0
+    assert parity.check_case(scfg, 1, calls=True)["status"] == 0
+
+
+def test_markov_workload_step():
+    from tests import parity
+    assert parity.check_case(synth.config(6), 2)["status"] == 0
