@@ -49,7 +49,9 @@ def algorithmic_bytes(s: synth.SpecConfig, mean_L: float, tau: float, rows=None)
     attn_kv = mean_L * s.Hkv * s.D * e * 2
     attn_rows = T * (s.Hq * s.D * e * 2 + s.Hkv * s.D * e * 2)
     per_req = dict(
-        tree=s.m * s.K * 8 + T * 36,
+        # lattice (+ a Markov head's rows: W1 of every candidate and the root,
+        # W2 of every candidate) and the tree rows
+        tree=s.m * s.K * 8 + T * 36 + (2 * s.m * s.K + 1) * s.markov_R * 4,
         gdn=s.n_gdn * (gdn_state + gdn_rows),
         attn=s.n_attn * (attn_kv + attn_rows),
         logits=T * s.V * e,

@@ -72,6 +72,37 @@ def test_zero_head_and_tied_bases():
     _check(SMALL, 6, R=0)
 
 
+@pytest.mark.parametrize("R", [1, 7, 33])
+def test_head_ranks_not_a_multiple_of_four(R):
+    _check(SMALL, 10 + R, R=R)                 # the 4-byte staging path
+
+
+@pytest.mark.parametrize("K", [17, 32])
+def test_wide_positions_use_full_warps(K):
+    _check(SMALL.replace(K=K), 20 + K, R=12)
+
+
+def test_out_of_range_token_is_reported_and_stays_local():
+    scfg = SMALL
+    g = torch.Generator().manual_seed(7)
+    lat_tok, _, root = synth.make_lattice(scfg, g)
+    base, W1, W2 = synth.make_markov(scfg, g, 8)
+    want = oracle.tree_build_markov(lat_tok, base, W1, W2, root, scfg.N)
+    bad_tok = lat_tok.clone()
+    bad_tok[1, 2, 3] = scfg.V                  # one past the head's last row
+    cfg = binding.make_cfg(scfg)
+    tree = binding.TreeBuffers(cfg)
+    ws = binding.alloc_workspace(cfg)
+    binding.spec_tree_build_markov(cfg, bad_tok.cuda(), base.cuda(), W1.cuda(), W2.cuda(),
+                                   root.cuda(), tree, ws)
+    torch.cuda.synchronize()
+    assert binding.spec_status_read(ws) & binding.SPEC_DEV_BADLAT
+    got = tree.to_numpy()
+    for b in (0, 2):                           # the other requests are untouched
+        for k in ("node_tok", "node_parent", "node_rank"):
+            np.testing.assert_array_equal(got[k][b], want[k][b], err_msg=k)
+
+
 def test_fused_step_with_markov_head():
     from tests import parity
     scfg = synth.config(6).replace(V=3000, L=500)
