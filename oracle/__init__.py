@@ -18,7 +18,10 @@ Algorithm Discovery and Systems Optimization for Speculative Decoding"
 Parity pins: every function here is pinned by tests under ``tests/``
 (brute-force tree enumeration, closed forms, an independent ancestor-expansion
 GDN formulation, float64 SDPA, torch.argmax, a plain chain verifier and the
-multi-step decode consistency check).
+multi-step decode consistency check; for stochastic acceptance, Philox's
+published known answers and an independent implementation, chi-square tests
+of the draws against the tempered softmax, and the exact law of the
+speculative-decoding tutorial's rejection rule).
 """
 from __future__ import annotations
 
@@ -63,8 +66,14 @@ def _load():
             for name in ("orc_tree_build", "orc_tree_build_ragged", "orc_tree_build_markov",
                          "orc_markov_edges", "orc_exp32_log32", "orc_gdn_tree",
                          "orc_attn_tree", "orc_argmax", "orc_accept", "orc_commit_gdn",
-                         "orc_commit_kv"):
+                         "orc_commit_kv", "orc_philox4x32_10", "orc_sample_rows",
+                         "orc_sample_gaps"):
                 getattr(lib, name).restype = ctypes.c_int
+            lib.orc_sample_rows.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p, ctypes.c_int] + \
+                [ctypes.c_void_p] * 2 + [ctypes.c_double, ctypes.c_uint64, ctypes.c_int] + \
+                [ctypes.c_void_p] * 2
+            lib.orc_sample_gaps.argtypes = [ctypes.c_int, ctypes.c_void_p] + [ctypes.c_int] * 4 + \
+                [ctypes.c_double, ctypes.c_uint64, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
             _lib = lib
     return _lib
 
@@ -285,6 +294,57 @@ def argmax(logits):
     rc = _load().orc_argmax(rows, V, _p(la), bf, _p(idx), _p(mar))
     _check(rc, "argmax")
     return idx.reshape(lead), mar.reshape(lead)
+
+
+SAMPLE_CHUNK = 4096
+
+
+def philox4x32_10(ctr, key) -> np.ndarray:
+    """Philox4x32-10 blocks: ctr uint32 [n][4], key uint32 [n][2] -> uint32 [n][4].
+
+    Definition: Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as easy
+    as 1, 2, 3" (SC 2011)."""
+    c = _np(ctr, np.uint32).reshape(-1, 4)
+    k = _np(key, np.uint32).reshape(-1, 2)
+    assert c.shape[0] == k.shape[0]
+    out = np.empty_like(c)
+    _load().orc_philox4x32_10(c.shape[0], _p(c), _p(k), _p(out))
+    return out
+
+
+def sample_rows(logits, n_nodes, kv_len, temperature: float, seed: int,
+                chunk: int = SAMPLE_CHUNK):
+    """The target's draw from softmax(logits / temperature) at every tree row
+    (two-level Gumbel-max, Philox4x32-10 noise keyed by seed and counted by
+    (index, row, request, kv_len)).
+
+    Speculative-decoding tutorial (mlqm.cn), section 2.3: with fixed draft
+    tokens the rejection rule is the same law as following the child whose
+    token equals the target's draw.  logits [B][T][V]; returns (int32 [B][T],
+    float64 [B][T] margin); padding rows get -1 and +inf."""
+    la, bf = _io(logits)
+    B, T, V = la.shape
+    nn = _np(n_nodes, np.int32)
+    kl = _np(kv_len, np.int32)
+    smp = np.empty((B, T), np.int32)
+    mar = np.empty((B, T), np.float64)
+    rc = _load().orc_sample_rows(B, T, V, _p(la), bf, _p(nn), _p(kl), float(temperature),
+                                 int(seed) & 0xFFFFFFFFFFFFFFFF, int(chunk), _p(smp), _p(mar))
+    _check(rc, "sample_rows")
+    return smp, mar
+
+
+def sample_gaps(row_logits, t: int, b: int, pos: int, temperature: float, seed: int, alt: int,
+                chunk: int = SAMPLE_CHUNK):
+    """How far token `alt` falls behind row (b, t)'s draw: (chunk-level gap,
+    token-level gap); both 0 when alt is the draw."""
+    la, bf = _io(row_logits)
+    gaps = np.empty((2,), np.float64)
+    rc = _load().orc_sample_gaps(la.shape[-1], _p(la), bf, int(t), int(b), int(pos),
+                                 float(temperature), int(seed) & 0xFFFFFFFFFFFFFFFF, int(chunk),
+                                 int(alt), _p(gaps))
+    _check(rc, "sample_gaps")
+    return float(gaps[0]), float(gaps[1])
 
 
 def accept(tree: dict, argmax_rows, m: int) -> dict:

@@ -30,6 +30,11 @@
  *   [MARK]  prerequisites / parallel drafter -- DSpark's Markov head conditions
  *           each position on the previous token:
  *           l_s(y) = bases(y) + <W1[x_{s-1}], W2[y]>.
+ * and the speculative-decoding tutorial (mlqm.cn, news/131545):
+ *   [RS]    section 2.3, the acceptance rule at temperature > 0: a draft token
+ *           x with draft probability q(x) and target probability p(x) is kept
+ *           with probability min(1, p(x)/q(x)); otherwise a token is drawn from
+ *           max(0, p - q), renormalised, and the output follows p exactly.
  *
  * Precision: every floating-point result is accumulated in double from the
  * exact values of the (bf16 or fp32) inputs.  The one exception is the tree
@@ -55,6 +60,16 @@
  *       LSE = M + log32(Z)).  exp32 and log32 are the fp32 functions defined
  *       below, so the scores are fixed to the bit.  Children of a parent are
  *       ranked by (edge desc, candidate index asc).
+ *   R15 Stochastic acceptance: the tree's drafts are fixed tokens (q is a point
+ *       mass), so at a node with children x_1..x_k the [RS] rule keeps x_i with
+ *       probability p'(x_i), p' being p with the earlier children removed and
+ *       renormalised, and otherwise draws the bonus from p without all of
+ *       them.  That is the same law as drawing y ~ p at the node and moving to
+ *       the child whose token is y (y is the bonus when there is none).  The
+ *       draw from p = softmax(l / theta) is a two-level Gumbel-max over chunks
+ *       of 4096 tokens (orc_sample_row), with Gumbel noise from Philox4x32-10
+ *       keyed by the 64-bit seed and counted by (index, row, request,
+ *       kv_len).  The walk is then C6 with the draws in place of the argmax.
  *   R12 Shared budget: request b drafts from its first m_b lattice positions;
  *       the batch's draft nodes are inserted best-first over the frontiers of
  *       all requests together (key: score desc, then request index asc, then
@@ -711,6 +726,166 @@ int orc_argmax(int rows, int V, const void *logits, int io_bf16,
         if (margin) margin[r] = (float)((double)bv - second);
     }
     return 0;
+}
+
+/* ---- R15: the target's draw at each row, for stochastic acceptance [RS] -- */
+
+/*
+ * Philox4x32-10, from its definition in J. Salmon, M. Moraes, R. Dror and
+ * D. Shaw, "Parallel random numbers: as easy as 1, 2, 3" (SC 2011): ten
+ * rounds of
+ *   (hi0, lo0) = 64-bit product 0xD2511F53 * c0,
+ *   (hi1, lo1) = 64-bit product 0xCD9E8D57 * c2,
+ *   c <- (hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0),
+ * the key (k0, k1) growing by (0x9E3779B9, 0xBB67AE85) before every round but
+ * the first.
+ */
+static void orc_philox(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4])
+{
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c0, p1 = (uint64_t)0xCD9E8D57u * c2;
+        const uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+        const uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+        c0 = hi1 ^ c1 ^ k0;
+        c1 = lo1;
+        c2 = hi0 ^ c3 ^ k1;
+        c3 = lo0;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+int orc_philox4x32_10(int n, const uint32_t *ctr, const uint32_t *key, uint32_t *out)
+{
+    for (int i = 0; i < n; ++i) orc_philox(ctr + 4 * (size_t)i, key + 2 * (size_t)i, out + 4 * (size_t)i);
+    return 0;
+}
+
+/* Gumbel noise of one 32-bit word: U = (floor(x / 2^9) + 1/2) / 2^23, which
+ * lies in (0, 1) and is exact in float; g = -ln(-ln U). */
+static double orc_gumbel(uint32_t x)
+{
+    const double u = ((double)(x >> 9) + 0.5) / 8388608.0;
+    return -log(-log(u));
+}
+
+/* Noise of index i (a token, or a chunk when `chunk_space`) of tree row t of
+ * request b at cache position pos: word i % 4 of Philox4x32-10 with counter
+ * (i / 4, t or t + 2^31, b, pos) and key (low, high 32 bits of seed). */
+static double orc_noise(uint64_t seed, uint32_t i, int chunk_space, uint32_t t, uint32_t b,
+                        uint32_t pos)
+{
+    const uint32_t ctr[4] = {i >> 2, chunk_space ? (t | 0x80000000u) : t, b, pos};
+    const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t w[4];
+    orc_philox(ctr, key, w);
+    return orc_gumbel(w[i & 3]);
+}
+
+/*
+ * One draw from softmax(l / theta) over the V logits of tree row t of request
+ * b (cache position pos), by the two-level Gumbel-max of R15:
+ *   chunk c holds tokens [c C, min(V, (c+1) C));
+ *   lambda_c = log sum_{v in c} exp(l_v / theta);
+ *   c* = the chunk with the largest lambda_c + g_chunk(c) (lowest c on ties);
+ *   v* = the token of c* with the largest l_v / theta + g_token(v) (lowest v).
+ * P(v*) = P(c*) P(v* | c*) = exp(l_v / theta) / sum_u exp(l_u / theta).
+ * *margin = the smaller of the two top-2 gaps (chunk scores; token scores in
+ * c*), +inf when a level has one entry.  With alt >= 0, gaps[0] = the best
+ * chunk score minus the score of alt's chunk and gaps[1] = the best token
+ * score in alt's chunk minus alt's score (both 0 when alt is the draw).
+ */
+static int orc_sample_row(int V, const void *logits, int io_bf16, size_t row_off, double theta,
+                          uint64_t seed, uint32_t t, uint32_t b, uint32_t pos, int C,
+                          int alt, int *out, double *margin, double *gaps)
+{
+    const int nc = (V + C - 1) / C;
+    double *score = (double *)malloc(sizeof(double) * (size_t)nc);
+    if (!score) return -3;
+    for (int c = 0; c < nc; ++c) {
+        const int lo = c * C, hi = lo + C < V ? lo + C : V;
+        double M = -INFINITY;
+        for (int v = lo; v < hi; ++v) {
+            const double l = orc_elem(logits, row_off + v, io_bf16) / theta;
+            if (l > M) M = l;
+        }
+        double S = 0.0;
+        for (int v = lo; v < hi; ++v) S += exp(orc_elem(logits, row_off + v, io_bf16) / theta - M);
+        score[c] = M + log(S) + orc_noise(seed, (uint32_t)c, 1, t, b, pos);
+    }
+    int cs = 0;
+    for (int c = 1; c < nc; ++c) if (score[c] > score[cs]) cs = c;
+    double second = INFINITY;
+    if (nc > 1) {
+        double s2 = -INFINITY;
+        for (int c = 0; c < nc; ++c) if (c != cs && score[c] > s2) s2 = score[c];
+        second = score[cs] - s2;
+    }
+    /* the token level inside chunk c: best token, top-2 gap, alt's gap */
+    int best = -1;
+    double gap_tok = INFINITY;
+    for (int pass = 0; pass < 2; ++pass) {
+        const int c = pass == 0 ? cs : (alt >= 0 ? alt / C : -1);
+        if (c < 0 || c >= nc) break;
+        const int lo = c * C, hi = lo + C < V ? lo + C : V;
+        int bv = -1;
+        double b1 = -INFINITY, b2 = -INFINITY, za = -INFINITY;
+        for (int v = lo; v < hi; ++v) {
+            const double z = orc_elem(logits, row_off + v, io_bf16) / theta +
+                             orc_noise(seed, (uint32_t)v, 0, t, b, pos);
+            if (z > b1) { b2 = b1; b1 = z; bv = v; }
+            else if (z > b2) b2 = z;
+            if (v == alt) za = z;
+        }
+        if (pass == 0) {
+            best = bv;
+            gap_tok = hi - lo > 1 ? b1 - b2 : INFINITY;
+        } else if (gaps) {
+            gaps[0] = score[cs] - score[c];
+            gaps[1] = b1 - za;
+        }
+    }
+    *out = best;
+    if (margin) *margin = second < gap_tok ? second : gap_tok;
+    free(score);
+    return 0;
+}
+
+/*
+ * orc_sample_rows: the draw of every row t < n_nodes[b] of every request
+ * (cache position kv_len[b]); padding rows get -1 and margin +inf.
+ * logits [B][T][V].  Returns -1 on bad sizes or theta <= 0.
+ */
+int orc_sample_rows(int B, int T, int V, const void *logits, int io_bf16,
+                    const int32_t *n_nodes, const int32_t *kv_len, double theta,
+                    uint64_t seed, int chunk, int32_t *sample, double *margin)
+{
+    if (V < 1 || chunk < 1 || !(theta > 0.0)) return -1;
+    for (int b = 0; b < B; ++b)
+        for (int t = 0; t < T; ++t) {
+            const size_t r = (size_t)b * T + t;
+            if (t >= n_nodes[b]) { sample[r] = -1; margin[r] = INFINITY; continue; }
+            int v;
+            const int rc = orc_sample_row(V, logits, io_bf16, r * (size_t)V, theta, seed,
+                                          (uint32_t)t, (uint32_t)b, (uint32_t)kv_len[b], chunk,
+                                          -1, &v, &margin[r], NULL);
+            if (rc) return rc;
+            sample[r] = v;
+        }
+    return 0;
+}
+
+/* Gaps of the token `alt` in one row's draw (see orc_sample_row): how far it
+ * falls behind the draw at the chunk and at the token level. */
+int orc_sample_gaps(int V, const void *row_logits, int io_bf16, int t, int b, int pos,
+                    double theta, uint64_t seed, int chunk, int alt, double *gaps)
+{
+    if (V < 1 || chunk < 1 || !(theta > 0.0) || alt < 0 || alt >= V) return -1;
+    int v;
+    return orc_sample_row(V, row_logits, io_bf16, 0, theta, seed, (uint32_t)t, (uint32_t)b,
+                          (uint32_t)pos, chunk, alt, &v, NULL, gaps);
 }
 
 /* ---- C6: greedy acceptance of the longest matching root path [SD][TREE] -- */

@@ -13,6 +13,11 @@ either one shows up as a disagreement:
   path(x) after a.  No dk x dv state is ever updated in place.
 * ``plain_chain_verify`` -- classic speculative verification of a chain of
   drafts (accept while draft_i equals the argmax of the previous row).
+* ``rejection_outcomes`` -- the exact law of a stochastic tree verification
+  under the literal rejection rule of the speculative-decoding tutorial
+  (section 2.3): keep a draft x with probability min(1, p(x) / q(x)), else go
+  on with max(0, p - q) renormalised, each draft being a fixed token (q a
+  point mass).  Outcomes are enumerated exactly, in float64.
 """
 from __future__ import annotations
 
@@ -254,3 +259,41 @@ def plain_chain_verify(root_tok, drafts, argmax_rows):
         row = i + 1
     out.append(int(argmax_rows[row]))
     return len(out), out
+
+
+def rejection_outcomes(node_tok, node_parent, n_nodes, p_rows, m):
+    """Exact law of (accepted draft tokens..., bonus) under the rejection rule.
+
+    At the current node the target distribution is p = p_rows[node]; its
+    children are tried in node order.  Child x (a fixed draft, so q = one-hot
+    at x) is kept with probability min(1, p(x) / q(x)) = p(x); if it is not,
+    p becomes max(0, p - q) renormalised, i.e. x removed.  When no child is
+    kept, the bonus is drawn from the final p.  Returns {tuple: probability}.
+    """
+    children = {}
+    for c in range(1, int(n_nodes)):
+        children.setdefault(int(node_parent[c]), []).append(c)
+    out = {}
+
+    def visit(node, depth, prefix, weight):
+        p = np.array(p_rows[node], dtype=np.float64)
+        p = p / p.sum()
+        for c in (children.get(node, []) if depth < m else []):
+            x = int(node_tok[c])
+            keep = min(1.0, p[x] / 1.0)
+            if keep > 0:
+                visit(c, depth + 1, prefix + (x,), weight * keep)
+            q = np.zeros_like(p)
+            q[x] = 1.0
+            r = np.maximum(0.0, p - q)
+            if r.sum() == 0:
+                return
+            p = r / r.sum()
+            weight = weight * (1.0 - keep)
+        for y in range(len(p)):
+            if p[y] > 0:
+                key = prefix + (y,)
+                out[key] = out.get(key, 0.0) + weight * p[y]
+
+    visit(0, 0, (), 1.0)
+    return out
