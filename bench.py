@@ -249,6 +249,15 @@ def oracle_tree(scfg, inp):
     return oracle.tree_build(inp["lat_tok"], inp["lat_score"], inp["root_tok"], scfg.N)
 
 
+def oracle_rows(scfg, inp, tree):
+    """The target's token at every row: the argmax, or at temperature > 0 the draw."""
+    import oracle
+    if scfg.temperature > 0:
+        return oracle.sample_rows(inp["logits"], tree["n_nodes"], inp["kv_len"],
+                                  scfg.temperature, scfg.sample_seed)[0]
+    return oracle.argmax(inp["logits"])[0]
+
+
 def oracle_step(scfg, inp):
     """One whole verify step of the CPU oracle."""
     import oracle
@@ -258,8 +267,7 @@ def oracle_step(scfg, inp):
     for lay in inp["attn"]:
         oracle.attn_tree(tree, lay["q"], lay["k_tree"], lay["v_tree"], lay["k_cache"],
                          lay["v_cache"], inp["kv_len"])
-    am, _ = oracle.argmax(inp["logits"])
-    acc = oracle.accept(tree, am, scfg.m)
+    acc = oracle.accept(tree, oracle_rows(scfg, inp, tree), scfg.m)
     for lay in inp["gdn"]:
         oracle.commit_gdn(acc, lay["h0"], lay["k"], lay["v"], lay["alpha"], lay["beta"])
     for lay in inp["attn"]:
@@ -275,7 +283,8 @@ def planted_inputs_cpu(scfg, seed):
     fc = (synth.first_child_tokens(tree["node_parent"], tree["node_rank"], tree["node_tok"],
                                    tree["n_nodes"]) if scfg.markov_R > 0 else None)
     synth.plant_logits(inp["logits"], inp["lat_tok"], inp["lat_score"], tree["node_depth"],
-                       tree["n_nodes"], scfg.p_plant, inp["plant_gen"], first_child=fc)
+                       tree["n_nodes"], scfg.p_plant, inp["plant_gen"], first_child=fc,
+                       gap=scfg.plant_gap)
     return inp
 
 
@@ -343,8 +352,7 @@ def oracle_step_parts(scfg, inp, j, g):
     i = j // grp
     t0 = time.perf_counter()
     tree = oracle_tree(scfg, inp)
-    am, _ = oracle.argmax(inp["logits"])
-    acc = oracle.accept(tree, am, scfg.m)
+    acc = oracle.accept(tree, oracle_rows(scfg, inp, tree), scfg.m)
     t1 = time.perf_counter()
     for lay in inp["gdn"]:
         sl = dict(h0=lay["h0"][:, j:j + 1], q=lay["q"][:, :, i:i + 1], k=lay["k"][:, :, i:i + 1],
@@ -392,7 +400,8 @@ def run_ours(args, rank, world, local):
     fc = (synth.first_child_tokens(t_np["node_parent"], t_np["node_rank"], t_np["node_tok"],
                                    t_np["n_nodes"]) if scfg.markov_R > 0 else None)
     synth.plant_logits(logits, inp["lat_tok"], inp["lat_score"], t_np["node_depth"],
-                       t_np["n_nodes"], scfg.p_plant, inp["plant_gen"], first_child=fc)
+                       t_np["n_nodes"], scfg.p_plant, inp["plant_gen"], first_child=fc,
+                       gap=scfg.plant_gap)
     x["logits"].copy_(logits.to(dev))
     kv0, root0 = x["kv_len"].clone(), x["root_tok"].clone()
 
@@ -532,6 +541,8 @@ def run_ours(args, rank, world, local):
                                   f"shared budget {scfg.budget} drafts "
                                   if scfg.ragged else "")
                                + (f"Markov head rank {scfg.markov_R} " if scfg.markov_R else "")
+                               + (f"sampled acceptance temperature {scfg.temperature:g} "
+                                  if scfg.temperature > 0 else "")
                                + f"GDN {scfg.n_gdn}x({scfg.Hk}qk/{scfg.Hv}v heads {scfg.dk}x{scfg.dv}) "
                                f"attn {scfg.n_attn}x({scfg.Hq}q/{scfg.Hkv}kv heads D={scfg.D}) "
                                f"KV={scfg.L} V={scfg.V}",

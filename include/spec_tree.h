@@ -62,10 +62,14 @@ enum {
 };
 
 /* Bits of the device status word (uint32 at byte 0 of the workspace). */
+/* Tokens per vocabulary chunk of the sampled acceptance's two-level draw. */
+#define SPEC_SAMPLE_CHUNK 4096
+
 #define SPEC_DEV_OVERFLOW 0x1u  /* a request's commit was skipped: no room in the cache */
 #define SPEC_DEV_BADLAT   0x2u  /* a lattice position repeats a token or has a NaN score */
 #define SPEC_DEV_TIMEOUT  0x4u  /* a bounded device-side wait gave up */
 #define SPEC_DEV_BADREQ   0x8u  /* a per-request position count was outside [1, m] (clamped) */
+#define SPEC_DEV_BADLOGIT 0x10u /* a sampled row had no finite score (NaN / inf logits) */
 
 enum { SPEC_IO_F32 = 0, SPEC_IO_BF16 = 1 };
 
@@ -117,6 +121,13 @@ typedef struct spec_accept {
     int32_t *accept_nodes;  /* [B][m+1] accepted root path (row 0 first), -1 beyond tau */
     int32_t *out_tok;       /* [B][m+1] emitted tokens: accepted drafts then the bonus, -1 beyond tau */
 } spec_accept;
+
+/* Sampled acceptance (temperature > 0). */
+typedef struct spec_sampling {
+    float temperature;      /* > 0 and finite */
+    uint32_t reserved;      /* must be 0 */
+    uint64_t seed;          /* Philox4x32-10 key: (low 32 bits, high 32 bits) */
+} spec_sampling;
 
 /* Bytes of device workspace the calls below need for `cfg` (0 on invalid cfg). */
 size_t spec_workspace_bytes(const spec_cfg *cfg);
@@ -202,6 +213,34 @@ int accept_and_commit(const spec_cfg *cfg, const spec_tree *tree, const void *lo
                       const spec_commit_io *io, const spec_accept *out, void *ws,
                       void *stream);
 
+/*
+ * accept_and_commit_sampled -- accept_and_commit at temperature > 0.
+ * Speculative-decoding tutorial (mlqm.cn), section 2.3: a draft x with draft
+ * probability q(x) is kept with probability min(1, p(x)/q(x)), else a token
+ * is drawn from max(0, p - q) renormalised, and the output follows the
+ * target's p exactly.  The tree's drafts are fixed tokens (q a point mass), so
+ * at a node the rule keeps child x with the probability of x under p with the
+ * earlier children removed; that is the law of drawing y from p at the row and
+ * moving to the child whose token is y.  So step (i) of accept_and_commit
+ * becomes a draw per row, and (ii)-(iii) are unchanged:
+ *   p = softmax(logits[b][n][:] / temperature);
+ *   chunk c = tokens [c C, min(V, (c+1) C)), C = SPEC_SAMPLE_CHUNK;
+ *   c* = argmax_c log(sum_{v in c} exp(l_v / temperature)) + G(c)  (lowest c on ties)
+ *   draw = argmax_{v in c*} l_v / temperature + G(v)                  (lowest v on ties)
+ *   G(i) = -ln(-ln U), U = (floor(x / 2^9) + 1/2) 2^-23, x = word i % 4 of
+ *   Philox4x32-10 with key (seed low, seed high) and counter
+ *   (i / 4, n (+ 2^31 for chunks), b, kv_len[b]);
+ * argmax[b][n] of `out` receives the draw.  A row whose scores are all NaN
+ * (NaN or +inf logits) draws the first token of its first chunk and raises
+ * SPEC_DEV_BADLOGIT.  The result is a draw from p (in
+ * exact arithmetic); draws whose top-2 score gap is within float rounding can
+ * differ from a float64 evaluation of the same definition.
+ * ST_EINVAL when temperature is not > 0 and finite or reserved != 0.
+ */
+int accept_and_commit_sampled(const spec_cfg *cfg, const spec_tree *tree, const void *logits,
+                              const spec_sampling *smp, const spec_commit_io *io,
+                              const spec_accept *out, void *ws, void *stream);
+
 /* Per-layer verify buffers of a whole step, stacked with the layer outermost
  * (layer l of gdn_q is the q that gdn_tree_verify would get for layer l). */
 typedef struct spec_step_io {
@@ -285,6 +324,16 @@ int spec_tree_build_ragged(const spec_cfg *cfg, const int32_t *lat_tok, const fl
 int spec_tree_build_markov(const spec_cfg *cfg, const int32_t *lat_tok, const float *lat_base,
                            const float *W1, const float *W2, int R, const int32_t *root_tok,
                            const spec_tree *out, void *ws, void *stream);
+
+/*
+ * spec_verify_step_sampled -- spec_verify_step with the acceptance of
+ * accept_and_commit_sampled; the same number of launches.
+ */
+int spec_verify_step_sampled(const spec_cfg *cfg, const int32_t *lat_tok, const float *lat_score,
+                             const spec_sampling *smp, const spec_tree *tree,
+                             const spec_step_io *step, const void *logits,
+                             const spec_commit_io *io, const spec_accept *out, void *ws,
+                             void *stream);
 
 /*
  * spec_verify_step_ragged -- spec_verify_step with the trees of

@@ -21,12 +21,15 @@ LIB_PATH = os.path.join(_HERE, "libspectree.so")
 ST_OK, ST_EINVAL, ST_EUNSUPPORTED, ST_ECUDA, ST_EOVERFLOW, ST_TIMEOUT, ST_ESCRATCH = range(7)
 NOALLOC_SCRATCH_BYTES = 8 << 20
 SPEC_DEV_OVERFLOW, SPEC_DEV_BADLAT, SPEC_DEV_TIMEOUT, SPEC_DEV_BADREQ = 0x1, 0x2, 0x4, 0x8
+SPEC_DEV_BADLOGIT = 0x10
 SPEC_IO_F32, SPEC_IO_BF16 = 0, 1
 EXPORTS = ("spec_workspace_bytes", "spec_tree_build", "gdn_tree_verify", "attn_tree_verify",
            "accept_and_commit", "spec_verify_step", "spec_status_read", "spec_status_clear",
            "spec_status_string", "spec_abi_version", "attn_tree_verify_noalloc",
            "spec_wait_probe", "spec_step_launches", "spec_tree_build_ragged",
-           "spec_verify_step_ragged", "spec_tree_build_markov", "spec_verify_step_markov")
+           "spec_verify_step_ragged", "spec_tree_build_markov", "spec_verify_step_markov",
+           "accept_and_commit_sampled", "spec_verify_step_sampled")
+SAMPLE_CHUNK = 4096
 
 _lock = threading.Lock()
 _lib = None
@@ -61,6 +64,11 @@ class SpecStepIO(ctypes.Structure):
 
 class SpecAccept(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("argmax", "accept_len", "accept_nodes", "out_tok")]
+
+
+class SpecSampling(ctypes.Structure):
+    _fields_ = [("temperature", ctypes.c_float), ("reserved", ctypes.c_uint32),
+                ("seed", ctypes.c_uint64)]
 
 
 def load(path: Optional[str] = None) -> ctypes.CDLL:
@@ -100,6 +108,14 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                                     ctypes.POINTER(SpecStepIO), vp,
                                                     ctypes.POINTER(SpecCommitIO),
                                                     ctypes.POINTER(SpecAccept), vp, vp]
+            smpp = ctypes.POINTER(SpecSampling)
+            lib.accept_and_commit_sampled.argtypes = [cfgp, ctypes.POINTER(SpecTree), vp, smpp,
+                                                      ctypes.POINTER(SpecCommitIO),
+                                                      ctypes.POINTER(SpecAccept), vp, vp]
+            lib.spec_verify_step_sampled.argtypes = [cfgp, vp, vp, smpp, ctypes.POINTER(SpecTree),
+                                                     ctypes.POINTER(SpecStepIO), vp,
+                                                     ctypes.POINTER(SpecCommitIO),
+                                                     ctypes.POINTER(SpecAccept), vp, vp]
             lib.spec_status_read.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
             lib.spec_status_clear.argtypes = [vp, vp]
             lib.spec_status_string.argtypes = [ctypes.c_int]
@@ -110,8 +126,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
             for n in ("spec_tree_build", "gdn_tree_verify", "attn_tree_verify",
                       "attn_tree_verify_noalloc", "spec_wait_probe", "spec_step_launches",
                       "spec_tree_build_ragged", "spec_verify_step_ragged", "spec_tree_build_markov",
-                      "spec_verify_step_markov",
-                      "accept_and_commit", "spec_verify_step", "spec_status_read",
+                      "spec_verify_step_markov", "accept_and_commit_sampled",
+                      "spec_verify_step_sampled", "accept_and_commit", "spec_verify_step", "spec_status_read",
                       "spec_status_clear", "spec_abi_version"):
                 getattr(lib, n).restype = ctypes.c_int
             _lib = lib
@@ -271,6 +287,20 @@ def accept_and_commit(cfg, tree: TreeBuffers, logits, io: dict, out: AcceptBuffe
         ctypes.byref(out.c()), _ptr(ws, name="ws"), _stream(stream)))
 
 
+def sampling(temperature: float, seed: int) -> SpecSampling:
+    return SpecSampling(float(temperature), 0, int(seed) & 0xFFFFFFFFFFFFFFFF)
+
+
+def accept_and_commit_sampled(cfg, tree: TreeBuffers, logits, smp: SpecSampling, io: dict,
+                              out: AcceptBuffers, ws, stream=None):
+    """accept_and_commit at temperature > 0: out.argmax receives each row's draw."""
+    dt = _io_dtype(cfg)
+    cio = _commit_io(cfg, io)
+    _check("accept_and_commit_sampled", load().accept_and_commit_sampled(
+        ctypes.byref(cfg), ctypes.byref(tree.c()), _ptr(logits, dt, "logits"), ctypes.byref(smp),
+        ctypes.byref(cio), ctypes.byref(out.c()), _ptr(ws, name="ws"), _stream(stream)))
+
+
 def spec_tree_build_ragged(cfg, lat_tok, lat_score, root_tok, m_req, node_budget: int,
                            tree: TreeBuffers, ws, stream=None):
     """Trees with per-request draft positions (m_req: CUDA int32 [B] or None) and
@@ -310,6 +340,18 @@ def spec_verify_step(cfg, lat_tok, lat_score, tree: TreeBuffers, step: dict, log
         _ptr(lat_score, torch.float32, "lat_score"), ctypes.byref(tree.c()), ctypes.byref(sio),
         _ptr(logits, dt, "logits"), ctypes.byref(_commit_io(cfg, io)), ctypes.byref(out.c()),
         _ptr(ws, name="ws"), _stream(stream)))
+
+
+def spec_verify_step_sampled(cfg, lat_tok, lat_score, smp: SpecSampling, tree: TreeBuffers,
+                             step: dict, logits, io: dict, out: AcceptBuffers, ws, stream=None):
+    """spec_verify_step with the sampled acceptance."""
+    dt = _io_dtype(cfg)
+    sio = _step_io(cfg, step)
+    _check("spec_verify_step_sampled", load().spec_verify_step_sampled(
+        ctypes.byref(cfg), _ptr(lat_tok, torch.int32, "lat_tok"),
+        _ptr(lat_score, torch.float32, "lat_score"), ctypes.byref(smp), ctypes.byref(tree.c()),
+        ctypes.byref(sio), _ptr(logits, dt, "logits"), ctypes.byref(_commit_io(cfg, io)),
+        ctypes.byref(out.c()), _ptr(ws, name="ws"), _stream(stream)))
 
 
 def spec_verify_step_ragged(cfg, lat_tok, lat_score, m_req, node_budget: int, tree: TreeBuffers,

@@ -99,8 +99,33 @@ int attn_tree_verify(const spec_cfg* cfg, const spec_tree* tree, const void* q, 
                                           o, ws, static_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+bool temperature_ok(const spec_sampling* s) {
+    return s && s->temperature > 0.0f && s->temperature <= 3.0e38f && s->reserved == 0u;
+}
+int accept_commit_impl(const spec_cfg* cfg, const spec_tree* tree, const void* logits,
+                       const spec_sampling* smp, const spec_commit_io* io, const spec_accept* out,
+                       void* ws, void* stream);
+}  // namespace
+
 int accept_and_commit(const spec_cfg* cfg, const spec_tree* tree, const void* logits,
                       const spec_commit_io* io, const spec_accept* out, void* ws, void* stream) {
+    return accept_commit_impl(cfg, tree, logits, nullptr, io, out, ws, stream);
+}
+
+int accept_and_commit_sampled(const spec_cfg* cfg, const spec_tree* tree, const void* logits,
+                              const spec_sampling* smp, const spec_commit_io* io,
+                              const spec_accept* out, void* ws, void* stream) {
+    if (!temperature_ok(smp)) return ST_EINVAL;
+    return accept_commit_impl(cfg, tree, logits, smp, io, out, ws, stream);
+}
+
+}  // extern "C"
+
+namespace {
+int accept_commit_impl(const spec_cfg* cfg, const spec_tree* tree, const void* logits,
+                       const spec_sampling* smp, const spec_commit_io* io, const spec_accept* out,
+                       void* ws, void* stream) {
     int rc = check_cfg(cfg);
     if (rc) return rc;
     if ((rc = check_tree(tree))) return rc;
@@ -116,8 +141,13 @@ int accept_and_commit(const spec_cfg* cfg, const spec_tree* tree, const void* lo
         !al16(out->out_tok))
         return ST_EINVAL;
     return cuda_rc(spec::launch_accept_commit(*cfg, *tree, logits, *io, *out, ws,
-                                              static_cast<cudaStream_t>(stream)));
+                                              static_cast<cudaStream_t>(stream), false,
+                                              smp ? &smp->temperature : nullptr,
+                                              smp ? smp->seed : 0));
 }
+}  // namespace
+
+extern "C" {
 
 int spec_tree_build_ragged(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_score,
                            const int32_t* root_tok, const int32_t* m_req, int node_budget,
@@ -161,10 +191,11 @@ struct MarkovHead {
 };
 
 // The fused step; m_req / node_budget as in spec_tree_build_ragged, markov as
-// in spec_tree_build_markov (NULL: the plain lattice).
+// in spec_tree_build_markov (NULL: the plain lattice), smp as in
+// accept_and_commit_sampled (NULL: the argmax).
 int verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_score,
                 const int32_t* m_req, int node_budget, const MarkovHead* markov,
-                const spec_tree* tree, const spec_step_io* step, const void* logits,
+                const spec_sampling* smp, const spec_tree* tree, const spec_step_io* step, const void* logits,
                 const spec_commit_io* io, const spec_accept* out, void* ws, void* stream) {
     int rc = check_cfg(cfg);
     if (rc) return rc;
@@ -232,7 +263,13 @@ int verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_sc
         attn_args(l, q, kt, vt, kc, vc, o);
         e = spec::launch_attn_partial(c, *tree, q, kt, vt, kc, vc, io->kv_len, ws, st, true, l & 1);
     }
-    if (e == cudaSuccess) e = spec::launch_argmax_accept(c, *tree, logits, *io, *out, ws, st, true);
+    // the tree (or the budget selection) is two launches back only when an
+    // attention layer sits between
+    if (e == cudaSuccess)
+        e = smp ? spec::launch_sample_accept(c, *tree, logits, smp->temperature, smp->seed, *io,
+                                             *out, ws, st, true, /*tree_early=*/na > 0)
+                : spec::launch_argmax_accept(c, *tree, logits, *io, *out, ws, st, true,
+                                             /*tree_early=*/na > 0);
     for (int l = 0; l < ng && e == cudaSuccess; ++l) {
         const size_t state = (size_t)l * B * c.Hv * c.dk * c.dv;
         const size_t kq = (size_t)l * B * T * c.Hk * c.dk * esz;
@@ -270,8 +307,18 @@ int spec_step_launches(const spec_cfg* cfg) {
 int spec_verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_score,
                      const spec_tree* tree, const spec_step_io* step, const void* logits,
                      const spec_commit_io* io, const spec_accept* out, void* ws, void* stream) {
-    return verify_step(cfg, lat_tok, lat_score, nullptr, -1, nullptr, tree, step, logits, io, out,
-                       ws, stream);
+    return verify_step(cfg, lat_tok, lat_score, nullptr, -1, nullptr, nullptr, tree, step, logits,
+                       io, out, ws, stream);
+}
+
+int spec_verify_step_sampled(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_score,
+                             const spec_sampling* smp, const spec_tree* tree,
+                             const spec_step_io* step, const void* logits,
+                             const spec_commit_io* io, const spec_accept* out, void* ws,
+                             void* stream) {
+    if (!temperature_ok(smp)) return ST_EINVAL;
+    return verify_step(cfg, lat_tok, lat_score, nullptr, -1, nullptr, smp, tree, step, logits, io,
+                       out, ws, stream);
 }
 
 int spec_verify_step_markov(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_base,
@@ -279,16 +326,16 @@ int spec_verify_step_markov(const spec_cfg* cfg, const int32_t* lat_tok, const f
                             const spec_step_io* step, const void* logits, const spec_commit_io* io,
                             const spec_accept* out, void* ws, void* stream) {
     const MarkovHead head{W1, W2, R};
-    return verify_step(cfg, lat_tok, lat_base, nullptr, -1, &head, tree, step, logits, io, out, ws,
-                       stream);
+    return verify_step(cfg, lat_tok, lat_base, nullptr, -1, &head, nullptr, tree, step, logits, io,
+                       out, ws, stream);
 }
 
 int spec_verify_step_ragged(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_score,
                             const int32_t* m_req, int node_budget, const spec_tree* tree,
                             const spec_step_io* step, const void* logits, const spec_commit_io* io,
                             const spec_accept* out, void* ws, void* stream) {
-    return verify_step(cfg, lat_tok, lat_score, m_req, node_budget, nullptr, tree, step, logits, io,
-                       out, ws, stream);
+    return verify_step(cfg, lat_tok, lat_score, m_req, node_budget, nullptr, nullptr, tree, step,
+                       logits, io, out, ws, stream);
 }
 
 int spec_status_read(const void* ws, uint32_t* host_status, void* stream) {

@@ -85,13 +85,17 @@ struct WsLayout {
     size_t attn_o_off1, attn_ml_off1;  // a second partial buffer: attention layer l uses l % 2
     size_t ticket_off;     // uint32 [B][Hkv][n_mt]
     size_t plan_off;       // int32  [B][4]: committed tau (0 = skip), old kv_len
-    size_t acc_ticket_off; // uint32 [B]: argmax CTAs finished per request
+    size_t acc_ticket_off; // uint32 [B]: argmax CTAs (or sampled rows) finished per request
+    size_t samp_off;       // float2 [B][T][n_vchunks]: (max, sum of exp) per vocabulary chunk
+    size_t samp_tok_off;   // int32  [B][T]: the target's draw of each row
+    size_t row_ticket_off; // uint32 [B][T]: chunk-scan CTAs finished per row
     size_t total;
     int n_split;           // cache chunks per (request, kv-head)
     int chunk;             // cache rows per chunk
     int n_chunks;          // n_split + 1 (the tree chunk)
     int n_mt;              // 128-row query tiles per (request, kv-head)
     int argmax_split;      // CTAs per logits row
+    int n_vchunks;         // vocabulary chunks of SPEC_SAMPLE_CHUNK tokens
 };
 
 static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -147,6 +151,13 @@ static inline WsLayout ws_layout(const spec_cfg& c, int num_sms = 152) {
     off = align_up(off + sizeof(int32_t) * 4 * (size_t)c.B, 256);
     w.acc_ticket_off = off;
     off = align_up(off + sizeof(uint32_t) * (size_t)c.B, 256);
+    w.n_vchunks = (int)(((long)c.V + SPEC_SAMPLE_CHUNK - 1) / SPEC_SAMPLE_CHUNK);
+    w.samp_off = off;
+    off = align_up(off + sizeof(float) * 2 * (size_t)rows * w.n_vchunks, 256);
+    w.samp_tok_off = off;
+    off = align_up(off + sizeof(int32_t) * (size_t)rows, 256);
+    w.row_ticket_off = off;
+    off = align_up(off + sizeof(uint32_t) * (size_t)rows, 256);
     w.total = off;
     return w;
 }

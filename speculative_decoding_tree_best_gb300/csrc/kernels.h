@@ -63,13 +63,23 @@ cudaError_t launch_attn_tc(const spec_cfg& c, const spec_tree& t, const void* q,
 // accept_and_commit = argmax/accept, then the commit.  early = false lets the
 // commit run before its pdl_wait (only valid when no GDN layer is the launch
 // just before it).
+// tree_early: the launch that wrote the tree is at least two back, so the
+// kernel may read n_nodes before its programmatic wait.
 cudaError_t launch_argmax_accept(const spec_cfg& c, const spec_tree& t, const void* logits,
                                  const spec_commit_io& io, const spec_accept& out, void* ws,
-                                 cudaStream_t st, bool pdl);
+                                 cudaStream_t st, bool pdl, bool tree_early);
+// Sampled acceptance: each row's token is a draw from softmax(logits /
+// temperature) (Philox4x32-10 noise keyed by seed), then the same walk.
+cudaError_t launch_sample_accept(const spec_cfg& c, const spec_tree& t, const void* logits,
+                                 float temperature, uint64_t seed, const spec_commit_io& io,
+                                 const spec_accept& out, void* ws, cudaStream_t st, bool pdl,
+                                 bool tree_early);
 cudaError_t launch_commit(const spec_cfg& c, const spec_commit_io& io, const spec_accept& out,
                           void* ws, cudaStream_t st, bool pdl, bool early);
+// temperature: nullptr for the argmax, else the sampled acceptance.
 cudaError_t launch_accept_commit(const spec_cfg& c, const spec_tree& t, const void* logits,
                                  const spec_commit_io& io, const spec_accept& out, void* ws,
-                                 cudaStream_t st, bool pdl = false);
+                                 cudaStream_t st, bool pdl = false,
+                                 const float* temperature = nullptr, uint64_t seed = 0);
 
 }  // namespace spec

@@ -141,7 +141,7 @@ __device__ __forceinline__ bool markov_fill(const spec_cfg& c, int R, int RP, in
     float* xs = xs_all + warp * 64;
     const int g0 = lane & ~(G - 1);          // the group's first lane
     const int nrows = (int)markov_rows(m, K);
-    const bool vec = (RP & 3) == 0;
+    const bool vec = (R & 3) == 0;           // RP = R + 4 then; R + 1 can be a multiple of 4 too
     bool bad = false;
     for (int rho0 = 0; rho0 < nrows; rho0 += groups) {
         const int rho = rho0 + grp;

@@ -80,8 +80,16 @@ class VerifyStep:
                     root_tok=x["root_tok"])
 
     def accept_commit(self, stream=None):
-        binding.accept_and_commit(self.cfg, self.tree, self.x["logits"], self.commit_io(),
-                                  self.acc, self.ws, stream)
+        if self.scfg.temperature > 0:
+            binding.accept_and_commit_sampled(self.cfg, self.tree, self.x["logits"],
+                                              self.sampling(), self.commit_io(), self.acc,
+                                              self.ws, stream)
+        else:
+            binding.accept_and_commit(self.cfg, self.tree, self.x["logits"], self.commit_io(),
+                                      self.acc, self.ws, stream)
+
+    def sampling(self):
+        return binding.sampling(self.scfg.temperature, self.scfg.sample_seed)
 
     def run_calls(self, stream=None):
         """The step as the four single-operation calls."""
@@ -95,7 +103,13 @@ class VerifyStep:
         step = dict(gdn_q=x["gdn_q"], gdn_o=self.gdn_o if self.cfg.n_gdn_layers else None,
                     gdn_c=None, attn_q=x["attn_q"],
                     attn_o=self.attn_o if self.cfg.n_attn_layers else None)
-        if self.scfg.markov_R > 0:
+        if self.scfg.temperature > 0:
+            if self.scfg.markov_R > 0 or self.scfg.ragged:
+                raise ValueError("the fused sampled step takes the plain lattice")
+            binding.spec_verify_step_sampled(self.cfg, x["lat_tok"], x["lat_score"],
+                                             self.sampling(), self.tree, step, x["logits"],
+                                             self.commit_io(), self.acc, self.ws, stream)
+        elif self.scfg.markov_R > 0:
             binding.spec_verify_step_markov(self.cfg, x["lat_tok"], x["lat_base"], x["W1"], x["W2"],
                                             self.tree, step, x["logits"], self.commit_io(), self.acc,
                                             self.ws, stream)

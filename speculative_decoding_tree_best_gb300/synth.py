@@ -22,6 +22,8 @@ hybrid Gated-DeltaNet / attention target, a 151936-token vocabulary):
             N = 24 per request, KV as 'batched'
   markov    'single' with a Markov-head drafter: base logits ~ N(0, 2^2) and
             two tables W1, W2 [V][32] ~ N(0, 32^-1/2)
+  sampled   'single' verified by sampling at temperature 1, planted logits at
+            the row maximum + 10 (about 0.88 of the row's probability)
 
 Value recipe: lattice scores are log-softmax over the K candidate logits
 ~ N(0, 2^2) of each position; candidate tokens are drawn uniformly without
@@ -71,6 +73,9 @@ class SpecConfig:
     m_cycle: Optional[tuple] = None   # draft positions per request, cycled over b
     budget: int = -1             # draft nodes shared by the batch (< 0: none)
     markov_R: int = 0            # > 0: a drafter with a Markov head of this rank
+    temperature: float = 0.0     # > 0: sampled acceptance at this temperature
+    sample_seed: int = 0         # the sampled acceptance's noise key
+    plant_gap: float = 1.0       # a planted logit is the row maximum + plant_gap
 
     @property
     def ragged(self) -> bool:
@@ -112,6 +117,10 @@ CONFIGS = {
                   m_cycle=(16, 12, 8), budget=192, **_BIG),
     # 'single' drafted by a drafter with a Markov head (parent-dependent edges)
     6: SpecConfig("markov", B=1, m=8, K=16, N=24, L=4096, p_plant=0.85, markov_R=32, **_BIG),
+    # 'single' verified by sampling at temperature 1 (planted tokens carry ~0.88
+    # of the target's probability)
+    7: SpecConfig("sampled", B=1, m=8, K=16, N=24, L=4096, p_plant=0.85, temperature=1.0,
+                  sample_seed=0x5EED_0F_7EE5, plant_gap=10.0, **_BIG),
 }
 
 
@@ -229,7 +238,7 @@ def first_child_tokens(node_parent, node_rank, node_tok, n_nodes) -> torch.Tenso
 
 
 def plant_logits(logits: torch.Tensor, lat_tok, lat_score, node_depth, n_nodes, p: float,
-                 gen: torch.Generator, first_child=None) -> torch.Tensor:
+                 gen: torch.Generator, first_child=None, gap: float = 1.0) -> torch.Tensor:
     """Plant the drafter's first choice as the argmax of tree rows (in place).
 
     node_depth [B][T] and n_nodes [B] describe the tree the logits belong to.
@@ -238,6 +247,7 @@ def plant_logits(logits: torch.Tensor, lat_tok, lat_score, node_depth, n_nodes, 
     the top candidate of the next lattice position, or, with first_child
     ([B][T] from first_child_tokens: for drafters whose ranking depends on the
     parent), the row's rank-0 child in the tree (no plant where it is absent).
+    The planted logit is the row maximum + gap.
     """
     B, T, V = logits.shape
     m = lat_tok.shape[1]
@@ -254,7 +264,7 @@ def plant_logits(logits: torch.Tensor, lat_tok, lat_score, node_depth, n_nodes, 
         tok = torch.as_tensor(first_child).long().to(dev)
         ok = ok & (tok >= 0)
         tok = tok.clamp(min=0)
-    val = (logits.float().amax(dim=-1) + 1.0).to(logits.dtype)
+    val = (logits.float().amax(dim=-1) + gap).to(logits.dtype)
     bi, ti = torch.nonzero(ok, as_tuple=True)
     logits[bi, ti, tok[bi, ti]] = val[bi, ti]
     return logits

@@ -2,8 +2,10 @@
 step through the CPU oracle on identical seeded inputs, and compare.
 
 Contract (the tree-verify library's parity bar):
-  * bit-exact: tree topology/scores, argmax (except rows whose top-2 margin is
-    below 1e-3), accepted lengths/paths, emitted tokens, KV-cache rows,
+  * bit-exact: tree topology/scores, argmax -- or, at temperature > 0, each
+    row's draw -- (except rows whose top-2 margin is below 1e-3, where the
+    GPU's token must be within 1e-3 of the best and the walk is checked on the
+    GPU's token), accepted lengths/paths, emitted tokens, KV-cache rows,
     kv_len and the new root token;
   * rel-L2 <= 2e-3 (computed in float64 against the float64 oracle) for GDN
     outputs, attention outputs and committed GDN states.
@@ -53,7 +55,8 @@ def prepare(scfg: synth.SpecConfig, seed: int, kv_len=None, lat_edit=None):
     fc = (synth.first_child_tokens(tree["node_parent"], tree["node_rank"], tree["node_tok"],
                                    tree["n_nodes"]) if scfg.markov_R > 0 else None)
     synth.plant_logits(inp["logits"], inp["lat_tok"], inp["lat_score"], tree["node_depth"],
-                       tree["n_nodes"], scfg.p_plant, inp["plant_gen"], first_child=fc)
+                       tree["n_nodes"], scfg.p_plant, inp["plant_gen"], first_child=fc,
+                       gap=scfg.plant_gap)
     return inp, tree
 
 
@@ -114,7 +117,7 @@ def compare(scfg, inp, tree_o, st, req=None, attn_kv_heads=None, gdn_layers=None
     kvh = list(range(scfg.Hkv)) if attn_kv_heads is None else list(attn_kv_heads)
     qh = [g * G + i for g in kvh for i in range(G)]
     worst = 0.0
-    kv_len = inp["kv_len"]
+    kv_len = inp["kv_len"]              # read-only input of the step (restored below)
     for l in al:
         lay = inp["attn"][l]
         want = oracle.attn_tree(
@@ -130,16 +133,37 @@ def compare(scfg, inp, tree_o, st, req=None, attn_kv_heads=None, gdn_layers=None
         worst = max(worst, e)
     res["attn_rel_l2"] = worst
 
-    # ---- argmax + acceptance: bit-exact -----------------------------------------
-    am_o, margin = oracle.argmax(inp["logits"])
+    # ---- argmax (or draw) + acceptance: bit-exact -------------------------------------
+    kv_len = inp["kv_len"]
+    sampled = scfg.temperature > 0
+    if sampled:
+        am_o, margin = oracle.sample_rows(inp["logits"], nn, kv_len, scfg.temperature,
+                                          scfg.sample_seed)
+    else:
+        am_o, margin = oracle.argmax(inp["logits"])
     am_g = st.acc.argmax.cpu().numpy()
+    rows = am_o.copy()
+    exempt = 0
     for b in range(B):
         for t in range(T):
             if t >= nn[b]:
                 assert am_g[b, t] == -1
-            elif margin[b, t] >= MARGIN_EXEMPT:
-                assert am_g[b, t] == am_o[b, t], f"argmax row ({b},{t})"
-    acc_o = oracle.accept(tree_o, am_o, m)
+            elif am_g[b, t] != am_o[b, t]:
+                what = "draw" if sampled else "argmax"
+                assert margin[b, t] < MARGIN_EXEMPT, f"{what} row ({b},{t})"
+                g = int(am_g[b, t])
+                assert 0 <= g < scfg.V, f"{what} row ({b},{t}) out of range"
+                if sampled:                       # the GPU's token nearly ties the draw
+                    gaps = oracle.sample_gaps(inp["logits"][b, t], t, b, int(kv_len[b]),
+                                              scfg.temperature, scfg.sample_seed, g)
+                    assert max(gaps) < MARGIN_EXEMPT, f"draw row ({b},{t}) gaps {gaps}"
+                else:
+                    row = inp["logits"][b, t].float()
+                    assert float(row[g]) >= float(row.max()) - MARGIN_EXEMPT
+                rows[b, t] = g                    # check the walk on the GPU's token
+                exempt += 1
+    res["exempt_rows"] = exempt
+    acc_o = oracle.accept(tree_o, rows, m)
     np.testing.assert_array_equal(st.acc.accept_len.cpu().numpy(), acc_o["accept_len"])
     np.testing.assert_array_equal(st.acc.accept_nodes.cpu().numpy(), acc_o["accept_nodes"])
     np.testing.assert_array_equal(st.acc.out_tok.cpu().numpy(), acc_o["out_tok"])

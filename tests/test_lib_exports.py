@@ -100,3 +100,26 @@ def test_null_and_misaligned_pointers_rejected(lib):
     rc = lib.accept_and_commit(ctypes.byref(cfg), ctypes.byref(tree), ctypes.c_void_p(16), None,
                                None, ctypes.c_void_p(16), None)
     assert rc == binding.ST_EINVAL
+
+
+@pytest.mark.parametrize("temperature,reserved", [(0.0, 0), (-1.0, 0), (float("nan"), 0),
+                                                  (float("inf"), 0), (1.0, 3)])
+def test_sampling_parameters_rejected_before_launch(lib, temperature, reserved):
+    cfg = binding.make_cfg(synth.config(7))
+    tree = binding.SpecTree(*([16] * 7))
+    smp = binding.SpecSampling(temperature, reserved, 1)
+    p = ctypes.c_void_p(16)
+    rc = lib.accept_and_commit_sampled(ctypes.byref(cfg), ctypes.byref(tree), p, ctypes.byref(smp),
+                                       ctypes.byref(binding.SpecCommitIO(*([16] * 11))),
+                                       ctypes.byref(binding.SpecAccept(*([16] * 4))), p, None)
+    assert rc == binding.ST_EINVAL
+    rc = lib.spec_verify_step_sampled(ctypes.byref(cfg), p, p, ctypes.byref(smp),
+                                      ctypes.byref(tree),
+                                      ctypes.byref(binding.SpecStepIO(*([16] * 5))), p,
+                                      ctypes.byref(binding.SpecCommitIO(*([16] * 11))),
+                                      ctypes.byref(binding.SpecAccept(*([16] * 4))), p, None)
+    assert rc == binding.ST_EINVAL
+    assert lib.accept_and_commit_sampled(ctypes.byref(cfg), ctypes.byref(tree), p, None,
+                                         ctypes.byref(binding.SpecCommitIO(*([16] * 11))),
+                                         ctypes.byref(binding.SpecAccept(*([16] * 4))), p,
+                                         None) == binding.ST_EINVAL
