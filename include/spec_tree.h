@@ -358,9 +358,38 @@ int spec_verify_step_markov(const spec_cfg *cfg, const int32_t *lat_tok, const f
                             const spec_commit_io *io, const spec_accept *out, void *ws,
                             void *stream);
 
+/*
+ * spec_verify_step_persistent -- spec_verify_step whose argmax, acceptance,
+ * KV append and every GDN layer's verify + commit run as one persistent,
+ * cooperative launch after the tree and the attention layers.  Digest:
+ * technical novelty (states recomputed along the root path, no per-node
+ * snapshots) with the sections of the four calls.
+ *
+ * A GDN (layer, request, v-head) item keeps its fp32 state in shared memory
+ * through the verify, waits for its request's acceptance (a flag raised by the
+ * request's last argmax item, which also appends the KV rows and advances
+ * kv_len / root_tok) and writes the state after the accepted path,
+ *   h = A h0 + sum_s dec(p_s -> p_last) k_{p_s} c_{p_s}^T,
+ * over h0: the state is read from HBM once and written once.  Every argmax
+ * item precedes every GDN item in the work queue and never waits; each wait
+ * is bounded (about a second: SPEC_DEV_TIMEOUT, that state left uncommitted).
+ * Results equal spec_verify_step's within float rounding (the commit sums the
+ * path's rank-one terms instead of stepping the recurrence).
+ * Supported: bf16 I/O, d_k = d_v = 128, T <= 32, at least one GDN layer
+ * (else ST_EUNSUPPORTED).  Launches: spec_step_launches_persistent(cfg).
+ */
+int spec_verify_step_persistent(const spec_cfg *cfg, const int32_t *lat_tok,
+                                const float *lat_score, const spec_tree *tree,
+                                const spec_step_io *step, const void *logits,
+                                const spec_commit_io *io, const spec_accept *out, void *ws,
+                                void *stream);
+
 /* Number of kernel launches one spec_verify_step(cfg) call makes (host only;
  * -1 on an invalid cfg): for sizing graphs and counting launches. */
 int spec_step_launches(const spec_cfg *cfg);
+
+/* The same for spec_verify_step_persistent (-1 when unsupported). */
+int spec_step_launches_persistent(const spec_cfg *cfg);
 
 /* Copy the device status word into *host_status (host pointer) and wait for
  * `stream`.  Returns ST_OK, or ST_ECUDA if the copy failed. */

@@ -28,7 +28,8 @@ EXPORTS = ("spec_workspace_bytes", "spec_tree_build", "gdn_tree_verify", "attn_t
            "spec_status_string", "spec_abi_version", "attn_tree_verify_noalloc",
            "spec_wait_probe", "spec_step_launches", "spec_tree_build_ragged",
            "spec_verify_step_ragged", "spec_tree_build_markov", "spec_verify_step_markov",
-           "accept_and_commit_sampled", "spec_verify_step_sampled")
+           "accept_and_commit_sampled", "spec_verify_step_sampled",
+           "spec_verify_step_persistent", "spec_step_launches_persistent")
 SAMPLE_CHUNK = 4096
 
 _lock = threading.Lock()
@@ -116,6 +117,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                                      ctypes.POINTER(SpecStepIO), vp,
                                                      ctypes.POINTER(SpecCommitIO),
                                                      ctypes.POINTER(SpecAccept), vp, vp]
+            lib.spec_verify_step_persistent.argtypes = lib.spec_verify_step.argtypes
+            lib.spec_step_launches_persistent.argtypes = [cfgp]
             lib.spec_status_read.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
             lib.spec_status_clear.argtypes = [vp, vp]
             lib.spec_status_string.argtypes = [ctypes.c_int]
@@ -127,7 +130,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                       "attn_tree_verify_noalloc", "spec_wait_probe", "spec_step_launches",
                       "spec_tree_build_ragged", "spec_verify_step_ragged", "spec_tree_build_markov",
                       "spec_verify_step_markov", "accept_and_commit_sampled",
-                      "spec_verify_step_sampled", "accept_and_commit", "spec_verify_step", "spec_status_read",
+                      "spec_verify_step_sampled", "spec_verify_step_persistent",
+                      "spec_step_launches_persistent", "accept_and_commit", "spec_verify_step", "spec_status_read",
                       "spec_status_clear", "spec_abi_version"):
                 getattr(lib, n).restype = ctypes.c_int
             _lib = lib
@@ -340,6 +344,23 @@ def spec_verify_step(cfg, lat_tok, lat_score, tree: TreeBuffers, step: dict, log
         _ptr(lat_score, torch.float32, "lat_score"), ctypes.byref(tree.c()), ctypes.byref(sio),
         _ptr(logits, dt, "logits"), ctypes.byref(_commit_io(cfg, io)), ctypes.byref(out.c()),
         _ptr(ws, name="ws"), _stream(stream)))
+
+
+def spec_verify_step_persistent(cfg, lat_tok, lat_score, tree: TreeBuffers, step: dict, logits,
+                                io: dict, out: AcceptBuffers, ws, stream=None):
+    """spec_verify_step with the argmax, acceptance and every GDN layer's
+    verify + commit in one persistent launch."""
+    dt = _io_dtype(cfg)
+    sio = _step_io(cfg, step)
+    _check("spec_verify_step_persistent", load().spec_verify_step_persistent(
+        ctypes.byref(cfg), _ptr(lat_tok, torch.int32, "lat_tok"),
+        _ptr(lat_score, torch.float32, "lat_score"), ctypes.byref(tree.c()), ctypes.byref(sio),
+        _ptr(logits, dt, "logits"), ctypes.byref(_commit_io(cfg, io)), ctypes.byref(out.c()),
+        _ptr(ws, name="ws"), _stream(stream)))
+
+
+def spec_step_launches_persistent(cfg) -> int:
+    return int(load().spec_step_launches_persistent(ctypes.byref(cfg)))
 
 
 def spec_verify_step_sampled(cfg, lat_tok, lat_score, smp: SpecSampling, tree: TreeBuffers,

@@ -195,7 +195,7 @@ struct MarkovHead {
 // accept_and_commit_sampled (NULL: the argmax).
 int verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_score,
                 const int32_t* m_req, int node_budget, const MarkovHead* markov,
-                const spec_sampling* smp, const spec_tree* tree, const spec_step_io* step, const void* logits,
+                const spec_sampling* smp, bool persistent, const spec_tree* tree, const spec_step_io* step, const void* logits,
                 const spec_commit_io* io, const spec_accept* out, void* ws, void* stream) {
     int rc = check_cfg(cfg);
     if (rc) return rc;
@@ -263,6 +263,20 @@ int verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_sc
         attn_args(l, q, kt, vt, kc, vc, o);
         e = spec::launch_attn_partial(c, *tree, q, kt, vt, kc, vc, io->kv_len, ws, st, true, l & 1);
     }
+    if (persistent) {
+        // the last merge, then one cooperative launch for the argmax, the
+        // acceptance, the KV append and every GDN layer's verify + commit
+        if (na > 0 && e == cudaSuccess) {
+            const void *q, *kt, *vt, *kc, *vc;
+            void* o;
+            attn_args(na - 1, q, kt, vt, kc, vc, o);
+            e = spec::launch_attn_merge(c, *tree, o, ws, st, true, (na - 1) & 1, /*early=*/true);
+        }
+        if (e == cudaSuccess)
+            e = spec::launch_verify_commit(c, *tree, *step, logits, *io, *out, ws, st, true,
+                                           /*tree_wait=*/na == 0);
+        return cuda_rc(e);
+    }
     // the tree (or the budget selection) is two launches back only when an
     // attention layer sits between
     if (e == cudaSuccess)
@@ -297,6 +311,11 @@ int verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_sc
 
 extern "C" {
 
+int spec_step_launches_persistent(const spec_cfg* cfg) {
+    if (check_cfg(cfg) != ST_OK || !spec::verify_commit_supported(*cfg)) return -1;
+    return 1 + 2 * cfg->n_attn_layers + 1;  // tree, partials + merges, the fused launch
+}
+
 int spec_step_launches(const spec_cfg* cfg) {
     if (check_cfg(cfg) != ST_OK) return -1;
     const int na = cfg->n_attn_layers, ng = cfg->n_gdn_layers;
@@ -307,8 +326,18 @@ int spec_step_launches(const spec_cfg* cfg) {
 int spec_verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_score,
                      const spec_tree* tree, const spec_step_io* step, const void* logits,
                      const spec_commit_io* io, const spec_accept* out, void* ws, void* stream) {
-    return verify_step(cfg, lat_tok, lat_score, nullptr, -1, nullptr, nullptr, tree, step, logits,
-                       io, out, ws, stream);
+    return verify_step(cfg, lat_tok, lat_score, nullptr, -1, nullptr, nullptr, false, tree, step,
+                       logits, io, out, ws, stream);
+}
+
+int spec_verify_step_persistent(const spec_cfg* cfg, const int32_t* lat_tok,
+                                const float* lat_score, const spec_tree* tree,
+                                const spec_step_io* step, const void* logits,
+                                const spec_commit_io* io, const spec_accept* out, void* ws,
+                                void* stream) {
+    if (check_cfg(cfg) == ST_OK && !spec::verify_commit_supported(*cfg)) return ST_EUNSUPPORTED;
+    return verify_step(cfg, lat_tok, lat_score, nullptr, -1, nullptr, nullptr, true, tree, step,
+                       logits, io, out, ws, stream);
 }
 
 int spec_verify_step_sampled(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_score,
@@ -317,8 +346,8 @@ int spec_verify_step_sampled(const spec_cfg* cfg, const int32_t* lat_tok, const 
                              const spec_commit_io* io, const spec_accept* out, void* ws,
                              void* stream) {
     if (!temperature_ok(smp)) return ST_EINVAL;
-    return verify_step(cfg, lat_tok, lat_score, nullptr, -1, nullptr, smp, tree, step, logits, io,
-                       out, ws, stream);
+    return verify_step(cfg, lat_tok, lat_score, nullptr, -1, nullptr, smp, false, tree, step,
+                       logits, io, out, ws, stream);
 }
 
 int spec_verify_step_markov(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_base,
@@ -326,16 +355,16 @@ int spec_verify_step_markov(const spec_cfg* cfg, const int32_t* lat_tok, const f
                             const spec_step_io* step, const void* logits, const spec_commit_io* io,
                             const spec_accept* out, void* ws, void* stream) {
     const MarkovHead head{W1, W2, R};
-    return verify_step(cfg, lat_tok, lat_base, nullptr, -1, &head, nullptr, tree, step, logits, io,
-                       out, ws, stream);
+    return verify_step(cfg, lat_tok, lat_base, nullptr, -1, &head, nullptr, false, tree, step,
+                       logits, io, out, ws, stream);
 }
 
 int spec_verify_step_ragged(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_score,
                             const int32_t* m_req, int node_budget, const spec_tree* tree,
                             const spec_step_io* step, const void* logits, const spec_commit_io* io,
                             const spec_accept* out, void* ws, void* stream) {
-    return verify_step(cfg, lat_tok, lat_score, m_req, node_budget, nullptr, nullptr, tree, step,
-                       logits, io, out, ws, stream);
+    return verify_step(cfg, lat_tok, lat_score, m_req, node_budget, nullptr, nullptr, false, tree,
+                       step, logits, io, out, ws, stream);
 }
 
 int spec_status_read(const void* ws, uint32_t* host_status, void* stream) {

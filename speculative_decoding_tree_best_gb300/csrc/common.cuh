@@ -89,6 +89,8 @@ struct WsLayout {
     size_t samp_off;       // float2 [B][T][n_vchunks]: (max, sum of exp) per vocabulary chunk
     size_t samp_tok_off;   // int32  [B][T]: the target's draw of each row
     size_t row_ticket_off; // uint32 [B][T]: chunk-scan CTAs finished per row
+    size_t fused_off;      // uint32 [2 + 2B]: persistent step's work queue, CTAs out,
+                           // acceptance flags [B], GDN items committed [B]
     size_t total;
     int n_split;           // cache chunks per (request, kv-head)
     int chunk;             // cache rows per chunk
@@ -158,6 +160,8 @@ static inline WsLayout ws_layout(const spec_cfg& c, int num_sms = 152) {
     off = align_up(off + sizeof(int32_t) * (size_t)rows, 256);
     w.row_ticket_off = off;
     off = align_up(off + sizeof(uint32_t) * (size_t)rows, 256);
+    w.fused_off = off;
+    off = align_up(off + sizeof(uint32_t) * (2 + 2 * (size_t)c.B), 256);
     w.total = off;
     return w;
 }

@@ -76,6 +76,16 @@ cudaError_t launch_sample_accept(const spec_cfg& c, const spec_tree& t, const vo
                                  bool tree_early);
 cudaError_t launch_commit(const spec_cfg& c, const spec_commit_io& io, const spec_accept& out,
                           void* ws, cudaStream_t st, bool pdl, bool early);
+// The fused, persistent verify + commit (bf16, d_k = d_v = 128, T <= 32, at
+// least one GDN layer: verify_commit_supported, a host-only shape check):
+// argmax + acceptance + KV append and every GDN layer's verify + commit in one
+// cooperative launch; tree_wait: the tree is the previous launch.
+bool verify_commit_supported(const spec_cfg& c);
+cudaError_t launch_verify_commit(const spec_cfg& c, const spec_tree& t, const spec_step_io& step,
+                                 const void* logits, const spec_commit_io& io,
+                                 const spec_accept& out, void* ws, cudaStream_t st, bool pdl,
+                                 bool tree_wait);
+
 // temperature: nullptr for the argmax, else the sampled acceptance.
 cudaError_t launch_accept_commit(const spec_cfg& c, const spec_tree& t, const void* logits,
                                  const spec_commit_io& io, const spec_accept& out, void* ws,

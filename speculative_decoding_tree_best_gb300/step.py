@@ -33,8 +33,9 @@ def stack_inputs(inp: dict, device="cuda") -> dict:
 class VerifyStep:
     """Buffers and calls of one verify step for a synthetic workload."""
 
-    def __init__(self, scfg: SpecConfig, x: dict, device="cuda"):
+    def __init__(self, scfg: SpecConfig, x: dict, device="cuda", persistent: bool = False):
         self.scfg = scfg
+        self.persistent = persistent
         self.cfg = binding.make_cfg(scfg)
         self.x = x
         self.device = device
@@ -103,7 +104,13 @@ class VerifyStep:
         step = dict(gdn_q=x["gdn_q"], gdn_o=self.gdn_o if self.cfg.n_gdn_layers else None,
                     gdn_c=None, attn_q=x["attn_q"],
                     attn_o=self.attn_o if self.cfg.n_attn_layers else None)
-        if self.scfg.temperature > 0:
+        if self.persistent:
+            if self.scfg.markov_R > 0 or self.scfg.ragged or self.scfg.temperature > 0:
+                raise ValueError("the persistent step takes the plain lattice and the argmax")
+            binding.spec_verify_step_persistent(self.cfg, x["lat_tok"], x["lat_score"], self.tree,
+                                                step, x["logits"], self.commit_io(), self.acc,
+                                                self.ws, stream)
+        elif self.scfg.temperature > 0:
             if self.scfg.markov_R > 0 or self.scfg.ragged:
                 raise ValueError("the fused sampled step takes the plain lattice")
             binding.spec_verify_step_sampled(self.cfg, x["lat_tok"], x["lat_score"],
@@ -123,5 +130,7 @@ class VerifyStep:
 
     @property
     def launches_per_step(self) -> int:
+        if self.persistent:
+            return binding.spec_step_launches_persistent(self.cfg)
         # the shared budget adds one launch (the selection) to the step
         return binding.spec_step_launches(self.cfg) + (1 if self.scfg.budget >= 0 else 0)

@@ -60,11 +60,11 @@ def prepare(scfg: synth.SpecConfig, seed: int, kv_len=None, lat_edit=None):
     return inp, tree
 
 
-def run_gpu(scfg, inp, calls=False):
-    """One step on the GPU: one spec_verify_step call, or (calls=True) the four
-    single-operation calls."""
+def run_gpu(scfg, inp, calls=False, persistent=False):
+    """One step on the GPU: one spec_verify_step call (the persistent variant
+    with persistent=True), or (calls=True) the four single-operation calls."""
     x = stack_inputs(inp, "cuda")
-    st = VerifyStep(scfg, x)
+    st = VerifyStep(scfg, x, persistent=persistent)
     if calls:
         st.run_calls()
     else:
@@ -213,8 +213,9 @@ def check_case(scfg, seed, **kw):
     kv_len = kw.pop("kv_len", None)
     lat_edit = kw.pop("lat_edit", None)
     calls = kw.pop("calls", False)
+    persistent = kw.pop("persistent", False)
     inp, tree_o = prepare(scfg, seed, kv_len=kv_len, lat_edit=lat_edit)
-    st = run_gpu(scfg, inp, calls=calls)
+    st = run_gpu(scfg, inp, calls=calls, persistent=persistent)
     res = compare(scfg, inp, tree_o, st, **kw)
     res["status"] = __import__("speculative_decoding_tree_best_gb300.binding",
                                fromlist=["x"]).spec_status_read(st.ws)

@@ -115,3 +115,13 @@ def test_multi_layer_stack_small():
     cfg = synth.config(4).replace(B=2, n_gdn=3, n_attn=2, L=257, V=3000)
     parity.check_case(cfg, 9)
     parity.check_case(cfg, 10, calls=True)
+
+
+def test_full_stack_sampled():
+    """The 64-layer stack at full size (8 requests, 48 GDN + 16 attention
+    layers, KV 8192) in the launch configuration the bench times: every tree,
+    argmax, acceptance and kv_len bit for bit; the floats of the first and last
+    layer of each kind, for two requests and one kv-head group."""
+    r = parity.check_case(synth.config(4), 0, req=[0, 5], attn_kv_heads=[3], gdn_layers=[0, 47],
+                          attn_layers=[0, 15])
+    assert r["status"] == 0 and min(r["tau"]) >= 1

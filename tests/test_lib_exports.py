@@ -123,3 +123,19 @@ def test_sampling_parameters_rejected_before_launch(lib, temperature, reserved):
                                          ctypes.byref(binding.SpecCommitIO(*([16] * 11))),
                                          ctypes.byref(binding.SpecAccept(*([16] * 4))), p,
                                          None) == binding.ST_EINVAL
+
+
+def test_persistent_step_shapes_and_launches(lib):
+    assert binding.spec_step_launches_persistent(binding.make_cfg(synth.config(1))) == 4
+    assert binding.spec_step_launches_persistent(binding.make_cfg(synth.config(4))) == 1 + 32 + 1
+    for bad in (synth.config(0), synth.config(2), synth.config(1).replace(n_gdn=0)):
+        cfg = binding.make_cfg(bad)                # fp32 / T > 32 / no GDN layer
+        assert lib.spec_step_launches_persistent(ctypes.byref(cfg)) == -1
+        p = ctypes.c_void_p(16)
+        rc = lib.spec_verify_step_persistent(ctypes.byref(cfg), p, p,
+                                             ctypes.byref(binding.SpecTree(*([16] * 7))),
+                                             ctypes.byref(binding.SpecStepIO(*([16] * 5))), p,
+                                             ctypes.byref(binding.SpecCommitIO(*([16] * 11))),
+                                             ctypes.byref(binding.SpecAccept(*([16] * 4))), p,
+                                             None)
+        assert rc == binding.ST_EUNSUPPORTED
