@@ -4,12 +4,15 @@
 // Digest "SpecPilot ...": prerequisites / draft-tree verification (one target
 // pass verifies the tree; every node sees only its ancestors).
 //
-// One CTA = one (request, kv-head, 128-row query tile, key chunk).  The query
-// tile holds the G = Hq/Hkv q-heads of the group for 128/G consecutive tree
-// rows (row r = node * G + head_in_group), loaded once by TMA.  The chunk's
-// keys stream through two-stage rings of 128-key K and V blocks (TMA, 128-byte
-// swizzle); a K stage is refilled as soon as its S product is done, a V stage
-// once its PV product is done.  Per block j:
+// A work unit = one (request, kv-head, 128-row query tile, key chunk) that
+// holds keys.  The launch is persistent: one CTA per SM (at most), each running
+// every grid-th unit, with its pipelines running from one unit into the next.
+// The query tile holds the G = Hq/Hkv q-heads of the group for 128/G
+// consecutive tree rows (row r = node * G + head_in_group), loaded by TMA once
+// the previous unit's S products are done.  The keys stream through two-stage
+// rings of 128-key K and V blocks (TMA, 128-byte swizzle) numbered across the
+// CTA's units; a K stage is refilled as soon as its S product is done, a V
+// stage once its PV product is done.  Per block j:
 //    S_j = Q K_j^T          tcgen05.mma (bf16, exact products), fp32 in tensor
 //                           memory, two S buffers so S_{j+1} is ready while
 //                           the softmax works on S_j
@@ -69,10 +72,14 @@ constexpr uint32_t OFF_P = OFF_V + 2 * TILE_BYTES;               // fp16 P, K-ma
 constexpr uint32_t OFF_RED = OFF_P + TILE_BYTES;                 // float [2][NWG][128] row maxima
 constexpr uint32_t OFF_REDL = OFF_RED + 2 * NWG * 128 * 4;       // float [NWG][128] row sums
 constexpr uint32_t OFF_BAR = OFF_REDL + NWG * 128 * 4;
-enum { B_Q = 0, B_KF, B_VF = B_KF + 2, B_KE = B_VF + 2, B_VE = B_KE + 2, B_SFULL = B_VE + 2,
-       B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_PVDONE, NBARS };
-constexpr uint32_t SMEM_BYTES = OFF_BAR + NBARS * 8 + 32 + 1024;  // + slack for alignment
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+enum { B_Q = 0, B_QE, B_KF, B_VF = B_KF + 2, B_KE = B_VF + 2, B_VE = B_KE + 2,
+       B_SFULL = B_VE + 2, B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_PVDONE, NBARS };
+constexpr uint32_t OFF_UNITS = OFF_BAR + NBARS * 8 + 32;         // int [4 B + 1]: the unit map
+constexpr uint32_t SMEM_LIMIT = 227 * 1024;
+
+__host__ __device__ constexpr uint32_t smem_bytes(int B) {
+    return OFF_UNITS + 4u * (4u * (uint32_t)B + 1u) + 1024;      // + slack for alignment
+}
 
 // Barrier over `nthreads` threads with id `id` that also ANDs a predicate, so
 // a pair of warps leaves a loop together.
@@ -115,6 +122,86 @@ struct TcParams {
     WsLayout w;
 };
 
+// The work units of one launch: the (request, kv-head, query tile, key chunk)
+// tiles that hold keys, longest first: the full cache chunks (request by
+// request), then the partial last chunks (by length, longest first), then the
+// tree chunks (which wait for the tree).  Every role of every CTA decodes the
+// same numbering from the per-request counts in shared memory.  Round r of
+// the grid takes units [r grid, (r + 1) grid), dealt to the CTAs in
+// alternating directions (a snake), which evens out the CTAs' loads; each
+// CTA's K/V rings run across its units' boundaries.
+struct Units {
+    const int* fpre;    // [B + 1]: full chunks of requests < b
+    const int* len;     // [B]: kv_len clamped to [0, Lmax]
+    const int* pord;    // [requests with a partial chunk]: longest partial first
+    int B, hg, n_mt, chunk, T, grid;
+    int n_full, n_part, total;   // units per region (x hg), all units
+
+    // the largest b with pre[b] <= q (pre non-decreasing, pre[0] = 0 <= q < pre[B])
+    __device__ __forceinline__ static int find(const int* pre, int B, int q) {
+        int lo = 0, hi = B;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (pre[mid] <= q) lo = mid;
+            else hi = mid;
+        }
+        return lo;
+    }
+    // the k-th unit of CTA i; the last round runs forwards, so its units go
+    // to the lowest CTAs (the highest are placed last: behind, say, the CTA
+    // of the launch before)
+    __device__ __forceinline__ int unit_of(int i, int k) const {
+        const int last = (total - 1) / grid;
+        return k * grid + (((last - k) & 1) ? grid - 1 - i : i);
+    }
+    // how many units CTA i runs
+    __device__ __forceinline__ int count(int i) const {
+        if (total <= 0) return 0;
+        const int last = (total - 1) / grid, rem = total - last * grid;
+        return last + (i < rem ? 1 : 0);
+    }
+};
+
+struct Unit {
+    int b, g, mt, ch;    // ch = n_split for the tree chunk
+    int k0, k1, nblk;
+    bool tree;
+};
+
+__device__ __forceinline__ Unit decode(const Units& U, int u, int n_split) {
+    Unit r;
+    int rem, q;
+    if (u < U.n_full) {
+        q = u / U.hg;
+        rem = u % U.hg;
+        r.b = Units::find(U.fpre, U.B, q);
+        r.ch = q - U.fpre[r.b];
+        r.k0 = r.ch * U.chunk;
+        r.k1 = r.k0 + U.chunk;
+        r.tree = false;
+    } else if (u < U.n_full + U.n_part) {
+        q = (u - U.n_full) / U.hg;
+        rem = (u - U.n_full) % U.hg;
+        r.b = U.pord[q];
+        r.ch = U.fpre[r.b + 1] - U.fpre[r.b];
+        r.k0 = r.ch * U.chunk;
+        r.k1 = U.len[r.b];
+        r.tree = false;
+    } else {
+        const int t = u - U.n_full - U.n_part;
+        r.b = t / U.hg;
+        rem = t % U.hg;
+        r.ch = n_split;
+        r.k0 = 0;
+        r.k1 = U.T;
+        r.tree = true;
+    }
+    r.g = rem / U.n_mt;
+    r.mt = rem % U.n_mt;
+    r.nblk = (r.k1 - r.k0 + NB - 1) / NB;
+    return r;
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mkc,
                 const __grid_constant__ CUtensorMap mvc, const __grid_constant__ CUtensorMap mkt,
@@ -127,33 +214,29 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* issued_k = reinterpret_cast<int*>(tmem_slot + 2);       // K blocks the producer issued
     int* issued_v = reinterpret_cast<int*>(tmem_slot + 3);       // V blocks the producer issued
+    int* issued_q = reinterpret_cast<int*>(tmem_slot + 4);       // Q tiles the producer issued
+    int* n_partial = reinterpret_cast<int*>(tmem_slot + 5);      // requests with a partial chunk
+    int* upre = reinterpret_cast<int*>(sm + OFF_UNITS);   // fpre [B+1] | len [B] | pnb [B] | pord [B]
 
     const spec_cfg& c = prm.c;
     const WsLayout& w = prm.w;
-    const int T = c.N + 1, G = c.Hq / c.Hkv;
-    const int ch = blockIdx.x, g = blockIdx.y % c.Hkv, mt = blockIdx.y / c.Hkv, b = blockIdx.z;
-    const bool tree_chunk = ch == w.n_split;
-    int L = prm.kv_len[b];
-    L = L < 0 ? 0 : (L > c.Lmax ? c.Lmax : L);
-    int k0 = 0, k1 = T;
-    if (!tree_chunk) {
-        k0 = ch * w.chunk;
-        if (k0 >= L) {
-            // no cache rows here: leave an empty partial (max -inf, sum 0) so the
-            // merge needs no kv_len, and exit (nothing allocated yet)
-            float2* wML = ws_ptr<float2>(prm.ws, w.attn_ml_off);
-            const size_t tile = (((size_t)b * c.Hkv + g) * w.n_mt + mt) * w.n_chunks + ch;
-            for (int row = threadIdx.x; row < BM; row += NTHREADS)
-                if (mt * BM + row < G * T) wML[tile * BM + row] = make_float2(-INFINITY, 0.0f);
-            return;
-        }
-        k1 = min(k0 + w.chunk, L);
-    }
-    const int nblk = (k1 - k0 + NB - 1) / NB;
+    const int T = c.N + 1, G = c.Hq / c.Hkv, B = c.B;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    Units U;
+    int* pnb = upre + (B + 1) + B;                              // partial chunk's blocks, or 0
+    U.fpre = upre;
+    U.len = upre + (B + 1);
+    U.pord = pnb + B;
+    U.B = B;
+    U.grid = gridDim.x;
+    U.n_mt = w.n_mt;
+    U.hg = c.Hkv * w.n_mt;
+    U.chunk = w.chunk;
+    U.T = T;
 
     if (threadIdx.x == 0) {
         mbar_init(&bar[B_Q], 1);
+        mbar_init(&bar[B_QE], 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bar[B_KF + s], 1);
             mbar_init(&bar[B_VF + s], 1);
@@ -167,59 +250,129 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         *abort_flag = 0;
         *issued_k = 0;
         *issued_v = 0;
+        *issued_q = 0;
         fence_mbar_init();
     }
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&mq);
-        tma_prefetch_desc(tree_chunk ? &mkt : &mkc);
-        tma_prefetch_desc(tree_chunk ? &mvt : &mvc);
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&mq);
+            tma_prefetch_desc(&mkc);
+            tma_prefetch_desc(&mvc);
+            tma_prefetch_desc(&mkt);
+            tma_prefetch_desc(&mvt);
+        }
+    } else if (warp == 2) {
+        // per-request full chunks and their prefix sums, 32 requests at a time;
+        // the requests with a partial last chunk, longest first (stable)
+        int cf = 0;
+        uint32_t present = 0;                            // partial lengths in blocks present
+        if (lane == 0) upre[0] = 0;
+        for (int b0 = 0; b0 < B; b0 += 32) {
+            const int b = b0 + lane;
+            int L = 0;
+            if (b < B) {
+                L = prm.kv_len[b];
+                L = L < 0 ? 0 : (L > c.Lmax ? c.Lmax : L);
+            }
+            int f = b < B ? L / w.chunk : 0;
+            const int pn = (L % w.chunk + NB - 1) / NB;  // 0 .. chunk / NB
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int fo = __shfl_up_sync(0xffffffffu, f, o);
+                if (lane >= o) f += fo;
+            }
+            if (b < B) {
+                upre[b + 1] = cf + f;
+                upre[B + 1 + b] = L;
+                pnb[b] = pn;
+                present |= 1u << pn;
+            }
+            cf += __shfl_sync(0xffffffffu, f, 31);
+        }
+        present = __reduce_or_sync(0xffffffffu, present) & ~1u;
+        __syncwarp();
+        int pos = 0;
+        while (present) {
+            const int v = 31 - __clz(present);
+            present &= ~(1u << v);
+            for (int b0 = 0; b0 < B; b0 += 32) {
+                const int b = b0 + lane;
+                const bool hit = b < B && pnb[b] == v;
+                const uint32_t m = __ballot_sync(0xffffffffu, hit);
+                if (hit) pnb[B + pos + __popc(m & ((1u << lane) - 1u))] = b;
+                pos += __popc(m);
+            }
+        }
+        if (lane == 0) *n_partial = pos;
+    } else if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
     }
-    if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tO = tmem + 256;                  // S buffers at +0 and +128
+    U.n_full = U.fpre[B] * U.hg;
+    U.n_part = n_partial[0] * U.hg;
+    U.total = U.n_full + U.n_part + B * U.hg;
+    const int nu = U.count(blockIdx.x);
+
     bool ok = true;
-    const CUtensorMap* mk = tree_chunk ? &mkt : &mkc;
-    const CUtensorMap* mv = tree_chunk ? &mvt : &mvc;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ Q and the K ring
+        // ------------------------------------------------------------ Q tiles and the K ring
         if (lane == 0) {
-            mbar_arrive_expect_tx(&bar[B_Q], TILE_BYTES);
-            const int node0 = mt * (BM / G);
-            for (int h = 0; h < 2; ++h)
-                tma_load_3d(sm + OFF_Q + h * HALF_BYTES, &mq, &bar[B_Q], h * 64, g * G,
-                            b * T + node0);
-            for (int j = 0; j < nblk; ++j) {
-                const int s = j & 1;
-                // stage s is free once S_{j-2} is done
-                if (j >= 2 && !mbar_wait(&bar[B_KE + s], ((j >> 1) - 1) & 1, abort_flag)) {
-                    ok = false;
-                    break;
+            int J = 0;                                   // global block index of this CTA
+            for (int k = 0; k < nu && ok; ++k) {
+                const Unit un = decode(U, U.unit_of(blockIdx.x, k), w.n_split);
+                const CUtensorMap* mk = un.tree ? &mkt : &mkc;
+                for (int j = 0; j < un.nblk; ++j, ++J) {
+                    const int s = J & 1;
+                    // stage s is free once S_{J-2} is done
+                    if (J >= 2 && !mbar_wait(&bar[B_KE + s], ((J >> 1) - 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bar[B_KF + s], TILE_BYTES);
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_4d(sm + OFF_K + s * TILE_BYTES + h * HALF_BYTES, mk,
+                                    &bar[B_KF + s], h * 64, un.g, un.k0 + j * NB, un.b);
+                    *issued_k = J + 1;
+                    if (j == 0) {
+                        // the Q tile is free once the previous unit's S products are done
+                        if (k >= 1 && !mbar_wait(&bar[B_QE], (k - 1) & 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&bar[B_Q], TILE_BYTES);
+                        const int node0 = un.mt * (BM / G);
+                        for (int h = 0; h < 2; ++h)
+                            tma_load_3d(sm + OFF_Q + h * HALF_BYTES, &mq, &bar[B_Q], h * 64,
+                                        un.g * G, un.b * T + node0);
+                        *issued_q = k + 1;
+                    }
                 }
-                mbar_arrive_expect_tx(&bar[B_KF + s], TILE_BYTES);
-                for (int h = 0; h < 2; ++h)
-                    tma_load_4d(sm + OFF_K + s * TILE_BYTES + h * HALF_BYTES, mk, &bar[B_KF + s],
-                                h * 64, g, k0 + j * NB, b);
-                *issued_k = j + 1;
             }
         }
     } else if (warp == 2) {
         // ------------------------------------------------------------ the V ring
         if (lane == 0) {
-            for (int j = 0; j < nblk; ++j) {
-                const int s = j & 1;
-                // stage s is free once PV_{j-2} is done
-                if (j >= 2 && !mbar_wait(&bar[B_VE + s], ((j >> 1) - 1) & 1, abort_flag)) {
-                    ok = false;
-                    break;
+            int J = 0;
+            for (int k = 0; k < nu && ok; ++k) {
+                const Unit un = decode(U, U.unit_of(blockIdx.x, k), w.n_split);
+                const CUtensorMap* mv = un.tree ? &mvt : &mvc;
+                for (int j = 0; j < un.nblk; ++j, ++J) {
+                    const int s = J & 1;
+                    // stage s is free once PV_{J-2} is done
+                    if (J >= 2 && !mbar_wait(&bar[B_VE + s], ((J >> 1) - 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bar[B_VF + s], TILE_BYTES);
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_4d(sm + OFF_V + s * TILE_BYTES + h * HALF_BYTES, mv,
+                                    &bar[B_VF + s], h * 64, un.g, un.k0 + j * NB, un.b);
+                    *issued_v = J + 1;
                 }
-                mbar_arrive_expect_tx(&bar[B_VF + s], TILE_BYTES);
-                for (int h = 0; h < 2; ++h)
-                    tma_load_4d(sm + OFF_V + s * TILE_BYTES + h * HALF_BYTES, mv, &bar[B_VF + s],
-                                h * 64, g, k0 + j * NB, b);
-                *issued_v = j + 1;
             }
         }
     } else if (warp == 1) {
@@ -229,12 +382,18 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
             const uint32_t idPV = idesc_f16_f32(128, HD, false, true);
             const uint32_t q_s = smem_u32(sm + OFF_Q);
             const uint32_t p_s = smem_u32(sm + OFF_P);
-            // S_i = Q K_i^T into S buffer i & 1
-            auto issue_s = [&](int i) -> bool {
-                const int s = i & 1;
-                if (!mbar_wait(&bar[B_KF + s], (i >> 1) & 1, abort_flag)) return false;
-                // the softmax has read S_{i-2} out of this buffer
-                if (i >= 2 && !mbar_wait(&bar[B_SFREE + s], ((i >> 1) - 1) & 1, abort_flag))
+            int nj = 0;                                  // blocks of all this CTA's units
+            for (int k = 0; k < nu; ++k) nj += decode(U, U.unit_of(blockIdx.x, k), w.n_split).nblk;
+            // the S cursor: unit ks, block js of it, global block JS
+            int ks = 0, js = 0, JS = 0;
+            int s_nblk = nu > 0 ? decode(U, U.unit_of(blockIdx.x, 0), w.n_split).nblk : 0;
+            // S_JS = Q K_JS^T into S buffer JS & 1, then advance the cursor
+            auto issue_s = [&]() -> bool {
+                const int s = JS & 1;
+                if (js == 0 && !mbar_wait(&bar[B_Q], ks & 1, abort_flag)) return false;
+                if (!mbar_wait(&bar[B_KF + s], (JS >> 1) & 1, abort_flag)) return false;
+                // the softmax has read S_{JS-2} out of this buffer
+                if (JS >= 2 && !mbar_wait(&bar[B_SFREE + s], ((JS >> 1) - 1) & 1, abort_flag))
                     return false;
                 tc_fence_after();
                 const uint32_t k_s = smem_u32(sm + OFF_K + s * TILE_BYTES);
@@ -246,26 +405,47 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
                 }
                 mma_commit(&bar[B_SFULL + s]);
                 mma_commit(&bar[B_KE + s]);
+                ++JS;
+                if (++js == s_nblk) {                    // the unit's last S: its Q tile is free
+                    mma_commit(&bar[B_QE]);
+                    js = 0;
+                    if (++ks < nu) s_nblk = decode(U, U.unit_of(blockIdx.x, ks), w.n_split).nblk;
+                }
                 return true;
             };
-            ok = mbar_wait(&bar[B_Q], 0, abort_flag);
-            if (ok) ok = issue_s(0);
-            if (ok && nblk > 1) ok = issue_s(1);
-            for (int j = 0; j < nblk && ok; ++j) {
-                const int s = j & 1;
-                // P_j written and V_j converted to fp16 by the softmax threads
-                if (!mbar_wait(&bar[B_PFULL], j & 1, abort_flag)) { ok = false; break; }
+            // S runs up to two blocks ahead of PV (two S buffers), except that a
+            // unit's first S, which waits for that unit's Q tile, is not issued
+            // while the PV of the block before it is still pending
+            auto catch_up = [&](int jp_done) -> bool {
+                while (JS < nj && JS <= jp_done + 2) {
+                    if (js == 0 && JS == jp_done + 2) break;
+                    if (!issue_s()) return false;
+                }
+                return true;
+            };
+            ok = catch_up(-1);
+            // the PV cursor: block jp of the current unit, global block J
+            int kp = 0, jp = 0;
+            int p_nblk = nu > 0 ? decode(U, U.unit_of(blockIdx.x, 0), w.n_split).nblk : 0;
+            for (int J = 0; J < nj && ok; ++J) {
+                const int s = J & 1;
+                // P_J written and V_J converted to fp16 by the softmax threads
+                if (!mbar_wait(&bar[B_PFULL], J & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t v_s = smem_u32(sm + OFF_V + s * TILE_BYTES);
 #pragma unroll
                 for (int k = 0; k < NB / 16; ++k) {
                     const uint32_t offp = (k >> 2) * HALF_BYTES + (k & 3) * 32;
                     mma_f16(tO, sdesc_sw128(p_s + offp, 16, 1024),
-                            sdesc_sw128(v_s + k * 2048, HALF_BYTES, 1024), idPV, (j > 0 || k > 0));
+                            sdesc_sw128(v_s + k * 2048, HALF_BYTES, 1024), idPV, (jp > 0 || k > 0));
                 }
                 mma_commit(&bar[B_PVDONE]);
                 mma_commit(&bar[B_VE + s]);
-                if (j + 2 < nblk) ok = issue_s(j + 2);
+                ok = catch_up(J);
+                if (++jp == p_nblk) {
+                    jp = 0;
+                    if (++kp < nu) p_nblk = decode(U, U.unit_of(blockIdx.x, kp), w.n_split).nblk;
+                }
             }
         }
     } else {
@@ -279,141 +459,168 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         const int wg = (warp - NROLE) >> 2;
         const int lg = warp & 3;
         const int row = lg * 32 + lane;
-        const int r = mt * BM + row;                     // query row within (request, kv-head)
-        const int x = r / G;
         const uint32_t lane_addr = static_cast<uint32_t>(lg * 32) << 16;
         const int cb0 = wg * CPT;                        // first column of this thread
         const int grp_bar = 1 + lg;
         constexpr int GRP_THREADS = 32 * NWG;
         float* red = reinterpret_cast<float*>(sm + OFF_RED);
         float* redl = reinterpret_cast<float*>(sm + OFF_REDL);
-        uint32_t visbits = 0xffffffffu;                  // tree chunk: visible keys among my columns
-        if (tree_chunk) {
-            pdl_wait();          // the tree may come from the launch just before
-            int nn = prm.tree.n_nodes[b];
-            nn = nn < 1 ? 1 : (nn > T ? T : nn);
-            visbits = 0u;
-            if (x < nn) {
-                const uint64_t a = prm.tree.node_anc[2 * ((size_t)b * T + x) + (cb0 >> 6)];
-                visbits = static_cast<uint32_t>(a >> (cb0 & 63));
-                if (cb0 + CPT > nn) visbits &= (nn - cb0 <= 0) ? 0u : (0xffffffffu >> (32 - (nn - cb0)));
-            }
-        }
         const float sl2 = 1.4426950408889634f * rsqrtf((float)HD);   // log2(e) / sqrt(D)
-        float m_ref = -INFINITY, l = 0.0f;                // m_ref in raw score units
         unsigned char* pbuf = sm + OFF_P;
         float sv[CPT];
-        for (int j = 0; j < nblk; ++j) {
-            const int s = j & 1;
-            bool w_ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL + s], (j >> 1) & 1, abort_flag));
-            float pm0 = -INFINITY, pm1 = -INFINITY, pm2 = -INFINITY, pm3 = -INFINITY;
-            if (w_ok) {
-                tc_fence_after();
-                tmem_ld32(tmem + s * 128 + lane_addr + cb0, sv);
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(&bar[B_SFREE + s]);
-                // visibility: all columns of a full cache block are visible
-                uint32_t vis = visbits;
-                if (!tree_chunk) {
-                    const int nvis = k1 - (k0 + j * NB + cb0);
-                    vis = nvis >= CPT ? 0xffffffffu : (nvis <= 0 ? 0u : (0xffffffffu >> (32 - nvis)));
+        {
+            // chunks past a request's KV length leave an empty partial (max
+            // -inf, sum 0), so the merge needs no kv_len: one softmax warp per
+            // (request, kv-head, tile, chunk), strided over the grid, while the
+            // first loads are in flight
+            float2* wML = ws_ptr<float2>(prm.ws, w.attn_ml_off);
+            const int n_tiles = B * U.hg * w.n_split;
+            for (int t = (int)blockIdx.x * (NSOFT / 32) + (st >> 5); t < n_tiles;
+                 t += (int)gridDim.x * (NSOFT / 32)) {
+                const int ch = t % w.n_split, bh = t / w.n_split;   // bh = b hg + g n_mt + mt
+                if (ch * w.chunk < U.len[bh / U.hg]) continue;
+                const size_t tile = (size_t)bh * w.n_chunks + ch;
+                const int mt = bh % w.n_mt;
+                for (int r = lane; r < BM; r += 32)
+                    if (mt * BM + r < G * T) wML[tile * BM + r] = make_float2(-INFINITY, 0.0f);
+            }
+        }
+        int J = 0;                                       // global block index
+        for (int k = 0; k < nu && ok; ++k) {
+            const Unit un = decode(U, U.unit_of(blockIdx.x, k), w.n_split);
+            const int r = un.mt * BM + row;              // query row within (request, kv-head)
+            const int x = r / G;
+            uint32_t visbits = 0xffffffffu;              // tree chunk: visible keys among my columns
+            if (un.tree) {
+                pdl_wait();      // the tree may come from the launch just before
+                int nn = prm.tree.n_nodes[un.b];
+                nn = nn < 1 ? 1 : (nn > T ? T : nn);
+                visbits = 0u;
+                if (x < nn) {
+                    const uint64_t a = prm.tree.node_anc[2 * ((size_t)un.b * T + x) + (cb0 >> 6)];
+                    visbits = static_cast<uint32_t>(a >> (cb0 & 63));
+                    if (cb0 + CPT > nn)
+                        visbits &= (nn - cb0 <= 0) ? 0u : (0xffffffffu >> (32 - (nn - cb0)));
                 }
-                if (vis != 0xffffffffu) {
-#pragma unroll
-                    for (int i = 0; i < CPT; ++i) sv[i] = ((vis >> i) & 1u) ? sv[i] : -INFINITY;
-                }
-#pragma unroll
-                for (int i = 0; i < CPT; i += 4) {
-                    pm0 = fmaxf(pm0, sv[i]);
-                    pm1 = fmaxf(pm1, sv[i + 1]);
-                    pm2 = fmaxf(pm2, sv[i + 2]);
-                    pm3 = fmaxf(pm3, sv[i + 3]);
-                }
-                red[((j & 1) * NWG + wg) * 128 + row] = fmaxf(fmaxf(pm0, pm1), fmaxf(pm2, pm3));
             }
-            if (!bar_and(grp_bar, GRP_THREADS, w_ok)) { ok = false; break; }
-            float mx = red[((j & 1) * NWG) * 128 + row];
-#pragma unroll
-            for (int k = 1; k < NWG; ++k) mx = fmaxf(mx, red[((j & 1) * NWG + k) * 128 + row]);
-            float factor = 1.0f;
-            bool rescale = false;
-            if (j == 0) {
-                m_ref = mx;
-            } else if ((mx - m_ref) * sl2 > 8.0f) {
-                factor = (m_ref == -INFINITY) ? 0.0f : ex2((m_ref - mx) * sl2);
-                m_ref = mx;
-                rescale = true;
-            }
-            const float mu = (m_ref == -INFINITY) ? 0.0f : m_ref * sl2;
-            l *= factor;
-            float l0 = 0.0f, l1 = 0.0f;
-#pragma unroll
-            for (int i = 0; i < CPT; i += 2) {
-                sv[i] = ex2(fmaf(sv[i], sl2, -mu));
-                sv[i + 1] = ex2(fmaf(sv[i + 1], sl2, -mu));
-                l0 += sv[i];
-                l1 += sv[i + 1];
-            }
-            l += l0 + l1;
-            // V_j to fp16 in place: 16 bytes x 4 per thread
-            w_ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_VF + s], (j >> 1) & 1, abort_flag));
-            if (w_ok) {
-                uint4* vs = reinterpret_cast<uint4*>(sm + OFF_V + s * TILE_BYTES);
-                uint4 vv[TILE_BYTES / 16 / NSOFT];
-#pragma unroll
-                for (int i = 0; i < TILE_BYTES / 16 / NSOFT; ++i) vv[i] = vs[st + i * NSOFT];
-#pragma unroll
-                for (int i = 0; i < TILE_BYTES / 16 / NSOFT; ++i)
-                    vs[st + i * NSOFT] = bf16x8_to_f16x8(vv[i]);
-            }
-            // P_j may only overwrite the P buffer once PV_{j-1} is done
-            if (j >= 1 && w_ok)
-                w_ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_PVDONE], (j - 1) & 1, abort_flag));
-            if (!bar_and(grp_bar, GRP_THREADS, w_ok)) { ok = false; break; }
-            if (j >= 1) tc_fence_after();
-            if (__any_sync(0xffffffffu, rescale)) {
-                float ov[32];
-#pragma unroll
-                for (int cc = 0; cc < CPT / 32; ++cc) {
-                    tmem_ld32(tO + lane_addr + cb0 + cc * 32, ov);
+            float m_ref = -INFINITY, l = 0.0f;           // m_ref in raw score units
+            for (int j = 0; j < un.nblk; ++j, ++J) {
+                const int s = J & 1;
+                bool w_ok = __all_sync(0xffffffffu,
+                                       mbar_wait(&bar[B_SFULL + s], (J >> 1) & 1, abort_flag));
+                float pm0 = -INFINITY, pm1 = -INFINITY, pm2 = -INFINITY, pm3 = -INFINITY;
+                if (w_ok) {
+                    tc_fence_after();
+                    tmem_ld32(tmem + s * 128 + lane_addr + cb0, sv);
                     tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(&bar[B_SFREE + s]);
+                    // visibility: all columns of a full cache block are visible
+                    uint32_t vis = visbits;
+                    if (!un.tree) {
+                        const int nvis = un.k1 - (un.k0 + j * NB + cb0);
+                        vis = nvis >= CPT ? 0xffffffffu
+                                          : (nvis <= 0 ? 0u : (0xffffffffu >> (32 - nvis)));
+                    }
+                    if (vis != 0xffffffffu) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) ov[i] *= factor;
-                    tmem_st32(tO + lane_addr + cb0 + cc * 32, ov);
+                        for (int i = 0; i < CPT; ++i) sv[i] = ((vis >> i) & 1u) ? sv[i] : -INFINITY;
+                    }
+#pragma unroll
+                    for (int i = 0; i < CPT; i += 4) {
+                        pm0 = fmaxf(pm0, sv[i]);
+                        pm1 = fmaxf(pm1, sv[i + 1]);
+                        pm2 = fmaxf(pm2, sv[i + 2]);
+                        pm3 = fmaxf(pm3, sv[i + 3]);
+                    }
+                    red[(s * NWG + wg) * 128 + row] = fmaxf(fmaxf(pm0, pm1), fmaxf(pm2, pm3));
                 }
-                tmem_wait_st();
-            }
+                if (!bar_and(grp_bar, GRP_THREADS, w_ok)) { ok = false; break; }
+                float mx = red[(s * NWG) * 128 + row];
 #pragma unroll
-            for (int cb = 0; cb < CPT / 8; ++cb) {         // 16-byte chunks of 8 keys
-                uint32_t hw[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const __half2 h2 = __floats2half2_rn(sv[cb * 8 + 2 * e], sv[cb * 8 + 2 * e + 1]);
-                    hw[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                for (int q = 1; q < NWG; ++q) mx = fmaxf(mx, red[(s * NWG + q) * 128 + row]);
+                float factor = 1.0f;
+                bool rescale = false;
+                if (j == 0) {
+                    m_ref = mx;
+                } else if ((mx - m_ref) * sl2 > 8.0f) {
+                    factor = (m_ref == -INFINITY) ? 0.0f : ex2((m_ref - mx) * sl2);
+                    m_ref = mx;
+                    rescale = true;
                 }
-                const int col = cb0 + cb * 8;              // key column within the block
-                const uint32_t off = (col >> 6) * HALF_BYTES + sw128_offset(row, col & 63);
-                *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                const float mu = (m_ref == -INFINITY) ? 0.0f : m_ref * sl2;
+                l *= factor;
+                float l0 = 0.0f, l1 = 0.0f;
+#pragma unroll
+                for (int i = 0; i < CPT; i += 2) {
+                    sv[i] = ex2(fmaf(sv[i], sl2, -mu));
+                    sv[i + 1] = ex2(fmaf(sv[i + 1], sl2, -mu));
+                    l0 += sv[i];
+                    l1 += sv[i + 1];
+                }
+                l += l0 + l1;
+                // V_J to fp16 in place: 16 bytes x 4 per thread
+                w_ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_VF + s], (J >> 1) & 1, abort_flag));
+                if (w_ok) {
+                    uint4* vs = reinterpret_cast<uint4*>(sm + OFF_V + s * TILE_BYTES);
+                    uint4 vv[TILE_BYTES / 16 / NSOFT];
+#pragma unroll
+                    for (int i = 0; i < TILE_BYTES / 16 / NSOFT; ++i) vv[i] = vs[st + i * NSOFT];
+#pragma unroll
+                    for (int i = 0; i < TILE_BYTES / 16 / NSOFT; ++i)
+                        vs[st + i * NSOFT] = bf16x8_to_f16x8(vv[i]);
+                }
+                // P_J may only overwrite the P buffer once PV_{J-1} is done (for a
+                // unit's first block the previous unit's epilogue has waited)
+                if (j >= 1 && w_ok)
+                    w_ok = __all_sync(0xffffffffu,
+                                      mbar_wait(&bar[B_PVDONE], (J - 1) & 1, abort_flag));
+                if (!bar_and(grp_bar, GRP_THREADS, w_ok)) { ok = false; break; }
+                if (j >= 1) tc_fence_after();
+                if (__any_sync(0xffffffffu, rescale)) {
+                    float ov[32];
+#pragma unroll
+                    for (int cc = 0; cc < CPT / 32; ++cc) {
+                        tmem_ld32(tO + lane_addr + cb0 + cc * 32, ov);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) ov[i] *= factor;
+                        tmem_st32(tO + lane_addr + cb0 + cc * 32, ov);
+                    }
+                    tmem_wait_st();
+                }
+#pragma unroll
+                for (int cb = 0; cb < CPT / 8; ++cb) {         // 16-byte chunks of 8 keys
+                    uint32_t hw[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const __half2 h2 = __floats2half2_rn(sv[cb * 8 + 2 * e], sv[cb * 8 + 2 * e + 1]);
+                        hw[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                    }
+                    const int col = cb0 + cb * 8;              // key column within the block
+                    const uint32_t off = (col >> 6) * HALF_BYTES + sw128_offset(row, col & 63);
+                    *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                }
+                fence_async_smem();
+                tc_fence_before();
+                mbar_arrive(&bar[B_PFULL]);
             }
-            fence_async_smem();
-            tc_fence_before();
-            mbar_arrive(&bar[B_PFULL]);
-        }
-        if (ok) {
-            const bool w_ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_PVDONE], (nblk - 1) & 1, abort_flag));
-            ok = bar_and(grp_bar, GRP_THREADS, w_ok);
-        }
-        if (ok) {
+            if (!ok) break;
+            // the unit's output once its last PV is done
+            {
+                const bool w_ok = __all_sync(0xffffffffu,
+                                             mbar_wait(&bar[B_PVDONE], (J - 1) & 1, abort_flag));
+                if (!bar_and(grp_bar, GRP_THREADS, w_ok)) { ok = false; break; }
+            }
             tc_fence_after();
             __half* wO = ws_ptr<__half>(prm.ws, w.attn_o_off);
             float2* wML = ws_ptr<float2>(prm.ws, w.attn_ml_off);
-            const size_t tile = (((size_t)b * c.Hkv + g) * w.n_mt + mt) * w.n_chunks + ch;
+            const size_t tile = (((size_t)un.b * c.Hkv + un.g) * w.n_mt + un.mt) * w.n_chunks + un.ch;
             redl[wg * 128 + row] = l;
             bar_and(grp_bar, GRP_THREADS, true);
             float lt = 0.0f;
 #pragma unroll
-            for (int k = 0; k < NWG; ++k) lt += redl[k * 128 + row];
+            for (int q = 0; q < NWG; ++q) lt += redl[q * 128 + row];
             const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
             float ov[32];
 #pragma unroll
@@ -438,6 +645,8 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
             if (wg == 0 && r < G * T)
                 // partial max in natural-log units of the scaled score s / sqrt(D)
                 wML[tile * BM + row] = make_float2(m_ref * rsqrtf((float)HD), lt);
+            // the next unit's first PV overwrites O: every thread's reads of it are done
+            tc_fence_before();
         }
     }
 
@@ -451,9 +660,9 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
     pdl_trigger();
     if (*abort_flag && threadIdx.x == 0) {
         // let the TMA copies still in flight land before the CTA's shared memory
-        // is released: wait (bounded) on the phases of the last issued blocks
+        // is released: wait (bounded) on the phases of the last issued loads
         int never = 0;
-        mbar_wait(&bar[B_Q], 0, &never);
+        if (*issued_q > 0) mbar_wait(&bar[B_Q], (*issued_q - 1) & 1, &never);
         for (int j = max(0, *issued_k - 2); j < *issued_k; ++j)
             mbar_wait(&bar[B_KF + (j & 1)], (j >> 1) & 1, &never);
         for (int j = max(0, *issued_v - 2); j < *issued_v; ++j)
@@ -499,7 +708,7 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 bool attn_tc_supported(const spec_cfg& c) {
     const int G = c.Hq / c.Hkv;
     return c.io_dtype == SPEC_IO_BF16 && c.D == HD && G >= 1 && G <= BM && (BM % G) == 0 &&
-           c.N + 1 <= NB && encode_fn() != nullptr;
+           c.N + 1 <= NB && smem_bytes(c.B) <= SMEM_LIMIT && encode_fn() != nullptr;
 }
 
 cudaError_t launch_attn_tc(const spec_cfg& c, const spec_tree& t, const void* q,
@@ -530,11 +739,19 @@ cudaError_t launch_attn_tc(const spec_cfg& c, const spec_tree& t, const void* q,
         if (!make_map(&mvt, v_tree, 4, dims, str, box)) return cudaErrorInvalidValue;
     }
     TcParams prm{c, t, kv_len, ws, w};
+    const uint32_t smem = smem_bytes(c.B);
     cudaError_t err = cudaFuncSetAttribute(attn_tc_partial,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    dim3 grid(w.n_chunks, c.Hkv * w.n_mt, c.B);
-    return launch_k(pdl, attn_tc_partial, grid, dim3(NTHREADS), SMEM_BYTES, st, mq, mkc, mvc, mkt,
+    // one CTA per SM at most (the units themselves are counted on the device
+    // from kv_len): at most every tile of every chunk
+    int dev = 0, sms = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return err;
+    const long units = (long)c.B * c.Hkv * w.n_mt * w.n_chunks;
+    const int grid = (int)(units < sms ? units : sms);
+    return launch_k(pdl, attn_tc_partial, dim3(grid), dim3(NTHREADS), smem, st, mq, mkc, mvc, mkt,
                     mvt, prm);
 }
 
