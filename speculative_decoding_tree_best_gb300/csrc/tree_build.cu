@@ -187,68 +187,77 @@ tree_build_kernel(spec_cfg c, const int32_t* __restrict__ lat_tok,
             fst[0] = s_sc[i_fst];
         }
     } else {
-    while (count < T) {
-        const uint32_t best_ord = __reduce_max_sync(0xffffffffu, bo);
-        if (best_ord == 0u) break;                                  // frontier empty
-        const uint32_t best_tie = __reduce_max_sync(0xffffffffu, bo == best_ord ? bt : 0u);
-        const int p = 255 - (int)(best_tie & 0xffu);
-        const int n = count++;
-        const int pl = p & 31, pk = p >> 5;
-        // the parent's lane publishes depth, offered rank, child score, the first
-        // edge score below the child, and its ancestor mask
-        int d = 0, r = 0;
-        float sc = 0.0f, fe = 0.0f;
-        uint64_t pa0 = 0ull, pa1 = 0ull;
+        // Larger trees: row x lives in slot x / 32 of lane x % 32.  The same
+        // branch-free step over every slot of every lane: the parent's slot is
+        // picked by selects (its index is warp-uniform) before the shuffles.
+        while (count < T) {
+            const uint32_t best_ord = __reduce_max_sync(0xffffffffu, bo);
+            if (best_ord == 0u) break;                              // frontier empty
+            const uint32_t best_tie = __reduce_max_sync(0xffffffffu, bo == best_ord ? bt : 0u);
+            const int p = 255 - (int)(best_tie & 0xffu);
+            const int n = count++;
+            const int pl = p & 31, pk = p >> 5, nl = n & 31, nk = n >> 5;
+            int d = nd[0], r = nx[0];
+            float sc = cs[0], fe = fst[0];
+            uint64_t pa0 = a0[0], pa1 = a1[0];
 #pragma unroll
-        for (int k = 0; k < SLOTS; ++k)
-            if (SLOTS == 1 || k == pk) { d = nd[k]; r = nx[k]; sc = cs[k]; fe = fst[k]; pa0 = a0[k]; pa1 = a1[k]; }
-        d = __shfl_sync(0xffffffffu, d, pl);
-        r = __shfl_sync(0xffffffffu, r, pl);
-        sc = __shfl_sync(0xffffffffu, sc, pl);
-        fe = __shfl_sync(0xffffffffu, fe, pl);
-        if (lane == pl) {
-#pragma unroll
-            for (int k = 0; k < SLOTS; ++k)
-                if (SLOTS == 1 || k == pk) {
-                    nx[k] = r + 1;
-                    if (r + 1 < K) { cs[k] = ns[k] + nxt[k]; co[k] = ord_f32(cs[k]); }
-                    else co[k] = 0u;
-                }
-        }
-        if (lane == (n & 31)) {
-            const int nk = n >> 5;
+            for (int k = 1; k < SLOTS; ++k) {
+                const bool sel = k == pk;
+                d = sel ? nd[k] : d;
+                r = sel ? nx[k] : r;
+                sc = sel ? cs[k] : sc;
+                fe = sel ? fst[k] : fe;
+                pa0 = sel ? a0[k] : pa0;
+                pa1 = sel ? a1[k] : pa1;
+            }
+            d = __shfl_sync(0xffffffffu, d, pl);
+            r = __shfl_sync(0xffffffffu, r, pl);
+            sc = __shfl_sync(0xffffffffu, sc, pl);
+            fe = __shfl_sync(0xffffffffu, fe, pl);
+            const float cs_n = sc + fe;
+            const uint32_t co_n = (d + 1 < mb) ? ord_f32(cs_n) : 0u;
 #pragma unroll
             for (int k = 0; k < SLOTS; ++k) {
-                if (SLOTS == 1 || k == nk) {
-                    nd[k] = d + 1; nx[k] = 0; ns[k] = sc; npar[k] = p; nrk[k] = r;
-                    if (d + 1 < mb) { cs[k] = sc + fe; co[k] = ord_f32(cs[k]); }
-                    else co[k] = 0u;
-                }
+                const bool isp = lane == pl && k == pk, isn = lane == nl && k == nk;
+                const float cs_p = ns[k] + nxt[k];
+                const uint32_t co_p = (r + 1 < K) ? ord_f32(cs_p) : 0u;
+                nx[k] = isp ? r + 1 : (isn ? 0 : nx[k]);
+                nd[k] = isn ? d + 1 : nd[k];
+                ns[k] = isn ? sc : ns[k];
+                npar[k] = isn ? p : npar[k];
+                nrk[k] = isn ? r : nrk[k];
+                cs[k] = isp ? cs_p : (isn ? cs_n : cs[k]);
+                co[k] = isp ? co_p : (isn ? co_n : co[k]);
             }
-        }
-        if (lane == pl || lane == (n & 31)) best_of_lane();
-        // off the critical path: ancestors, token, prefetches
-        pa0 = __shfl_sync(0xffffffffu, pa0, pl);
-        pa1 = __shfl_sync(0xffffffffu, pa1, pl);
-        if (lane == pl) {
+            best_of_lane();
+            // off the critical path: ancestors, token, the changed slots' edge scores
+            pa0 = __shfl_sync(0xffffffffu, pa0, pl);
+            pa1 = __shfl_sync(0xffffffffu, pa1, pl);
+            const int tkn = s_tok[d * K + r];
+            // slot pk of lane pl and slot nk of lane nl changed (the same lane
+            // when p and n are 32 apart); each lane reloads both candidates
+            int dp = nd[0], xp = nx[0], dn = nd[0], xn = nx[0];
 #pragma unroll
-            for (int k = 0; k < SLOTS; ++k)
-                if (SLOTS == 1 || k == pk) prefetch(k);
-        }
-        if (lane == (n & 31)) {
-            const int nk = n >> 5;
+            for (int k = 1; k < SLOTS; ++k) {
+                dp = k == pk ? nd[k] : dp;
+                xp = k == pk ? nx[k] : xp;
+                dn = k == nk ? nd[k] : dn;
+                xn = k == nk ? nx[k] : xn;
+            }
+            const float nxt_p = s_sc[(dp < mb && xp + 1 < K) ? dp * K + xp + 1 : 0];
+            const float fst_p = s_sc[(dp + 1 < mb) ? (dp + 1) * K : 0];
+            const float nxt_n = s_sc[(dn < mb && xn + 1 < K) ? dn * K + xn + 1 : 0];
+            const float fst_n = s_sc[(dn + 1 < mb) ? (dn + 1) * K : 0];
 #pragma unroll
             for (int k = 0; k < SLOTS; ++k) {
-                if (SLOTS == 1 || k == nk) {
-                    ntk[k] = s_tok[d * K + r];
-                    a0[k] = pa0 | (n < 64 ? 1ull << n : 0ull);
-                    a1[k] = pa1 | (n >= 64 ? 1ull << (n - 64) : 0ull);
-                    prefetch(k);
-                }
+                const bool isp = lane == pl && k == pk, isn = lane == nl && k == nk;
+                a0[k] = isn ? (pa0 | (n < 64 ? 1ull << n : 0ull)) : a0[k];
+                a1[k] = isn ? (pa1 | (n >= 64 ? 1ull << (n - 64) : 0ull)) : a1[k];
+                ntk[k] = isn ? tkn : ntk[k];
+                nxt[k] = isn ? nxt_n : (isp ? nxt_p : nxt[k]);
+                fst[k] = isn ? fst_n : (isp ? fst_p : fst[k]);
             }
         }
-    }
-
     }
 
     // ---- write the tree ----------------------------------------------------------
