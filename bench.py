@@ -71,10 +71,10 @@ def algorithmic_bytes(s: synth.SpecConfig, mean_L: float, tau: float, rows=None)
 ATTN_SOURCES = ("speculative_decoding_tree_best_gb300/csrc/attn_tree_tc.cu",
                 "speculative_decoding_tree_best_gb300/csrc/attn_tree.cu",
                 "speculative_decoding_tree_best_gb300/csrc/common.cuh")
-ATTN_TRAFFIC_SHA256 = "c90a50e0f6cddc32ced357912cc8bda85e8d25260e348b22a67e49c8ac5f72d2"
-ATTN_TRAFFIC_BYTES = {"single": 17128704 + 0 + 3628544 + 0,
-                      "long": 72053760 + 3496192 + 4983552 + 0,
-                      "batched": 440008192 + 16598528 + 19070720 + 0}
+ATTN_TRAFFIC_SHA256 = "726a904c8ed673869a9bb45852c1dd4ecff27955a46525d7abf343d404b10466"
+ATTN_TRAFFIC_BYTES = {"single": 17164288 + 0 + 3630848 + 0,
+                      "long": 67987968 + 776960 + 4986624 + 0,
+                      "batched": 447560704 + 10724864 + 30551040 + 0}
 
 
 def attn_traffic(name: str):
