@@ -9,23 +9,28 @@
 // every grid-th unit, with its pipelines running from one unit into the next.
 // The query tile holds the G = Hq/Hkv q-heads of the group for 128/G
 // consecutive tree rows (row r = node * G + head_in_group), loaded by TMA once
-// the previous unit's S products are done.  The keys stream through two-stage
-// rings of 128-key K and V blocks (TMA, 128-byte swizzle) numbered across the
-// CTA's units; a K stage is refilled as soon as its S product is done, a V
-// stage once its PV product is done.  Per block j:
+// the previous unit's S products are done.  The keys stream through rings of
+// 128-key K blocks (two stages) and V blocks (three stages), TMA with 128-byte
+// swizzle, numbered across the CTA's units; a K stage is refilled as soon as
+// its S product is done, a V stage once its PV product is done.  Per block j:
 //    S_j = Q K_j^T          tcgen05.mma (bf16, exact products), fp32 in tensor
 //                           memory, two S buffers so S_{j+1} is ready while
 //                           the softmax works on S_j
 //    P_j = exp2(S_j c - m)  one thread per (row, 32 keys), written as fp16
 //                           (11 significant bits; a bf16 P would cost ~1.7e-3
-//                           relative error on O)
+//                           relative error on O) into one of two P buffers in
+//                           tensor memory, so P_j is written while PV_{j-1}
+//                           still reads P_{j-1}
 //    V_j -> fp16            the softmax threads convert V_j in place (the same
 //                           swizzled layout), so PV runs as kind::f16 with f16
 //                           operands
-//    O += P_j V_j           tcgen05.mma, fp32 in tensor memory
+//    O += P_j V_j           tcgen05.mma with A (P) read from tensor memory, fp32
+//                           in tensor memory
+// Keeping P out of shared memory leaves room for the third V stage: more
+// bytes in flight per SM, which is what bounds the stream rate.
 // The MMA order is S_0, S_1, PV_0, S_2, PV_1, ...  The running maximum is only
-// raised (and O rescaled in tensor memory) when a block's maximum exceeds it by
-// more than 2^8, so P <= 256.  The chunk's output is stored normalised
+// raised (and O rescaled in tensor memory, after PV_{j-1} is done) when a
+// block's maximum exceeds it by more than 2^8, so P <= 256.  The chunk's output is stored normalised
 // (O / sum) in fp16 with its (max, sum); |V| must stay below the fp16 range
 // (65504).  Warp roles: warp 0 loads Q and the K ring, warp 1 issues the MMAs
 // (one thread each), warp 2 loads the V ring, warps 3-18 run the softmax: four
@@ -67,13 +72,15 @@ constexpr uint32_t TMEM_COLS = 512;              // S0, S1, O (128 columns each)
 // shared-memory map (offsets from the 1024-aligned base)
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;                   // 2 stages
-constexpr uint32_t OFF_V = OFF_K + 2 * TILE_BYTES;               // 2 stages
-constexpr uint32_t OFF_P = OFF_V + 2 * TILE_BYTES;               // fp16 P, K-major
-constexpr uint32_t OFF_RED = OFF_P + TILE_BYTES;                 // float [2][NWG][128] row maxima
+constexpr int NVS = 3;                                          // V ring stages
+constexpr uint32_t OFF_V = OFF_K + 2 * TILE_BYTES;               // NVS stages
+constexpr uint32_t OFF_RED = OFF_V + NVS * TILE_BYTES;           // float [2][NWG][128] row maxima
 constexpr uint32_t OFF_REDL = OFF_RED + 2 * NWG * 128 * 4;       // float [NWG][128] row sums
 constexpr uint32_t OFF_BAR = OFF_REDL + NWG * 128 * 4;
-enum { B_Q = 0, B_QE, B_KF, B_VF = B_KF + 2, B_KE = B_VF + 2, B_VE = B_KE + 2,
-       B_SFULL = B_VE + 2, B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_PVDONE, NBARS };
+enum { B_Q = 0, B_QE, B_KF, B_VF = B_KF + 2, B_KE = B_VF + NVS, B_VE = B_KE + 2,
+       B_SFULL = B_VE + NVS, B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_PVD, NBARS = B_PVD + 2 };
+// tensor-memory columns: S buffers 0 and 128, O 256, fp16 P buffers 384 and 448
+constexpr uint32_t TM_O = 256, TM_P = 384;
 constexpr uint32_t OFF_UNITS = OFF_BAR + NBARS * 8 + 32;         // int [4 B + 1]: the unit map
 constexpr uint32_t SMEM_LIMIT = 227 * 1024;
 
@@ -239,14 +246,16 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         mbar_init(&bar[B_QE], 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bar[B_KF + s], 1);
-            mbar_init(&bar[B_VF + s], 1);
             mbar_init(&bar[B_KE + s], 1);
-            mbar_init(&bar[B_VE + s], 1);
             mbar_init(&bar[B_SFULL + s], 1);
             mbar_init(&bar[B_SFREE + s], NSOFT);
+            mbar_init(&bar[B_PVD + s], 1);
+        }
+        for (int s = 0; s < NVS; ++s) {
+            mbar_init(&bar[B_VF + s], 1);
+            mbar_init(&bar[B_VE + s], 1);
         }
         mbar_init(&bar[B_PFULL], NSOFT);
-        mbar_init(&bar[B_PVDONE], 1);
         *abort_flag = 0;
         *issued_k = 0;
         *issued_v = 0;
@@ -310,7 +319,7 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tO = tmem + 256;                  // S buffers at +0 and +128
+    const uint32_t tO = tmem + TM_O;                 // S buffers at +0 and +128
     U.n_full = U.fpre[B] * U.hg;
     U.n_part = n_partial[0] * U.hg;
     U.total = U.n_full + U.n_part + B * U.hg;
@@ -361,9 +370,9 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
                 const Unit un = decode(U, U.unit_of(blockIdx.x, k), w.n_split);
                 const CUtensorMap* mv = un.tree ? &mvt : &mvc;
                 for (int j = 0; j < un.nblk; ++j, ++J) {
-                    const int s = J & 1;
-                    // stage s is free once PV_{J-2} is done
-                    if (J >= 2 && !mbar_wait(&bar[B_VE + s], ((J >> 1) - 1) & 1, abort_flag)) {
+                    const int s = J % NVS;
+                    // stage s is free once PV_{J-NVS} is done
+                    if (J >= NVS && !mbar_wait(&bar[B_VE + s], (J / NVS - 1) & 1, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -381,7 +390,6 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
             const uint32_t idS = idesc_bf16_f32(128, NB, false, false);
             const uint32_t idPV = idesc_f16_f32(128, HD, false, true);
             const uint32_t q_s = smem_u32(sm + OFF_Q);
-            const uint32_t p_s = smem_u32(sm + OFF_P);
             int nj = 0;                                  // blocks of all this CTA's units
             for (int k = 0; k < nu; ++k) nj += decode(U, U.unit_of(blockIdx.x, k), w.n_split).nblk;
             // the S cursor: unit ks, block js of it, global block JS
@@ -428,18 +436,17 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
             int kp = 0, jp = 0;
             int p_nblk = nu > 0 ? decode(U, U.unit_of(blockIdx.x, 0), w.n_split).nblk : 0;
             for (int J = 0; J < nj && ok; ++J) {
-                const int s = J & 1;
-                // P_J written and V_J converted to fp16 by the softmax threads
+                const int s = J % NVS;
+                // P_J written (tensor memory) and V_J converted to fp16 by the softmax threads
                 if (!mbar_wait(&bar[B_PFULL], J & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t v_s = smem_u32(sm + OFF_V + s * TILE_BYTES);
+                const uint32_t p_t = tmem + TM_P + (J & 1) * (NB / 2);
 #pragma unroll
-                for (int k = 0; k < NB / 16; ++k) {
-                    const uint32_t offp = (k >> 2) * HALF_BYTES + (k & 3) * 32;
-                    mma_f16(tO, sdesc_sw128(p_s + offp, 16, 1024),
-                            sdesc_sw128(v_s + k * 2048, HALF_BYTES, 1024), idPV, (jp > 0 || k > 0));
-                }
-                mma_commit(&bar[B_PVDONE]);
+                for (int k = 0; k < NB / 16; ++k)
+                    mma_f16_tmem_a(tO, p_t + k * 8, sdesc_sw128(v_s + k * 2048, HALF_BYTES, 1024),
+                                   idPV, (jp > 0 || k > 0));
+                mma_commit(&bar[B_PVD + (J & 1)]);
                 mma_commit(&bar[B_VE + s]);
                 ok = catch_up(J);
                 if (++jp == p_nblk) {
@@ -466,7 +473,6 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         float* red = reinterpret_cast<float*>(sm + OFF_RED);
         float* redl = reinterpret_cast<float*>(sm + OFF_REDL);
         const float sl2 = 1.4426950408889634f * rsqrtf((float)HD);   // log2(e) / sqrt(D)
-        unsigned char* pbuf = sm + OFF_P;
         float sv[CPT];
         {
             // chunks past a request's KV length leave an empty partial (max
@@ -560,9 +566,11 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
                 }
                 l += l0 + l1;
                 // V_J to fp16 in place: 16 bytes x 4 per thread
-                w_ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_VF + s], (J >> 1) & 1, abort_flag));
+                const int vst = J % NVS;
+                w_ok = __all_sync(0xffffffffu,
+                                  mbar_wait(&bar[B_VF + vst], (J / NVS) & 1, abort_flag));
                 if (w_ok) {
-                    uint4* vs = reinterpret_cast<uint4*>(sm + OFF_V + s * TILE_BYTES);
+                    uint4* vs = reinterpret_cast<uint4*>(sm + OFF_V + vst * TILE_BYTES);
                     uint4 vv[TILE_BYTES / 16 / NSOFT];
 #pragma unroll
                     for (int i = 0; i < TILE_BYTES / 16 / NSOFT; ++i) vv[i] = vs[st + i * NSOFT];
@@ -570,14 +578,18 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
                     for (int i = 0; i < TILE_BYTES / 16 / NSOFT; ++i)
                         vs[st + i * NSOFT] = bf16x8_to_f16x8(vv[i]);
                 }
-                // P_J may only overwrite the P buffer once PV_{J-1} is done (for a
-                // unit's first block the previous unit's epilogue has waited)
-                if (j >= 1 && w_ok)
-                    w_ok = __all_sync(0xffffffffu,
-                                      mbar_wait(&bar[B_PVDONE], (J - 1) & 1, abort_flag));
+                // P_J goes to tensor-memory buffer J & 1 once PV_{J-2}, which read
+                // it, is done; O is rescaled only once PV_{J-1} is done too
+                const bool any_rescale = __any_sync(0xffffffffu, rescale);
+                if (J >= 2 && w_ok)
+                    w_ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_PVD + (J & 1)],
+                                                             ((J >> 1) - 1) & 1, abort_flag));
+                if (any_rescale && w_ok)
+                    w_ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_PVD + ((J - 1) & 1)],
+                                                             ((J - 1) >> 1) & 1, abort_flag));
                 if (!bar_and(grp_bar, GRP_THREADS, w_ok)) { ok = false; break; }
-                if (j >= 1) tc_fence_after();
-                if (__any_sync(0xffffffffu, rescale)) {
+                tc_fence_after();
+                if (any_rescale) {
                     float ov[32];
 #pragma unroll
                     for (int cc = 0; cc < CPT / 32; ++cc) {
@@ -587,29 +599,26 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
                         for (int i = 0; i < 32; ++i) ov[i] *= factor;
                         tmem_st32(tO + lane_addr + cb0 + cc * 32, ov);
                     }
-                    tmem_wait_st();
                 }
+                {
+                    uint32_t hw[CPT / 2];                  // keys 2i, 2i + 1 as one half2
 #pragma unroll
-                for (int cb = 0; cb < CPT / 8; ++cb) {         // 16-byte chunks of 8 keys
-                    uint32_t hw[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const __half2 h2 = __floats2half2_rn(sv[cb * 8 + 2 * e], sv[cb * 8 + 2 * e + 1]);
-                        hw[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                    for (int i = 0; i < CPT / 2; ++i) {
+                        const __half2 h2 = __floats2half2_rn(sv[2 * i], sv[2 * i + 1]);
+                        hw[i] = *reinterpret_cast<const uint32_t*>(&h2);
                     }
-                    const int col = cb0 + cb * 8;              // key column within the block
-                    const uint32_t off = (col >> 6) * HALF_BYTES + sw128_offset(row, col & 63);
-                    *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    tmem_st16(tmem + TM_P + (J & 1) * (NB / 2) + lane_addr + cb0 / 2, hw);
                 }
-                fence_async_smem();
+                tmem_wait_st();
+                fence_async_smem();                        // the converted V, for the MMA
                 tc_fence_before();
                 mbar_arrive(&bar[B_PFULL]);
             }
             if (!ok) break;
             // the unit's output once its last PV is done
             {
-                const bool w_ok = __all_sync(0xffffffffu,
-                                             mbar_wait(&bar[B_PVDONE], (J - 1) & 1, abort_flag));
+                const bool w_ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_PVD + ((J - 1) & 1)],
+                                                                   ((J - 1) >> 1) & 1, abort_flag));
                 if (!bar_and(grp_bar, GRP_THREADS, w_ok)) { ok = false; break; }
             }
             tc_fence_after();
@@ -665,8 +674,8 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         if (*issued_q > 0) mbar_wait(&bar[B_Q], (*issued_q - 1) & 1, &never);
         for (int j = max(0, *issued_k - 2); j < *issued_k; ++j)
             mbar_wait(&bar[B_KF + (j & 1)], (j >> 1) & 1, &never);
-        for (int j = max(0, *issued_v - 2); j < *issued_v; ++j)
-            mbar_wait(&bar[B_VF + (j & 1)], (j >> 1) & 1, &never);
+        for (int j = max(0, *issued_v - NVS); j < *issued_v; ++j)
+            mbar_wait(&bar[B_VF + j % NVS], (j / NVS) & 1, &never);
     }
     if (warp == 1) {
         tc_fence_after();
