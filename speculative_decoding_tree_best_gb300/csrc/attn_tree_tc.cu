@@ -78,7 +78,13 @@ constexpr uint32_t OFF_RED = OFF_V + NVS * TILE_BYTES;           // float [2][NW
 constexpr uint32_t OFF_REDL = OFF_RED + 2 * NWG * 128 * 4;       // float [NWG][128] row sums
 constexpr uint32_t OFF_BAR = OFF_REDL + NWG * 128 * 4;
 enum { B_Q = 0, B_QE, B_KF, B_VF = B_KF + 2, B_KE = B_VF + NVS, B_VE = B_KE + 2,
-       B_SFULL = B_VE + NVS, B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_PVD, NBARS = B_PVD + 2 };
+       B_SFULL = B_VE + NVS, B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_PVD = B_PFULL + 2,
+       NBARS = B_PVD + 2 };
+// Every barrier that a role may pass twice before another role's wait on it
+// sees the first pass is split per buffer (S, P) or per stage (K, V): a
+// parity wait must never be two phases behind.  P_{j+1} can be written before
+// the MMA thread has seen P_j (two P buffers), hence one PFULL barrier per P
+// buffer.
 // tensor-memory columns: S buffers 0 and 128, O 256, fp16 P buffers 384 and 448
 constexpr uint32_t TM_O = 256, TM_P = 384;
 constexpr uint32_t OFF_UNITS = OFF_BAR + NBARS * 8 + 32;         // int [4 B + 1]: the unit map
@@ -250,12 +256,12 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
             mbar_init(&bar[B_SFULL + s], 1);
             mbar_init(&bar[B_SFREE + s], NSOFT);
             mbar_init(&bar[B_PVD + s], 1);
+            mbar_init(&bar[B_PFULL + s], NSOFT);
         }
         for (int s = 0; s < NVS; ++s) {
             mbar_init(&bar[B_VF + s], 1);
             mbar_init(&bar[B_VE + s], 1);
         }
-        mbar_init(&bar[B_PFULL], NSOFT);
         *abort_flag = 0;
         *issued_k = 0;
         *issued_v = 0;
@@ -438,7 +444,7 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
             for (int J = 0; J < nj && ok; ++J) {
                 const int s = J % NVS;
                 // P_J written (tensor memory) and V_J converted to fp16 by the softmax threads
-                if (!mbar_wait(&bar[B_PFULL], J & 1, abort_flag)) { ok = false; break; }
+                if (!mbar_wait(&bar[B_PFULL + (J & 1)], (J >> 1) & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t v_s = smem_u32(sm + OFF_V + s * TILE_BYTES);
                 const uint32_t p_t = tmem + TM_P + (J & 1) * (NB / 2);
@@ -612,7 +618,7 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
                 tmem_wait_st();
                 fence_async_smem();                        // the converted V, for the MMA
                 tc_fence_before();
-                mbar_arrive(&bar[B_PFULL]);
+                mbar_arrive(&bar[B_PFULL + (J & 1)]);
             }
             if (!ok) break;
             // the unit's output once its last PV is done

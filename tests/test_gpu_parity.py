@@ -125,3 +125,29 @@ def test_full_stack_sampled():
     r = parity.check_case(synth.config(4), 0, req=[0, 5], attn_kv_heads=[3], gdn_layers=[0, 47],
                           attn_layers=[0, 15])
     assert r["status"] == 0 and min(r["tau"]) >= 1
+
+
+def test_repeated_batched_attention_no_timeout():
+    """Sixty batched attention launches in a row (the persistent partial runs
+    several units per CTA with its rings crossing unit boundaries): every
+    bounded wait completes (no timeout bit) and every launch gives the same
+    bits."""
+    from speculative_decoding_tree_best_gb300.step import VerifyStep, stack_inputs
+    cfg = synth.config(3)
+    inp, _ = parity.prepare(cfg, 4)
+    st = VerifyStep(cfg, stack_inputs(inp, "cuda"))
+    st.build_tree()
+    x, c = st.x, st.cfg
+
+    def attn():
+        binding.attn_tree_verify(c, st.tree, x["attn_q"][0], x["k_tree"][0], x["v_tree"][0],
+                                 x["k_cache"][0], x["v_cache"][0], x["kv_len"], st.attn_o[0],
+                                 st.ws)
+    attn()
+    torch.cuda.synchronize()
+    first = st.attn_o.clone()
+    for _ in range(60):
+        attn()
+    torch.cuda.synchronize()
+    assert binding.spec_status_read(st.ws) == 0
+    assert torch.equal(st.attn_o, first)
