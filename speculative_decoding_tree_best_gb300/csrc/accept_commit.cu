@@ -307,37 +307,38 @@ sample_accept(spec_cfg c, const typename io_t<IO>::T* __restrict__ logits, spec_
     }
 }
 
-// Gated-delta steps of the accepted rows on 32 state columns (rows split over
-// the CTA's 8 warps, held in registers), written back in place.
-template <int IO, int DK>
+// Gated-delta steps of the accepted rows on CB columns (from c0) of a d_k x d_v
+// state: thread (row group g, column col) of the 4 CB threads holds rows
+// [g DK/4, (g+1) DK/4) of column c0 + col in registers; written back in place.
+template <int IO, int DK, int DV, int CB>
 __device__ __forceinline__ void commit_state(const spec_cfg& c, const spec_commit_io& io,
                                              const spec_accept& acc, const int32_t* plan,
-                                             float* hr, float* h, int b, int j, int layer, int cb,
+                                             float* hr, float* h, int b, int j, int layer, int c0,
                                              float* sc) {
     using E = typename io_t<IO>::T;
-    constexpr int CB = 32, NG = NT / 32, RPT = DK / NG;
+    constexpr int NTC = 4 * CB, RPT = DK / 4;
     const int T = c.N + 1, m = c.m, tid = threadIdx.x;
-    const int ih = j / (c.Hv / c.Hk), c0 = cb * CB, col = tid & 31, grp = tid >> 5;
+    const int ih = j / (c.Hv / c.Hk), col = tid % CB, grp = tid / CB;
     const int tau = plan[4 * b];
     if (tau == 0) return;
     float* ks = sc;                     // [tau][DK]
     float* vsm = ks + (m + 1) * DK;     // [tau][CB]
     float* ab = vsm + (m + 1) * CB;     // [tau][2]
-    float* red = ab + 2 * (m + 1);      // [2][NG][CB]
+    float* red = ab + 2 * (m + 1);      // [2][4][CB]
     const E* kl = static_cast<const E*>(io.gdn_k) + (size_t)layer * c.B * T * c.Hk * DK;
-    const E* vl = static_cast<const E*>(io.gdn_v) + (size_t)layer * c.B * T * c.Hv * c.dv;
+    const E* vl = static_cast<const E*>(io.gdn_v) + (size_t)layer * c.B * T * c.Hv * DV;
     const float* al = io.alpha + (size_t)layer * c.B * T * c.Hv;
     const float* be = io.beta + (size_t)layer * c.B * T * c.Hv;
     const int32_t* nodes = acc.accept_nodes + (size_t)b * (m + 1);
-    for (int idx = tid; idx < tau * DK; idx += NT) {
+    for (int idx = tid; idx < tau * DK; idx += NTC) {
         const int s = idx / DK, r = idx % DK, x = nodes[s];
         ks[idx] = io_t<IO>::ld(kl, (((size_t)b * T + x) * c.Hk + ih) * DK + r);
     }
-    for (int idx = tid; idx < tau * CB; idx += NT) {
-        const int s = idx / CB, cc = idx % CB, x = nodes[s];
-        vsm[idx] = io_t<IO>::ld(vl, (((size_t)b * T + x) * c.Hv + j) * c.dv + c0 + cc);
+    for (int idx = tid; idx < tau * CB; idx += NTC) {
+        const int s = idx / CB, r = idx % CB, x = nodes[s];
+        vsm[idx] = io_t<IO>::ld(vl, (((size_t)b * T + x) * c.Hv + j) * DV + c0 + r);
     }
-    for (int s = tid; s < tau; s += NT) {
+    for (int s = tid; s < tau; s += NTC) {
         const int x = nodes[s];
         ab[2 * s] = al[((size_t)b * T + x) * c.Hv + j];
         ab[2 * s + 1] = be[((size_t)b * T + x) * c.Hv + j];
@@ -348,18 +349,16 @@ __device__ __forceinline__ void commit_state(const spec_cfg& c, const spec_commi
         float part = 0.0f;
 #pragma unroll
         for (int i = 0; i < RPT; ++i) part = fmaf(hr[i], kk[i], part);
-        float* rb = red + (s & 1) * NG * CB;
+        float* rb = red + (s & 1) * 4 * CB;
         rb[grp * CB + col] = part;
         __syncthreads();
-        float u = 0.0f;
-#pragma unroll
-        for (int g2 = 0; g2 < NG; ++g2) u += rb[g2 * CB + col];
+        const float u = (rb[col] + rb[CB + col]) + (rb[2 * CB + col] + rb[3 * CB + col]);
         const float a = ab[2 * s], bb = ab[2 * s + 1], vv = vsm[s * CB + col];
 #pragma unroll
         for (int i = 0; i < RPT; ++i) hr[i] = a * (hr[i] - bb * kk[i] * u) + bb * kk[i] * vv;
     }
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) h[(size_t)(grp * RPT + i) * c.dv + c0 + col] = hr[i];
+    for (int i = 0; i < RPT; ++i) h[(size_t)(grp * RPT + i) * DV + c0 + col] = hr[i];
 }
 
 // Copy the tree K/V row of accepted path slot s of (layer, request) into the
@@ -383,7 +382,7 @@ __device__ __forceinline__ void append_kv(const spec_cfg& c, const spec_commit_i
     const char* vt = static_cast<const char*>(io.v_tree);
     char* kc = static_cast<char*>(io.k_cache);
     char* vc = static_cast<char*>(io.v_cache);
-    for (size_t o = (size_t)tid * 16; o < row; o += NT * 16) {
+    for (size_t o = (size_t)tid * 16; o < row; o += (size_t)blockDim.x * 16) {
         *reinterpret_cast<uint4*>(kc + dst + o) = *reinterpret_cast<const uint4*>(kt + src + o);
         *reinterpret_cast<uint4*>(vc + dst + o) = *reinterpret_cast<const uint4*>(vt + src + o);
     }
@@ -391,33 +390,35 @@ __device__ __forceinline__ void append_kv(const spec_cfg& c, const spec_commit_i
 
 // early: the acceptance, or a GDN layer that still reads h0, may be the launch
 // just before this one, so wait before anything else; otherwise both are at
-// least two launches back and the wait moves to the end.
-template <int IO, int DK>
-__global__ void __launch_bounds__(NT)
+// least two launches back and the wait moves to the end.  One block per CB
+// columns of a GDN (layer, request, v-head) state (4 CB threads: the whole
+// state when there are enough states to fill the GPU, 32 columns otherwise),
+// then one block per KV row append.
+template <int IO, int DK, int DV, int CB>
+__global__ void __launch_bounds__(4 * CB)
 commit_kernel(spec_cfg c, spec_commit_io io, spec_accept acc, void* ws, WsLayout w, int gdn_blocks,
               bool early) {
     extern __shared__ __align__(16) float sc[];
     const int32_t* plan = ws_ptr<const int32_t>(ws, w.plan_off);
     const int tid = threadIdx.x;
     if ((int)blockIdx.x < gdn_blocks) {
-        constexpr int CB = 32, NG = NT / 32, RPT = DK / NG;
-        const int nb = c.dv / CB;
+        constexpr int RPT = DK / 4;
         int id = blockIdx.x;
-        const int cb = id % nb; id /= nb;
+        const int c0 = (id % (DV / CB)) * CB; id /= DV / CB;
         const int j = id % c.Hv; id /= c.Hv;
         const int b = id % c.B;
         const int layer = id / c.B;
-        const int c0 = cb * CB, col = tid & 31, grp = tid >> 5;
-        // the state slice does not depend on the acceptance: load it first
-        float* h = io.h0 + (size_t)layer * c.B * c.Hv * DK * c.dv + ((size_t)b * c.Hv + j) * DK * c.dv;
+        const int col = tid % CB, grp = tid / CB;
+        // the state does not depend on the acceptance: load it first
+        float* h = io.h0 + (size_t)layer * c.B * c.Hv * DK * DV + ((size_t)b * c.Hv + j) * DK * DV;
         float hr[RPT];
 #pragma unroll
-        for (int i = 0; i < RPT; ++i) hr[i] = h[(size_t)(grp * RPT + i) * c.dv + c0 + col];
+        for (int i = 0; i < RPT; ++i) hr[i] = h[(size_t)(grp * RPT + i) * DV + c0 + col];
         if (early) {
             pdl_wait();
             pdl_trigger();
         }
-        commit_state<IO, DK>(c, io, acc, plan, hr, h, b, j, layer, cb, sc);
+        commit_state<IO, DK, DV, CB>(c, io, acc, plan, hr, h, b, j, layer, c0, sc);
     } else {
         if (early) {
             pdl_wait();
@@ -431,18 +432,18 @@ commit_kernel(spec_cfg c, spec_commit_io io, spec_accept acc, void* ws, WsLayout
     }
 }
 
-template <int IO, int DK>
+template <int IO, int DK, int DV, int CB>
 cudaError_t launch_commit_k(const spec_cfg& c, const spec_commit_io& io, const spec_accept& out,
                             void* ws, const WsLayout& w, cudaStream_t st, bool pdl, bool early) {
-    const int gdn_blocks = c.n_gdn_layers * c.B * c.Hv * (c.dv / 32);
+    const int gdn_blocks = c.n_gdn_layers * c.B * c.Hv * (DV / CB);
     const int kv_blocks = c.n_attn_layers * c.B * (c.m + 1);
     if (gdn_blocks + kv_blocks == 0) return cudaSuccess;
-    const size_t smem = sizeof(float) * ((size_t)(c.m + 1) * (DK + 32 + 2) + 2 * 8 * 32);
-    auto kern = commit_kernel<IO, DK>;
+    const size_t smem = sizeof(float) * ((size_t)(c.m + 1) * (DK + CB + 2) + 2 * 4 * CB);
+    auto kern = commit_kernel<IO, DK, DV, CB>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_k(pdl, kern, dim3(gdn_blocks + kv_blocks), dim3(NT), smem, st, c, io, out, ws, w,
-                    gdn_blocks, early);
+    return launch_k(pdl, kern, dim3(gdn_blocks + kv_blocks), dim3(4 * CB), smem, st, c, io, out, ws,
+                    w, gdn_blocks, early);
 }
 
 }  // namespace
@@ -476,14 +477,32 @@ cudaError_t launch_sample_accept(const spec_cfg& c, const spec_tree& t, const vo
                    tree_early);
 }
 
+template <int IO>
+static cudaError_t launch_commit_io(const spec_cfg& c, const spec_commit_io& io,
+                                    const spec_accept& out, void* ws, const WsLayout& w,
+                                    cudaStream_t st, bool pdl, bool early) {
+    // whole states when they fill the GPU four times over, else 32-column slices
+    const bool whole = (long)c.n_gdn_layers * c.B * c.Hv >= 4L * 152;
+    if (c.dk == 128) {
+        if (c.dv == 128)
+            return whole ? launch_commit_k<IO, 128, 128, 128>(c, io, out, ws, w, st, pdl, early)
+                         : launch_commit_k<IO, 128, 128, 32>(c, io, out, ws, w, st, pdl, early);
+        return whole ? launch_commit_k<IO, 128, 64, 64>(c, io, out, ws, w, st, pdl, early)
+                     : launch_commit_k<IO, 128, 64, 32>(c, io, out, ws, w, st, pdl, early);
+    }
+    if (c.dv == 128)
+        return whole ? launch_commit_k<IO, 64, 128, 128>(c, io, out, ws, w, st, pdl, early)
+                     : launch_commit_k<IO, 64, 128, 32>(c, io, out, ws, w, st, pdl, early);
+    return whole ? launch_commit_k<IO, 64, 64, 64>(c, io, out, ws, w, st, pdl, early)
+                 : launch_commit_k<IO, 64, 64, 32>(c, io, out, ws, w, st, pdl, early);
+}
+
 cudaError_t launch_commit(const spec_cfg& c, const spec_commit_io& io, const spec_accept& out,
                           void* ws, cudaStream_t st, bool pdl, bool early) {
     const WsLayout w = ws_layout(c);
-    if (c.io_dtype == SPEC_IO_BF16)
-        return c.dk == 128 ? launch_commit_k<SPEC_IO_BF16, 128>(c, io, out, ws, w, st, pdl, early)
-                           : launch_commit_k<SPEC_IO_BF16, 64>(c, io, out, ws, w, st, pdl, early);
-    return c.dk == 128 ? launch_commit_k<SPEC_IO_F32, 128>(c, io, out, ws, w, st, pdl, early)
-                       : launch_commit_k<SPEC_IO_F32, 64>(c, io, out, ws, w, st, pdl, early);
+    return c.io_dtype == SPEC_IO_BF16
+        ? launch_commit_io<SPEC_IO_BF16>(c, io, out, ws, w, st, pdl, early)
+        : launch_commit_io<SPEC_IO_F32>(c, io, out, ws, w, st, pdl, early);
 }
 
 cudaError_t launch_accept_commit(const spec_cfg& c, const spec_tree& t, const void* logits,

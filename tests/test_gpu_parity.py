@@ -151,3 +151,8 @@ def test_repeated_batched_attention_no_timeout():
     torch.cuda.synchronize()
     assert binding.spec_status_read(st.ws) == 0
     assert torch.equal(st.attn_o, first)
+
+
+@pytest.mark.parametrize("dk,dv", [(128, 64), (64, 128)])
+def test_unequal_key_and_value_head_dims(dk, dv):
+    parity.check_case(SMALL.replace(dk=dk, dv=dv, Hk=2, Hv=4), 11)
