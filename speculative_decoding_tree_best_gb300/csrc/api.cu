@@ -293,7 +293,7 @@ int verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_sc
                                   at(io->gdn_v, vo * esz), io->alpha + gate, io->beta + gate,
                                   const_cast<char*>(at(step->gdn_o, vo * esz)),
                                   step->gdn_c ? step->gdn_c + vo : nullptr, ws, st, true,
-                                  /*early=*/false);
+                                  /*early=*/false, /*trigger_first=*/l == ng - 1 && na > 0);
     }
     if (na > 0 && e == cudaSuccess) {
         const void *q, *kt, *vt, *kc, *vc;
