@@ -48,10 +48,14 @@ using acc::scan_segment;
 template <int IO>
 __global__ void __launch_bounds__(NT)
 argmax_accept(spec_cfg c, const typename io_t<IO>::T* __restrict__ logits, spec_tree tree,
-              spec_commit_io io, spec_accept acc, void* ws, WsLayout w, bool tree_early) {
+              spec_commit_io io, spec_accept acc, void* ws, WsLayout w, bool tree_early,
+              bool trigger_first) {
     using E = typename io_t<IO>::T;
     constexpr int VEC = 16 / sizeof(E);
     const int sp = blockIdx.x, row = blockIdx.y;
+    // trigger_first: the launches after this one read nothing it writes before
+    // their own waits, so they may start at once
+    if (trigger_first) pdl_trigger();
     const int T = c.N + 1, b = row / T, t = row % T;
     // n_nodes may only be read before the wait when the launch that wrote the
     // tree is at least two back
@@ -70,7 +74,7 @@ argmax_accept(spec_cfg c, const typename io_t<IO>::T* __restrict__ logits, spec_
     // The acceptance reads the tree and rewrites kv_len: everything before this
     // launch must be done.
     pdl_wait();
-    pdl_trigger();
+    if (!trigger_first) pdl_trigger();
     // Every CTA of the request takes a ticket; the last one runs the acceptance.
     __shared__ bool last;
     if (threadIdx.x == 0) {
@@ -211,8 +215,9 @@ template <int IO>
 __global__ void __launch_bounds__(NT)
 sample_accept(spec_cfg c, const typename io_t<IO>::T* __restrict__ logits, spec_tree tree,
               spec_commit_io io, spec_accept acc, void* ws, WsLayout w, float inv_temp,
-              uint32_t key0, uint32_t key1, bool tree_early) {
+              uint32_t key0, uint32_t key1, bool tree_early, bool trigger_first) {
     using E = typename io_t<IO>::T;
+    if (trigger_first) pdl_trigger();       // as in argmax_accept
     constexpr int VEC = 16 / sizeof(E);
     const int row = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int T = c.N + 1, b = row / T, t = row % T, V = c.V, nvc = w.n_vchunks;
@@ -231,7 +236,7 @@ sample_accept(spec_cfg c, const typename io_t<IO>::T* __restrict__ logits, spec_
     }
     // kv_len (the noise counter) and the acceptance need every earlier launch
     pdl_wait();
-    pdl_trigger();
+    if (!trigger_first) pdl_trigger();
     __shared__ bool last;
     if (tid == 0) {
         __threadfence();
@@ -450,20 +455,22 @@ cudaError_t launch_commit_k(const spec_cfg& c, const spec_commit_io& io, const s
 
 cudaError_t launch_argmax_accept(const spec_cfg& c, const spec_tree& t, const void* logits,
                                  const spec_commit_io& io, const spec_accept& out, void* ws,
-                                 cudaStream_t st, bool pdl, bool tree_early) {
+                                 cudaStream_t st, bool pdl, bool tree_early, bool trigger_first) {
     const WsLayout w = ws_layout(c);
     dim3 g1(w.argmax_split, c.B * (c.N + 1));
     return c.io_dtype == SPEC_IO_BF16
         ? launch_k(pdl, argmax_accept<SPEC_IO_BF16>, g1, dim3(NT), 0, st, c,
-                   static_cast<const __nv_bfloat16*>(logits), t, io, out, ws, w, tree_early)
+                   static_cast<const __nv_bfloat16*>(logits), t, io, out, ws, w, tree_early,
+                   trigger_first)
         : launch_k(pdl, argmax_accept<SPEC_IO_F32>, g1, dim3(NT), 0, st, c,
-                   static_cast<const float*>(logits), t, io, out, ws, w, tree_early);
+                   static_cast<const float*>(logits), t, io, out, ws, w, tree_early,
+                   trigger_first);
 }
 
 cudaError_t launch_sample_accept(const spec_cfg& c, const spec_tree& t, const void* logits,
                                  float temperature, uint64_t seed, const spec_commit_io& io,
                                  const spec_accept& out, void* ws, cudaStream_t st, bool pdl,
-                                 bool tree_early) {
+                                 bool tree_early, bool trigger_first) {
     const WsLayout w = ws_layout(c);
     dim3 g1((w.n_vchunks + NT / 32 - 1) / (NT / 32), c.B * (c.N + 1));
     const float inv_temp = 1.0f / temperature;
@@ -471,10 +478,10 @@ cudaError_t launch_sample_accept(const spec_cfg& c, const spec_tree& t, const vo
     return c.io_dtype == SPEC_IO_BF16
         ? launch_k(pdl, sample_accept<SPEC_IO_BF16>, g1, dim3(NT), 0, st, c,
                    static_cast<const __nv_bfloat16*>(logits), t, io, out, ws, w, inv_temp, k0, k1,
-                   tree_early)
+                   tree_early, trigger_first)
         : launch_k(pdl, sample_accept<SPEC_IO_F32>, g1, dim3(NT), 0, st, c,
                    static_cast<const float*>(logits), t, io, out, ws, w, inv_temp, k0, k1,
-                   tree_early);
+                   tree_early, trigger_first);
 }
 
 template <int IO>

@@ -221,11 +221,11 @@ int verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_sc
         return static_cast<const char*>(p) + bytes;
     };
     // Launch order (each kernel's wait placement relies on it; see common.cuh):
-    //   tree -> attention partials (layer l, merge of l-1 between) -> argmax +
-    //   acceptance -> GDN layers -> merge of the last attention layer -> commit.
+    //   tree -> attention partials (layer l, merge of l-1 between) -> merge of
+    //   the last attention layer -> argmax + acceptance -> GDN layers -> commit.
     // Attention starts with the tree (its cache blocks do not need it); the
     // acceptance follows the last attention layer, which is the last reader of
-    // kv_len; the GDN layers and the last merge then run before their waits.
+    // kv_len; the merge, the logits scan and the GDN layers then overlap.
     const int na = c.n_attn_layers, ng = c.n_gdn_layers;
     auto attn_args = [&](int l, const void*& q, const void*& kt, const void*& vt, const void*& kc,
                          const void*& vc, void*& o) {
@@ -277,13 +277,28 @@ int verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_sc
                                            /*tree_wait=*/na == 0);
         return cuda_rc(e);
     }
-    // the tree (or the budget selection) is two launches back only when an
-    // attention layer sits between
+    // The last merge comes right after the last partial (it waits for it, then
+    // lets the next launch start).  The acceptance then starts its scan at once
+    // and lets the GDN layers start too: nothing after it reads, before its own
+    // wait, anything it or the merge writes.  The tree is then complete (the
+    // merge waited for the partials, which waited for the tree), unless there is
+    // no attention layer: then the GDN layers wait before they read the tree.
+    // The sampled acceptance keeps one CTA per SM busy through its serial
+    // draw, so it lets the GDN layers start only after its wait.
+    // The commit waits first: it needs the plan and the GDN layers' last read
+    // of h0.
+    if (na > 0 && e == cudaSuccess) {
+        const void *q, *kt, *vt, *kc, *vc;
+        void* o;
+        attn_args(na - 1, q, kt, vt, kc, vc, o);
+        e = spec::launch_attn_merge(c, *tree, o, ws, st, true, (na - 1) & 1, /*early=*/true);
+    }
     if (e == cudaSuccess)
         e = smp ? spec::launch_sample_accept(c, *tree, logits, smp->temperature, smp->seed, *io,
-                                             *out, ws, st, true, /*tree_early=*/na > 0)
+                                             *out, ws, st, true, /*tree_early=*/na > 0,
+                                             /*trigger_first=*/false)
                 : spec::launch_argmax_accept(c, *tree, logits, *io, *out, ws, st, true,
-                                             /*tree_early=*/na > 0);
+                                             /*tree_early=*/na > 0, /*trigger_first=*/true);
     for (int l = 0; l < ng && e == cudaSuccess; ++l) {
         const size_t state = (size_t)l * B * c.Hv * c.dk * c.dv;
         const size_t kq = (size_t)l * B * T * c.Hk * c.dk * esz;
@@ -293,17 +308,9 @@ int verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_sc
                                   at(io->gdn_v, vo * esz), io->alpha + gate, io->beta + gate,
                                   const_cast<char*>(at(step->gdn_o, vo * esz)),
                                   step->gdn_c ? step->gdn_c + vo : nullptr, ws, st, true,
-                                  /*early=*/false, /*trigger_first=*/l == ng - 1 && na > 0);
+                                  /*early=*/na == 0 && !smp);
     }
-    if (na > 0 && e == cudaSuccess) {
-        const void *q, *kt, *vt, *kc, *vc;
-        void* o;
-        attn_args(na - 1, q, kt, vt, kc, vc, o);
-        e = spec::launch_attn_merge(c, *tree, o, ws, st, true, (na - 1) & 1, /*early=*/false);
-    }
-    // the commit may skip its early wait only when a merge sits between it and
-    // the last GDN layer / the acceptance
-    if (e == cudaSuccess) e = spec::launch_commit(c, *io, *out, ws, st, true, /*early=*/na == 0);
+    if (e == cudaSuccess) e = spec::launch_commit(c, *io, *out, ws, st, true, /*early=*/true);
     return cuda_rc(e);
 }
 

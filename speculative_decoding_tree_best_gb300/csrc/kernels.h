@@ -65,16 +65,19 @@ cudaError_t launch_attn_tc(const spec_cfg& c, const spec_tree& t, const void* q,
 // commit run before its pdl_wait (only valid when no GDN layer is the launch
 // just before it).
 // tree_early: the launch that wrote the tree is at least two back, so the
-// kernel may read n_nodes before its programmatic wait.
+// kernel may read n_nodes before its programmatic wait.  trigger_first: the
+// launches after it read nothing it writes before their own waits, so they may
+// start at once (it still waits before the acceptance).
 cudaError_t launch_argmax_accept(const spec_cfg& c, const spec_tree& t, const void* logits,
                                  const spec_commit_io& io, const spec_accept& out, void* ws,
-                                 cudaStream_t st, bool pdl, bool tree_early);
+                                 cudaStream_t st, bool pdl, bool tree_early,
+                                 bool trigger_first = false);
 // Sampled acceptance: each row's token is a draw from softmax(logits /
 // temperature) (Philox4x32-10 noise keyed by seed), then the same walk.
 cudaError_t launch_sample_accept(const spec_cfg& c, const spec_tree& t, const void* logits,
                                  float temperature, uint64_t seed, const spec_commit_io& io,
                                  const spec_accept& out, void* ws, cudaStream_t st, bool pdl,
-                                 bool tree_early);
+                                 bool tree_early, bool trigger_first = false);
 cudaError_t launch_commit(const spec_cfg& c, const spec_commit_io& io, const spec_accept& out,
                           void* ws, cudaStream_t st, bool pdl, bool early);
 // The fused, persistent verify + commit (bf16, d_k = d_v = 128, T <= 32, at
