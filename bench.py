@@ -568,9 +568,13 @@ def run_ours(args, rank, world, local):
                              + (", argmax/accept/GDN verify+commit in one persistent launch"
                                 if args.persistent else ""), "parallelism": "replicas" if world > 1 else "1 GPU"},
         "verify_step_us": ms_step_max * 1e3,
+        "verify_step_us_median_p10_p90": [1e3 * statistics.median(per_ms),
+                                          1e3 * sorted(per_ms)[len(per_ms) // 10],
+                                          1e3 * sorted(per_ms)[(9 * len(per_ms)) // 10]],
         "tree_nodes_per_s": value,
         "step_hbm_gbs": step_gbs,
         "step_roofline_frac": step_gbs / peak,
+        "step_frac_of_nominal_8tbs": step_gbs / 8000.0,
         "phases_us": ph_us,
         "tau_mean": taus,
         "roofline": {"bound": "hbm", "kernel": "attn_tree_verify (split-KV + merge)",
