@@ -71,10 +71,10 @@ def algorithmic_bytes(s: synth.SpecConfig, mean_L: float, tau: float, rows=None)
 ATTN_SOURCES = ("speculative_decoding_tree_best_gb300/csrc/attn_tree_tc.cu",
                 "speculative_decoding_tree_best_gb300/csrc/attn_tree.cu",
                 "speculative_decoding_tree_best_gb300/csrc/common.cuh")
-ATTN_TRAFFIC_SHA256 = "726a904c8ed673869a9bb45852c1dd4ecff27955a46525d7abf343d404b10466"
-ATTN_TRAFFIC_BYTES = {"single": 17164288 + 0 + 3630848 + 0,
-                      "long": 67987968 + 776960 + 4986624 + 0,
-                      "batched": 447560704 + 10724864 + 30551040 + 0}
+ATTN_TRAFFIC_SHA256 = "01f57db2102be4baa6690d652ad9e11d66f13bf8fa726f95107ccea8aeead88d"
+ATTN_TRAFFIC_BYTES = {"single": 17161728 + 0 + 3630848 + 0,
+                      "long": 67984896 + 611584 + 4986112 + 0,
+                      "batched": 447251968 + 10449920 + 30543872 + 0}
 
 
 def attn_traffic(name: str):
