@@ -117,7 +117,6 @@ def run(units, seed, split_pfull=True, NKS=2, NVS=3):
     if not split_pfull:
         bar["PF0"] = Bar(1)
     vconv = [None] * NVS
-    state = {"rescaling": False}
 
     def k_loader():
         J = 0
@@ -171,8 +170,9 @@ def run(units, seed, split_pfull=True, NKS=2, NVS=3):
             k, j, nb = blocks[J]
             yield wait(*pf(J))
             assert buf.get(f"P{J & 1}") == ("P", J) and vconv[J % NVS] == J
-            assert not state["rescaling"]
-            mma([f"P{J & 1}", f"V{J % NVS}"], [("O", ("O", k, j))])
+            # the accumulation reads O as well (the first product of a unit
+            # overwrites it, after the previous unit's epilogue)
+            mma([f"P{J & 1}", f"V{J % NVS}", "O"], [("O", ("O", k, j))])
             commit(f"PVD{J & 1}")
             commit(f"VE{J % NVS}")
             yield from catch_up(J)
