@@ -489,7 +489,11 @@ static cudaError_t launch_commit_io(const spec_cfg& c, const spec_commit_io& io,
                                     const spec_accept& out, void* ws, const WsLayout& w,
                                     cudaStream_t st, bool pdl, bool early) {
     // whole states when they fill the GPU four times over, else 32-column slices
-    const bool whole = (long)c.n_gdn_layers * c.B * c.Hv >= 4L * 152;
+    int dev = 0, sms = 152;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaErrorInvalidDevice;
+    const bool whole = (long)c.n_gdn_layers * c.B * c.Hv >= 4L * sms;
     if (c.dk == 128) {
         if (c.dv == 128)
             return whole ? launch_commit_k<IO, 128, 128, 128>(c, io, out, ws, w, st, pdl, early)
