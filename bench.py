@@ -513,13 +513,27 @@ def run_ours(args, rank, world, local):
     ph_us = {k: 1e3 * statistics.median(v) for k, v in phase.items()}
 
     # ---- end to end through the public API with host buffers ----------------------
-    host_in = {k: x[k].cpu().pin_memory() for k in
-               ("lat_tok", "lat_score", "gdn_q", "gdn_k", "gdn_v", "gdn_alpha", "gdn_beta",
-                "attn_q", "k_tree", "v_tree", "logits", "m_req", "lat_base")
-               if x.get(k) is not None}
+    # The step's inputs arrive in one pinned host buffer and go over in one copy
+    # per step; the step reads them in place (its input tensors are views of
+    # one device buffer, each at a 256-byte boundary).
+    in_keys = [k for k in ("lat_tok", "lat_score", "gdn_q", "gdn_k", "gdn_v", "gdn_alpha",
+                           "gdn_beta", "attn_q", "k_tree", "v_tree", "logits", "m_req", "lat_base")
+               if x.get(k) is not None]
+    offs, total = {}, 0
+    for k in in_keys:
+        offs[k] = total
+        total += (x[k].numel() * x[k].element_size() + 255) // 256 * 256
+    dev_pack = torch.empty(total, dtype=torch.uint8, device=dev)
+    host_pack = torch.empty(total, dtype=torch.uint8).pin_memory()
+    for k in in_keys:
+        n = x[k].numel() * x[k].element_size()
+        view = dev_pack[offs[k]:offs[k] + n].view(x[k].dtype).view(x[k].shape)
+        view.copy_(x[k])
+        host_pack[offs[k]:offs[k] + n].copy_(x[k].cpu().contiguous().view(-1).view(torch.uint8))
+        x[k] = view
     host_out = {k: torch.empty_like(getattr(st.acc, k), device="cpu").pin_memory()
                 for k in ("accept_len", "out_tok")}
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    h2d = total
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
     e2e_ms = []
     for i in range(args.warmup + args.steps):
@@ -527,8 +541,7 @@ def run_ours(args, rank, world, local):
         reset()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for k, t in host_in.items():
-            x[k].copy_(t, non_blocking=True)
+        dev_pack.copy_(host_pack, non_blocking=True)
         st.run()
         for k, t in host_out.items():
             t.copy_(getattr(st.acc, k), non_blocking=True)
