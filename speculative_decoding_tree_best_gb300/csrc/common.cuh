@@ -72,10 +72,9 @@ __device__ __forceinline__ void raise_status(void* ws, uint32_t bits) {
 
 // ---- workspace layout ---------------------------------------------------------
 // byte 0: device status word; then argmax partials, attention split-KV
-// partials, per-(request, kv-head, m-tile) merge tickets and the per-request
-// commit plan written by the acceptance kernel.
+// partials, the per-request commit plan written by the acceptance kernel, and
+// the tickets and queues of the kernels that hand work between CTAs.
 constexpr int kArgmaxSplit = 16;         // CTAs per logits row (upper bound)
-constexpr int kAttnRowsMax = 128 * 2;    // query rows of one (request, kv-head) tile group
 
 struct WsLayout {
     size_t argmax_off;     // float2 [B][T][kArgmaxSplit]: (value, index bits)
@@ -83,7 +82,6 @@ struct WsLayout {
                            // PT = fp16 for bf16 I/O, fp32 for fp32 I/O
     size_t attn_ml_off;    // float2 [B][Hkv][n_mt][n_chunks][128]: (max, sum)
     size_t attn_o_off1, attn_ml_off1;  // a second partial buffer: attention layer l uses l % 2
-    size_t ticket_off;     // uint32 [B][Hkv][n_mt]
     size_t plan_off;       // int32  [B][4]: committed tau (0 = skip), old kv_len
     size_t acc_ticket_off; // uint32 [B]: argmax CTAs (or sampled rows) finished per request
     size_t samp_off;       // float2 [B][T][n_vchunks]: (max, sum of exp) per vocabulary chunk
@@ -147,8 +145,6 @@ static inline WsLayout ws_layout(const spec_cfg& c, int num_sms = 152) {
         w.attn_o_off1 = w.attn_o_off;
         w.attn_ml_off1 = w.attn_ml_off;
     }
-    w.ticket_off = off;
-    off = align_up(off + sizeof(uint32_t) * (size_t)c.B * c.Hkv * w.n_mt, 256);
     w.plan_off = off;
     off = align_up(off + sizeof(int32_t) * 4 * (size_t)c.B, 256);
     w.acc_ticket_off = off;
