@@ -42,7 +42,7 @@ __device__ __forceinline__ uint32_t tie_key(int depth, int parent) {
     return ((uint32_t)(255 - depth) << 8) | (uint32_t)(255 - parent);
 }
 
-// SLOTS = rows per lane (1 for trees of up to 32 rows, else 2 or 4).
+// SLOTS = rows per lane: ceil(T / 32), 1 to 4.
 template <int SLOTS>
 __global__ void __launch_bounds__(32)
 tree_build_kernel(spec_cfg c, const int32_t* __restrict__ lat_tok,
@@ -356,6 +356,9 @@ cudaError_t launch_tree_build(const spec_cfg& c, const int32_t* lat_tok, const f
                         lat_score, root_tok, out, ws, m_req);
     if (T <= 64)
         return launch_k(pdl, tree_build_kernel<2>, dim3(c.B), dim3(32), smem, st, c, lat_tok,
+                        lat_score, root_tok, out, ws, m_req);
+    if (T <= 96)
+        return launch_k(pdl, tree_build_kernel<3>, dim3(c.B), dim3(32), smem, st, c, lat_tok,
                         lat_score, root_tok, out, ws, m_req);
     return launch_k(pdl, tree_build_kernel<4>, dim3(c.B), dim3(32), smem, st, c, lat_tok,
                     lat_score, root_tok, out, ws, m_req);
