@@ -75,3 +75,10 @@ def test_reference_arm_under_torchrun_prints_one_line():
     assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
     assert rec["cpu_baseline"]["kind"] == "oracle"
     assert rec["e2e"]["h2d_bytes_per_step"] == 0
+    # the rest of the line's contract
+    for k in ("metric", "unit", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+              "vs_baseline", "dtype", "data", "config"):
+        assert k in rec, k
+    assert rec["steps"] == 3 and rec["warmup"] == 3 and rec["higher_is_better"] is True
+    assert rec["cpu_baseline"]["cores"] >= 1 and rec["cpu_baseline"]["value"] == rec["value"]
+    assert rec["e2e"]["value"] == rec["value"] and "workload" in rec["config"]
