@@ -19,17 +19,13 @@ using namespace gdn_tc;
 // One CTA = one (request, v-head) item; 66 KB of shared memory: three CTAs
 // share an SM.  early: the tree may come from the launch just before, so the
 // programmatic wait precedes the first read of it; otherwise it ends the kernel.
-// trigger_first: the launch after this one reads nothing this one writes (the
-// last merge of the fused step), so it may start at once; it still waits for
-// this launch's completion before it completes.
 __global__ void __launch_bounds__(NT, 3)
 gdn_tc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mq,
               const __grid_constant__ CUtensorMap mv, spec_cfg c, spec_tree tree,
               const float* __restrict__ h0, const float* __restrict__ alpha,
               const float* __restrict__ beta, __nv_bfloat16* __restrict__ o,
-              float* __restrict__ c_out, void* ws, bool early, bool trigger_first) {
+              float* __restrict__ c_out, void* ws, bool early) {
     extern __shared__ unsigned char smem_raw[];
-    if (trigger_first) pdl_trigger();
     unsigned char* sm = aligned_base(smem_raw);
     const Layout L = layout(false);
     const uint32_t tmem = setup(sm, L);
@@ -60,8 +56,7 @@ bool gdn_tc_supported(const spec_cfg& c) {
 
 cudaError_t launch_gdn_tc(const spec_cfg& c, const spec_tree& t, const float* h0, const void* q,
                           const void* k, const void* v, const float* alpha, const float* beta,
-                          void* o, float* c_out, void* ws, cudaStream_t st, bool pdl, bool early,
-                          bool trigger_first) {
+                          void* o, float* c_out, void* ws, cudaStream_t st, bool pdl, bool early) {
     const int T = c.N + 1;
     const Layout L = layout(false);
     CUtensorMap mk, mq, mv;
@@ -73,8 +68,7 @@ cudaError_t launch_gdn_tc(const spec_cfg& c, const spec_tree& t, const float* h0
                                          (int)L.total);
     if (e != cudaSuccess) return e;
     return launch_k(pdl, gdn_tc_kernel, dim3(c.Hv, c.B), dim3(NT), L.total, st, mk, mq, mv, c, t,
-                    h0, alpha, beta, static_cast<__nv_bfloat16*>(o), c_out, ws, early,
-                    trigger_first);
+                    h0, alpha, beta, static_cast<__nv_bfloat16*>(o), c_out, ws, early);
 }
 
 }  // namespace spec
