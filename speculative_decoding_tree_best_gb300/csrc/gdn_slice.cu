@@ -1,0 +1,426 @@
+// gdn_slice.cu -- tree-masked Gated DeltaNet, bf16 I/O, d_k = d_v = 128, trees
+// of up to 32 rows: one CTA per (request, v-head, 64-column half of the state).
+//
+// Digest "SpecPilot ...": prerequisites / hybrid recurrent target (gated delta
+// rule h_t = a_t (I - b_t k_t k_t^T) h_{t-1} + b_t k_t v_t^T, o_t = h_t^T q_t)
+// and technical novelty (recompute along the root path, no per-node
+// snapshots).  With c_t = b_t v_t - a_t b_t u_t and u_t = h_par^T k_t, one step
+// is h_t = a_t h_par + k_t c_t^T, so along a root path
+//     c_x = b_x v_x - a_x b_x A_par Pk_x + sum_{a on path(par)} w_xa c_a
+//     o_x = A_x Pq_x + sum_{a on path(x)} dec(a -> x) (k_a . q_x) c_a
+// with w_xa = -a_x b_x dec(a -> par) (k_a . k_x) and P = h0^T [K; Q] the only
+// d_k x d_v-sized work.  Every state column evolves on its own once P, the
+// Gram rows [K; Q] K^T and the decays exist, so the state is cut into two
+// column halves and each CTA owns one.  Four warps, two roles:
+//
+//  * warps 2/3 split the half's fp32 state (TMA-staged, 128 rows x 64
+//    columns) into two bf16 terms (hi = h truncated to bf16, lo = bf16(h - hi):
+//    ~16 significant bits), in place, one 64-row half of d_k at a time, and
+//    after each half issue its tcgen05 products
+//        D[col][x] += sum_k h0[k][col] [K; Q][x][k]    (state as MN-major A)
+//    so that tensor-memory lane `col` holds that column's Pk_x, Pq_x;
+//  * warp 0 issues the TMA copies and, once K and Q are in, the Gram rows
+//    G = [K; Q] K^T (exact bf16 products) into tensor memory; then warps 0/1
+//    turn Gram row x (lane x) and the tree into the weight row of c_x (warp 0)
+//    or o_x (warp 1): decay x Gram entry on the root path, zero elsewhere.
+//    After the products they run, one state column per lane, the write-vector
+//    recursion with the write vectors in registers and no branch
+//    (right-looking: row x adds its weighted c_x into every later row, two
+//    rows per packed FMA, so a row waits for one FMA after its predecessor;
+//    padding rows carry zero weights), then every output o_x from the same
+//    registers.
+//
+// 54 KB of shared memory and 128 tensor-memory columns per CTA: four CTAs per
+// SM, so one CTA's state stream overlaps the others' arithmetic.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "gdn_tc_body.cuh"
+#include "kernels.h"
+#include "tc_util.cuh"
+
+namespace spec {
+
+namespace {
+
+using namespace tc;
+
+constexpr int DKV = 128;                 // d_k = d_v
+constexpr int SW = 64;                   // state columns per CTA
+constexpr int NSL = DKV / SW;            // column halves per state
+constexpr int NT = 128;                  // threads per CTA
+constexpr int TP = 32;                   // tree rows (padded)
+constexpr uint32_t kTmemCols = 128;      // P^T: 64 columns ([K; Q] rows), Gram rows: 32
+constexpr int WS = TP + 4;               // row stride of the o weights
+
+// byte offsets from the 1024-aligned base
+constexpr uint32_t OFF_KQ = 0;                           // [2 halves][64 rows][64] bf16, swizzled
+constexpr uint32_t OFF_ST = OFF_KQ + 2 * 64 * 128;       // fp32 [128][64]; in place, per 64-row
+                                                         // half h: lo tile, then hi tile
+constexpr uint32_t OFF_V = OFF_ST + DKV * SW * 4;        // bf16 [32 rows][64]
+constexpr uint32_t OFF_SM = OFF_V + TP * SW * 2;         // al be A ca [32] fp32
+constexpr uint32_t OFF_BAR = OFF_SM + 4 * TP * 4;        // 4 mbarriers, TMEM slot
+constexpr uint32_t SMEM_BYTES = OFF_BAR + 48 + 1024;     // + alignment slack
+// the weights WuT[a][y] (c_a in c_y) and Wo[x][WS] (c_a in o_x) fp32 go over
+// the K/Q tile once every product has read it
+constexpr uint32_t OFF_WU = OFF_KQ;
+constexpr uint32_t OFF_WO = OFF_KQ + TP * TP * 4;
+constexpr uint32_t TX_KQV = 4 * TP * 128 + TP * SW * 2;  // K, Q (two halves each), v
+constexpr uint32_t TX_ST = DKV * SW * 4;                 // the state half
+constexpr uint32_t TILE = 64 * SW * 2;                   // one bf16 term of 64 d_k rows: 8 KB
+constexpr uint32_t LBO_A = 1024;                         // A rows 64..127 (unused): any smem
+
+static_assert(OFF_WO + TP * WS * 4 <= OFF_ST, "weights fit over the K/Q tile");
+// the Gram products read A rows 64..127 past each 64-row half of the K/Q tile:
+// for the second half those rows are the staged state (valid shared memory);
+// the state products read their unused rows LBO_A past each tile
+static_assert(OFF_KQ + 64 * 128 + 128 * 128 <= OFF_ST + DKV * SW * 4, "A rows stay in smem");
+static_assert(OFF_ST + 3 * TILE + TILE + LBO_A <= OFF_BAR, "A rows stay in smem");
+
+__device__ __forceinline__ unsigned char* align1024(unsigned char* raw) {
+    return reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+// (x, y) -> bf16x2 of x and y truncated to their upper 16 bits (x in the low half)
+__device__ __forceinline__ uint32_t bf16x2_trunc(float x, float y) {
+    return __byte_perm(__float_as_uint(x), __float_as_uint(y), 0x7632);
+}
+__device__ __forceinline__ float trunc_rest(float x) {
+    return x - __uint_as_float(__float_as_uint(x) & 0xffff0000u);
+}
+__device__ __forceinline__ uint32_t bf16x2_rn(float x, float y) {
+    __nv_bfloat162 t = __floats2bfloat162_rn(x, y);
+    return *reinterpret_cast<uint32_t*>(&t);
+}
+
+// named barrier for a pair of warps (ids 1, 2; 0 is __syncthreads)
+__device__ __forceinline__ void pair_sync(int id) {
+    asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+}
+
+// Grid (NSL x Hv, B): block x = j NSL + half, so the CTAs sharing a q-k head's
+// K/Q rows are adjacent.  early: the tree may come from the launch just
+// before, so the programmatic wait precedes the first read of it; otherwise
+// the tree is complete at the start (read at once) and the wait ends the
+// kernel.
+__global__ void __launch_bounds__(NT, 4)
+gdn_slice_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__ CUtensorMap mk,
+                 const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mv,
+                 spec_cfg c, spec_tree tree, const float* __restrict__ alpha,
+                 const float* __restrict__ beta, __nv_bfloat16* __restrict__ o,
+                 float* __restrict__ c_out, void* ws, bool early) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = align1024(smem_raw);
+    const int T = c.N + 1, Hv = c.Hv;
+    const int j = blockIdx.x / NSL, sl = blockIdx.x % NSL, b = blockIdx.y;
+    const int ih = j / (Hv / c.Hk);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int row0 = b * T, col0 = sl * SW;
+    // [0] K/Q/v in, [1] state in, [2] state products done, [3] Gram products done
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 4);
+    float* al = reinterpret_cast<float*>(sm + OFF_SM);
+    float* be = al + TP;
+    float* A = be + TP;
+    float* ca = A + TP;                        // -alpha_x beta_x A_par(x)
+    int nn = 0;
+    uint32_t anc = 0;
+    auto read_tree = [&]() {
+        nn = tree.n_nodes[b];
+        nn = nn < 1 ? 1 : (nn > T ? T : nn);
+        if (warp < 2)
+            anc = lane < nn ? static_cast<uint32_t>(tree.node_anc[2 * ((size_t)b * T + lane)]) : 0u;
+    };
+    if (!early) read_tree();
+
+    // ---- TMA first, then the tensor memory ------------------------------------------------
+    if (tid == 0) {
+        for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&bar[1], TX_ST);
+        tma_load_2d(sm + OFF_ST, &mh, &bar[1], col0, (b * Hv + j) * DKV);
+        mbar_arrive_expect_tx(&bar[0], TX_KQV);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            tma_load_3d(sm + OFF_KQ + h * 64 * 128, &mk, &bar[0], h * 64, ih, row0);
+            tma_load_3d(sm + OFF_KQ + h * 64 * 128 + TP * 128, &mq, &bar[0], h * 64, ih, row0);
+        }
+        tma_load_3d(sm + OFF_V, &mv, &bar[0], col0, j, row0);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    if (tid < TP) {
+        al[tid] = tid < T ? alpha[((size_t)b * T + tid) * Hv + j] : 0.0f;
+        be[tid] = tid < T ? beta[((size_t)b * T + tid) * Hv + j] : 0.0f;
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t kq_s = smem_u32(sm + OFF_KQ), st_s = smem_u32(sm + OFF_ST);
+    bool ok = true;
+
+    if (warp >= 2) {
+        // ---- state split and products (warps 2/3) ---------------------------------------
+        const int t = tid - 64;                // 0..63
+        ok = mbar_wait(&bar[1], 0, nullptr);
+        ok = __all_sync(0xffffffffu, ok);
+        const uint32_t idp = idesc_bf16_f32(128, 2 * TP, /*a_mn=*/true, /*b_mn=*/false);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            // d_k rows 64 h .. 64 h + 63 (16 KB of fp32 at OFF_ST + 16 KB h); unit
+            // u = t + 64 i: row 64 h + u / 8, columns 8 (u % 8) .. + 7
+            const float4* hs = reinterpret_cast<const float4*>(sm + OFF_ST + h * 2 * TILE);
+            float4 xv[16];
+            if (ok) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    xv[2 * i] = hs[2 * (t + 64 * i)];
+                    xv[2 * i + 1] = hs[2 * (t + 64 * i) + 1];
+                }
+            }
+            pair_sync(1);                      // both warps hold their values
+            if (ok) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int u = t + 64 * i, k = u >> 3, ch = u & 7;
+                    const float4 a = xv[2 * i], e = xv[2 * i + 1];
+                    const uint4 hi = make_uint4(bf16x2_trunc(a.x, a.y), bf16x2_trunc(a.z, a.w),
+                                                bf16x2_trunc(e.x, e.y), bf16x2_trunc(e.z, e.w));
+                    const uint4 lo = make_uint4(bf16x2_rn(trunc_rest(a.x), trunc_rest(a.y)),
+                                                bf16x2_rn(trunc_rest(a.z), trunc_rest(a.w)),
+                                                bf16x2_rn(trunc_rest(e.x), trunc_rest(e.y)),
+                                                bf16x2_rn(trunc_rest(e.z), trunc_rest(e.w)));
+                    const uint32_t off = sw128_offset(k, ch * 8);
+                    *reinterpret_cast<uint4*>(sm + OFF_ST + h * 2 * TILE + off) = lo;
+                    *reinterpret_cast<uint4*>(sm + OFF_ST + h * 2 * TILE + TILE + off) = hi;
+                }
+                fence_async_smem();
+            }
+            pair_sync(1);
+            if (ok && t == 0) {
+                tc_fence_after();
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t a_s = st_s + h * 2 * TILE + part * TILE + kk * 2048;
+                        const uint32_t b_s = kq_s + h * 64 * 128 + kk * 32;
+                        mma_bf16(tmem, sdesc_sw128(a_s, LBO_A, 1024), sdesc_sw128(b_s, 16, 1024),
+                                 idp, (h | part | kk) != 0);
+                    }
+                }
+            }
+        }
+        if (t == 0) mma_commit(&bar[2]);       // also when nothing was issued
+        if (early) {
+            pdl_wait();
+            pdl_trigger();
+        }
+    } else {
+        // ---- Gram rows (thread 0) and the weights (warps 0/1) ---------------------------
+        if (tid == 0) {
+            ok = mbar_wait(&bar[0], 0, nullptr);
+            if (ok) {
+                const uint32_t idg = idesc_bf16_f32(128, TP, false, false);
+#pragma unroll
+                for (int ks = 0; ks < DKV / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * 64 * 128 + (ks & 3) * 32;
+                    mma_bf16(tmem + 2 * TP, sdesc_sw128(kq_s + off, 16, 1024),
+                             sdesc_sw128(kq_s + off, 16, 1024), idg, ks != 0);
+                }
+            }
+            mma_commit(&bar[3]);
+        }
+        ok = __all_sync(0xffffffffu, __shfl_sync(0xffffffffu, ok, 0) && mbar_wait(&bar[3], 0, nullptr));
+        if (warp == 1) ok = ok && mbar_wait(&bar[0], 0, nullptr);   // (warp 0 knows via thread 0)
+        ok = __all_sync(0xffffffffu, ok);
+        float w[TP];
+        float acc = 1.0f;
+        if (early) {
+            pdl_wait();
+            pdl_trigger();
+            read_tree();
+        }
+        if (ok) {
+            tc_fence_after();
+            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 2 * TP, w);   // Gram row (lane x)
+            tmem_wait_ld();
+            const int x = lane;
+            const uint32_t path = warp == 0 ? anc & ~(1u << x) : anc;     // parent's path / x's
+#pragma unroll
+            for (int a = TP - 1; a >= 0; --a) {
+                const bool on = (path >> a) & 1u;
+                w[a] = on ? acc * w[a] : 0.0f;
+                acc = on ? acc * al[a] : acc;
+            }
+            if (warp == 0) {
+                const float s = -al[x] * be[x];
+#pragma unroll
+                for (int a = 0; a < TP; ++a) w[a] *= s;
+                ca[x] = s * acc;
+            } else {
+                A[x] = acc;
+            }
+        }
+        // the K/Q tile is free once the state products are done
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(&bar[2], 0, nullptr));
+        if (ok) {
+            tc_fence_after();
+            if (warp == 0) {
+                float* WuT = reinterpret_cast<float*>(sm + OFF_WU);
+#pragma unroll
+                for (int a = 0; a < TP; ++a) WuT[a * TP + lane] = w[a];
+            } else {
+                float4* Wo = reinterpret_cast<float4*>(sm + OFF_WO + lane * WS * 4);
+#pragma unroll
+                for (int a4 = 0; a4 < TP / 4; ++a4)
+                    Wo[a4] = make_float4(w[4 * a4], w[4 * a4 + 1], w[4 * a4 + 2], w[4 * a4 + 3]);
+            }
+        }
+        pair_sync(2);
+
+        // ---- write vectors and outputs: one state column per lane ---------------------
+        if (ok) {
+            const int cl = warp * 32 + lane;   // column in the half = tensor-memory lane
+            const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+            float pk[TP];
+            tmem_ld32(tl, pk);                 // Pk_x of this column, x = 0..31
+            tmem_wait_ld();
+            const float* WuT = reinterpret_cast<const float*>(sm + OFF_WU);
+            const __nv_bfloat16* vs = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_V);
+            float2 u[TP / 2];                  // rows 2p, 2p + 1
+#pragma unroll
+            for (int p = 0; p < TP / 2; ++p) {
+                u[p].x = fmaf(be[2 * p], __bfloat162float(vs[(2 * p) * SW + cl]), ca[2 * p] * pk[2 * p]);
+                u[p].y = fmaf(be[2 * p + 1], __bfloat162float(vs[(2 * p + 1) * SW + cl]),
+                              ca[2 * p + 1] * pk[2 * p + 1]);
+            }
+#pragma unroll
+            for (int x = 0; x < TP - 1; ++x) {
+                const float cx = (x & 1) ? u[x >> 1].y : u[x >> 1].x;   // final
+                const float2 cxx = make_float2(cx, cx);
+#pragma unroll
+                for (int q = (x + 1) / 4; q < TP / 4; ++q) {         // rows 4q .. 4q + 3
+                    const float4 wq = *reinterpret_cast<const float4*>(WuT + x * TP + 4 * q);
+                    if (4 * q > x) {
+                        u[2 * q] = __ffma2_rn(make_float2(wq.x, wq.y), cxx, u[2 * q]);
+                    } else if (4 * q + 1 > x) {
+                        u[2 * q].y = fmaf(wq.y, cx, u[2 * q].y);
+                    }
+                    if (4 * q + 2 > x) {
+                        u[2 * q + 1] = __ffma2_rn(make_float2(wq.z, wq.w), cxx, u[2 * q + 1]);
+                    } else {
+                        u[2 * q + 1].y = fmaf(wq.w, cx, u[2 * q + 1].y);
+                    }
+                }
+            }
+            // padding rows' write vectors read as zero (their inputs may be anything)
+#pragma unroll
+            for (int p = 0; p < TP / 2; ++p) {
+                if (2 * p >= nn) u[p].x = 0.0f;
+                if (2 * p + 1 >= nn) u[p].y = 0.0f;
+            }
+            const size_t rs = (size_t)Hv * DKV;                          // row stride
+            const size_t ob = ((size_t)b * T * Hv + j) * DKV + col0 + cl;
+            if (c_out) {
+#pragma unroll
+                for (int p = 0; p < TP / 2; ++p) {
+                    if (2 * p < T) c_out[ob + (2 * p) * rs] = u[p].x;
+                    if (2 * p + 1 < T) c_out[ob + (2 * p + 1) * rs] = u[p].y;
+                }
+            }
+            float pq[TP];
+            tmem_ld32(tl + TP, pq);            // Pq_x of this column
+            tmem_wait_ld();
+            const float* Wo = reinterpret_cast<const float*>(sm + OFF_WO);
+#pragma unroll
+            for (int x = 0; x < TP; ++x) {
+                if (x >= T) break;
+                // pairs p <= x / 2 cover every a <= x (the weights beyond x are zero)
+                float2 acc2 = make_float2(A[x] * pq[x], 0.0f);
+#pragma unroll
+                for (int q = 0; q <= x / 4; ++q) {
+                    const float4 wq = *reinterpret_cast<const float4*>(Wo + x * WS + 4 * q);
+                    acc2 = __ffma2_rn(make_float2(wq.x, wq.y), u[2 * q], acc2);
+                    if (4 * q + 2 <= x) acc2 = __ffma2_rn(make_float2(wq.z, wq.w), u[2 * q + 1], acc2);
+                }
+                o[ob + x * rs] = __float2bfloat16_rn(x < nn ? acc2.x + acc2.y : 0.0f);
+            }
+        }
+    }
+
+    // ---- teardown ------------------------------------------------------------------------
+    ok = __syncthreads_and(ok);
+    if (!ok) {
+        raise_status(ws, SPEC_DEV_TIMEOUT);
+        if (tid == 0) {      // let the copies and the products land before leaving
+            for (int i = 0; i < 4; ++i) mbar_wait(&bar[i], 0, nullptr);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    if (!early) {
+        pdl_wait();
+        pdl_trigger();
+    }
+}
+
+// fp32 state [rows][128] as a 2-D tensor map, box {64 columns, 128 rows}.
+bool state_map(CUtensorMap* m, const float* base, int rows) {
+    gdn_tc::EncodeTiledFn enc = gdn_tc::encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)DKV, (cuuint64_t)rows};
+    cuuint64_t str[1] = {(cuuint64_t)DKV * 4};
+    cuuint32_t box[2] = {(cuuint32_t)SW, (cuuint32_t)DKV};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, str, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// bf16 rows [rows][H][128] as a 3-D tensor map, box {64 columns, 1, TP rows}.
+bool vslice_map(CUtensorMap* m, const void* base, int H, int rows) {
+    gdn_tc::EncodeTiledFn enc = gdn_tc::encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)DKV, (cuuint64_t)H, (cuuint64_t)rows};
+    cuuint64_t str[2] = {(cuuint64_t)DKV * 2, (cuuint64_t)H * DKV * 2};
+    cuuint32_t box[3] = {(cuuint32_t)SW, 1, (cuuint32_t)TP};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, str, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool gdn_slice_supported(const spec_cfg& c) {
+    return c.io_dtype == SPEC_IO_BF16 && c.dk == DKV && c.dv == DKV && c.N + 1 <= TP &&
+           gdn_tc::encode_fn() != nullptr;
+}
+
+cudaError_t launch_gdn_slice(const spec_cfg& c, const spec_tree& t, const float* h0,
+                             const void* q, const void* k, const void* v, const float* alpha,
+                             const float* beta, void* o, float* c_out, void* ws, cudaStream_t st,
+                             bool pdl, bool early) {
+    const int T = c.N + 1;
+    CUtensorMap mh, mk, mq, mv;
+    if (!state_map(&mh, h0, c.B * c.Hv * DKV) ||
+        !gdn_tc::rows_map(&mk, k, c.Hk, c.B * T, TP, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !gdn_tc::rows_map(&mq, q, c.Hk, c.B * T, TP, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !vslice_map(&mv, v, c.Hv, c.B * T))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(gdn_slice_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    // without programmatic launch the tree is complete when the kernel starts
+    return launch_k(pdl, gdn_slice_kernel, dim3(NSL * c.Hv, c.B), dim3(NT), SMEM_BYTES, st, mh,
+                    mk, mq, mv, c, t, alpha, beta, static_cast<__nv_bfloat16*>(o), c_out, ws,
+                    early && pdl);
+}
+
+}  // namespace spec

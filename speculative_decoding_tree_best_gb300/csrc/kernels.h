@@ -32,12 +32,14 @@ cudaError_t launch_gdn_tree(const spec_cfg& c, const spec_tree& t, const float* 
                             const void* q, const void* k, const void* v, const float* alpha,
                             const float* beta, void* o, float* c_out, void* ws, cudaStream_t st,
                             bool pdl = false, bool early = true);
-// tensor-core variant (bf16 I/O, d_k = d_v = 128): launch_gdn_tree uses it when supported
-bool gdn_tc_supported(const spec_cfg& c);
-cudaError_t launch_gdn_tc(const spec_cfg& c, const spec_tree& t, const float* h0, const void* q,
-                          const void* k, const void* v, const float* alpha, const float* beta,
-                          void* o, float* c_out, void* ws, cudaStream_t st, bool pdl, bool early);
 size_t gdn_tree_smem(const spec_cfg& c);
+// tensor-core variant (bf16 I/O, d_k = d_v = 128, T <= 32): one CTA per
+// (request, v-head, 64 state columns); launch_gdn_tree uses it when supported
+bool gdn_slice_supported(const spec_cfg& c);
+cudaError_t launch_gdn_slice(const spec_cfg& c, const spec_tree& t, const float* h0,
+                             const void* q, const void* k, const void* v, const float* alpha,
+                             const float* beta, void* o, float* c_out, void* ws, cudaStream_t st,
+                             bool pdl, bool early);
 
 cudaError_t launch_attn_tree(const spec_cfg& c, const spec_tree& t, const void* q,
                              const void* k_tree, const void* v_tree, const void* k_cache,

@@ -111,3 +111,37 @@ def test_lossy_gdn_shortcut_is_rejected(clean):
     sut.gdn_o[:, :, :, 0] *= 1.01         # one head 1% off: rel-L2 ~5e-3
     with pytest.raises(AssertionError, match="GDN"):
         parity.compare(scfg, inp, tree, sut)
+
+
+def _bigger():
+    """A case with enough rows that one bad row hides in the whole-tensor
+    figure: 2 requests, N = 20, 8 v-heads / 8 q-heads."""
+    scfg = synth.config(0).replace(B=2, m=4, K=4, N=20, Hk=4, Hv=8, Hq=8, Hkv=2, L=64, V=256)
+    inp, tree = parity.prepare(scfg, 5)
+    return scfg, inp, tree
+
+
+@pytest.mark.parametrize("what", ["gdn", "attn", "state"])
+def test_one_bad_row_is_caught_by_the_row_bound(what):
+    """A 2% error on a single (request, node, head) row -- or on one row of one
+    committed state -- stays under the whole-tensor 2e-3 bound but breaks the
+    per-row bound."""
+    scfg, inp, tree = _bigger()
+    sut = _oracle_system(scfg, _clone(inp))
+    if what == "gdn":
+        sut.gdn_o[0, 1, 7, 3] *= 1.02                      # request 1, node 7, v-head 3
+        t = sut.gdn_o[0]
+    elif what == "attn":
+        sut.attn_o[0, 0, 12, 5] *= 1.02                    # request 0, node 12, q-head 5
+        t = sut.attn_o[0]
+    else:
+        sut.x["gdn_h0"][0, 1, 2, 17] *= 1.02               # request 1, v-head 2, d_k row 17
+        t = sut.x["gdn_h0"][0]
+    assert float(t.double().norm()) > 0
+    with pytest.raises(AssertionError, match="row"):
+        parity.compare(scfg, inp, tree, sut)
+    # the whole-tensor figure alone would have let it through
+    clean_sut = _oracle_system(scfg, _clone(inp))
+    ref = {"gdn": clean_sut.gdn_o[0], "attn": clean_sut.attn_o[0],
+           "state": clean_sut.x["gdn_h0"][0]}[what]
+    assert parity.rel_l2(t.double().numpy(), ref.double().numpy()) < parity.REL_L2
