@@ -30,8 +30,8 @@
 //    padding rows carry zero weights), then every output o_x from the same
 //    registers.
 //
-// 54 KB of shared memory and 128 tensor-memory columns per CTA: four CTAs per
-// SM, so one CTA's state stream overlaps the others' arithmetic.
+// 66 KB of shared memory and 128 tensor-memory columns per CTA: three CTAs per
+// SM, each with two items in flight.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -57,25 +57,25 @@ constexpr int WS = TP + 4;               // row stride of the o weights
 constexpr uint32_t OFF_KQ = 0;                           // [2 halves][64 rows][64] bf16, swizzled
 constexpr uint32_t OFF_ST = OFF_KQ + 2 * 64 * 128;       // fp32 [128][64]; in place, per 64-row
                                                          // half h: lo tile, then hi tile
-constexpr uint32_t OFF_V = OFF_ST + DKV * SW * 4;        // bf16 [32 rows][64]
-constexpr uint32_t OFF_SM = OFF_V + TP * SW * 2;         // al be A ca [32] fp32
-constexpr uint32_t OFF_BAR = OFF_SM + 4 * TP * 4;        // 4 mbarriers, TMEM slot
-constexpr uint32_t SMEM_BYTES = OFF_BAR + 48 + 1024;     // + alignment slack
-// the weights WuT[a][y] (c_a in c_y) and Wo[x][WS] (c_a in o_x) fp32 go over
-// the K/Q tile once every product has read it
-constexpr uint32_t OFF_WU = OFF_KQ;
-constexpr uint32_t OFF_WO = OFF_KQ + TP * TP * 4;
+constexpr uint32_t OFF_V = OFF_ST + DKV * SW * 4;        // bf16 [2 items][32 rows][64]
+constexpr uint32_t OFF_WU = OFF_V + 2 * TP * SW * 2;     // WuT[a][y]: c_a in c_y
+constexpr uint32_t OFF_WO = OFF_WU + TP * TP * 4;        // Wo[x][WS]: c_a in o_x
+constexpr uint32_t OFF_SM = OFF_WO + TP * WS * 4;        // al be [2][32], A ca [32] fp32
+constexpr int NBAR = 5;
+constexpr uint32_t OFF_BAR = OFF_SM + 6 * TP * 4;        // mbarriers, TMEM slot, abort flag
+constexpr uint32_t SMEM_BYTES = OFF_BAR + 8 * NBAR + 16 + 1024;   // + alignment slack
 constexpr uint32_t TX_KQV = 4 * TP * 128 + TP * SW * 2;  // K, Q (two halves each), v
 constexpr uint32_t TX_ST = DKV * SW * 4;                 // the state half
 constexpr uint32_t TILE = 64 * SW * 2;                   // one bf16 term of 64 d_k rows: 8 KB
 constexpr uint32_t LBO_A = 1024;                         // A rows 64..127 (unused): any smem
 
-static_assert(OFF_WO + TP * WS * 4 <= OFF_ST, "weights fit over the K/Q tile");
 // the Gram products read A rows 64..127 past each 64-row half of the K/Q tile:
 // for the second half those rows are the staged state (valid shared memory);
 // the state products read their unused rows LBO_A past each tile
 static_assert(OFF_KQ + 64 * 128 + 128 * 128 <= OFF_ST + DKV * SW * 4, "A rows stay in smem");
 static_assert(OFF_ST + 3 * TILE + TILE + LBO_A <= OFF_BAR, "A rows stay in smem");
+static_assert(OFF_BAR % 8 == 0 && OFF_WO % 16 == 0, "alignment");
+static_assert(3 * (SMEM_BYTES + 1024) <= 228 * 1024, "three CTAs per SM");
 
 __device__ __forceinline__ unsigned char* align1024(unsigned char* raw) {
     return reinterpret_cast<unsigned char*>(
@@ -99,90 +99,131 @@ __device__ __forceinline__ void pair_sync(int id) {
     asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
 }
 
-// Grid (NSL x Hv, B): block x = j NSL + half, so the CTAs sharing a q-k head's
-// K/Q rows are adjacent.  early: the tree may come from the launch just
-// before, so the programmatic wait precedes the first read of it; otherwise
-// the tree is complete at the start (read at once) and the wait ends the
-// kernel.
-__global__ void __launch_bounds__(NT, 4)
+__device__ __forceinline__ bool pair_sync_and(int id, bool p) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.and.pred po, %2, 64, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)p), "r"(id)
+        : "memory");
+    return r != 0;
+}
+
+struct ItemIdx {
+    int b, j, sl, ih;
+};
+__device__ __forceinline__ ItemIdx decode(int it, const spec_cfg& c) {
+    ItemIdx d;
+    const int hj = it / NSL;
+    d.sl = it % NSL;
+    d.b = hj / c.Hv;
+    d.j = hj % c.Hv;
+    d.ih = d.j / (c.Hv / c.Hk);
+    return d;
+}
+
+// A persistent grid of at most three CTAs per SM runs the items (request,
+// v-head, column half) it = blockIdx.x, blockIdx.x + gridDim.x, ...  Item
+// it + 1 of the same (request, v-head) is its other column half, so the CTAs
+// running at one time share K/Q rows in L2.  Per item k of a CTA, the four
+// mbarriers [0] K/Q/v in, [1] state in, [2] state products done, [3] Gram
+// rows done complete once (parity k & 1), and [4] (P^T read, tensor memory
+// free) completes once its outputs are done.  As soon as item k's products
+// have read the staging buffer and the K/Q tile, item k + 1's state and K/Q/v
+// copies start (v into the other of two buffers), so warps 2/3 split item
+// k + 1's state while warps 0/1 run item k's rows.  early: the tree may come
+// from the launch just before, so the programmatic wait precedes the first
+// read of it; otherwise the wait ends the kernel.
+__global__ void __launch_bounds__(NT, 3)
 gdn_slice_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__ CUtensorMap mk,
                  const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mv,
                  spec_cfg c, spec_tree tree, const float* __restrict__ alpha,
                  const float* __restrict__ beta, __nv_bfloat16* __restrict__ o,
-                 float* __restrict__ c_out, void* ws, bool early) {
+                 float* __restrict__ c_out, void* ws, bool early, int n_items) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = align1024(smem_raw);
-    const int T = c.N + 1, Hv = c.Hv;
-    const int j = blockIdx.x / NSL, sl = blockIdx.x % NSL, b = blockIdx.y;
-    const int ih = j / (Hv / c.Hk);
+    const int T = c.N + 1, Hv = c.Hv, G = gridDim.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int row0 = b * T, col0 = sl * SW;
-    // [0] K/Q/v in, [1] state in, [2] state products done, [3] Gram products done
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 4);
-    float* al = reinterpret_cast<float*>(sm + OFF_SM);
-    float* be = al + TP;
-    float* A = be + TP;
-    float* ca = A + TP;                        // -alpha_x beta_x A_par(x)
-    int nn = 0;
-    uint32_t anc = 0;
-    auto read_tree = [&]() {
-        nn = tree.n_nodes[b];
-        nn = nn < 1 ? 1 : (nn > T ? T : nn);
-        if (warp < 2)
-            anc = lane < nn ? static_cast<uint32_t>(tree.node_anc[2 * ((size_t)b * T + lane)]) : 0u;
-    };
-    if (!early) read_tree();
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + NBAR);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* al2 = reinterpret_cast<float*>(sm + OFF_SM);    // [2][TP]: gates of items k, k + 1
+    float* be2 = al2 + 2 * TP;
+    float* A = be2 + 2 * TP;                               // [TP]
+    float* ca = A + TP;                                    // -alpha_x beta_x A_par(x)
+    const uint32_t kq_s = smem_u32(sm + OFF_KQ), st_s = smem_u32(sm + OFF_ST);
 
-    // ---- TMA first, then the tensor memory ------------------------------------------------
-    if (tid == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
-        fence_mbar_init();
+    auto load_gates = [&](int it, int buf) {               // the lanes of one warp
+        const ItemIdx d = decode(it, c);
+        al2[buf * TP + lane] = lane < T ? alpha[((size_t)d.b * T + lane) * Hv + d.j] : 0.0f;
+        be2[buf * TP + lane] = lane < T ? beta[((size_t)d.b * T + lane) * Hv + d.j] : 0.0f;
+    };
+    int n_st = 0, n_kq = 0;                                // copies issued (thread 0)
+    auto issue_state = [&](int it) {
+        const ItemIdx d = decode(it, c);
         mbar_arrive_expect_tx(&bar[1], TX_ST);
-        tma_load_2d(sm + OFF_ST, &mh, &bar[1], col0, (b * Hv + j) * DKV);
+        tma_load_2d(sm + OFF_ST, &mh, &bar[1], d.sl * SW, (d.b * Hv + d.j) * DKV);
+        ++n_st;
+    };
+    auto issue_kqv = [&](int it, int kv) {             // kv: the item's index in this CTA
+        const ItemIdx d = decode(it, c);
+        const int row0 = d.b * T;
         mbar_arrive_expect_tx(&bar[0], TX_KQV);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            tma_load_3d(sm + OFF_KQ + h * 64 * 128, &mk, &bar[0], h * 64, ih, row0);
-            tma_load_3d(sm + OFF_KQ + h * 64 * 128 + TP * 128, &mq, &bar[0], h * 64, ih, row0);
+            tma_load_3d(sm + OFF_KQ + h * 64 * 128, &mk, &bar[0], h * 64, d.ih, row0);
+            tma_load_3d(sm + OFF_KQ + h * 64 * 128 + TP * 128, &mq, &bar[0], h * 64, d.ih, row0);
         }
-        tma_load_3d(sm + OFF_V, &mv, &bar[0], col0, j, row0);
+        tma_load_3d(sm + OFF_V + (kv & 1) * TP * SW * 2, &mv, &bar[0], d.sl * SW, d.j, row0);
+        ++n_kq;
+    };
+
+    const int it0 = blockIdx.x;
+    if (tid == 0) {
+        for (int i = 0; i < NBAR; ++i) mbar_init(&bar[i], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        issue_state(it0);
+        issue_kqv(it0, 0);
     }
     if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
-    if (tid < TP) {
-        al[tid] = tid < T ? alpha[((size_t)b * T + tid) * Hv + j] : 0.0f;
-        be[tid] = tid < T ? beta[((size_t)b * T + tid) * Hv + j] : 0.0f;
-    }
+    if (warp == 0) load_gates(it0, 0);
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t kq_s = smem_u32(sm + OFF_KQ), st_s = smem_u32(sm + OFF_ST);
     bool ok = true;
 
     if (warp >= 2) {
         // ---- state split and products (warps 2/3) ---------------------------------------
         const int t = tid - 64;                // 0..63
-        ok = mbar_wait(&bar[1], 0, nullptr);
-        ok = __all_sync(0xffffffffu, ok);
         const uint32_t idp = idesc_bf16_f32(128, 2 * TP, /*a_mn=*/true, /*b_mn=*/false);
+        int n_p = 0;                           // product commits (thread 64)
+        bool pending = false;                  // products issued, not yet committed
+        int k = 0;
+        for (int it = it0; it < n_items && ok; it += G, ++k) {
+            const uint32_t ph = k & 1;
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar[1], ph, abort_flag));
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            // d_k rows 64 h .. 64 h + 63 (16 KB of fp32 at OFF_ST + 16 KB h); unit
-            // u = t + 64 i: row 64 h + u / 8, columns 8 (u % 8) .. + 7
-            const float4* hs = reinterpret_cast<const float4*>(sm + OFF_ST + h * 2 * TILE);
-            float4 xv[16];
-            if (ok) {
+            for (int h = 0; h < 2; ++h) {
+                // d_k rows 64 h .. 64 h + 63 (16 KB of fp32 at OFF_ST + 16 KB h); unit
+                // u = t + 64 i: row 64 h + u / 8, columns 8 (u % 8) .. + 7
+                const float4* hs = reinterpret_cast<const float4*>(sm + OFF_ST + h * 2 * TILE);
+                float4 xv[16];
+                if (ok) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    xv[2 * i] = hs[2 * (t + 64 * i)];
-                    xv[2 * i + 1] = hs[2 * (t + 64 * i) + 1];
+                    for (int i = 0; i < 8; ++i) {
+                        xv[2 * i] = hs[2 * (t + 64 * i)];
+                        xv[2 * i + 1] = hs[2 * (t + 64 * i) + 1];
+                    }
                 }
-            }
-            pair_sync(1);                      // both warps hold their values
-            if (ok) {
+                ok = pair_sync_and(1, ok);     // both warps hold their values
+                if (!ok) break;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const int u = t + 64 * i, k = u >> 3, ch = u & 7;
+                    const int u = t + 64 * i, kr = u >> 3, ch = u & 7;
                     const float4 a = xv[2 * i], e = xv[2 * i + 1];
                     const uint4 hi = make_uint4(bf16x2_trunc(a.x, a.y), bf16x2_trunc(a.z, a.w),
                                                 bf16x2_trunc(e.x, e.y), bf16x2_trunc(e.z, e.w));
@@ -190,104 +231,161 @@ gdn_slice_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
                                                 bf16x2_rn(trunc_rest(a.z), trunc_rest(a.w)),
                                                 bf16x2_rn(trunc_rest(e.x), trunc_rest(e.y)),
                                                 bf16x2_rn(trunc_rest(e.z), trunc_rest(e.w)));
-                    const uint32_t off = sw128_offset(k, ch * 8);
+                    const uint32_t off = sw128_offset(kr, ch * 8);
                     *reinterpret_cast<uint4*>(sm + OFF_ST + h * 2 * TILE + off) = lo;
                     *reinterpret_cast<uint4*>(sm + OFF_ST + h * 2 * TILE + TILE + off) = hi;
                 }
                 fence_async_smem();
+                bool go = true;
+                if (t == 0 && h == 0) {
+                    // item k - 1's P^T has been read, and this item's K/Q rows are in
+                    if (k > 0) go = mbar_wait(&bar[4], (k - 1) & 1, abort_flag);
+                    go = go && mbar_wait(&bar[0], ph, abort_flag);
+                }
+                ok = pair_sync_and(1, go);
+                if (!ok) break;
+                if (t == 0) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t a_s = st_s + h * 2 * TILE + part * TILE + kk * 2048;
+                            const uint32_t b_s = kq_s + h * 64 * 128 + kk * 32;
+                            mma_bf16(tmem, sdesc_sw128(a_s, LBO_A, 1024),
+                                     sdesc_sw128(b_s, 16, 1024), idp, (h | part | kk) != 0);
+                        }
+                    }
+                    pending = true;
+                }
             }
-            pair_sync(1);
-            if (ok && t == 0) {
-                tc_fence_after();
+            if (t == 0 && pending) {
+                mma_commit(&bar[2]);
+                ++n_p;
+                pending = false;
+            }
+            if (k == 0 && early) {
+                pdl_wait();
+                pdl_trigger();
+            }
+        }
+        if (t == 0 && pending) {               // products left in flight by a failure
+            mma_commit(&bar[2]);
+            ++n_p;
+        }
+        if (!ok) *abort_flag = 1;
+        if (t == 0 && n_p > 0) mbar_wait(&bar[2], (n_p - 1) & 1, nullptr);
+    } else {
+        // ---- Gram rows, weights, write vectors and outputs (warps 0/1) ----------------
+        int n_g = 0;                           // Gram commits (thread 0)
+        // the next item's tree rows and gates are loaded one item ahead (both loads
+        // independent of each other); rows past n_nodes are masked at use
+        auto tree_of = [&](int it, int& nn, uint32_t& anc) {
+            const ItemIdx d = decode(it, c);
+            nn = tree.n_nodes[d.b];
+            anc = lane < T ? static_cast<uint32_t>(tree.node_anc[2 * ((size_t)d.b * T + lane)]) : 0u;
+        };
+        auto gates_of = [&](int it, float& a, float& bb) {
+            const ItemIdx d = decode(it, c);
+            a = lane < T ? alpha[((size_t)d.b * T + lane) * Hv + d.j] : 0.0f;
+            bb = lane < T ? beta[((size_t)d.b * T + lane) * Hv + d.j] : 0.0f;
+        };
+        int nn_next = 0;
+        uint32_t anc_next = 0;
+        float al_next = 0.0f, be_next = 0.0f;
+        if (early) {
+            pdl_wait();
+            pdl_trigger();
+        }
+        tree_of(it0, nn_next, anc_next);
+        int k = 0;
+        for (int it = it0; it < n_items; it += G, ++k) {
+            const uint32_t ph = k & 1;
+            const ItemIdx d = decode(it, c);
+            const float* al = al2 + ph * TP;
+            const float* be = be2 + ph * TP;
+            const int nn = nn_next < 1 ? 1 : (nn_next > T ? T : nn_next);
+            const uint32_t anc = lane < nn ? anc_next : 0u;
+            const bool more = it + G < n_items;
+            if (more) {                                         // in flight meanwhile
+                tree_of(it + G, nn_next, anc_next);
+                if (warp == 0) gates_of(it + G, al_next, be_next);
+            }
+            bool go = true;
+            if (tid == 0) {
+                go = mbar_wait(&bar[0], ph, abort_flag);
+                if (go) {
+                    tc_fence_after();
+                    const uint32_t idg = idesc_bf16_f32(128, TP, false, false);
 #pragma unroll
-                for (int part = 0; part < 2; ++part) {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t a_s = st_s + h * 2 * TILE + part * TILE + kk * 2048;
-                        const uint32_t b_s = kq_s + h * 64 * 128 + kk * 32;
-                        mma_bf16(tmem, sdesc_sw128(a_s, LBO_A, 1024), sdesc_sw128(b_s, 16, 1024),
-                                 idp, (h | part | kk) != 0);
+                    for (int ks = 0; ks < DKV / 16; ++ks) {
+                        const uint32_t off = (ks >> 2) * 64 * 128 + (ks & 3) * 32;
+                        mma_bf16(tmem + 2 * TP, sdesc_sw128(kq_s + off, 16, 1024),
+                                 sdesc_sw128(kq_s + off, 16, 1024), idg, ks != 0);
                     }
                 }
+                mma_commit(&bar[3]);
+                ++n_g;
+                if (!go) *abort_flag = 1;
             }
-        }
-        if (t == 0) mma_commit(&bar[2]);       // also when nothing was issued
-        if (early) {
-            pdl_wait();
-            pdl_trigger();
-        }
-    } else {
-        // ---- Gram rows (thread 0) and the weights (warps 0/1) ---------------------------
-        if (tid == 0) {
-            ok = mbar_wait(&bar[0], 0, nullptr);
-            if (ok) {
-                const uint32_t idg = idesc_bf16_f32(128, TP, false, false);
+            go = __all_sync(0xffffffffu, mbar_wait(&bar[3], ph, abort_flag));
+            if (go) {
+                // the weight rows (item k - 1's readers are done): lane x, Gram row x
+                float w[TP], alr[TP];
+                float acc = 1.0f;
+                tc_fence_after();
+                tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 2 * TP, w);
 #pragma unroll
-                for (int ks = 0; ks < DKV / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * 64 * 128 + (ks & 3) * 32;
-                    mma_bf16(tmem + 2 * TP, sdesc_sw128(kq_s + off, 16, 1024),
-                             sdesc_sw128(kq_s + off, 16, 1024), idg, ks != 0);
+                for (int a4 = 0; a4 < TP / 4; ++a4) {
+                    const float4 t4 = *reinterpret_cast<const float4*>(al + 4 * a4);
+                    alr[4 * a4] = t4.x;
+                    alr[4 * a4 + 1] = t4.y;
+                    alr[4 * a4 + 2] = t4.z;
+                    alr[4 * a4 + 3] = t4.w;
+                }
+                tmem_wait_ld();
+                const uint32_t path = warp == 0 ? anc & ~(1u << lane) : anc;  // parent's path / x's
+#pragma unroll
+                for (int a = TP - 1; a >= 0; --a) {
+                    const bool on = (path >> a) & 1u;
+                    w[a] = on ? acc * w[a] : 0.0f;
+                    acc = on ? acc * alr[a] : acc;
+                }
+                if (warp == 0) {
+                    const float s = -al[lane] * be[lane];
+                    float* WuT = reinterpret_cast<float*>(sm + OFF_WU);
+#pragma unroll
+                    for (int a = 0; a < TP; ++a) WuT[a * TP + lane] = s * w[a];
+                    ca[lane] = s * acc;
+                } else {
+                    float4* Wo = reinterpret_cast<float4*>(sm + OFF_WO + lane * WS * 4);
+#pragma unroll
+                    for (int a4 = 0; a4 < TP / 4; ++a4)
+                        Wo[a4] = make_float4(w[4 * a4], w[4 * a4 + 1], w[4 * a4 + 2], w[4 * a4 + 3]);
+                    A[lane] = acc;
                 }
             }
-            mma_commit(&bar[3]);
-        }
-        ok = __all_sync(0xffffffffu, __shfl_sync(0xffffffffu, ok, 0) && mbar_wait(&bar[3], 0, nullptr));
-        if (warp == 1) ok = ok && mbar_wait(&bar[0], 0, nullptr);   // (warp 0 knows via thread 0)
-        ok = __all_sync(0xffffffffu, ok);
-        float w[TP];
-        float acc = 1.0f;
-        if (early) {
-            pdl_wait();
-            pdl_trigger();
-            read_tree();
-        }
-        if (ok) {
+            go = go && mbar_wait(&bar[2], ph, abort_flag);
+            ok = pair_sync_and(2, go && *abort_flag == 0);       // the weights are visible
+            if (!ok) break;
             tc_fence_after();
-            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 2 * TP, w);   // Gram row (lane x)
-            tmem_wait_ld();
-            const int x = lane;
-            const uint32_t path = warp == 0 ? anc & ~(1u << x) : anc;     // parent's path / x's
-#pragma unroll
-            for (int a = TP - 1; a >= 0; --a) {
-                const bool on = (path >> a) & 1u;
-                w[a] = on ? acc * w[a] : 0.0f;
-                acc = on ? acc * al[a] : acc;
+            // this item's products have read the staging buffer and the K/Q tile
+            if (tid == 0 && more) {
+                issue_state(it + G);
+                issue_kqv(it + G, k + 1);
             }
-            if (warp == 0) {
-                const float s = -al[x] * be[x];
-#pragma unroll
-                for (int a = 0; a < TP; ++a) w[a] *= s;
-                ca[x] = s * acc;
-            } else {
-                A[x] = acc;
-            }
-        }
-        // the K/Q tile is free once the state products are done
-        ok = __all_sync(0xffffffffu, ok && mbar_wait(&bar[2], 0, nullptr));
-        if (ok) {
-            tc_fence_after();
-            if (warp == 0) {
-                float* WuT = reinterpret_cast<float*>(sm + OFF_WU);
-#pragma unroll
-                for (int a = 0; a < TP; ++a) WuT[a * TP + lane] = w[a];
-            } else {
-                float4* Wo = reinterpret_cast<float4*>(sm + OFF_WO + lane * WS * 4);
-#pragma unroll
-                for (int a4 = 0; a4 < TP / 4; ++a4)
-                    Wo[a4] = make_float4(w[4 * a4], w[4 * a4 + 1], w[4 * a4 + 2], w[4 * a4 + 3]);
-            }
-        }
-        pair_sync(2);
 
-        // ---- write vectors and outputs: one state column per lane ---------------------
-        if (ok) {
+            // one state column per lane
             const int cl = warp * 32 + lane;   // column in the half = tensor-memory lane
             const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
-            float pk[TP];
-            tmem_ld32(tl, pk);                 // Pk_x of this column, x = 0..31
+            float pk[TP], pq[TP];
+            tmem_ld32(tl, pk);                 // Pk_x, Pq_x of this column, x = 0..31
+            tmem_ld32(tl + TP, pq);
             tmem_wait_ld();
+            tc_fence_before();
             const float* WuT = reinterpret_cast<const float*>(sm + OFF_WU);
-            const __nv_bfloat16* vs = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_V);
+            const __nv_bfloat16* vs =
+                reinterpret_cast<const __nv_bfloat16*>(sm + OFF_V + ph * TP * SW * 2);
             float2 u[TP / 2];                  // rows 2p, 2p + 1
 #pragma unroll
             for (int p = 0; p < TP / 2; ++p) {
@@ -321,7 +419,7 @@ gdn_slice_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
                 if (2 * p + 1 >= nn) u[p].y = 0.0f;
             }
             const size_t rs = (size_t)Hv * DKV;                          // row stride
-            const size_t ob = ((size_t)b * T * Hv + j) * DKV + col0 + cl;
+            const size_t ob = ((size_t)d.b * T * Hv + d.j) * DKV + d.sl * SW + cl;
             if (c_out) {
 #pragma unroll
                 for (int p = 0; p < TP / 2; ++p) {
@@ -329,32 +427,41 @@ gdn_slice_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
                     if (2 * p + 1 < T) c_out[ob + (2 * p + 1) * rs] = u[p].y;
                 }
             }
-            float pq[TP];
-            tmem_ld32(tl + TP, pq);            // Pq_x of this column
-            tmem_wait_ld();
             const float* Wo = reinterpret_cast<const float*>(sm + OFF_WO);
+            // rows of the tree only; pairs p <= x / 2 cover every a <= x (the weights
+            // beyond x are zero)
 #pragma unroll
             for (int x = 0; x < TP; ++x) {
                 if (x >= T) break;
-                // pairs p <= x / 2 cover every a <= x (the weights beyond x are zero)
-                float2 acc2 = make_float2(A[x] * pq[x], 0.0f);
+                float2 acc0 = make_float2(A[x] * pq[x], 0.0f), acc1 = make_float2(0.0f, 0.0f);
 #pragma unroll
                 for (int q = 0; q <= x / 4; ++q) {
                     const float4 wq = *reinterpret_cast<const float4*>(Wo + x * WS + 4 * q);
-                    acc2 = __ffma2_rn(make_float2(wq.x, wq.y), u[2 * q], acc2);
-                    if (4 * q + 2 <= x) acc2 = __ffma2_rn(make_float2(wq.z, wq.w), u[2 * q + 1], acc2);
+                    acc0 = __ffma2_rn(make_float2(wq.x, wq.y), u[2 * q], acc0);
+                    if (4 * q + 2 <= x) acc1 = __ffma2_rn(make_float2(wq.z, wq.w), u[2 * q + 1], acc1);
                 }
-                o[ob + x * rs] = __float2bfloat16_rn(x < nn ? acc2.x + acc2.y : 0.0f);
+                o[ob + x * rs] = __float2bfloat16_rn(x < nn ? (acc0.x + acc1.x) + (acc0.y + acc1.y) : 0.0f);
             }
+            // the next item's gates go to the other buffer (this item's readers are done
+            // once both warps pass the barrier below)
+            if (warp == 0 && more) {
+                al2[(ph ^ 1) * TP + lane] = al_next;
+                be2[(ph ^ 1) * TP + lane] = be_next;
+            }
+            pair_sync(2);
+            if (tid == 0) mbar_arrive(&bar[4]);                 // P^T has been read
         }
+        if (!ok) *abort_flag = 1;
+        if (tid == 0 && n_g > 0) mbar_wait(&bar[3], (n_g - 1) & 1, nullptr);
     }
 
     // ---- teardown ------------------------------------------------------------------------
-    ok = __syncthreads_and(ok);
+    ok = __syncthreads_and(ok && *abort_flag == 0);
     if (!ok) {
         raise_status(ws, SPEC_DEV_TIMEOUT);
-        if (tid == 0) {      // let the copies and the products land before leaving
-            for (int i = 0; i < 4; ++i) mbar_wait(&bar[i], 0, nullptr);
+        if (tid == 0) {      // let the copies in flight land before leaving
+            if (n_kq > 0) mbar_wait(&bar[0], (n_kq - 1) & 1, nullptr);
+            if (n_st > 0) mbar_wait(&bar[1], (n_st - 1) & 1, nullptr);
         }
     }
     tc_fence_before();
@@ -417,10 +524,16 @@ cudaError_t launch_gdn_slice(const spec_cfg& c, const spec_tree& t, const float*
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    const int n_items = NSL * c.Hv * c.B;
+    const int grid = n_items < 3 * sms ? n_items : 3 * sms;       // three CTAs per SM
     // without programmatic launch the tree is complete when the kernel starts
-    return launch_k(pdl, gdn_slice_kernel, dim3(NSL * c.Hv, c.B), dim3(NT), SMEM_BYTES, st, mh,
-                    mk, mq, mv, c, t, alpha, beta, static_cast<__nv_bfloat16*>(o), c_out, ws,
-                    early && pdl);
+    return launch_k(pdl, gdn_slice_kernel, dim3(grid), dim3(NT), SMEM_BYTES, st, mh, mk, mq, mv,
+                    c, t, alpha, beta, static_cast<__nv_bfloat16*>(o), c_out, ws, early && pdl,
+                    n_items);
 }
 
 }  // namespace spec
