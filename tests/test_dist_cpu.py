@@ -82,3 +82,9 @@ def test_reference_arm_under_torchrun_prints_one_line():
     assert rec["steps"] == 3 and rec["warmup"] == 3 and rec["higher_is_better"] is True
     assert rec["cpu_baseline"]["cores"] >= 1 and rec["cpu_baseline"]["value"] == rec["value"]
     assert rec["e2e"]["value"] == rec["value"] and "workload" in rec["config"]
+    # the same workload string as the GPU arm's line
+    import bench
+    from speculative_decoding_tree_best_gb300 import synth
+    assert rec["config"]["workload"] == bench.workload_str(synth.config(0))
+    # whole oracle steps: the line's time per step is what the run took
+    assert rec["ms_per_step"] > 0
