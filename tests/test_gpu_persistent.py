@@ -86,8 +86,10 @@ def test_same_results_as_the_unfused_step_over_three_steps(ci):
             assert torch.equal(getattr(p.tree, k), getattr(u.tree, k)), (step, k)
         assert torch.equal(p.attn_o, u.attn_o), step
         # the same sums in another rounding order (and, after the first step,
-        # states committed by another exact formula)
-        assert _rel(p.gdn_o, u.gdn_o) < 1e-4, step
+        # states committed by another exact formula); the two GDN kernels also
+        # split the fp32 state into bf16 terms differently (rounded or
+        # truncated high term), so a few bf16 outputs round the other way
+        assert _rel(p.gdn_o, u.gdn_o) < 1e-3, step
         for k in ("argmax", "accept_len", "accept_nodes", "out_tok"):
             assert torch.equal(getattr(p.acc, k), getattr(u.acc, k)), (step, k)
         for k in ("k_cache", "v_cache", "kv_len", "root_tok"):
