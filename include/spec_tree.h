@@ -11,7 +11,10 @@
  * ---------------------------------------
  *  - Every pointer argument is a DEVICE pointer to a caller-owned, contiguous,
  *    row-major buffer in the layout stated next to it, unless it says "host".
- *    The library allocates no memory and keeps no state between calls.
+ *    The library allocates no memory and keeps no state between calls, with
+ *    one exception: attn_tree_verify_noalloc's scratch, a static device array
+ *    of the library's module (one per device) whose address the library
+ *    caches after that call's first use on a device.
  *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
  *    NULL means the legacy default stream).  Calls on different streams must
  *    use different buffers and workspaces.
@@ -31,7 +34,10 @@
  *  - The workspace `ws` is caller-owned device memory of at least
  *    spec_workspace_bytes(cfg) bytes, zero-filled ONCE after allocation; every
  *    call leaves its internal counters at zero again.  One workspace serves
- *    one stream at a time.
+ *    one stream at a time.  Its layout (how the attention's keys are chunked,
+ *    how the logits scan is split) follows the SM count of the device the
+ *    calls run on: size it with that device current, and use it on that
+ *    device (or one with the same SM count).
  */
 #ifndef SPEC_TREE_H
 #define SPEC_TREE_H
@@ -70,6 +76,12 @@ enum {
 #define SPEC_DEV_TIMEOUT  0x4u  /* a bounded device-side wait gave up */
 #define SPEC_DEV_BADREQ   0x8u  /* a per-request position count was outside [1, m] (clamped) */
 #define SPEC_DEV_BADLOGIT 0x10u /* a sampled row had no finite score (NaN / inf logits) */
+#define SPEC_DEV_RANGE    0x20u /* attention, bf16 I/O: a V value among the keys the tree rows
+                                   see (cache rows below kv_len, real tree rows) is beyond
+                                   fp16's range (|v| > 65504) or not finite.  The attention
+                                   keeps its P.V operands (D = 128) or its split-KV partials
+                                   (D = 64) in fp16, so outputs of the affected request are
+                                   then not finite. */
 
 enum { SPEC_IO_F32 = 0, SPEC_IO_BF16 = 1 };
 
@@ -129,8 +141,14 @@ typedef struct spec_sampling {
     uint64_t seed;          /* Philox4x32-10 key: (low 32 bits, high 32 bits) */
 } spec_sampling;
 
-/* Bytes of device workspace the calls below need for `cfg` (0 on invalid cfg). */
+/* Bytes of device workspace the calls below need for `cfg` on the current
+ * device (0 on an invalid cfg, or when no device is visible). */
 size_t spec_workspace_bytes(const spec_cfg *cfg);
+
+/* The same for a device with `num_sms` SMs (host only: no device needed; 0 on
+ * an invalid cfg or num_sms < 1).  The calls lay the workspace out for the SM
+ * count of the device they run on, so size with that device's count. */
+size_t spec_workspace_bytes_for_sms(const spec_cfg *cfg, int num_sms);
 
 /*
  * spec_tree_build -- best-first draft tree over the drafter's lattice.
@@ -433,15 +451,19 @@ int spec_wait_probe(uint32_t limit_us, int satisfy, void *ws, void *stream);
  *     work (with Hkv = 8, D = 128, bf16, T <= 32: one request up to Lmax ~ 61K,
  *     two up to ~ 28K, four up to ~ 12K);
  *   - dev_status: NULL, or a 4-byte-aligned device word the call ORs its
- *     SPEC_DEV_* bits into (the caller zeroes it when it wants); the scratch
- *     status word itself starts at zero and every call leaves it at zero.
- * Returns ST_EINVAL on an invalid cfg or a NULL/misaligned pointer.
+ *     SPEC_DEV_* bits into (the caller zeroes it when it wants); each call
+ *     clears the scratch status word on its stream before its kernels (a
+ *     memset, no allocation) and moves its bits to dev_status after them.
+ * Returns the codes attn_tree_verify returns for an invalid cfg, tree or
+ * pointer (ST_EINVAL, or ST_EUNSUPPORTED for an unsupported io_dtype).
  * The first call on a device (with that device current) sets up: it looks up
  * the array's address and clears its status word synchronously, so make it
- * before any stream capture or latency-critical section.  All calls on one
- * device share the one scratch array: calls that overlap in time (other
- * streams, other host threads, other layers in flight) race on it and give
- * wrong results; order them on one stream or serialise them.
+ * before any stream capture or latency-critical section.  The address stays
+ * cached for the life of the process: make no call after a cudaDeviceReset of
+ * that device.  All calls on one device share the one scratch array: calls
+ * that overlap in time (other streams, other host threads, other layers in
+ * flight) race on it and give wrong results; order them on one stream or
+ * serialise them.
  */
 #define SPEC_NOALLOC_SCRATCH_BYTES (8u << 20)
 int attn_tree_verify_noalloc(const spec_cfg *cfg, const spec_tree *tree, const void *q,

@@ -21,9 +21,9 @@ LIB_PATH = os.path.join(_HERE, "libspectree.so")
 ST_OK, ST_EINVAL, ST_EUNSUPPORTED, ST_ECUDA, ST_EOVERFLOW, ST_TIMEOUT, ST_ESCRATCH = range(7)
 NOALLOC_SCRATCH_BYTES = 8 << 20
 SPEC_DEV_OVERFLOW, SPEC_DEV_BADLAT, SPEC_DEV_TIMEOUT, SPEC_DEV_BADREQ = 0x1, 0x2, 0x4, 0x8
-SPEC_DEV_BADLOGIT = 0x10
+SPEC_DEV_BADLOGIT, SPEC_DEV_RANGE = 0x10, 0x20
 SPEC_IO_F32, SPEC_IO_BF16 = 0, 1
-EXPORTS = ("spec_workspace_bytes", "spec_tree_build", "gdn_tree_verify", "attn_tree_verify",
+EXPORTS = ("spec_workspace_bytes", "spec_workspace_bytes_for_sms", "spec_tree_build", "gdn_tree_verify", "attn_tree_verify",
            "accept_and_commit", "spec_verify_step", "spec_status_read", "spec_status_clear",
            "spec_status_string", "spec_abi_version", "attn_tree_verify_noalloc",
            "spec_wait_probe", "spec_step_launches", "spec_tree_build_ragged",
@@ -85,6 +85,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
             vp, cfgp = ctypes.c_void_p, ctypes.POINTER(SpecCfg)
             lib.spec_workspace_bytes.argtypes = [cfgp]
             lib.spec_workspace_bytes.restype = ctypes.c_size_t
+            lib.spec_workspace_bytes_for_sms.argtypes = [cfgp, ctypes.c_int]
+            lib.spec_workspace_bytes_for_sms.restype = ctypes.c_size_t
             lib.spec_tree_build.argtypes = [cfgp, vp, vp, vp, ctypes.POINTER(SpecTree), vp, vp]
             lib.gdn_tree_verify.argtypes = [cfgp, ctypes.POINTER(SpecTree)] + [vp] * 10
             lib.attn_tree_verify.argtypes = [cfgp, ctypes.POINTER(SpecTree)] + [vp] * 9
@@ -220,9 +222,19 @@ class AcceptBuffers:
 # ------------------------------------------------------------- entry points
 
 def spec_workspace_bytes(cfg: SpecCfg) -> int:
+    """Workspace bytes for the current device."""
     n = load().spec_workspace_bytes(ctypes.byref(cfg))
     if n == 0:
-        raise SpecError("spec_workspace_bytes", ST_EINVAL, "invalid configuration")
+        raise SpecError("spec_workspace_bytes", ST_EINVAL,
+                        "invalid configuration (or no CUDA device visible)")
+    return int(n)
+
+
+def spec_workspace_bytes_for_sms(cfg: SpecCfg, num_sms: int) -> int:
+    """Workspace bytes for a device with num_sms SMs (host only)."""
+    n = load().spec_workspace_bytes_for_sms(ctypes.byref(cfg), int(num_sms))
+    if n == 0:
+        raise SpecError("spec_workspace_bytes_for_sms", ST_EINVAL, "invalid configuration")
     return int(n)
 
 

@@ -456,7 +456,7 @@ cudaError_t launch_commit_k(const spec_cfg& c, const spec_commit_io& io, const s
 cudaError_t launch_argmax_accept(const spec_cfg& c, const spec_tree& t, const void* logits,
                                  const spec_commit_io& io, const spec_accept& out, void* ws,
                                  cudaStream_t st, bool pdl, bool tree_early, bool trigger_first) {
-    const WsLayout w = ws_layout(c);
+    const WsLayout w = ws_layout(c, device_sm_count());
     dim3 g1(w.argmax_split, c.B * (c.N + 1));
     return c.io_dtype == SPEC_IO_BF16
         ? launch_k(pdl, argmax_accept<SPEC_IO_BF16>, g1, dim3(NT), 0, st, c,
@@ -471,7 +471,7 @@ cudaError_t launch_sample_accept(const spec_cfg& c, const spec_tree& t, const vo
                                  float temperature, uint64_t seed, const spec_commit_io& io,
                                  const spec_accept& out, void* ws, cudaStream_t st, bool pdl,
                                  bool tree_early, bool trigger_first) {
-    const WsLayout w = ws_layout(c);
+    const WsLayout w = ws_layout(c, device_sm_count());
     dim3 g1((w.n_vchunks + NT / 32 - 1) / (NT / 32), c.B * (c.N + 1));
     const float inv_temp = 1.0f / temperature;
     const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
@@ -510,7 +510,7 @@ static cudaError_t launch_commit_io(const spec_cfg& c, const spec_commit_io& io,
 
 cudaError_t launch_commit(const spec_cfg& c, const spec_commit_io& io, const spec_accept& out,
                           void* ws, cudaStream_t st, bool pdl, bool early) {
-    const WsLayout w = ws_layout(c);
+    const WsLayout w = ws_layout(c, device_sm_count());
     return c.io_dtype == SPEC_IO_BF16
         ? launch_commit_io<SPEC_IO_BF16>(c, io, out, ws, w, st, pdl, early)
         : launch_commit_io<SPEC_IO_F32>(c, io, out, ws, w, st, pdl, early);

@@ -2,35 +2,16 @@
 // argument validation, workspace sizing and the kernel launches.
 #include <stdint.h>
 
+#include "checks.h"
 #include "common.cuh"
 #include "kernels.h"
 
 namespace {
 
 using spec::WsLayout;
-
-bool al16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-int check_cfg(const spec_cfg* c) {
-    if (!c) return ST_EINVAL;
-    if (c->B < 1 || c->m < 1 || c->m > SPEC_MAX_M || c->K < 1 || c->K > SPEC_MAX_K) return ST_EINVAL;
-    if (c->N < 0 || c->N + 1 > SPEC_MAX_ROWS || c->V < 1 || c->Lmax < 0) return ST_EINVAL;
-    if (c->Hk < 1 || c->Hv < 1 || c->Hv % c->Hk != 0) return ST_EINVAL;
-    if (c->Hq < 1 || c->Hkv < 1 || c->Hq % c->Hkv != 0) return ST_EINVAL;
-    if ((c->dk != 64 && c->dk != 128) || (c->dv != 64 && c->dv != 128)) return ST_EINVAL;
-    if (c->D != 64 && c->D != 128) return ST_EINVAL;
-    if (c->n_gdn_layers < 0 || c->n_attn_layers < 0) return ST_EINVAL;
-    if (c->io_dtype != SPEC_IO_F32 && c->io_dtype != SPEC_IO_BF16) return ST_EUNSUPPORTED;
-    return ST_OK;
-}
-
-int check_tree(const spec_tree* t) {
-    if (!t) return ST_EINVAL;
-    if (!al16(t->node_tok) || !al16(t->node_parent) || !al16(t->node_depth) ||
-        !al16(t->node_rank) || !al16(t->node_score) || !al16(t->node_anc) || !al16(t->n_nodes))
-        return ST_EINVAL;
-    return ST_OK;
-}
+using spec::al16;
+using spec::check_cfg;
+using spec::check_tree;
 
 int cuda_rc(cudaError_t e) {
     if (e == cudaSuccess) return ST_OK;
@@ -59,7 +40,14 @@ const char* spec_status_string(int code) {
 
 size_t spec_workspace_bytes(const spec_cfg* cfg) {
     if (check_cfg(cfg) != ST_OK) return 0;
-    return spec::ws_layout(*cfg).total;
+    const int sms = spec::device_sm_count();
+    if (sms < 1) return 0;
+    return spec::ws_layout(*cfg, sms).total;
+}
+
+size_t spec_workspace_bytes_for_sms(const spec_cfg* cfg, int num_sms) {
+    if (check_cfg(cfg) != ST_OK || num_sms < 1) return 0;
+    return spec::ws_layout(*cfg, num_sms).total;
 }
 
 int spec_tree_build(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_score,

@@ -14,6 +14,7 @@
 // launch shapes), so results are identical to that call's.
 #include <mutex>
 
+#include "checks.h"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -33,7 +34,8 @@ void* g_scratch_ptr[kMaxDevices];
 
 // Address of this device's copy of the scratch array.  The first call on a
 // device (with that device current) looks it up and clears the status word
-// synchronously; later calls only read the cached pointer.
+// synchronously; later calls only read the cached pointer (which a device
+// reset would leave stale: calls must not span a cudaDeviceReset).
 int scratch_for_current_device(void** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return ST_ECUDA;
@@ -58,12 +60,10 @@ __global__ void fold_status(unsigned int* scratch_status, unsigned int* dev_stat
     if (dev_status != nullptr && s != 0u) atomicOr(dev_status, s);
 }
 
-bool al16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 // Bytes of scratch the attention of `c` touches: status word, argmax reserve
 // (unused here) and partial buffer 0 of the workspace layout.
 size_t attn_scratch_need(const spec_cfg& c) {
-    const spec::WsLayout w = spec::ws_layout(c);
+    const spec::WsLayout w = spec::ws_layout(c, spec::device_sm_count());
     const size_t tiles = (size_t)c.B * c.Hkv * w.n_mt * w.n_chunks;
     return w.attn_ml_off + sizeof(float) * 2 * tiles * 128;
 }
@@ -75,23 +75,27 @@ extern "C" int attn_tree_verify_noalloc(const spec_cfg* cfg, const spec_tree* tr
                                         const void* k_cache, const void* v_cache,
                                         const int32_t* kv_len, void* o, uint32_t* dev_status,
                                         void* stream) {
-    // shape and pointer checks first: nothing touches the device before them
-    if (spec_workspace_bytes(cfg) == 0) return ST_EINVAL;
-    if (!tree || !al16(tree->node_tok) || !al16(tree->node_parent) || !al16(tree->node_depth) ||
-        !al16(tree->node_rank) || !al16(tree->node_score) || !al16(tree->node_anc) ||
-        !al16(tree->n_nodes))
-        return ST_EINVAL;
+    // shape and pointer checks first (the codes attn_tree_verify returns):
+    // nothing touches the device before them
+    using spec::al16;
+    int rc = spec::check_cfg(cfg);
+    if (rc != ST_OK) return rc;
+    if ((rc = spec::check_tree(tree)) != ST_OK) return rc;
     if (!al16(q) || !al16(k_tree) || !al16(v_tree) || !al16(k_cache) || !al16(v_cache) ||
         !al16(kv_len) || !al16(o))
         return ST_EINVAL;
     if (dev_status && (reinterpret_cast<uintptr_t>(dev_status) & 3u)) return ST_EINVAL;
     if (attn_scratch_need(*cfg) > kScratchBytes) return ST_ESCRATCH;
     void* scratch = nullptr;
-    int rc = scratch_for_current_device(&scratch);
+    rc = scratch_for_current_device(&scratch);
     if (rc != ST_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = spec::launch_attn_tree(*cfg, *tree, q, k_tree, v_tree, k_cache, v_cache,
-                                           kv_len, o, scratch, st);
+    // the status word starts this call at zero, whatever a failed call before
+    // left in it (a memset, not an allocation)
+    cudaError_t e = cudaMemsetAsync(scratch, 0, sizeof(uint32_t), st);
+    if (e == cudaSuccess)
+        e = spec::launch_attn_tree(*cfg, *tree, q, k_tree, v_tree, k_cache, v_cache, kv_len, o,
+                                   scratch, st);
     if (e == cudaSuccess) {
         fold_status<<<1, 1, 0, st>>>(static_cast<unsigned int*>(scratch),
                                      reinterpret_cast<unsigned int*>(dev_status));

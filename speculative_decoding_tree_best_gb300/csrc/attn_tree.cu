@@ -109,9 +109,15 @@ attn_partial_simt(spec_cfg c, spec_tree tree, const typename io_t<IO>::T* __rest
         const int mt = r / 128, rr = r % 128;
         const size_t tile = (((size_t)b * Hkv + g) * w.n_mt + mt) * w.n_chunks + ch;
         const float inv = sum > 0.0f ? 1.0f / sum : 0.0f;
+        bool range = false;      // an fp16 partial that is not finite (bf16 I/O)
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) wO[(tile * 128 + rr) * D + lane * EPL + e] = static_cast<PT>(acc[e] * inv);
+        for (int e = 0; e < EPL; ++e) {
+            const float y = acc[e] * inv;
+            if constexpr (IO == SPEC_IO_BF16) range |= !(fabsf(y) <= 65504.0f);
+            wO[(tile * 128 + rr) * D + lane * EPL + e] = static_cast<PT>(y);
+        }
         if (lane == 0) wML[tile * 128 + rr] = make_float2(mx, sum);
+        if (__any_sync(0xffffffffu, range) && lane == 0) raise_status(ws, SPEC_DEV_RANGE);
     }
 }
 
@@ -258,7 +264,7 @@ cudaError_t launch_partial(const spec_cfg& c, const spec_tree& t, const void* q,
                            const void* vt, const void* kc, const void* vc, const int32_t* kv_len,
                            void* ws, cudaStream_t st, bool pdl, int part_buf) {
     using E = typename io_t<IO>::T;
-    const WsLayout w = with_attn_buf(ws_layout(c), part_buf);
+    const WsLayout w = with_attn_buf(ws_layout(c, device_sm_count()), part_buf);
     if (attn_tc_supported(c)) return launch_attn_tc(c, t, q, kt, vt, kc, vc, kv_len, ws, w, st, pdl);
     return launch_k(pdl, attn_partial_simt<IO, D>, dim3(w.n_chunks, c.Hkv, c.B), dim3(NT), 0, st,
                     c, t, static_cast<const E*>(q), static_cast<const E*>(kt),
@@ -270,7 +276,7 @@ template <int IO, int D>
 cudaError_t launch_merge(const spec_cfg& c, const spec_tree& t, void* o, void* ws, cudaStream_t st,
                          bool pdl, int part_buf, bool early) {
     using E = typename io_t<IO>::T;
-    const WsLayout w = with_attn_buf(ws_layout(c), part_buf);
+    const WsLayout w = with_attn_buf(ws_layout(c, device_sm_count()), part_buf);
     const int G = c.Hq / c.Hkv;
     return launch_k(pdl, attn_merge<IO, D>, dim3((G * (c.N + 1) + NW - 1) / NW, c.Hkv, c.B),
                     dim3(NT), 0, st, c, t, ws, w, static_cast<E*>(o), early);

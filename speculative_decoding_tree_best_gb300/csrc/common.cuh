@@ -100,14 +100,25 @@ struct WsLayout {
 
 static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// SMs of the current device (0 when there is none or the query fails).  The
+// workspace layout (chunking of the attention's keys, split of the logits
+// scan) follows the device the calls run on.
+static inline int device_sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms > 0 ? sms : 0;
+}
+
 // Cache rows per chunk: about one CTA per SM over B x Hkv x tiles x chunks
 // for small problems, chunks of 256 to 2048 rows (multiples of 128).  Larger
 // chunks amortise each CTA's prologue (Q and the first K/V blocks in flight,
 // the first softmax) over more blocks and leave the merge fewer partials; past
 // 2048 the load imbalance between long and short requests costs more (batched
 // and long-tree steps measured fastest at 2048 of 1024, 1536, 2048, 3072, 4096).
-static inline WsLayout ws_layout(const spec_cfg& c, int num_sms = 152) {
+static inline WsLayout ws_layout(const spec_cfg& c, int num_sms) {
     WsLayout w{};
+    if (num_sms < 1) num_sms = 1;
     const int T = c.N + 1;
     const int G = c.Hq / c.Hkv;
     w.n_mt = (G * T + 127) / 128;

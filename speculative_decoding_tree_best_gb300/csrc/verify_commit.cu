@@ -319,7 +319,7 @@ cudaError_t launch_verify_commit(const spec_cfg& c, const spec_tree& t, const sp
     a.gdn_o = static_cast<__nv_bfloat16*>(step.gdn_o);
     a.gdn_c = step.gdn_c;
     a.ws = ws;
-    a.w = ws_layout(c);
+    a.w = ws_layout(c, device_sm_count());
     a.w.argmax_split = split;
     a.n_arg = c.B * T * split;
     a.n_items = a.n_arg + n_gdn;

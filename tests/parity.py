@@ -257,7 +257,10 @@ def check_case(scfg, seed, **kw):
     lat_edit = kw.pop("lat_edit", None)
     calls = kw.pop("calls", False)
     persistent = kw.pop("persistent", False)
+    edit = kw.pop("edit", None)             # edit(inp, tree): after the tree is known
     inp, tree_o = prepare(scfg, seed, kv_len=kv_len, lat_edit=lat_edit)
+    if edit is not None:
+        edit(inp, tree_o)
     st = run_gpu(scfg, inp, calls=calls, persistent=persistent)
     res = compare(scfg, inp, tree_o, st, **kw)
     res["status"] = __import__("speculative_decoding_tree_best_gb300.binding",

@@ -156,3 +156,69 @@ def test_repeated_batched_attention_no_timeout():
 @pytest.mark.parametrize("dk,dv", [(128, 64), (64, 128)])
 def test_unequal_key_and_value_head_dims(dk, dv):
     parity.check_case(SMALL.replace(dk=dk, dv=dv, Hk=2, Hv=4), 11)
+
+
+@pytest.mark.parametrize("N", [90, 95])
+def test_trees_with_a_full_third_row_slot(N):
+    """Trees of 91 and 96 rows: the tree builder's third 32-row slot then
+    holds many rows (a parent and its new child both there, on different
+    lanes); bit-exact like every tree, and the step around them at parity."""
+    parity.check_case(SMALL.replace(m=8, K=16, N=N), 12 + N % 2)
+
+
+def _inf_where_unread(inp, tree_o):
+    """inf in every input row the step must not read: cache rows at or past
+    kv_len, and the tree-row inputs (and gates) of the padding rows."""
+    nn = tree_o["n_nodes"]
+    inf = float("inf")
+    for b in range(len(nn)):
+        L, n = int(inp["kv_len"][b]), int(nn[b])
+        for lay in inp["attn"]:
+            lay["k_cache"][b, L:] = inf
+            lay["v_cache"][b, L:] = inf
+            for k in ("q", "k_tree", "v_tree"):
+                lay[k][b, n:] = inf
+        for lay in inp["gdn"]:
+            for k in ("q", "k", "v", "alpha", "beta"):
+                lay[k][b, n:] = inf
+
+
+@pytest.mark.parametrize("case", ["tiny_fp32", "bf16", "bf16_persistent", "bf16_long_tree"])
+def test_rows_outside_the_valid_ranges_are_never_read(case):
+    """Results do not depend on cache rows at or past kv_len, nor on the
+    padding rows of the tree-row inputs: with inf in all of them (0 x inf is
+    NaN, so a masked product over them would show) every output matches the
+    oracle, which never reads them, and no status bit is raised."""
+    if case == "tiny_fp32":
+        cfg, kv, kw = synth.config(0).replace(N=12, L=200), None, {}
+    else:
+        cfg = SMALL.replace(B=2, L=700, N=40 if case == "bf16_long_tree" else 20, m=4, K=8)
+        kv, kw = [650, 333], {"persistent": case == "bf16_persistent"}
+    r = parity.check_case(cfg, 14, kv_len=kv, edit=_inf_where_unread, **kw)
+    assert r["status"] == 0
+
+
+@pytest.mark.parametrize("where,value,flagged", [("cache", 7.0e4, True), ("tree", 7.0e4, True),
+                                                 ("cache", 6.5e4, False)])
+def test_v_beyond_fp16_range_is_flagged(where, value, flagged):
+    """The attention's P.V product takes V in fp16: a visible bf16 V value of
+    7e4 (beyond fp16's 65504) in request 1 raises SPEC_DEV_RANGE and makes its
+    outputs non-finite, while request 0 still matches the oracle; 6.5e4 is in
+    range, raises nothing, and both requests match."""
+    cfg = SMALL.replace(B=2, L=700)
+    inp, tree_o = parity.prepare(cfg, 13, kv_len=[650, 333])
+    lay = inp["attn"][0]
+    if where == "cache":
+        lay["v_cache"][1, 100, 3, 17] = value
+    else:
+        lay["v_tree"][1, 0, 3, 17] = value          # the root row: every row sees it
+    st = parity.run_gpu(cfg, inp)
+    status = binding.spec_status_read(st.ws)
+    G = cfg.Hq // cfg.Hkv
+    if flagged:
+        assert status & binding.SPEC_DEV_RANGE
+        assert not torch.isfinite(st.attn_o[0][1, :, 3 * G:4 * G].float()).all()
+        parity.compare(cfg, inp, tree_o, st, req=[0])
+    else:
+        assert status == 0
+        parity.compare(cfg, inp, tree_o, st)

@@ -51,10 +51,28 @@ def test_abi_version_and_strings(lib):
 def test_workspace_sizing_is_host_only(lib):
     for i in range(5):
         cfg = binding.make_cfg(synth.config(i))
-        n = binding.spec_workspace_bytes(cfg)
+        n = binding.spec_workspace_bytes_for_sms(cfg, 152)
         assert n > 256 and n % 256 == 0
     bad = binding.make_cfg(synth.config(1), dk=96)
     assert lib.spec_workspace_bytes(ctypes.byref(bad)) == 0
+    assert lib.spec_workspace_bytes_for_sms(ctypes.byref(bad), 152) == 0
+    assert lib.spec_workspace_bytes_for_sms(ctypes.byref(binding.make_cfg(synth.config(1))), 0) == 0
+
+
+def test_workspace_layout_follows_the_sm_count(lib):
+    """The attention's keys are cut into about one chunk per SM for small
+    problems: a single request's 4096-key cache gives 256-key chunks on 152
+    SMs but 2048-key chunks on 16, so the split-KV partials shrink; 24 requests
+    already fill the device with 2048-key chunks at either count."""
+    one = binding.make_cfg(synth.config(1))
+    assert binding.spec_workspace_bytes_for_sms(one, 16) < binding.spec_workspace_bytes_for_sms(one, 152)
+    # 152 SMs: 17 chunks of 256 keys + the tree chunk, 8 kv-heads x 1 tile, fp16
+    # partials [..][128][128] and (max, sum) [..][128]
+    tiles = 8 * (16 + 1)
+    assert binding.spec_workspace_bytes_for_sms(one, 152) >= tiles * 128 * (128 * 2 + 8)
+    many = binding.make_cfg(synth.config(3))
+    assert (binding.spec_workspace_bytes_for_sms(many, 132)
+            == binding.spec_workspace_bytes_for_sms(many, 152))
 
 
 def test_step_launch_count_is_host_only(lib):
@@ -139,3 +157,21 @@ def test_persistent_step_shapes_and_launches(lib):
                                              ctypes.byref(binding.SpecAccept(*([16] * 4))), p,
                                              None)
         assert rc == binding.ST_EUNSUPPORTED
+
+
+def test_bad_io_dtype_same_code_on_both_attention_entry_points(lib):
+    """An unsupported io_dtype is refused on the host, with the same code by
+    the workspace call and the no-allocation call (nothing reaches a device)."""
+    cfg = binding.make_cfg(synth.config(1), io_dtype=7)
+    tree = binding.SpecTree(*([16] * 7))
+    p = ctypes.c_void_p(16)
+    rc = lib.attn_tree_verify(ctypes.byref(cfg), ctypes.byref(tree), *([p] * 8), None)
+    assert rc == binding.ST_EUNSUPPORTED
+    rc = lib.attn_tree_verify_noalloc(ctypes.byref(cfg), ctypes.byref(tree), *([p] * 7), None,
+                                      None)
+    assert rc == binding.ST_EUNSUPPORTED
+    # a NULL tree is ST_EINVAL on both
+    good = binding.make_cfg(synth.config(1))
+    assert lib.attn_tree_verify(ctypes.byref(good), None, *([p] * 8), None) == binding.ST_EINVAL
+    assert lib.attn_tree_verify_noalloc(ctypes.byref(good), None, *([p] * 7), None,
+                                        None) == binding.ST_EINVAL
