@@ -65,18 +65,29 @@ def algorithmic_bytes(s: synth.SpecConfig, mean_L: float, tau: float, rows=None)
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# dominant kernels from ncu captures, keyed by workload, with the SHA-256 of the
-# sources they were taken on: once a kernel's sources change, its figure is
-# dropped (reported as null) until it is captured again.
+# step's kernels from ncu captures (one pass, caches flushed before each
+# launch), keyed by workload, with the SHA-256 of the sources they were taken
+# on: once a kernel's sources change, its figure is dropped (reported as null)
+# until it is captured again.  "attn" is one attention layer: the split-KV
+# partial launch plus its merge.
+_CSRC = "speculative_decoding_tree_best_gb300/csrc/"
 TRAFFIC = {
-    "attn": {"sources": ("speculative_decoding_tree_best_gb300/csrc/attn_tree_tc.cu",
-                         "speculative_decoding_tree_best_gb300/csrc/attn_tree.cu",
-                         "speculative_decoding_tree_best_gb300/csrc/common.cuh"),
-             "sha256": None, "bytes": {}},
-    "gdn": {"sources": ("speculative_decoding_tree_best_gb300/csrc/gdn_slice.cu",
-                        "speculative_decoding_tree_best_gb300/csrc/tc_util.cuh",
-                        "speculative_decoding_tree_best_gb300/csrc/common.cuh"),
-            "sha256": None, "bytes": {}},
+    "attn": {"sources": tuple(_CSRC + f for f in ("attn_tree_tc.cu", "attn_tree.cu", "common.cuh",
+                                                   "tc_util.cuh")),
+             "sha256": "9f30092e6fae93241e92394929e3695c0e2547afd8007f47ea31f4c2bd1c56a1",
+             "bytes": {"single": 20795769, "batched": 484530652}},
+    "gdn": {"sources": tuple(_CSRC + f for f in ("gdn_state.cu", "gdn_tc_body.cuh", "tc_util.cuh",
+                                                  "common.cuh")),
+            "sha256": "322a8792c5d6789da4eb9e1d91aabf052618f1dde432533a3b0531c43a605191",
+            "bytes": {"single": 2583200, "batched": 60400448}},
+    "argmax": {"sources": tuple(_CSRC + f for f in ("accept_commit.cu", "accept_util.cuh",
+                                                     "common.cuh")),
+               "sha256": "733e0bc407dc0c8728aee1752c597fd12019633ba3b836d07a32138bca0f23a7",
+               "bytes": {"single": 7619840, "batched": 182581248}},
+    "commit": {"sources": tuple(_CSRC + f for f in ("accept_commit.cu", "accept_util.cuh",
+                                                     "common.cuh")),
+               "sha256": "733e0bc407dc0c8728aee1752c597fd12019633ba3b836d07a32138bca0f23a7",
+               "bytes": {"single": 2183808, "batched": 51926560}},
 }
 
 
@@ -650,6 +661,7 @@ def summarize(scfg, res, world, peak, peak_kind):
         "roofline": dict(kernel="attn_tree_verify (split-KV partial + merge)", **roof("attn", "attn_kernel")),
         "gdn_roofline": dict(kernel="gdn_tree_verify", **roof("gdn", "gdn_kernel")),
         "algorithmic_bytes": byts,
+        "dram_traffic_per_launch": {k: kernel_traffic(k, scfg.name) for k in TRAFFIC},
     }
     if "e2e_ms" in res:
         out["e2e"] = {"value": nodes_total / (res["e2e_ms"] * 1e-3), "unit": UNIT,

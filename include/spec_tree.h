@@ -76,12 +76,11 @@ enum {
 #define SPEC_DEV_TIMEOUT  0x4u  /* a bounded device-side wait gave up */
 #define SPEC_DEV_BADREQ   0x8u  /* a per-request position count was outside [1, m] (clamped) */
 #define SPEC_DEV_BADLOGIT 0x10u /* a sampled row had no finite score (NaN / inf logits) */
-#define SPEC_DEV_RANGE    0x20u /* attention, bf16 I/O: a V value among the keys the tree rows
-                                   see (cache rows below kv_len, real tree rows) is beyond
-                                   fp16's range (|v| > 65504) or not finite.  The attention
-                                   keeps its P.V operands (D = 128) or its split-KV partials
-                                   (D = 64) in fp16, so outputs of the affected request are
-                                   then not finite. */
+#define SPEC_DEV_RANGE    0x20u /* attention: an output of a real tree row is not finite.  With
+                                   bf16 I/O the attention keeps V and the split-KV partials in
+                                   fp16, so a V value beyond fp16's range (|v| > 65504) among
+                                   the keys the row sees (cache rows below kv_len, its tree
+                                   ancestors) gives this, as do non-finite inputs there. */
 
 enum { SPEC_IO_F32 = 0, SPEC_IO_BF16 = 1 };
 

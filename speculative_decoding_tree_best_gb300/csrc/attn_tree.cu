@@ -109,15 +109,9 @@ attn_partial_simt(spec_cfg c, spec_tree tree, const typename io_t<IO>::T* __rest
         const int mt = r / 128, rr = r % 128;
         const size_t tile = (((size_t)b * Hkv + g) * w.n_mt + mt) * w.n_chunks + ch;
         const float inv = sum > 0.0f ? 1.0f / sum : 0.0f;
-        bool range = false;      // an fp16 partial that is not finite (bf16 I/O)
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-            const float y = acc[e] * inv;
-            if constexpr (IO == SPEC_IO_BF16) range |= !(fabsf(y) <= 65504.0f);
-            wO[(tile * 128 + rr) * D + lane * EPL + e] = static_cast<PT>(y);
-        }
+        for (int e = 0; e < EPL; ++e) wO[(tile * 128 + rr) * D + lane * EPL + e] = static_cast<PT>(acc[e] * inv);
         if (lane == 0) wML[tile * 128 + rr] = make_float2(mx, sum);
-        if (__any_sync(0xffffffffu, range) && lane == 0) raise_status(ws, SPEC_DEV_RANGE);
     }
 }
 
@@ -254,6 +248,12 @@ __device__ __forceinline__ void merge_row(const spec_cfg& c, const spec_tree& tr
 #pragma unroll
         for (int e = 0; e < EPL; ++e) acc[e] *= inv;
     }
+    // a real row whose output is not finite: an fp16 V operand or partial out
+    // of range (bf16 I/O), or non-finite inputs among the keys it sees
+    bool bad = false;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) bad |= !(fabsf(acc[e]) <= 3.402823466e38f);
+    if (__any_sync(0xffffffffu, bad) && lane == 0) raise_status(ws, SPEC_DEV_RANGE);
 #pragma unroll
     for (int e = 0; e < EPL; ++e)
         io_t<IO>::st(o, (((size_t)b * T + x) * c.Hq + h) * D + lane * EPL + e, acc[e]);

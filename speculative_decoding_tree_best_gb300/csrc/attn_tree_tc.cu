@@ -115,17 +115,14 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// Eight bf16 (one 16-byte chunk) to eight fp16, in place.  `range` gets a
-// non-zero bit for every result that is not a finite fp16 (|v| beyond 65504,
-// or a non-finite input): the P V product would then be inf or NaN.
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, uint32_t& range) {
+// Eight bf16 (one 16-byte chunk) to eight fp16, in place.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
     uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
         const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
         const __half2 h = __floats2half2_rn(lo, hi);
         w[e] = *reinterpret_cast<const uint32_t*>(&h);
-        range |= __vcmpgeu2(w[e] & 0x7fff7fffu, 0x7c007c00u);    // exponent all ones
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
@@ -335,7 +332,6 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
     const int nu = U.count(blockIdx.x);
 
     bool ok = true;
-    uint32_t v_range = 0;        // V values converted to fp16 that are not finite
 
     if (warp == 0) {
         // ------------------------------------------------------------ Q tiles and the K ring
@@ -577,12 +573,13 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
                     l1 += sv[i + 1];
                 }
                 l += l0 + l1;
-                // V_J to fp16 in place: 16 bytes x 4 per thread.  Rows past the
-                // block's keys (cache rows at or beyond kv_len, padding tree rows)
-                // become 0: their P is 0, but 0 x inf or 0 x NaN in the product
-                // would not be, and the caller's buffer there is arbitrary.  In
-                // the 128-byte-swizzled halves a 16-byte chunk's row is its index
-                // / 8 (the swizzle permutes chunks within a row).
+                // V_J to fp16 in place: 16 bytes x 4 per thread.  In a block with
+                // fewer keys than rows (a chunk's last block, the tree block) the
+                // rows past its keys (cache rows at or beyond kv_len, padding tree
+                // rows) become 0: their P is 0, but 0 x inf or 0 x NaN in the
+                // product would not be, and the caller's buffer there is
+                // arbitrary.  In the 128-byte-swizzled halves a 16-byte chunk's
+                // row is its index / 8 (the swizzle permutes chunks within a row).
                 const int vst = J % NVS;
                 const int vrows = un.tree ? tree_rows : un.k1 - (un.k0 + j * NB);
                 w_ok = __all_sync(0xffffffffu,
@@ -592,11 +589,17 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
                     uint4 vv[TILE_BYTES / 16 / NSOFT];
 #pragma unroll
                     for (int i = 0; i < TILE_BYTES / 16 / NSOFT; ++i) vv[i] = vs[st + i * NSOFT];
+                    if (vrows >= NB) {
 #pragma unroll
-                    for (int i = 0; i < TILE_BYTES / 16 / NSOFT; ++i) {
-                        const int vr = ((st + i * NSOFT) >> 3) & (NB - 1);
-                        vs[st + i * NSOFT] = vr < vrows ? bf16x8_to_f16x8(vv[i], v_range)
-                                                        : make_uint4(0u, 0u, 0u, 0u);
+                        for (int i = 0; i < TILE_BYTES / 16 / NSOFT; ++i)
+                            vs[st + i * NSOFT] = bf16x8_to_f16x8(vv[i]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < TILE_BYTES / 16 / NSOFT; ++i) {
+                            const int vr = ((st + i * NSOFT) >> 3) & (NB - 1);
+                            vs[st + i * NSOFT] = vr < vrows ? bf16x8_to_f16x8(vv[i])
+                                                            : make_uint4(0u, 0u, 0u, 0u);
+                        }
                     }
                 }
                 // P_J goes to tensor-memory buffer J & 1 once PV_{J-2}, which read
@@ -684,8 +687,6 @@ attn_tc_partial(const __grid_constant__ CUtensorMap mq, const __grid_constant__ 
         *abort_flag = 1;
         raise_status(prm.ws, SPEC_DEV_TIMEOUT);
     }
-    if (__any_sync(0xffffffffu, v_range != 0u) && (threadIdx.x & 31) == 0)
-        raise_status(prm.ws, SPEC_DEV_RANGE);
     tc_fence_before();
     __syncthreads();
     pdl_wait();

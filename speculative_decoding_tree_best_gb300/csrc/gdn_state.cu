@@ -1,5 +1,5 @@
-// gdn_slice.cu -- tree-masked Gated DeltaNet, bf16 I/O, d_k = d_v = 128, trees
-// of up to 32 rows: one CTA per (request, v-head, 64-column half of the state).
+// gdn_state.cu -- tree-masked Gated DeltaNet, bf16 I/O, d_k = d_v = 128, trees
+// of up to 32 rows: one CTA per (request, v-head) state at a time.
 //
 // Digest "SpecPilot ...": prerequisites / hybrid recurrent target (gated delta
 // rule h_t = a_t (I - b_t k_t k_t^T) h_{t-1} + b_t k_t v_t^T, o_t = h_t^T q_t)
@@ -10,28 +10,30 @@
 //     o_x = A_x Pq_x + sum_{a on path(x)} dec(a -> x) (k_a . q_x) c_a
 // with w_xa = -a_x b_x dec(a -> par) (k_a . k_x) and P = h0^T [K; Q] the only
 // d_k x d_v-sized work.  Every state column evolves on its own once P, the
-// Gram rows [K; Q] K^T and the decays exist, so the state is cut into two
-// column halves and each CTA owns one.  Four warps, two roles:
+// Gram rows [K; Q] K^T and the decays exist.  Eight warps in two warpgroups:
 //
-//  * warps 2/3 split the half's fp32 state (TMA-staged, 128 rows x 64
-//    columns) into two bf16 terms (hi = h truncated to bf16, lo = bf16(h - hi):
-//    ~16 significant bits), in place, one 64-row half of d_k at a time, and
-//    after each half issue its tcgen05 products
-//        D[col][x] += sum_k h0[k][col] [K; Q][x][k]    (state as MN-major A)
+//  * warpgroup 1 (warps 4-7) splits the fp32 state (TMA-staged, 128 rows x
+//    128 columns as two 64-column halves) into two bf16 terms (hi = h
+//    truncated to bf16, lo = bf16(h - hi): ~16 significant bits), in place,
+//    one 64-row half of d_k at a time, and after each half issues its tcgen05
+//    products
+//        D[col][x] += sum_k h0[k][col] [K; Q][x][k]    (state as MN-major A,
+//                                                        M = 128 columns)
 //    so that tensor-memory lane `col` holds that column's Pk_x, Pq_x;
-//  * warp 0 issues the TMA copies and, once K and Q are in, the Gram rows
-//    G = [K; Q] K^T (exact bf16 products) into tensor memory; then warps 0/1
-//    turn Gram row x (lane x) and the tree into the weight row of c_x (warp 0)
-//    or o_x (warp 1): decay x Gram entry on the root path, zero elsewhere.
-//    After the products they run, one state column per lane, the write-vector
-//    recursion with the write vectors in registers and no branch
-//    (right-looking: row x adds its weighted c_x into every later row, two
-//    rows per packed FMA, so a row waits for one FMA after its predecessor;
-//    padding rows carry zero weights), then every output o_x from the same
-//    registers.
+//  * warpgroup 0 (warps 0-3): thread 0 issues the TMA copies and, once K and
+//    Q are in, the Gram rows G = [K; Q] K^T (exact bf16 products) into tensor
+//    memory; warps 0/1 turn Gram row x (lane x) and the tree into the weight
+//    row of c_x (warp 0) or o_x (warp 1): decay x Gram entry on the root path,
+//    zero elsewhere.  Then each of the four warps takes 32 state columns (its
+//    tensor-memory lane quarter: one warp per SM sub-partition) and runs, one
+//    column per lane, the write-vector recursion with the write vectors in
+//    registers and no branch (right-looking: row x adds its weighted c_x into
+//    every later row, two rows per packed FMA; padding rows carry zero
+//    weights), then every output o_x from the same registers.
 //
-// 66 KB of shared memory and 128 tensor-memory columns per CTA: three CTAs per
-// SM, each with two items in flight.
+// About 106 KB of shared memory and 128 tensor-memory columns per CTA: two
+// CTAs per SM, each with two states in flight (one being split while the
+// other's rows run).
 #include <cuda.h>
 
 #include "common.cuh"
@@ -46,36 +48,37 @@ namespace {
 using namespace tc;
 
 constexpr int DKV = 128;                 // d_k = d_v
-constexpr int SW = 64;                   // state columns per CTA
-constexpr int NSL = DKV / SW;            // column halves per state
-constexpr int NT = 128;                  // threads per CTA
+constexpr int HC = 64;                   // columns per state half (one TMA box, one MMA atom)
+constexpr int NT = 256;                  // threads per CTA: two warpgroups
 constexpr int TP = 32;                   // tree rows (padded)
-constexpr uint32_t kTmemCols = 128;      // P^T: 64 columns ([K; Q] rows), Gram rows: 32
+constexpr uint32_t kTmemCols = 256;      // P^T of two items (64 columns each: [K; Q] rows),
+                                         // Gram rows (32) at column 128
+constexpr uint32_t TM_G = 128;
 constexpr int WS = TP + 4;               // row stride of the o weights
 
 // byte offsets from the 1024-aligned base
 constexpr uint32_t OFF_KQ = 0;                           // [2 halves][64 rows][64] bf16, swizzled
-constexpr uint32_t OFF_ST = OFF_KQ + 2 * 64 * 128;       // fp32 [128][64]; in place, per 64-row
-                                                         // half h: lo tile, then hi tile
-constexpr uint32_t OFF_V = OFF_ST + DKV * SW * 4;        // bf16 [2 items][32 rows][64]
-constexpr uint32_t OFF_WU = OFF_V + 2 * TP * SW * 2;     // WuT[a][y]: c_a in c_y
+constexpr uint32_t HALF_ST = DKV * HC * 4;               // one column half of the state: 32 KB
+constexpr uint32_t OFF_ST = OFF_KQ + 2 * 64 * 128;       // fp32 [2 column halves][128][64]; in
+                                                         // place, per 64-row half kh of a
+                                                         // column half: lo tile, then hi tile
+constexpr uint32_t VBUF = 2 * TP * HC * 2;               // v of one item: [2 halves][32 rows][64]
+constexpr uint32_t OFF_V = OFF_ST + 2 * HALF_ST;         // bf16, two items
+constexpr uint32_t OFF_WU = OFF_V + 2 * VBUF;            // WuT[a][y]: c_a in c_y
 constexpr uint32_t OFF_WO = OFF_WU + TP * TP * 4;        // Wo[x][WS]: c_a in o_x
 constexpr uint32_t OFF_SM = OFF_WO + TP * WS * 4;        // al be [2][32], A ca [32] fp32
-constexpr int NBAR = 5;
+constexpr int NBAR = 6;
 constexpr uint32_t OFF_BAR = OFF_SM + 6 * TP * 4;        // mbarriers, TMEM slot, abort flag
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 8 * NBAR + 16 + 1024;   // + alignment slack
-constexpr uint32_t TX_KQV = 4 * TP * 128 + TP * SW * 2;  // K, Q (two halves each), v
-constexpr uint32_t TX_ST = DKV * SW * 4;                 // the state half
-constexpr uint32_t TILE = 64 * SW * 2;                   // one bf16 term of 64 d_k rows: 8 KB
-constexpr uint32_t LBO_A = 1024;                         // A rows 64..127 (unused): any smem
+constexpr uint32_t TX_KQV = 4 * TP * 128 + VBUF;         // K, Q (two halves each), v
+constexpr uint32_t TX_ST = 2 * HALF_ST;                  // the state
+constexpr uint32_t TILE = 64 * HC * 2;                   // one bf16 term of 64 d_k rows: 8 KB
 
 // the Gram products read A rows 64..127 past each 64-row half of the K/Q tile:
-// for the second half those rows are the staged state (valid shared memory);
-// the state products read their unused rows LBO_A past each tile
-static_assert(OFF_KQ + 64 * 128 + 128 * 128 <= OFF_ST + DKV * SW * 4, "A rows stay in smem");
-static_assert(OFF_ST + 3 * TILE + TILE + LBO_A <= OFF_BAR, "A rows stay in smem");
-static_assert(OFF_BAR % 8 == 0 && OFF_WO % 16 == 0, "alignment");
-static_assert(3 * (SMEM_BYTES + 1024) <= 228 * 1024, "three CTAs per SM");
+// for the second half those rows are the staged state (valid shared memory)
+static_assert(OFF_KQ + 64 * 128 + 128 * 128 <= OFF_ST + 2 * HALF_ST, "A rows stay in smem");
+static_assert(OFF_BAR % 8 == 0 && OFF_WO % 16 == 0 && OFF_ST % 1024 == 0, "alignment");
+static_assert(2 * (SMEM_BYTES + 1024) <= 228 * 1024, "two CTAs per SM");
 
 __device__ __forceinline__ unsigned char* align1024(unsigned char* raw) {
     return reinterpret_cast<unsigned char*>(
@@ -94,17 +97,18 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float x, float y) {
     return *reinterpret_cast<uint32_t*>(&t);
 }
 
-// named barrier for a pair of warps (ids 1, 2; 0 is __syncthreads)
-__device__ __forceinline__ void pair_sync(int id) {
-    asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+// named barrier over one warpgroup (id 1: warpgroup 1, id 2: warpgroup 0;
+// 0 is __syncthreads)
+__device__ __forceinline__ void wg_sync(int id) {
+    asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
 }
 
-__device__ __forceinline__ bool pair_sync_and(int id, bool p) {
+__device__ __forceinline__ bool wg_sync_and(int id, bool p) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred pi, po;\n\t"
         "setp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.and.pred po, %2, 64, pi;\n\t"
+        "bar.red.and.pred po, %2, 128, pi;\n\t"
         "selp.u32 %0, 1, 0, po;\n\t}"
         : "=r"(r)
         : "r"((uint32_t)p), "r"(id)
@@ -113,32 +117,32 @@ __device__ __forceinline__ bool pair_sync_and(int id, bool p) {
 }
 
 struct ItemIdx {
-    int b, j, sl, ih;
+    int b, j, ih;
 };
 __device__ __forceinline__ ItemIdx decode(int it, const spec_cfg& c) {
     ItemIdx d;
-    const int hj = it / NSL;
-    d.sl = it % NSL;
-    d.b = hj / c.Hv;
-    d.j = hj % c.Hv;
+    d.b = it / c.Hv;
+    d.j = it % c.Hv;
     d.ih = d.j / (c.Hv / c.Hk);
     return d;
 }
 
-// A persistent grid of at most three CTAs per SM runs the items (request,
-// v-head, column half) it = blockIdx.x, blockIdx.x + gridDim.x, ...  Item
-// it + 1 of the same (request, v-head) is its other column half, so the CTAs
-// running at one time share K/Q rows in L2.  Per item k of a CTA, the four
+// A persistent grid of at most two CTAs per SM runs the items (request,
+// v-head) it = blockIdx.x, blockIdx.x + gridDim.x, ...  Consecutive items of
+// one request share K/Q rows (Hv / Hk v-heads per q-k head), so the CTAs
+// running at one time share them in L2.  Per item k of a CTA, the four
 // mbarriers [0] K/Q/v in, [1] state in, [2] state products done, [3] Gram
-// rows done complete once (parity k & 1), and [4] (P^T read, tensor memory
-// free) completes once its outputs are done.  As soon as item k's products
-// have read the staging buffer and the K/Q tile, item k + 1's state and K/Q/v
-// copies start (v into the other of two buffers), so warps 2/3 split item
-// k + 1's state while warps 0/1 run item k's rows.  early: the tree may come
-// from the launch just before, so the programmatic wait precedes the first
-// read of it; otherwise the wait ends the kernel.
-__global__ void __launch_bounds__(NT, 3)
-gdn_slice_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__ CUtensorMap mk,
+// rows done complete once (parity k & 1).  Item k's products go to the
+// tensor-memory buffer k & 1, and [4 + (k & 1)] completes once all four row
+// warps have read that buffer (parity (k >> 1) & 1), so the products of item
+// k + 1 never wait for item k's rows.  As soon as item k's
+// products have read the staging buffer and the K/Q tile, item k + 1's state
+// and K/Q/v copies start (v into the other of two buffers), so warpgroup 1
+// splits item k + 1's state while warpgroup 0 runs item k's rows.  early: the
+// tree may come from the launch just before, so the programmatic wait
+// precedes the first read of it; otherwise the wait ends the kernel.
+__global__ void __launch_bounds__(NT, 2)
+gdn_state_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__ CUtensorMap mk,
                  const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mv,
                  spec_cfg c, spec_tree tree, const float* __restrict__ alpha,
                  const float* __restrict__ beta, __nv_bfloat16* __restrict__ o,
@@ -165,7 +169,9 @@ gdn_slice_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
     auto issue_state = [&](int it) {
         const ItemIdx d = decode(it, c);
         mbar_arrive_expect_tx(&bar[1], TX_ST);
-        tma_load_2d(sm + OFF_ST, &mh, &bar[1], d.sl * SW, (d.b * Hv + d.j) * DKV);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            tma_load_2d(sm + OFF_ST + h * HALF_ST, &mh, &bar[1], h * HC, (d.b * Hv + d.j) * DKV);
         ++n_st;
     };
     auto issue_kqv = [&](int it, int kv) {             // kv: the item's index in this CTA
@@ -176,14 +182,15 @@ gdn_slice_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
         for (int h = 0; h < 2; ++h) {
             tma_load_3d(sm + OFF_KQ + h * 64 * 128, &mk, &bar[0], h * 64, d.ih, row0);
             tma_load_3d(sm + OFF_KQ + h * 64 * 128 + TP * 128, &mq, &bar[0], h * 64, d.ih, row0);
+            tma_load_3d(sm + OFF_V + (kv & 1) * VBUF + h * (VBUF / 2), &mv, &bar[0], h * HC, d.j,
+                        row0);
         }
-        tma_load_3d(sm + OFF_V + (kv & 1) * TP * SW * 2, &mv, &bar[0], d.sl * SW, d.j, row0);
         ++n_kq;
     };
 
     const int it0 = blockIdx.x;
     if (tid == 0) {
-        for (int i = 0; i < NBAR; ++i) mbar_init(&bar[i], 1);
+        for (int i = 0; i < NBAR; ++i) mbar_init(&bar[i], i >= 4 ? 4 : 1);
         *abort_flag = 0;
         fence_mbar_init();
         issue_state(it0);
@@ -196,34 +203,36 @@ gdn_slice_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
 
-    if (warp >= 2) {
-        // ---- state split and products (warps 2/3) ---------------------------------------
-        const int t = tid - 64;                // 0..63
+    if (warp >= 4) {
+        // ---- state split and products (warpgroup 1) -------------------------------------
+        const int t = tid - 128;               // 0..127
+        const int t6 = t & 63;                 // 64 threads per column half
+        const uint32_t hbase = OFF_ST + (t >> 6) * HALF_ST;
         const uint32_t idp = idesc_bf16_f32(128, 2 * TP, /*a_mn=*/true, /*b_mn=*/false);
-        int n_p = 0;                           // product commits (thread 64)
+        int n_p = 0;                           // product commits (thread 128)
         bool pending = false;                  // products issued, not yet committed
         int k = 0;
         for (int it = it0; it < n_items && ok; it += G, ++k) {
             const uint32_t ph = k & 1;
             ok = __all_sync(0xffffffffu, mbar_wait(&bar[1], ph, abort_flag));
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                // d_k rows 64 h .. 64 h + 63 (16 KB of fp32 at OFF_ST + 16 KB h); unit
-                // u = t + 64 i: row 64 h + u / 8, columns 8 (u % 8) .. + 7
-                const float4* hs = reinterpret_cast<const float4*>(sm + OFF_ST + h * 2 * TILE);
+            for (int kh = 0; kh < 2; ++kh) {
+                // d_k rows 64 kh .. 64 kh + 63 of this thread's column half (16 KB of fp32);
+                // unit u = t6 + 64 i: row 64 kh + u / 8, columns 8 (u % 8) .. + 7
+                const float4* hs = reinterpret_cast<const float4*>(sm + hbase + kh * 2 * TILE);
                 float4 xv[16];
                 if (ok) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        xv[2 * i] = hs[2 * (t + 64 * i)];
-                        xv[2 * i + 1] = hs[2 * (t + 64 * i) + 1];
+                        xv[2 * i] = hs[2 * (t6 + 64 * i)];
+                        xv[2 * i + 1] = hs[2 * (t6 + 64 * i) + 1];
                     }
                 }
-                ok = pair_sync_and(1, ok);     // both warps hold their values
+                ok = wg_sync_and(1, ok);       // the warpgroup holds its values
                 if (!ok) break;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const int u = t + 64 * i, kr = u >> 3, ch = u & 7;
+                    const int u = t6 + 64 * i, kr = u >> 3, ch = u & 7;
                     const float4 a = xv[2 * i], e = xv[2 * i + 1];
                     const uint4 hi = make_uint4(bf16x2_trunc(a.x, a.y), bf16x2_trunc(a.z, a.w),
                                                 bf16x2_trunc(e.x, e.y), bf16x2_trunc(e.z, e.w));
@@ -232,17 +241,18 @@ gdn_slice_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
                                                 bf16x2_rn(trunc_rest(e.x), trunc_rest(e.y)),
                                                 bf16x2_rn(trunc_rest(e.z), trunc_rest(e.w)));
                     const uint32_t off = sw128_offset(kr, ch * 8);
-                    *reinterpret_cast<uint4*>(sm + OFF_ST + h * 2 * TILE + off) = lo;
-                    *reinterpret_cast<uint4*>(sm + OFF_ST + h * 2 * TILE + TILE + off) = hi;
+                    *reinterpret_cast<uint4*>(sm + hbase + kh * 2 * TILE + off) = lo;
+                    *reinterpret_cast<uint4*>(sm + hbase + kh * 2 * TILE + TILE + off) = hi;
                 }
                 fence_async_smem();
                 bool go = true;
-                if (t == 0 && h == 0) {
-                    // item k - 1's P^T has been read, and this item's K/Q rows are in
-                    if (k > 0) go = mbar_wait(&bar[4], (k - 1) & 1, abort_flag);
+                if (t == 0 && kh == 0) {
+                    // item k - 2's P^T (the same tensor-memory buffer) has been read,
+                    // and this item's K/Q rows are in
+                    if (k >= 2) go = mbar_wait(&bar[4 + ph], ((k >> 1) - 1) & 1, abort_flag);
                     go = go && mbar_wait(&bar[0], ph, abort_flag);
                 }
-                ok = pair_sync_and(1, go);
+                ok = wg_sync_and(1, go);
                 if (!ok) break;
                 if (t == 0) {
                     tc_fence_after();
@@ -250,10 +260,11 @@ gdn_slice_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
                     for (int part = 0; part < 2; ++part) {
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
-                            const uint32_t a_s = st_s + h * 2 * TILE + part * TILE + kk * 2048;
-                            const uint32_t b_s = kq_s + h * 64 * 128 + kk * 32;
-                            mma_bf16(tmem, sdesc_sw128(a_s, LBO_A, 1024),
-                                     sdesc_sw128(b_s, 16, 1024), idp, (h | part | kk) != 0);
+                            // columns 0..63 and, HALF_ST further, 64..127 (M = 128)
+                            const uint32_t a_s = st_s + kh * 2 * TILE + part * TILE + kk * 2048;
+                            const uint32_t b_s = kq_s + kh * 64 * 128 + kk * 32;
+                            mma_bf16(tmem + 2 * TP * ph, sdesc_sw128(a_s, HALF_ST, 1024),
+                                     sdesc_sw128(b_s, 16, 1024), idp, (kh | part | kk) != 0);
                         }
                     }
                     pending = true;
@@ -276,7 +287,7 @@ gdn_slice_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
         if (!ok) *abort_flag = 1;
         if (t == 0 && n_p > 0) mbar_wait(&bar[2], (n_p - 1) & 1, nullptr);
     } else {
-        // ---- Gram rows, weights, write vectors and outputs (warps 0/1) ----------------
+        // ---- Gram rows, weights, write vectors and outputs (warpgroup 0) ------------------
         int n_g = 0;                           // Gram commits (thread 0)
         // the next item's tree rows and gates are loaded one item ahead (both loads
         // independent of each other); rows past n_nodes are masked at use
@@ -312,61 +323,64 @@ gdn_slice_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
                 if (warp == 0) gates_of(it + G, al_next, be_next);
             }
             bool go = true;
-            if (tid == 0) {
-                go = mbar_wait(&bar[0], ph, abort_flag);
-                if (go) {
-                    tc_fence_after();
-                    const uint32_t idg = idesc_bf16_f32(128, TP, false, false);
+            if (warp < 2) {
+                if (tid == 0) {
+                    go = mbar_wait(&bar[0], ph, abort_flag);
+                    if (go) {
+                        tc_fence_after();
+                        const uint32_t idg = idesc_bf16_f32(128, TP, false, false);
 #pragma unroll
-                    for (int ks = 0; ks < DKV / 16; ++ks) {
-                        const uint32_t off = (ks >> 2) * 64 * 128 + (ks & 3) * 32;
-                        mma_bf16(tmem + 2 * TP, sdesc_sw128(kq_s + off, 16, 1024),
-                                 sdesc_sw128(kq_s + off, 16, 1024), idg, ks != 0);
+                        for (int ks = 0; ks < DKV / 16; ++ks) {
+                            const uint32_t off = (ks >> 2) * 64 * 128 + (ks & 3) * 32;
+                            mma_bf16(tmem + TM_G, sdesc_sw128(kq_s + off, 16, 1024),
+                                     sdesc_sw128(kq_s + off, 16, 1024), idg, ks != 0);
+                        }
                     }
+                    mma_commit(&bar[3]);
+                    ++n_g;
+                    if (!go) *abort_flag = 1;
                 }
-                mma_commit(&bar[3]);
-                ++n_g;
-                if (!go) *abort_flag = 1;
-            }
-            go = __all_sync(0xffffffffu, mbar_wait(&bar[3], ph, abort_flag));
-            if (go) {
-                // the weight rows (item k - 1's readers are done): lane x, Gram row x
-                float w[TP], alr[TP];
-                float acc = 1.0f;
-                tc_fence_after();
-                tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 2 * TP, w);
+                go = __all_sync(0xffffffffu, mbar_wait(&bar[3], ph, abort_flag));
+                if (go) {
+                    // the weight rows (item k - 1's readers are done): lane x, Gram row x
+                    float w[TP], alr[TP];
+                    float acc = 1.0f;
+                    tc_fence_after();
+                    tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + TM_G, w);
 #pragma unroll
-                for (int a4 = 0; a4 < TP / 4; ++a4) {
-                    const float4 t4 = *reinterpret_cast<const float4*>(al + 4 * a4);
-                    alr[4 * a4] = t4.x;
-                    alr[4 * a4 + 1] = t4.y;
-                    alr[4 * a4 + 2] = t4.z;
-                    alr[4 * a4 + 3] = t4.w;
-                }
-                tmem_wait_ld();
-                const uint32_t path = warp == 0 ? anc & ~(1u << lane) : anc;  // parent's path / x's
+                    for (int a4 = 0; a4 < TP / 4; ++a4) {
+                        const float4 t4 = *reinterpret_cast<const float4*>(al + 4 * a4);
+                        alr[4 * a4] = t4.x;
+                        alr[4 * a4 + 1] = t4.y;
+                        alr[4 * a4 + 2] = t4.z;
+                        alr[4 * a4 + 3] = t4.w;
+                    }
+                    tmem_wait_ld();
+                    const uint32_t path = warp == 0 ? anc & ~(1u << lane) : anc;  // parent's / x's
 #pragma unroll
-                for (int a = TP - 1; a >= 0; --a) {
-                    const bool on = (path >> a) & 1u;
-                    w[a] = on ? acc * w[a] : 0.0f;
-                    acc = on ? acc * alr[a] : acc;
-                }
-                if (warp == 0) {
-                    const float s = -al[lane] * be[lane];
-                    float* WuT = reinterpret_cast<float*>(sm + OFF_WU);
+                    for (int a = TP - 1; a >= 0; --a) {
+                        const bool on = (path >> a) & 1u;
+                        w[a] = on ? acc * w[a] : 0.0f;
+                        acc = on ? acc * alr[a] : acc;
+                    }
+                    if (warp == 0) {
+                        const float s = -al[lane] * be[lane];
+                        float* WuT = reinterpret_cast<float*>(sm + OFF_WU);
 #pragma unroll
-                    for (int a = 0; a < TP; ++a) WuT[a * TP + lane] = s * w[a];
-                    ca[lane] = s * acc;
-                } else {
-                    float4* Wo = reinterpret_cast<float4*>(sm + OFF_WO + lane * WS * 4);
+                        for (int a = 0; a < TP; ++a) WuT[a * TP + lane] = s * w[a];
+                        ca[lane] = s * acc;
+                    } else {
+                        float4* Wo = reinterpret_cast<float4*>(sm + OFF_WO + lane * WS * 4);
 #pragma unroll
-                    for (int a4 = 0; a4 < TP / 4; ++a4)
-                        Wo[a4] = make_float4(w[4 * a4], w[4 * a4 + 1], w[4 * a4 + 2], w[4 * a4 + 3]);
-                    A[lane] = acc;
+                        for (int a4 = 0; a4 < TP / 4; ++a4)
+                            Wo[a4] = make_float4(w[4 * a4], w[4 * a4 + 1], w[4 * a4 + 2],
+                                                 w[4 * a4 + 3]);
+                        A[lane] = acc;
+                    }
                 }
             }
             go = go && mbar_wait(&bar[2], ph, abort_flag);
-            ok = pair_sync_and(2, go && *abort_flag == 0);       // the weights are visible
+            ok = wg_sync_and(2, go && *abort_flag == 0);        // the weights are visible
             if (!ok) break;
             tc_fence_after();
             // this item's products have read the staging buffer and the K/Q tile
@@ -375,22 +389,20 @@ gdn_slice_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
                 issue_kqv(it + G, k + 1);
             }
 
-            // one state column per lane
-            const int cl = warp * 32 + lane;   // column in the half = tensor-memory lane
-            const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
-            float pk[TP], pq[TP];
-            tmem_ld32(tl, pk);                 // Pk_x, Pq_x of this column, x = 0..31
-            tmem_ld32(tl + TP, pq);
+            // one state column per lane: warp w owns columns 32 w .. 32 w + 31
+            const int cl = warp * 32 + lane;   // column of the state = tensor-memory lane
+            const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16) + 2 * TP * ph;
+            float pk[TP];
+            tmem_ld32(tl, pk);                 // Pk_x of this column, x = 0..31
             tmem_wait_ld();
-            tc_fence_before();
             const float* WuT = reinterpret_cast<const float*>(sm + OFF_WU);
-            const __nv_bfloat16* vs =
-                reinterpret_cast<const __nv_bfloat16*>(sm + OFF_V + ph * TP * SW * 2);
+            const __nv_bfloat16* vs = reinterpret_cast<const __nv_bfloat16*>(
+                sm + OFF_V + ph * VBUF + (cl >> 6) * (VBUF / 2)) + (cl & (HC - 1));
             float2 u[TP / 2];                  // rows 2p, 2p + 1
 #pragma unroll
             for (int p = 0; p < TP / 2; ++p) {
-                u[p].x = fmaf(be[2 * p], __bfloat162float(vs[(2 * p) * SW + cl]), ca[2 * p] * pk[2 * p]);
-                u[p].y = fmaf(be[2 * p + 1], __bfloat162float(vs[(2 * p + 1) * SW + cl]),
+                u[p].x = fmaf(be[2 * p], __bfloat162float(vs[(2 * p) * HC]), ca[2 * p] * pk[2 * p]);
+                u[p].y = fmaf(be[2 * p + 1], __bfloat162float(vs[(2 * p + 1) * HC]),
                               ca[2 * p + 1] * pk[2 * p + 1]);
             }
 #pragma unroll
@@ -419,7 +431,7 @@ gdn_slice_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
                 if (2 * p + 1 >= nn) u[p].y = 0.0f;
             }
             const size_t rs = (size_t)Hv * DKV;                          // row stride
-            const size_t ob = ((size_t)d.b * T * Hv + d.j) * DKV + d.sl * SW + cl;
+            const size_t ob = ((size_t)d.b * T * Hv + d.j) * DKV + cl;
             if (c_out) {
 #pragma unroll
                 for (int p = 0; p < TP / 2; ++p) {
@@ -427,6 +439,12 @@ gdn_slice_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
                     if (2 * p + 1 < T) c_out[ob + (2 * p + 1) * rs] = u[p].y;
                 }
             }
+            float pq[TP];
+            tmem_ld32(tl + TP, pq);            // Pq_x of this column
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[4 + ph]);   // this P^T buffer is free again
             const float* Wo = reinterpret_cast<const float*>(sm + OFF_WO);
             // rows of the tree only; pairs p <= x / 2 cover every a <= x (the weights
             // beyond x are zero)
@@ -443,13 +461,12 @@ gdn_slice_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
                 o[ob + x * rs] = __float2bfloat16_rn(x < nn ? (acc0.x + acc1.x) + (acc0.y + acc1.y) : 0.0f);
             }
             // the next item's gates go to the other buffer (this item's readers are done
-            // once both warps pass the barrier below)
+            // once the warpgroup passes the barrier below)
             if (warp == 0 && more) {
                 al2[(ph ^ 1) * TP + lane] = al_next;
                 be2[(ph ^ 1) * TP + lane] = be_next;
             }
-            pair_sync(2);
-            if (tid == 0) mbar_arrive(&bar[4]);                 // P^T has been read
+            wg_sync(2);
         }
         if (!ok) *abort_flag = 1;
         if (tid == 0 && n_g > 0) mbar_wait(&bar[3], (n_g - 1) & 1, nullptr);
@@ -482,7 +499,7 @@ bool state_map(CUtensorMap* m, const float* base, int rows) {
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)DKV, (cuuint64_t)rows};
     cuuint64_t str[1] = {(cuuint64_t)DKV * 4};
-    cuuint32_t box[2] = {(cuuint32_t)SW, (cuuint32_t)DKV};
+    cuuint32_t box[2] = {(cuuint32_t)HC, (cuuint32_t)DKV};
     cuuint32_t es[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, str, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -495,7 +512,7 @@ bool vslice_map(CUtensorMap* m, const void* base, int H, int rows) {
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)DKV, (cuuint64_t)H, (cuuint64_t)rows};
     cuuint64_t str[2] = {(cuuint64_t)DKV * 2, (cuuint64_t)H * DKV * 2};
-    cuuint32_t box[3] = {(cuuint32_t)SW, 1, (cuuint32_t)TP};
+    cuuint32_t box[3] = {(cuuint32_t)HC, 1, (cuuint32_t)TP};
     cuuint32_t es[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, str, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -504,12 +521,12 @@ bool vslice_map(CUtensorMap* m, const void* base, int H, int rows) {
 
 }  // namespace
 
-bool gdn_slice_supported(const spec_cfg& c) {
+bool gdn_state_supported(const spec_cfg& c) {
     return c.io_dtype == SPEC_IO_BF16 && c.dk == DKV && c.dv == DKV && c.N + 1 <= TP &&
            gdn_tc::encode_fn() != nullptr;
 }
 
-cudaError_t launch_gdn_slice(const spec_cfg& c, const spec_tree& t, const float* h0,
+cudaError_t launch_gdn_state(const spec_cfg& c, const spec_tree& t, const float* h0,
                              const void* q, const void* k, const void* v, const float* alpha,
                              const float* beta, void* o, float* c_out, void* ws, cudaStream_t st,
                              bool pdl, bool early) {
@@ -520,7 +537,7 @@ cudaError_t launch_gdn_slice(const spec_cfg& c, const spec_tree& t, const float*
         !gdn_tc::rows_map(&mq, q, c.Hk, c.B * T, TP, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !vslice_map(&mv, v, c.Hv, c.B * T))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(gdn_slice_kernel,
+    cudaError_t e = cudaFuncSetAttribute(gdn_state_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -528,10 +545,10 @@ cudaError_t launch_gdn_slice(const spec_cfg& c, const spec_tree& t, const float*
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return e;
-    const int n_items = NSL * c.Hv * c.B;
-    const int grid = n_items < 3 * sms ? n_items : 3 * sms;       // three CTAs per SM
+    const int n_items = c.Hv * c.B;
+    const int grid = n_items < 2 * sms ? n_items : 2 * sms;       // two CTAs per SM
     // without programmatic launch the tree is complete when the kernel starts
-    return launch_k(pdl, gdn_slice_kernel, dim3(grid), dim3(NT), SMEM_BYTES, st, mh, mk, mq, mv,
+    return launch_k(pdl, gdn_state_kernel, dim3(grid), dim3(NT), SMEM_BYTES, st, mh, mk, mq, mv,
                     c, t, alpha, beta, static_cast<__nv_bfloat16*>(o), c_out, ws, early && pdl,
                     n_items);
 }

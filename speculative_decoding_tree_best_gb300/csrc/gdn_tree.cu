@@ -372,8 +372,8 @@ cudaError_t launch_gdn_tree(const spec_cfg& c, const spec_tree& t, const float* 
                             const void* q, const void* k, const void* v, const float* alpha,
                             const float* beta, void* o, float* c_out, void* ws, cudaStream_t st,
                             bool pdl, bool early) {
-    if (gdn_slice_supported(c))
-        return launch_gdn_slice(c, t, h0, q, k, v, alpha, beta, o, c_out, ws, st, pdl, early);
+    if (gdn_state_supported(c))
+        return launch_gdn_state(c, t, h0, q, k, v, alpha, beta, o, c_out, ws, st, pdl, early);
     const size_t smem = gdn_tree_smem(c);
     if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
     const int T = c.N + 1;
