@@ -51,10 +51,11 @@ constexpr int DKV = 128;                 // d_k = d_v
 constexpr int HC = 64;                   // columns per state half (one TMA box, one MMA atom)
 constexpr int NT = 256;                  // threads per CTA: two warpgroups
 constexpr int TP = 32;                   // tree rows (padded)
-constexpr uint32_t kTmemCols = 256;      // P^T of two items (64 columns each: [K; Q] rows),
-                                         // Gram rows (32) at column 128
-constexpr uint32_t TM_G = 128;
-constexpr int WS = TP + 4;               // row stride of the o weights
+// tensor-memory columns: P^T of two items (64 each: [K; Q] rows), the Gram
+// rows, the write vectors split into two bf16 terms (two per column), and the
+// outputs
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t TM_G = 128, TM_C = 160, TM_O = 192;
 
 // byte offsets from the 1024-aligned base
 constexpr uint32_t OFF_KQ = 0;                           // [2 halves][64 rows][64] bf16, swizzled
@@ -65,9 +66,10 @@ constexpr uint32_t OFF_ST = OFF_KQ + 2 * 64 * 128;       // fp32 [2 column halve
 constexpr uint32_t VBUF = 2 * TP * HC * 2;               // v of one item: [2 halves][32 rows][64]
 constexpr uint32_t OFF_V = OFF_ST + 2 * HALF_ST;         // bf16, two items
 constexpr uint32_t OFF_WU = OFF_V + 2 * VBUF;            // WuT[a][y]: c_a in c_y
-constexpr uint32_t OFF_WO = OFF_WU + TP * TP * 4;        // Wo[x][WS]: c_a in o_x
-constexpr uint32_t OFF_SM = OFF_WO + TP * WS * 4;        // al be [2][32], A ca [32] fp32
-constexpr int NBAR = 6;
+constexpr uint32_t OFF_WO = OFF_WU + TP * TP * 4;        // Wo [x][hi a | lo a] bf16, swizzled:
+                                                         // c_a in o_x
+constexpr uint32_t OFF_SM = OFF_WO + TP * 128;           // al be [2][32], A ca [32] fp32
+constexpr int NBAR = 7;
 constexpr uint32_t OFF_BAR = OFF_SM + 6 * TP * 4;        // mbarriers, TMEM slot, abort flag
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 8 * NBAR + 16 + 1024;   // + alignment slack
 constexpr uint32_t TX_KQV = 4 * TP * 128 + VBUF;         // K, Q (two halves each), v
@@ -77,7 +79,7 @@ constexpr uint32_t TILE = 64 * HC * 2;                   // one bf16 term of 64 
 // the Gram products read A rows 64..127 past each 64-row half of the K/Q tile:
 // for the second half those rows are the staged state (valid shared memory)
 static_assert(OFF_KQ + 64 * 128 + 128 * 128 <= OFF_ST + 2 * HALF_ST, "A rows stay in smem");
-static_assert(OFF_BAR % 8 == 0 && OFF_WO % 16 == 0 && OFF_ST % 1024 == 0, "alignment");
+static_assert(OFF_BAR % 8 == 0 && OFF_WO % 1024 == 0 && OFF_ST % 1024 == 0, "alignment");
 static_assert(2 * (SMEM_BYTES + 1024) <= 228 * 1024, "two CTAs per SM");
 
 __device__ __forceinline__ unsigned char* align1024(unsigned char* raw) {
@@ -91,6 +93,15 @@ __device__ __forceinline__ uint32_t bf16x2_trunc(float x, float y) {
 }
 __device__ __forceinline__ float trunc_rest(float x) {
     return x - __uint_as_float(__float_as_uint(x) & 0xffff0000u);
+}
+// x as two bf16 terms hi + lo (hi = bf16(x), lo = bf16(x - hi): ~16 significant
+// bits), packed with y's: (hi_x | hi_y << 16), (lo_x | lo_y << 16)
+__device__ __forceinline__ void bf16x2_split(float x, float y, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x - hf.x, y - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 __device__ __forceinline__ uint32_t bf16x2_rn(float x, float y) {
     __nv_bfloat162 t = __floats2bfloat162_rn(x, y);
@@ -132,10 +143,11 @@ __device__ __forceinline__ ItemIdx decode(int it, const spec_cfg& c) {
 // one request share K/Q rows (Hv / Hk v-heads per q-k head), so the CTAs
 // running at one time share them in L2.  Per item k of a CTA, the four
 // mbarriers [0] K/Q/v in, [1] state in, [2] state products done, [3] Gram
-// rows done complete once (parity k & 1).  Item k's products go to the
-// tensor-memory buffer k & 1, and [4 + (k & 1)] completes once all four row
-// warps have read that buffer (parity (k >> 1) & 1), so the products of item
-// k + 1 never wait for item k's rows.  As soon as item k's
+// rows done complete once (parity k & 1), as does [6], the output products.
+// Item k's products go to the tensor-memory buffer k & 1, and [4 + (k & 1)]
+// completes once all four row warps have read that buffer (parity
+// (k >> 1) & 1), so the products of item k + 1 never wait for item k's rows.
+// As soon as item k's
 // products have read the staging buffer and the K/Q tile, item k + 1's state
 // and K/Q/v copies start (v into the other of two buffers), so warpgroup 1
 // splits item k + 1's state while warpgroup 0 runs item k's rows.  early: the
@@ -165,7 +177,9 @@ gdn_state_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
         al2[buf * TP + lane] = lane < T ? alpha[((size_t)d.b * T + lane) * Hv + d.j] : 0.0f;
         be2[buf * TP + lane] = lane < T ? beta[((size_t)d.b * T + lane) * Hv + d.j] : 0.0f;
     };
-    int n_st = 0, n_kq = 0;                                // copies issued (thread 0)
+    // copies issued: thread 0 issues the first item's, thread 128 the rest (its
+    // counts start at 1 so that (n - 1) & 1 is the parity of its last copy)
+    int n_st = tid == 128 ? 1 : 0, n_kq = n_st;
     auto issue_state = [&](int it) {
         const ItemIdx d = decode(it, c);
         mbar_arrive_expect_tx(&bar[1], TX_ST);
@@ -187,10 +201,20 @@ gdn_state_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
         }
         ++n_kq;
     };
+    auto prefetch_l2 = [&](int it) {       // the item's state and rows into L2
+        const ItemIdx d = decode(it, c);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            tma_prefetch_l2_2d(&mh, h * HC, (d.b * Hv + d.j) * DKV);
+            tma_prefetch_l2_3d(&mk, h * 64, d.ih, d.b * T);
+            tma_prefetch_l2_3d(&mq, h * 64, d.ih, d.b * T);
+            tma_prefetch_l2_3d(&mv, h * HC, d.j, d.b * T);
+        }
+    };
 
     const int it0 = blockIdx.x;
     if (tid == 0) {
-        for (int i = 0; i < NBAR; ++i) mbar_init(&bar[i], i >= 4 ? 4 : 1);
+        for (int i = 0; i < NBAR; ++i) mbar_init(&bar[i], i == 4 || i == 5 ? 4 : 1);
         *abort_flag = 0;
         fence_mbar_init();
         issue_state(it0);
@@ -215,6 +239,8 @@ gdn_state_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
         for (int it = it0; it < n_items && ok; it += G, ++k) {
             const uint32_t ph = k & 1;
             ok = __all_sync(0xffffffffu, mbar_wait(&bar[1], ph, abort_flag));
+            // the next item's inputs start towards L2 while this one is split
+            if (t == 0 && it + G < n_items) prefetch_l2(it + G);
 #pragma unroll
             for (int kh = 0; kh < 2; ++kh) {
                 // d_k rows 64 kh .. 64 kh + 63 of this thread's column half (16 KB of fp32);
@@ -274,7 +300,23 @@ gdn_state_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
                 mma_commit(&bar[2]);
                 ++n_p;
                 pending = false;
+                if (it + G < n_items) {
+                    // the next item's copies once this item's products and Gram rows
+                    // have read the staging buffer and the K/Q tile, and item k - 1's
+                    // rows (the other v buffer) have read their inputs
+                    bool free = mbar_wait(&bar[2], ph, abort_flag) &&
+                                mbar_wait(&bar[3], ph, abort_flag);
+                    if (k >= 1) free = free && mbar_wait(&bar[4 + (ph ^ 1)], ((k - 1) >> 1) & 1,
+                                                         abort_flag);
+                    if (free) {
+                        issue_state(it + G);
+                        issue_kqv(it + G, k + 1);
+                    } else {
+                        ok = false;
+                    }
+                }
             }
+            ok = __all_sync(0xffffffffu, ok);
             if (k == 0 && early) {
                 pdl_wait();
                 pdl_trigger();
@@ -288,7 +330,7 @@ gdn_state_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
         if (t == 0 && n_p > 0) mbar_wait(&bar[2], (n_p - 1) & 1, nullptr);
     } else {
         // ---- Gram rows, weights, write vectors and outputs (warpgroup 0) ------------------
-        int n_g = 0;                           // Gram commits (thread 0)
+        int n_g = 0, n_o = 0;                  // Gram and output commits (thread 0)
         // the next item's tree rows and gates are loaded one item ahead (both loads
         // independent of each other); rows past n_nodes are masked at use
         auto tree_of = [&](int it, int& nn, uint32_t& anc) {
@@ -370,11 +412,22 @@ gdn_state_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
                         for (int a = 0; a < TP; ++a) WuT[a * TP + lane] = s * w[a];
                         ca[lane] = s * acc;
                     } else {
-                        float4* Wo = reinterpret_cast<float4*>(sm + OFF_WO + lane * WS * 4);
+                        // row x = lane of Wo as [hi(a = 0..31) | lo(a = 0..31)] bf16,
+                        // K-major with the 128-byte swizzle (16-byte chunk j of row x
+                        // at j ^ (x % 8))
 #pragma unroll
-                        for (int a4 = 0; a4 < TP / 4; ++a4)
-                            Wo[a4] = make_float4(w[4 * a4], w[4 * a4 + 1], w[4 * a4 + 2],
-                                                 w[4 * a4 + 3]);
+                        for (int j = 0; j < TP / 8; ++j) {
+                            uint4 hi, lo;
+                            bf16x2_split(w[8 * j], w[8 * j + 1], hi.x, lo.x);
+                            bf16x2_split(w[8 * j + 2], w[8 * j + 3], hi.y, lo.y);
+                            bf16x2_split(w[8 * j + 4], w[8 * j + 5], hi.z, lo.z);
+                            bf16x2_split(w[8 * j + 6], w[8 * j + 7], hi.w, lo.w);
+                            *reinterpret_cast<uint4*>(sm + OFF_WO + lane * 128 +
+                                                      ((j ^ (lane & 7)) << 4)) = hi;
+                            *reinterpret_cast<uint4*>(sm + OFF_WO + lane * 128 +
+                                                      (((j + 4) ^ (lane & 7)) << 4)) = lo;
+                        }
+                        fence_async_smem();
                         A[lane] = acc;
                     }
                 }
@@ -383,11 +436,6 @@ gdn_state_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
             ok = wg_sync_and(2, go && *abort_flag == 0);        // the weights are visible
             if (!ok) break;
             tc_fence_after();
-            // this item's products have read the staging buffer and the K/Q tile
-            if (tid == 0 && more) {
-                issue_state(it + G);
-                issue_kqv(it + G, k + 1);
-            }
 
             // one state column per lane: warp w owns columns 32 w .. 32 w + 31
             const int cl = warp * 32 + lane;   // column of the state = tensor-memory lane
@@ -405,22 +453,29 @@ gdn_state_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
                 u[p].y = fmaf(be[2 * p + 1], __bfloat162float(vs[(2 * p + 1) * HC]),
                               ca[2 * p + 1] * pk[2 * p + 1]);
             }
+            // rows with descendants (the strict ancestors of some row): a leaf's
+            // weight row is zero, so its step is skipped (a warp-uniform branch)
+            const uint32_t inner = __reduce_or_sync(0xffffffffu, anc & ~(1u << lane));
 #pragma unroll
             for (int x = 0; x < TP - 1; ++x) {
+                if (!((inner >> x) & 1u)) continue;
+                float4 wq[TP / 4];
+#pragma unroll
+                for (int q = (x + 1) / 4; q < TP / 4; ++q)           // the row's weights first
+                    wq[q] = *reinterpret_cast<const float4*>(WuT + x * TP + 4 * q);
                 const float cx = (x & 1) ? u[x >> 1].y : u[x >> 1].x;   // final
                 const float2 cxx = make_float2(cx, cx);
 #pragma unroll
                 for (int q = (x + 1) / 4; q < TP / 4; ++q) {         // rows 4q .. 4q + 3
-                    const float4 wq = *reinterpret_cast<const float4*>(WuT + x * TP + 4 * q);
                     if (4 * q > x) {
-                        u[2 * q] = __ffma2_rn(make_float2(wq.x, wq.y), cxx, u[2 * q]);
+                        u[2 * q] = __ffma2_rn(make_float2(wq[q].x, wq[q].y), cxx, u[2 * q]);
                     } else if (4 * q + 1 > x) {
-                        u[2 * q].y = fmaf(wq.y, cx, u[2 * q].y);
+                        u[2 * q].y = fmaf(wq[q].y, cx, u[2 * q].y);
                     }
                     if (4 * q + 2 > x) {
-                        u[2 * q + 1] = __ffma2_rn(make_float2(wq.z, wq.w), cxx, u[2 * q + 1]);
+                        u[2 * q + 1] = __ffma2_rn(make_float2(wq[q].z, wq[q].w), cxx, u[2 * q + 1]);
                     } else {
-                        u[2 * q + 1].y = fmaf(wq.w, cx, u[2 * q + 1].y);
+                        u[2 * q + 1].y = fmaf(wq[q].w, cx, u[2 * q + 1].y);
                     }
                 }
             }
@@ -439,44 +494,84 @@ gdn_state_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
                     if (2 * p + 1 < T) c_out[ob + (2 * p + 1) * rs] = u[p].y;
                 }
             }
+            // outputs on the tensor cores: O[col][x] = sum_a c[col][a] Wo[x][a] as three
+            // bf16 products of the split terms (hi hi, lo hi, hi lo), the write vectors
+            // of this warp's columns as A in tensor memory (lane = column; c hi in
+            // columns TM_C .. + 15, c lo in the next 16)
+            {
+                uint32_t ch[TP / 2], clo[TP / 2];
+#pragma unroll
+                for (int p = 0; p < TP / 2; ++p) bf16x2_split(u[p].x, u[p].y, ch[p], clo[p]);
+                const uint32_t tq = tmem + ((uint32_t)(warp * 32) << 16);
+                tmem_st16(tq + TM_C, ch);
+                tmem_st16(tq + TM_C + TP / 2, clo);
+            }
             float pq[TP];
             tmem_ld32(tl + TP, pq);            // Pq_x of this column
             tmem_wait_ld();
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[4 + ph]);   // this P^T buffer is free again
-            const float* Wo = reinterpret_cast<const float*>(sm + OFF_WO);
-            // rows of the tree only; pairs p <= x / 2 cover every a <= x (the weights
-            // beyond x are zero)
+            tc_fence_before();
+            wg_sync(2);                        // every column's write vectors are in place
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t idt = idesc_bf16_f32(128, TP, false, false);
+                const uint32_t wo_s = smem_u32(sm + OFF_WO);
 #pragma unroll
-            for (int x = 0; x < TP; ++x) {
-                if (x >= T) break;
-                float2 acc0 = make_float2(A[x] * pq[x], 0.0f), acc1 = make_float2(0.0f, 0.0f);
+                for (int m3 = 0; m3 < 3; ++m3) {
+                    const uint32_t a_c = TM_C + (m3 == 1 ? TP / 2 : 0);   // c hi, c lo, c hi
+                    const uint32_t b_w = wo_s + (m3 == 2 ? 2 * TP : 0);   // Wo hi, hi, lo
 #pragma unroll
-                for (int q = 0; q <= x / 4; ++q) {
-                    const float4 wq = *reinterpret_cast<const float4*>(Wo + x * WS + 4 * q);
-                    acc0 = __ffma2_rn(make_float2(wq.x, wq.y), u[2 * q], acc0);
-                    if (4 * q + 2 <= x) acc1 = __ffma2_rn(make_float2(wq.z, wq.w), u[2 * q + 1], acc1);
+                    for (int s16 = 0; s16 < TP / 16; ++s16)             // K = 16 per product
+                        mma_f16_tmem_a(tmem + TM_O, tmem + a_c + 8 * s16,
+                                       sdesc_sw128(b_w + s16 * 32, 16, 1024), idt,
+                                       (m3 | s16) != 0);
                 }
-                o[ob + x * rs] = __float2bfloat16_rn(x < nn ? (acc0.x + acc1.x) + (acc0.y + acc1.y) : 0.0f);
+                mma_commit(&bar[6]);
+                ++n_o;
             }
-            // the next item's gates go to the other buffer (this item's readers are done
-            // once the warpgroup passes the barrier below)
+            const bool o_ok = __all_sync(0xffffffffu, mbar_wait(&bar[6], ph, abort_flag));
+            if (o_ok) {
+                tc_fence_after();
+                float ov[TP];
+                tmem_ld32(tl - 2 * TP * ph + TM_O, ov);
+                tmem_wait_ld();
+                tc_fence_before();
+                const size_t rs = (size_t)Hv * DKV;                      // row stride
+                const size_t ob = ((size_t)d.b * T * Hv + d.j) * DKV + cl;
+#pragma unroll
+                for (int x4 = 0; x4 < TP / 4; ++x4) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(A + 4 * x4);   // A_x
+                    const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int x = 4 * x4 + e;
+                        if (x < T)
+                            o[ob + x * rs] = __float2bfloat16_rn(
+                                x < nn ? fmaf(av[e], pq[x], ov[x]) : 0.0f);
+                    }
+                }
+            }
+            // the next item's gates go to the other buffer (this item's readers are done)
             if (warp == 0 && more) {
                 al2[(ph ^ 1) * TP + lane] = al_next;
                 be2[(ph ^ 1) * TP + lane] = be_next;
             }
-            wg_sync(2);
+            ok = wg_sync_and(2, o_ok && *abort_flag == 0);
+            if (!ok) break;
         }
         if (!ok) *abort_flag = 1;
         if (tid == 0 && n_g > 0) mbar_wait(&bar[3], (n_g - 1) & 1, nullptr);
+        if (tid == 0 && n_o > 0) mbar_wait(&bar[6], (n_o - 1) & 1, nullptr);
     }
 
     // ---- teardown ------------------------------------------------------------------------
     ok = __syncthreads_and(ok && *abort_flag == 0);
     if (!ok) {
         raise_status(ws, SPEC_DEV_TIMEOUT);
-        if (tid == 0) {      // let the copies in flight land before leaving
+        if (tid == 0 || tid == 128) {      // let the copies in flight land before leaving
             if (n_kq > 0) mbar_wait(&bar[0], (n_kq - 1) & 1, nullptr);
             if (n_st > 0) mbar_wait(&bar[1], (n_st - 1) & 1, nullptr);
         }
