@@ -575,44 +575,30 @@ def measure(scfg, args, rank, world, dev, flush, steps, warmup, kernels=True, e2
         res["kernel_us"] = kus
 
     # ---- end to end through the public API with host buffers ----------------------
-    # The step's inputs arrive in one pinned host buffer and go over in one copy
-    # per step; the step reads them in place (its input tensors are views of
-    # one device buffer, each at a 256-byte boundary).
+    # step.HostStep: the step's inputs arrive from pinned host memory in four
+    # pieces on a copy stream (lattice, attention rows, GDN rows, logits), each
+    # phase waiting only for its piece, so the logits copy overlaps the tree,
+    # attention and GDN; the accepted lengths and tokens go back to pinned host
+    # memory.  Captured once as a CUDA graph; every timed step replays it.
     if e2e:
-        in_keys = [k for k in ("lat_tok", "lat_score", "gdn_q", "gdn_k", "gdn_v", "gdn_alpha",
-                               "gdn_beta", "attn_q", "k_tree", "v_tree", "logits", "m_req",
-                               "lat_base") if x.get(k) is not None]
-        offs, total = {}, 0
-        for k in in_keys:
-            offs[k] = total
-            total += (x[k].numel() * x[k].element_size() + 255) // 256 * 256
-        dev_pack = torch.empty(total, dtype=torch.uint8, device=dev)
-        host_pack = torch.empty(total, dtype=torch.uint8).pin_memory()
-        for k in in_keys:
-            n = x[k].numel() * x[k].element_size()
-            view = dev_pack[offs[k]:offs[k] + n].view(x[k].dtype).view(x[k].shape)
-            view.copy_(x[k])
-            host_pack[offs[k]:offs[k] + n].copy_(x[k].cpu().contiguous().view(-1).view(torch.uint8))
-            x[k] = view
-        host_out = {k: torch.empty_like(getattr(st.acc, k), device="cpu").pin_memory()
-                    for k in ("accept_len", "out_tok")}
+        from speculative_decoding_tree_best_gb300.step import HostStep
+        hs = HostStep(st)
+        reset()
+        hs.capture()
         e2e_ms = []
         for i in range(warmup + steps):
             flush.zero_()
             reset()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            dev_pack.copy_(host_pack, non_blocking=True)
-            st.run()
-            for k, t in host_out.items():
-                t.copy_(getattr(st.acc, k), non_blocking=True)
+            hs.run()
             b.record(stream)
             torch.cuda.synchronize()
             if i >= warmup:
                 e2e_ms.append(a.elapsed_time(b))
         res["e2e_ms"] = max_over_ranks(sum(e2e_ms) / len(e2e_ms), world)
-        res["h2d"] = total
-        res["d2h"] = sum(t.numel() * t.element_size() for t in host_out.values())
+        res["h2d"] = hs.h2d_bytes
+        res["d2h"] = hs.d2h_bytes
     return res
 
 

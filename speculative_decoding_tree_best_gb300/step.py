@@ -62,16 +62,23 @@ class VerifyStep:
             binding.spec_tree_build(self.cfg, x["lat_tok"], x["lat_score"], x["root_tok"],
                                     self.tree, self.ws, stream)
 
-    def verify(self, stream=None):
+    def verify_gdn(self, stream=None):
         x, c = self.x, self.cfg
         for l in range(c.n_gdn_layers):
             binding.gdn_tree_verify(c, self.tree, x["gdn_h0"][l], x["gdn_q"][l], x["gdn_k"][l],
                                     x["gdn_v"][l], x["gdn_alpha"][l], x["gdn_beta"][l],
                                     self.gdn_o[l], None, self.ws, stream)
+
+    def verify_attention(self, stream=None):
+        x, c = self.x, self.cfg
         for l in range(c.n_attn_layers):
             binding.attn_tree_verify(c, self.tree, x["attn_q"][l], x["k_tree"][l], x["v_tree"][l],
                                      x["k_cache"][l], x["v_cache"][l], x["kv_len"],
                                      self.attn_o[l], self.ws, stream)
+
+    def verify(self, stream=None):
+        self.verify_gdn(stream)
+        self.verify_attention(stream)
 
     def commit_io(self) -> dict:
         x = self.x
@@ -134,3 +141,97 @@ class VerifyStep:
             return binding.spec_step_launches_persistent(self.cfg)
         # the shared budget adds one launch (the selection) to the step
         return binding.spec_step_launches(self.cfg) + (1 if self.scfg.budget >= 0 else 0)
+
+
+# The step's per-step inputs by the phase that first reads them, in the order
+# the copies are issued (the phases' order on the compute stream).
+HOST_PIECES = (("tree", ("lat_tok", "lat_score", "m_req", "lat_base")),
+               ("attn", ("attn_q", "k_tree", "v_tree")),
+               ("gdn", ("gdn_q", "gdn_k", "gdn_v", "gdn_alpha", "gdn_beta")),
+               ("logits", ("logits",)))
+
+
+class HostStep:
+    """A verify step whose per-step inputs come from pinned host memory.
+
+    The inputs are copied in four pieces (lattice, attention rows, GDN rows,
+    logits) on a copy stream, in the order the step reads them, and each phase
+    on the compute stream waits only for its own piece: the tree build starts
+    once the lattice is in, and the logits -- most of the bytes -- are copied
+    while the tree, attention and GDN layers run; the acceptance and commit
+    wait for them.  The accepted lengths and tokens come back to pinned host
+    memory at the end.  The whole sequence is captured once as a CUDA graph
+    and replayed per step.
+
+    st: a VerifyStep whose per-step input tensors this object re-points at
+    its device pieces (their current values are copied into the pinned host
+    buffers, which the caller then refills per step through `views`).
+    """
+
+    def __init__(self, st: "VerifyStep"):
+        self.st = st
+        x = st.x
+        self.host, self.dev, self.views = {}, {}, {}
+        self.h2d_bytes = 0
+        for piece, keys in HOST_PIECES:
+            keys = [k for k in keys if x.get(k) is not None]
+            if not keys:
+                continue
+            offs, total = {}, 0
+            for k in keys:
+                offs[k] = total
+                total += (x[k].numel() * x[k].element_size() + 255) // 256 * 256
+            dev = torch.empty(total, dtype=torch.uint8, device=st.device)
+            host = torch.empty(total, dtype=torch.uint8).pin_memory()
+            for k in keys:
+                n = x[k].numel() * x[k].element_size()
+                view = dev[offs[k]:offs[k] + n].view(x[k].dtype).view(x[k].shape)
+                view.copy_(x[k])
+                host[offs[k]:offs[k] + n].copy_(x[k].cpu().contiguous().view(-1).view(torch.uint8))
+                x[k] = view
+                self.views[k] = host[offs[k]:offs[k] + n].view(view.dtype).view(view.shape)
+            self.host[piece], self.dev[piece] = host, dev
+            self.h2d_bytes += sum(x[k].numel() * x[k].element_size() for k in keys)
+        self.out = {k: torch.empty_like(getattr(st.acc, k), device="cpu").pin_memory()
+                    for k in ("accept_len", "out_tok")}
+        self.d2h_bytes = sum(t.numel() * t.element_size() for t in self.out.values())
+        self.copy_stream = torch.cuda.Stream(device=st.device)
+        self.graph = None
+
+    def _sequence(self):
+        st = self.st
+        comp = torch.cuda.current_stream()
+        cs = self.copy_stream
+        cs.wait_stream(comp)                 # the previous step's readers are done
+        ev = {}
+        with torch.cuda.stream(cs):
+            for piece, _ in HOST_PIECES:
+                if piece in self.dev:
+                    self.dev[piece].copy_(self.host[piece], non_blocking=True)
+                    ev[piece] = torch.cuda.Event()
+                    ev[piece].record(cs)
+        for piece, run in (("tree", st.build_tree), ("attn", st.verify_attention),
+                           ("gdn", st.verify_gdn), ("logits", st.accept_commit)):
+            if piece in ev:
+                comp.wait_event(ev[piece])
+            run()
+        comp.wait_stream(cs)
+        for k, t in self.out.items():
+            t.copy_(getattr(st.acc, k), non_blocking=True)
+
+    def capture(self):
+        """Run the copies, the four phases and the result read-back once,
+        then capture them as a CUDA graph."""
+        self._sequence()
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, capture_error_mode="thread_local"):
+            self._sequence()
+        torch.cuda.synchronize()
+
+    def run(self):
+        """One step: copies in, the step, results out (asynchronous on the
+        current stream; synchronize before reading self.out)."""
+        if self.graph is None:
+            self.capture()
+        self.graph.replay()

@@ -222,3 +222,33 @@ def test_v_beyond_fp16_range_is_flagged(where, value, flagged):
     else:
         assert status == 0
         parity.compare(cfg, inp, tree_o, st)
+
+
+@pytest.mark.parametrize("ci", [1, 4])
+def test_host_step_equals_the_device_step(ci):
+    """step.HostStep (inputs copied from pinned host memory in pieces on a copy
+    stream, each phase waiting for its own piece, captured as a graph) gives
+    the same bits as the fused step on device-resident inputs: after its eager
+    first run and after a graph replay (two consecutive steps)."""
+    from speculative_decoding_tree_best_gb300.step import HostStep, VerifyStep, stack_inputs
+    cfg = synth.config(ci) if ci == 1 else synth.config(4).replace(B=2, n_gdn=3, n_attn=2, L=300)
+    inp, _ = parity.prepare(cfg, 3)
+    a = VerifyStep(cfg, stack_inputs(inp, "cuda"))
+    b = VerifyStep(cfg, stack_inputs(inp, "cuda"))
+    hs = HostStep(b)
+    for rep in range(2):
+        a.run()
+        if rep == 0:
+            hs.capture()          # runs the sequence once, then captures it
+        else:
+            hs.run()
+        torch.cuda.synchronize()
+        for k in ("node_tok", "node_parent", "node_anc", "n_nodes"):
+            assert torch.equal(getattr(a.tree, k), getattr(b.tree, k)), k
+        assert torch.equal(a.gdn_o, b.gdn_o) and torch.equal(a.attn_o, b.attn_o)
+        for k in ("argmax", "accept_len", "accept_nodes", "out_tok"):
+            assert torch.equal(getattr(a.acc, k), getattr(b.acc, k)), k
+        for k in ("gdn_h0", "k_cache", "v_cache", "kv_len", "root_tok"):
+            assert torch.equal(a.x[k], b.x[k]), k
+        assert torch.equal(hs.out["accept_len"], a.acc.accept_len.cpu())
+        assert torch.equal(hs.out["out_tok"], a.acc.out_tok.cpu())
