@@ -146,7 +146,9 @@ __device__ __forceinline__ ItemIdx decode(int it, const spec_cfg& c) {
 // rows done complete once (parity k & 1), as does [6], the output products.
 // Item k's products go to the tensor-memory buffer k & 1, and [4 + (k & 1)]
 // completes once all four row warps have read that buffer (parity
-// (k >> 1) & 1), so the products of item k + 1 never wait for item k's rows.
+// (k >> 1) & 1).  Item k + 1's products wait for that (the start of item k's
+// rows, not their end), which also keeps [2] from completing item k + 1
+// before every row warp has waited for item k.
 // As soon as item k's
 // products have read the staging buffer and the K/Q tile, item k + 1's state
 // and K/Q/v copies start (v into the other of two buffers), so warpgroup 1
@@ -273,9 +275,12 @@ gdn_state_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
                 fence_async_smem();
                 bool go = true;
                 if (t == 0 && kh == 0) {
-                    // item k - 2's P^T (the same tensor-memory buffer) has been read,
-                    // and this item's K/Q rows are in
-                    if (k >= 2) go = mbar_wait(&bar[4 + ph], ((k >> 1) - 1) & 1, abort_flag);
+                    // item k - 1's P^T has been read -- so every row warp has seen item
+                    // k - 1's products complete before item k's can complete (the
+                    // products barrier never runs two phases ahead of a waiter) -- and
+                    // this item's K/Q rows are in.  Item k writes the other buffer, so
+                    // it waits only for the start of item k - 1's rows.
+                    if (k >= 1) go = mbar_wait(&bar[4 + (ph ^ 1)], ((k - 1) >> 1) & 1, abort_flag);
                     go = go && mbar_wait(&bar[0], ph, abort_flag);
                 }
                 ok = wg_sync_and(1, go);
@@ -300,7 +305,7 @@ gdn_state_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
                 mma_commit(&bar[2]);
                 ++n_p;
                 pending = false;
-                if (it + G < n_items) {
+                if (ok && it + G < n_items) {
                     // the next item's copies once this item's products and Gram rows
                     // have read the staging buffer and the K/Q tile, and item k - 1's
                     // rows (the other v buffer) have read their inputs
@@ -316,7 +321,7 @@ gdn_state_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__
                     }
                 }
             }
-            ok = __all_sync(0xffffffffu, ok);
+            ok = wg_sync_and(1, ok);           // the warpgroup leaves the loop together
             if (k == 0 && early) {
                 pdl_wait();
                 pdl_trigger();
