@@ -74,20 +74,20 @@ _CSRC = "speculative_decoding_tree_best_gb300/csrc/"
 TRAFFIC = {
     "attn": {"sources": tuple(_CSRC + f for f in ("attn_tree_tc.cu", "attn_tree.cu", "common.cuh",
                                                    "tc_util.cuh")),
-             "sha256": "9f30092e6fae93241e92394929e3695c0e2547afd8007f47ea31f4c2bd1c56a1",
-             "bytes": {"single": 20795769, "batched": 484530652}},
+             "sha256": "aef6015e309e6fdeed51e357bc60f8a03f5aed501c95ed171a0f1cf0e62bf9fc",
+             "bytes": {"single": 20793838, "batched": 484581003}},
     "gdn": {"sources": tuple(_CSRC + f for f in ("gdn_state.cu", "gdn_tc_body.cuh", "tc_util.cuh",
                                                   "common.cuh")),
-            "sha256": "322a8792c5d6789da4eb9e1d91aabf052618f1dde432533a3b0531c43a605191",
-            "bytes": {"single": 2583200, "batched": 60400448}},
+            "sha256": "1e639ddea5ed13162b5a85fcd4578c466973b172275dd9767e7125d01d7ea151",
+            "bytes": {"single": 2617120, "batched": 60736320}},
     "argmax": {"sources": tuple(_CSRC + f for f in ("accept_commit.cu", "accept_util.cuh",
                                                      "common.cuh")),
                "sha256": "733e0bc407dc0c8728aee1752c597fd12019633ba3b836d07a32138bca0f23a7",
-               "bytes": {"single": 7619840, "batched": 182581248}},
+               "bytes": {"single": 7619488, "batched": 182588928}},
     "commit": {"sources": tuple(_CSRC + f for f in ("accept_commit.cu", "accept_util.cuh",
                                                      "common.cuh")),
                "sha256": "733e0bc407dc0c8728aee1752c597fd12019633ba3b836d07a32138bca0f23a7",
-               "bytes": {"single": 2183808, "batched": 51926560}},
+               "bytes": {"single": 2184352, "batched": 51945280}},
 }
 
 
