@@ -143,23 +143,22 @@ class VerifyStep:
         return binding.spec_step_launches(self.cfg) + (1 if self.scfg.budget >= 0 else 0)
 
 
-# The step's per-step inputs by the phase that first reads them, in the order
-# the copies are issued (the phases' order on the compute stream).
-HOST_PIECES = (("tree", ("lat_tok", "lat_score", "m_req", "lat_base")),
-               ("attn", ("attn_q", "k_tree", "v_tree")),
-               ("gdn", ("gdn_q", "gdn_k", "gdn_v", "gdn_alpha", "gdn_beta")),
+# The step's per-step inputs in two pieces, in the order the copies are
+# issued: the rows the tree build, the attention and the GDN layers read (the
+# lattice first), then the logits, read only by the acceptance.
+HOST_PIECES = (("rows", ("lat_tok", "lat_score", "m_req", "lat_base", "attn_q", "k_tree",
+                         "v_tree", "gdn_q", "gdn_k", "gdn_v", "gdn_alpha", "gdn_beta")),
                ("logits", ("logits",)))
 
 
 class HostStep:
     """A verify step whose per-step inputs come from pinned host memory.
 
-    The inputs are copied in four pieces (lattice, attention rows, GDN rows,
-    logits) on a copy stream, in the order the step reads them, and each phase
-    on the compute stream waits only for its own piece: the tree build starts
-    once the lattice is in, and the logits -- most of the bytes -- are copied
-    while the tree, attention and GDN layers run; the acceptance and commit
-    wait for them.  The accepted lengths and tokens come back to pinned host
+    The inputs are copied in two pieces on a copy stream: first the rows the
+    tree build, the attention and the GDN layers read (one copy: each copy
+    costs a few microseconds of its own), then the logits -- most of the
+    bytes -- while the tree, attention and GDN layers run; only the
+    acceptance and commit wait for the logits.  The accepted lengths and tokens come back to pinned host
     memory at the end.  The whole sequence is captured once as a CUDA graph
     and replayed per step.
 
@@ -210,8 +209,8 @@ class HostStep:
                     self.dev[piece].copy_(self.host[piece], non_blocking=True)
                     ev[piece] = torch.cuda.Event()
                     ev[piece].record(cs)
-        for piece, run in (("tree", st.build_tree), ("attn", st.verify_attention),
-                           ("gdn", st.verify_gdn), ("logits", st.accept_commit)):
+        for piece, run in (("rows", st.build_tree), (None, st.verify_attention),
+                           (None, st.verify_gdn), ("logits", st.accept_commit)):
             if piece in ev:
                 comp.wait_event(ev[piece])
             run()
