@@ -69,25 +69,26 @@ def algorithmic_bytes(s: synth.SpecConfig, mean_L: float, tau: float, rows=None)
 # launch), keyed by workload, with the SHA-256 of the sources they were taken
 # on: once a kernel's sources change, its figure is dropped (reported as null)
 # until it is captured again.  "attn" is one attention layer: the split-KV
-# partial launch plus its merge.
+# partial launch plus its merge, as attn_tree_verify launches them (the fused
+# step at one request runs the last merge inside the acceptance's launch).
 _CSRC = "speculative_decoding_tree_best_gb300/csrc/"
 TRAFFIC = {
     "attn": {"sources": tuple(_CSRC + f for f in ("attn_tree_tc.cu", "attn_tree.cu", "common.cuh",
-                                                   "tc_util.cuh")),
-             "sha256": "aef6015e309e6fdeed51e357bc60f8a03f5aed501c95ed171a0f1cf0e62bf9fc",
-             "bytes": {"single": 20793838, "batched": 484581003}},
+                                                   "tc_util.cuh", "accept_util.cuh")),
+             "sha256": "23b5a9ed983f190c91f1a6caf5ffe1b6c3acebefed3b558ee296028c0fcbb7f1",
+             "bytes": {"single": 20796116, "batched": 484524798}},
     "gdn": {"sources": tuple(_CSRC + f for f in ("gdn_state.cu", "gdn_tc_body.cuh", "tc_util.cuh",
                                                   "common.cuh")),
             "sha256": "1e639ddea5ed13162b5a85fcd4578c466973b172275dd9767e7125d01d7ea151",
-            "bytes": {"single": 2617120, "batched": 60736320}},
+            "bytes": {"single": 2601194, "batched": 60716050}},
     "argmax": {"sources": tuple(_CSRC + f for f in ("accept_commit.cu", "accept_util.cuh",
                                                      "common.cuh")),
-               "sha256": "733e0bc407dc0c8728aee1752c597fd12019633ba3b836d07a32138bca0f23a7",
-               "bytes": {"single": 7619488, "batched": 182588928}},
+               "sha256": "f2a90cd8cbb95939256d1025babfc227414b10c995af42546221a3e362fc21a0",
+               "bytes": {"single": 7619763, "batched": 182567109}},
     "commit": {"sources": tuple(_CSRC + f for f in ("accept_commit.cu", "accept_util.cuh",
                                                      "common.cuh")),
-               "sha256": "733e0bc407dc0c8728aee1752c597fd12019633ba3b836d07a32138bca0f23a7",
-               "bytes": {"single": 2184352, "batched": 51945280}},
+               "sha256": "f2a90cd8cbb95939256d1025babfc227414b10c995af42546221a3e362fc21a0",
+               "bytes": {"single": 2184241, "batched": 51943010}},
 }
 
 

@@ -402,7 +402,12 @@ int spec_verify_step_persistent(const spec_cfg *cfg, const int32_t *lat_tok,
                                 void *stream);
 
 /* Number of kernel launches one spec_verify_step(cfg) call makes (host only;
- * -1 on an invalid cfg): for sizing graphs and counting launches. */
+ * -1 on an invalid cfg): for sizing graphs and counting launches.  The same
+ * for spec_verify_step_ragged and _markov (the ragged step adds one launch
+ * for the budget selection when a budget is given).  With an attention layer
+ * and at most 64 logits rows (B x (N + 1)) the argmax + acceptance shares the
+ * last merge's launch; spec_verify_step_sampled then makes one launch more
+ * (its acceptance is always a launch of its own). */
 int spec_step_launches(const spec_cfg *cfg);
 
 /* The same for spec_verify_step_persistent (-1 when unsupported). */

@@ -50,45 +50,8 @@ __global__ void __launch_bounds__(NT)
 argmax_accept(spec_cfg c, const typename io_t<IO>::T* __restrict__ logits, spec_tree tree,
               spec_commit_io io, spec_accept acc, void* ws, WsLayout w, bool tree_early,
               bool trigger_first) {
-    using E = typename io_t<IO>::T;
-    constexpr int VEC = 16 / sizeof(E);
-    const int sp = blockIdx.x, row = blockIdx.y;
-    // trigger_first: the launches after this one read nothing it writes before
-    // their own waits, so they may start at once
-    if (trigger_first) pdl_trigger();
-    const int T = c.N + 1, b = row / T, t = row % T;
-    // n_nodes may only be read before the wait when the launch that wrote the
-    // tree is at least two back
-    if (!tree_early) pdl_wait();
-    if (t < tree.n_nodes[b]) {                           // CTA-uniform
-        int seg = (c.V + w.argmax_split - 1) / w.argmax_split;
-        seg = (seg + VEC - 1) / VEC * VEC;
-        const int lo = sp * seg, hi = min(c.V, lo + seg);
-        float bv;
-        int bi;
-        scan_segment<IO>(logits + (size_t)row * c.V, c.V, lo, hi, bv, bi);
-        if (threadIdx.x == 0)
-            ws_ptr<float2>(ws, w.argmax_off)[(size_t)row * kArgmaxSplit + sp] =
-                make_float2(bv, __int_as_float(bi));
-    }
-    // The acceptance reads the tree and rewrites kv_len: everything before this
-    // launch must be done.
-    pdl_wait();
-    if (!trigger_first) pdl_trigger();
-    // Every CTA of the request takes a ticket; the last one runs the acceptance.
-    __shared__ bool last;
-    if (threadIdx.x == 0) {
-        __threadfence();
-        unsigned int* tk = ws_ptr<unsigned int>(ws, w.acc_ticket_off) + b;
-        const unsigned int done = atomicAdd(tk, 1u);
-        last = done == (unsigned int)(T * w.argmax_split) - 1u;
-        if (last) *tk = 0u;                 // leave the ticket at zero for the next call
-    }
-    __syncthreads();
-    if (last && threadIdx.x < 32) {
-        __threadfence();
-        accept_request(c, tree, io, acc, ws, w, b);
-    }
+    acc::argmax_block<IO>(c, logits, tree, io, acc, ws, w, tree_early, trigger_first, blockIdx.x,
+                          blockIdx.y);
 }
 
 // ---- sampled acceptance ------------------------------------------------------------

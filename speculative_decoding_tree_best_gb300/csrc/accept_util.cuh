@@ -155,5 +155,54 @@ __device__ inline void scan_segment(const typename io_t<IO>::T* __restrict__ rp,
 }
 
 
+// One CTA of the argmax + acceptance launch: segment `sp` of logits row `row`
+// (request row / T, tree row row % T), reduced to (max, first index) in the
+// workspace; the last CTA of a request (atomic ticket) runs its acceptance.
+// tree_early: the launch that wrote the tree is at least two back, so n_nodes
+// may be read before the wait.  trigger_first: the launches after this one
+// read nothing it writes before their own waits, so they may start at once.
+template <int IO>
+__device__ inline void argmax_block(const spec_cfg& c, const typename io_t<IO>::T* __restrict__ logits,
+                                    const spec_tree& tree, const spec_commit_io& io,
+                                    const spec_accept& out, void* ws, const WsLayout& w,
+                                    bool tree_early, bool trigger_first, int sp, int row) {
+    using E = typename io_t<IO>::T;
+    constexpr int VEC = 16 / sizeof(E);
+    if (trigger_first) pdl_trigger();
+    const int T = c.N + 1, b = row / T, t = row % T;
+    // n_nodes may only be read before the wait when the launch that wrote the
+    // tree is at least two back
+    if (!tree_early) pdl_wait();
+    if (t < tree.n_nodes[b]) {                           // CTA-uniform
+        int seg = (c.V + w.argmax_split - 1) / w.argmax_split;
+        seg = (seg + VEC - 1) / VEC * VEC;
+        const int lo = sp * seg, hi = min(c.V, lo + seg);
+        float bv;
+        int bi;
+        scan_segment<IO>(logits + (size_t)row * c.V, c.V, lo, hi, bv, bi);
+        if (threadIdx.x == 0)
+            ws_ptr<float2>(ws, w.argmax_off)[(size_t)row * kArgmaxSplit + sp] =
+                make_float2(bv, __int_as_float(bi));
+    }
+    // The acceptance reads the tree and rewrites kv_len: everything before this
+    // launch must be done.
+    pdl_wait();
+    if (!trigger_first) pdl_trigger();
+    // Every CTA of the request takes a ticket; the last one runs the acceptance.
+    __shared__ bool last;
+    if (threadIdx.x == 0) {
+        __threadfence();
+        unsigned int* tk = ws_ptr<unsigned int>(ws, w.acc_ticket_off) + b;
+        const unsigned int done = atomicAdd(tk, 1u);
+        last = done == (unsigned int)(T * w.argmax_split) - 1u;
+        if (last) *tk = 0u;                 // leave the ticket at zero for the next call
+    }
+    __syncthreads();
+    if (last && threadIdx.x < 32) {
+        __threadfence();
+        accept_request(c, tree, io, out, ws, w, b);
+    }
+}
+
 }  // namespace acc
 }  // namespace spec

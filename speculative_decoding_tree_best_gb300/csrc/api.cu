@@ -275,13 +275,22 @@ int verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_sc
     // draw, so it lets the GDN layers start only after its wait.
     // The commit waits first: it needs the plan and the GDN layers' last read
     // of h0.
+    // With the argmax acceptance and few logits rows, the last merge and the
+    // acceptance are one launch (merge CTAs, then argmax CTAs): the launch it
+    // saves is a large share of a small step.  With more rows the argmax CTAs
+    // run better as a launch of their own (fewer registers, more CTAs per SM
+    // for the scan): measured 203 -> 213 us at 24 requests, 37.4 -> 36.4 us at
+    // one.
+    const bool merge_accept = na > 0 && !smp && spec::merge_accept_fits(c);
     if (na > 0 && e == cudaSuccess) {
         const void *q, *kt, *vt, *kc, *vc;
         void* o;
         attn_args(na - 1, q, kt, vt, kc, vc, o);
-        e = spec::launch_attn_merge(c, *tree, o, ws, st, true, (na - 1) & 1, /*early=*/true);
+        e = merge_accept
+            ? spec::launch_merge_accept(c, *tree, o, ws, st, true, (na - 1) & 1, logits, *io, *out)
+            : spec::launch_attn_merge(c, *tree, o, ws, st, true, (na - 1) & 1, /*early=*/true);
     }
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && !merge_accept)
         e = smp ? spec::launch_sample_accept(c, *tree, logits, smp->temperature, smp->seed, *io,
                                              *out, ws, st, true, /*tree_early=*/na > 0,
                                              /*trigger_first=*/false)
@@ -315,7 +324,10 @@ int spec_step_launches(const spec_cfg* cfg) {
     if (check_cfg(cfg) != ST_OK) return -1;
     const int na = cfg->n_attn_layers, ng = cfg->n_gdn_layers;
     const int commit = (na + ng) > 0 ? 1 : 0;
-    return 1 + 2 * na + 1 + ng + commit;    // tree, partials + merges, argmax, GDN, commit
+    // tree, partials + merges (the last merge also runs the argmax when there is
+    // an attention layer and few logits rows), argmax, GDN, commit
+    const bool merged = na > 0 && spec::merge_accept_fits(*cfg);
+    return 1 + 2 * na + (merged ? 0 : 1) + ng + commit;
 }
 
 int spec_verify_step(const spec_cfg* cfg, const int32_t* lat_tok, const float* lat_score,

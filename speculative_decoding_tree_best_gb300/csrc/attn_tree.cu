@@ -19,6 +19,7 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include "accept_util.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -259,6 +260,33 @@ __device__ __forceinline__ void merge_row(const spec_cfg& c, const spec_tree& tr
         io_t<IO>::st(o, (((size_t)b * T + x) * c.Hq + h) * D + lane * EPL + e, acc[e]);
 }
 
+// The last attention layer's merge and the argmax + acceptance in one launch
+// (the step's merge and logits scan have no data in common): blocks
+// [0, n_merge) are the merge's (merge_x row groups per (kv-head, request);
+// they wait for the partials first, as the merge launched with early does),
+// the others the argmax + acceptance CTAs in (segment, row) order (they let
+// the next launch start at once, scan, and wait before their tickets).
+template <int IO, int D>
+__global__ void __launch_bounds__(NT, 3)
+merge_accept(spec_cfg c, spec_tree tree, void* ws, WsLayout w, typename io_t<IO>::T* __restrict__ o,
+             const typename io_t<IO>::T* __restrict__ logits, spec_commit_io io, spec_accept out,
+             int n_merge, int merge_x) {
+    const int id = blockIdx.x;
+    if (id < n_merge) {
+        const int bx = id % merge_x, g = (id / merge_x) % c.Hkv, b = id / (merge_x * c.Hkv);
+        const int T = c.N + 1, G = c.Hq / c.Hkv;
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        const int r = bx * NW + warp;
+        pdl_wait();
+        pdl_trigger();
+        if (r < G * T) merge_row<IO, D>(c, tree, ws, w, o, r, g, b, lane);
+    } else {
+        const int a = id - n_merge;
+        acc::argmax_block<IO>(c, logits, tree, io, out, ws, w, /*tree_early=*/true,
+                              /*trigger_first=*/true, a % w.argmax_split, a / w.argmax_split);
+    }
+}
+
 template <int IO, int D>
 cudaError_t launch_partial(const spec_cfg& c, const spec_tree& t, const void* q, const void* kt,
                            const void* vt, const void* kc, const void* vc, const int32_t* kv_len,
@@ -282,6 +310,21 @@ cudaError_t launch_merge(const spec_cfg& c, const spec_tree& t, void* o, void* w
                     dim3(NT), 0, st, c, t, ws, w, static_cast<E*>(o), early);
 }
 
+template <int IO, int D>
+cudaError_t launch_merge_accept_k(const spec_cfg& c, const spec_tree& t, void* o, void* ws,
+                                  cudaStream_t st, bool pdl, int part_buf, const void* logits,
+                                  const spec_commit_io& io, const spec_accept& out) {
+    using E = typename io_t<IO>::T;
+    static_assert(NT == acc::NT, "the argmax CTAs run with the merge's block size");
+    const WsLayout w = with_attn_buf(ws_layout(c, device_sm_count()), part_buf);
+    const int G = c.Hq / c.Hkv;
+    const int merge_x = (G * (c.N + 1) + NW - 1) / NW;
+    const int n_merge = merge_x * c.Hkv * c.B;
+    const int n_arg = w.argmax_split * c.B * (c.N + 1);
+    return launch_k(pdl, merge_accept<IO, D>, dim3(n_merge + n_arg), dim3(NT), 0, st, c, t, ws, w,
+                    static_cast<E*>(o), static_cast<const E*>(logits), io, out, n_merge, merge_x);
+}
+
 }  // namespace
 
 #define SPEC_ATTN_DISPATCH(FN, ...)                                                      \
@@ -300,6 +343,11 @@ cudaError_t launch_attn_partial(const spec_cfg& c, const spec_tree& t, const voi
 cudaError_t launch_attn_merge(const spec_cfg& c, const spec_tree& t, void* o, void* ws,
                               cudaStream_t st, bool pdl, int part_buf, bool early) {
     SPEC_ATTN_DISPATCH(launch_merge, c, t, o, ws, st, pdl, part_buf, early);
+}
+cudaError_t launch_merge_accept(const spec_cfg& c, const spec_tree& t, void* o, void* ws,
+                                cudaStream_t st, bool pdl, int part_buf, const void* logits,
+                                const spec_commit_io& io, const spec_accept& out) {
+    SPEC_ATTN_DISPATCH(launch_merge_accept_k, c, t, o, ws, st, pdl, part_buf, logits, io, out);
 }
 #undef SPEC_ATTN_DISPATCH
 

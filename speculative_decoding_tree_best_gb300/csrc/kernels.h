@@ -41,6 +41,13 @@ cudaError_t launch_gdn_state(const spec_cfg& c, const spec_tree& t, const float*
                              const float* beta, void* o, float* c_out, void* ws, cudaStream_t st,
                              bool pdl, bool early);
 
+// The last attention layer's merge and the argmax + acceptance as one launch
+// (the fused step's, with programmatic launch: the merge CTAs wait for the
+// partials, the argmax CTAs scan at once).
+inline bool merge_accept_fits(const spec_cfg& c) { return (long)c.B * (c.N + 1) <= 64; }
+cudaError_t launch_merge_accept(const spec_cfg& c, const spec_tree& t, void* o, void* ws,
+                                cudaStream_t st, bool pdl, int part_buf, const void* logits,
+                                const spec_commit_io& io, const spec_accept& out);
 cudaError_t launch_attn_tree(const spec_cfg& c, const spec_tree& t, const void* q,
                              const void* k_tree, const void* v_tree, const void* k_cache,
                              const void* v_cache, const int32_t* kv_len, void* o, void* ws,

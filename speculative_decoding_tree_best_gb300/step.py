@@ -139,8 +139,13 @@ class VerifyStep:
     def launches_per_step(self) -> int:
         if self.persistent:
             return binding.spec_step_launches_persistent(self.cfg)
-        # the shared budget adds one launch (the selection) to the step
-        return binding.spec_step_launches(self.cfg) + (1 if self.scfg.budget >= 0 else 0)
+        # the shared budget adds one launch (the selection) to the step; the
+        # sampled acceptance is a launch of its own (the argmax shares the last
+        # attention merge's)
+        extra = (1 if self.scfg.budget >= 0 else 0)
+        merged = self.cfg.n_attn_layers > 0 and self.cfg.B * (self.cfg.N + 1) <= 64
+        extra += 1 if (self.scfg.temperature > 0 and merged) else 0
+        return binding.spec_step_launches(self.cfg) + extra
 
 
 # The step's per-step inputs in two pieces, in the order the copies are

@@ -77,8 +77,14 @@ def test_workspace_layout_follows_the_sm_count(lib):
 
 def test_step_launch_count_is_host_only(lib):
     # tree, attention partials + merge, argmax/accept, GDN, commit
-    assert binding.spec_step_launches(binding.make_cfg(synth.config(0))) == 6
+    # tree, partials + merges, argmax (in the last merge's launch for at most
+    # 64 logits rows), GDN, commit
+    assert binding.spec_step_launches(binding.make_cfg(synth.config(0))) == 5
+    assert binding.spec_step_launches(binding.make_cfg(synth.config(1))) == 5
+    assert binding.spec_step_launches(binding.make_cfg(synth.config(3))) == 6
     assert binding.spec_step_launches(binding.make_cfg(synth.config(4))) == 1 + 32 + 1 + 48 + 1
+    # without attention layers the argmax is a launch of its own
+    assert binding.spec_step_launches(binding.make_cfg(synth.config(1).replace(n_attn=0))) == 4
     bad = binding.make_cfg(synth.config(1), dk=96)
     assert lib.spec_step_launches(ctypes.byref(bad)) == -1
 
