@@ -148,22 +148,26 @@ class VerifyStep:
         return binding.spec_step_launches(self.cfg) + extra
 
 
-# The step's per-step inputs in two pieces, in the order the copies are
-# issued: the rows the tree build, the attention and the GDN layers read (the
-# lattice first), then the logits, read only by the acceptance.
+# The step's per-step inputs in three pieces, in the order the copies are
+# issued: the lattice with the attention rows (the tree build and the
+# attention layers), the GDN rows, then the logits, read only by the
+# acceptance.  Each copy costs a few microseconds of its own, so small pieces
+# go together; the GDN rows stay apart because with many GDN layers they are
+# most of the non-logits bytes and the attention need not wait for them.
 HOST_PIECES = (("rows", ("lat_tok", "lat_score", "m_req", "lat_base", "attn_q", "k_tree",
-                         "v_tree", "gdn_q", "gdn_k", "gdn_v", "gdn_alpha", "gdn_beta")),
+                         "v_tree")),
+               ("gdn", ("gdn_q", "gdn_k", "gdn_v", "gdn_alpha", "gdn_beta")),
                ("logits", ("logits",)))
 
 
 class HostStep:
     """A verify step whose per-step inputs come from pinned host memory.
 
-    The inputs are copied in two pieces on a copy stream: first the rows the
-    tree build, the attention and the GDN layers read (one copy: each copy
-    costs a few microseconds of its own), then the logits -- most of the
-    bytes -- while the tree, attention and GDN layers run; only the
-    acceptance and commit wait for the logits.  The accepted lengths and tokens come back to pinned host
+    The inputs are copied in three pieces on a copy stream (the lattice with
+    the attention rows, the GDN rows, the logits), in the order the step reads
+    them, and each phase on the compute stream waits only for its own piece:
+    the logits -- most of the bytes -- are copied while the tree, attention
+    and GDN layers run, and only the acceptance and commit wait for them.  The accepted lengths and tokens come back to pinned host
     memory at the end.  The whole sequence is captured once as a CUDA graph
     and replayed per step.
 
@@ -215,7 +219,7 @@ class HostStep:
                     ev[piece] = torch.cuda.Event()
                     ev[piece].record(cs)
         for piece, run in (("rows", st.build_tree), (None, st.verify_attention),
-                           (None, st.verify_gdn), ("logits", st.accept_commit)):
+                           ("gdn", st.verify_gdn), ("logits", st.accept_commit)):
             if piece in ev:
                 comp.wait_event(ev[piece])
             run()
