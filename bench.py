@@ -75,20 +75,20 @@ _CSRC = "speculative_decoding_tree_best_gb300/csrc/"
 TRAFFIC = {
     "attn": {"sources": tuple(_CSRC + f for f in ("attn_tree_tc.cu", "attn_tree.cu", "common.cuh",
                                                    "tc_util.cuh", "accept_util.cuh")),
-             "sha256": "23b5a9ed983f190c91f1a6caf5ffe1b6c3acebefed3b558ee296028c0fcbb7f1",
-             "bytes": {"single": 20796116, "batched": 484524798}},
+             "sha256": "b287844655f4c2939e19a19e7302266d0d6f5ac98ddadb0227fb74853fe3f5eb",
+             "bytes": {"single": 20794445, "batched": 484542276}},
     "gdn": {"sources": tuple(_CSRC + f for f in ("gdn_state.cu", "gdn_tc_body.cuh", "tc_util.cuh",
                                                   "common.cuh")),
-            "sha256": "1e639ddea5ed13162b5a85fcd4578c466973b172275dd9767e7125d01d7ea151",
-            "bytes": {"single": 2601194, "batched": 60716050}},
+            "sha256": "b4d940efea1f4cdf684e144259cdc25e4c38ca1263660190b0b2abcefeb4a98e",
+            "bytes": {"single": 2601609, "batched": 60718354}},
     "argmax": {"sources": tuple(_CSRC + f for f in ("accept_commit.cu", "accept_util.cuh",
                                                      "common.cuh")),
-               "sha256": "f2a90cd8cbb95939256d1025babfc227414b10c995af42546221a3e362fc21a0",
-               "bytes": {"single": 7619763, "batched": 182567109}},
+               "sha256": "14a58ebe89787f70a42e400331dfe607baa0650600bbee01ed49d1f8fafe8ff0",
+               "bytes": {"single": 7620531, "batched": 182578058}},
     "commit": {"sources": tuple(_CSRC + f for f in ("accept_commit.cu", "accept_util.cuh",
                                                      "common.cuh")),
-               "sha256": "f2a90cd8cbb95939256d1025babfc227414b10c995af42546221a3e362fc21a0",
-               "bytes": {"single": 2184241, "batched": 51943010}},
+               "sha256": "14a58ebe89787f70a42e400331dfe607baa0650600bbee01ed49d1f8fafe8ff0",
+               "bytes": {"single": 2184326, "batched": 51938245}},
 }
 
 
