@@ -75,20 +75,20 @@ _CSRC = "speculative_decoding_tree_best_gb300/csrc/"
 TRAFFIC = {
     "attn": {"sources": tuple(_CSRC + f for f in ("attn_tree_tc.cu", "attn_tree.cu", "common.cuh",
                                                    "tc_util.cuh", "accept_util.cuh")),
-             "sha256": "b287844655f4c2939e19a19e7302266d0d6f5ac98ddadb0227fb74853fe3f5eb",
-             "bytes": {"single": 20794445, "batched": 484542276}},
+             "sha256": "bf68d689be48eb3c4896edaffb96ca5aaba7af0f92117820e0af0d8d9f436d0d",
+             "bytes": {"single": 20795010, "batched": 484539173}},
     "gdn": {"sources": tuple(_CSRC + f for f in ("gdn_state.cu", "gdn_tc_body.cuh", "tc_util.cuh",
                                                   "common.cuh")),
-            "sha256": "b4d940efea1f4cdf684e144259cdc25e4c38ca1263660190b0b2abcefeb4a98e",
-            "bytes": {"single": 2601609, "batched": 60718354}},
+            "sha256": "e6aadbab45768a061c4bd888b7740d8f8ff93f3089938d37e2c585cfd570ba53",
+            "bytes": {"single": 2601786, "batched": 60716288}},
     "argmax": {"sources": tuple(_CSRC + f for f in ("accept_commit.cu", "accept_util.cuh",
                                                      "common.cuh")),
-               "sha256": "14a58ebe89787f70a42e400331dfe607baa0650600bbee01ed49d1f8fafe8ff0",
-               "bytes": {"single": 7620531, "batched": 182578058}},
+               "sha256": "4b423f98cfdf98e67d765d2f27167a0738072068b9a3f60b5667c1fc7b1e6cbd",
+               "bytes": {"single": 7620634, "batched": 182559153}},
     "commit": {"sources": tuple(_CSRC + f for f in ("accept_commit.cu", "accept_util.cuh",
                                                      "common.cuh")),
-               "sha256": "14a58ebe89787f70a42e400331dfe607baa0650600bbee01ed49d1f8fafe8ff0",
-               "bytes": {"single": 2184326, "batched": 51938245}},
+               "sha256": "4b423f98cfdf98e67d765d2f27167a0738072068b9a3f60b5667c1fc7b1e6cbd",
+               "bytes": {"single": 2183997, "batched": 51951596}},
 }
 
 

@@ -1,6 +1,7 @@
-// accept_util.cuh -- the pieces of the acceptance shared by accept_commit.cu
-// and verify_commit.cu: the vocabulary argmax of a logits segment and the
-// greedy walk of one request.
+// accept_util.cuh -- the pieces of the acceptance shared by accept_commit.cu,
+// verify_commit.cu and attn_tree.cu (the merge + acceptance launch): the
+// vocabulary argmax of a logits segment, the greedy walk of one request, and
+// one CTA of the argmax + acceptance launch.
 //
 // Digest "SpecPilot ...": prerequisites / speculative decoding (greedy: accept
 // the longest prefix equal to the target argmax, plus one bonus token,

@@ -19,19 +19,23 @@
 //    products
 //        D[col][x] += sum_k h0[k][col] [K; Q][x][k]    (state as MN-major A,
 //                                                        M = 128 columns)
-//    so that tensor-memory lane `col` holds that column's Pk_x, Pq_x;
-//  * warpgroup 0 (warps 0-3): thread 0 issues the TMA copies and, once K and
-//    Q are in, the Gram rows G = [K; Q] K^T (exact bf16 products) into tensor
-//    memory; warps 0/1 turn Gram row x (lane x) and the tree into the weight
-//    row of c_x (warp 0) or o_x (warp 1): decay x Gram entry on the root path,
-//    zero elsewhere.  Then each of the four warps takes 32 state columns (its
-//    tensor-memory lane quarter: one warp per SM sub-partition) and runs, one
-//    column per lane, the write-vector recursion with the write vectors in
-//    registers and no branch (right-looking: row x adds its weighted c_x into
-//    every later row, two rows per packed FMA; padding rows carry zero
-//    weights), then every output o_x from the same registers.
+//    so that tensor-memory lane `col` holds that column's Pk_x, Pq_x.  Its
+//    first thread also issues the next item's state and K/Q/v copies and
+//    prefetches the item after into L2;
+//  * warpgroup 0 (warps 0-3): thread 0 issues, once K and Q are in, the Gram
+//    rows G = [K; Q] K^T (exact bf16 products) into tensor memory; warps 0/1
+//    turn Gram row x (lane x) and the tree into the weight row of c_x (warp 0)
+//    or o_x (warp 1): decay x Gram entry on the root path, zero elsewhere.
+//    Then each of the four warps takes 32 state columns (its tensor-memory
+//    lane quarter: one warp per SM sub-partition) and runs, one column per
+//    lane, the write-vector recursion with the write vectors in registers
+//    (right-looking: row x adds its weighted c_x into every later row, two
+//    rows per packed FMA; a row without descendants is skipped; padding rows
+//    carry zero weights).  The outputs O = C Wo^T + A Pq are three more
+//    tcgen05 products (the write vectors and the o weights as bf16 hi/lo
+//    terms, the write vectors as A in tensor memory), read back per column.
 //
-// About 106 KB of shared memory and 128 tensor-memory columns per CTA: two
+// About 107 KB of shared memory and 256 tensor-memory columns per CTA: two
 // CTAs per SM, each with two states in flight (one being split while the
 // other's rows run).
 #include <cuda.h>
@@ -148,11 +152,11 @@ __device__ __forceinline__ ItemIdx decode(int it, const spec_cfg& c) {
 // completes once all four row warps have read that buffer (parity
 // (k >> 1) & 1).  Item k + 1's products wait for that (the start of item k's
 // rows, not their end), which also keeps [2] from completing item k + 1
-// before every row warp has waited for item k.
-// As soon as item k's
-// products have read the staging buffer and the K/Q tile, item k + 1's state
-// and K/Q/v copies start (v into the other of two buffers), so warpgroup 1
-// splits item k + 1's state while warpgroup 0 runs item k's rows.  early: the
+// before every row warp has waited for item k.  As soon as item k's products
+// and Gram rows have read the staging buffer and the K/Q tile, item k + 1's
+// state and K/Q/v copies start (v into the other of two buffers), so
+// warpgroup 1 splits item k + 1's state while warpgroup 0 runs item k's
+// rows.  early: the
 // tree may come from the launch just before, so the programmatic wait
 // precedes the first read of it; otherwise the wait ends the kernel.
 __global__ void __launch_bounds__(NT, 2)

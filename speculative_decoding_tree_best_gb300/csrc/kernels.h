@@ -34,7 +34,7 @@ cudaError_t launch_gdn_tree(const spec_cfg& c, const spec_tree& t, const float* 
                             bool pdl = false, bool early = true);
 size_t gdn_tree_smem(const spec_cfg& c);
 // tensor-core variant (bf16 I/O, d_k = d_v = 128, T <= 32): one CTA per
-// (request, v-head, 64 state columns); launch_gdn_tree uses it when supported
+// (request, v-head) state at a time; launch_gdn_tree uses it when supported
 bool gdn_state_supported(const spec_cfg& c);
 cudaError_t launch_gdn_state(const spec_cfg& c, const spec_tree& t, const float* h0,
                              const void* q, const void* k, const void* v, const float* alpha,
